@@ -1,0 +1,228 @@
+// (a) CSA2 cache write: compressor -> RMSNorm -> RoPE -> FP4 main KV, and the
+// 512->128 index-K projection -> MXFP4.
+//
+// Sources: "4. 层维度(下):CSA2 与每 token 890 字节" §4.2 (compressor
+// c_j = (w0 x_{2j-1} + w1 x_{2j}) / (w0 + w1) per channel), §4.4 (288 B main
+// entry = 256 B E2M1 + 32 B E4M3 scales; 68 B index entry = 64 B E2M1 + 4 B
+// E8M0); "DeepSeek-V4.1 Flash: 把 KV Cache 压缩推到极致" §2.3.1 (index K is a
+// projection of the main KV entry), §2.4.4 (RMSNorm, then RoPE, then FP4 with
+// one E4M3 scale per 16 channels and no global scale).
+//
+// Every binary32 operation that feeds a quantised byte is an explicit
+// round-to-nearest intrinsic in a fixed order, so the bytes are reproducible on
+// any IEEE machine that follows the same order:
+//   compress   c = fma(w0, x0, w1*x1) / (w0 + w1)
+//   RMSNorm    lane i owns channels 16i..16i+15: p_i = fma-chain of c^2 in
+//              channel order; butterfly sum over lanes (xor 16,8,4,2,1);
+//              r = 1/sqrt(ss/512 + 1e-6); y = c*r
+//   RoPE       pairs (448+2i, 449+2i): y0' = fma(y0,cos,-(y1*sin)),
+//              y1' = fma(y0,sin,y1*cos)
+//   main FP4   per 16: s = E4M3(amax/6), code = E2M1(y/s); s == 0 -> codes +0
+//   index K    k[o] = fma chain over channels 0..511 of y'[ch]*W[o][ch] from 0
+//   MXFP4      per 32: X = floor(log2 amax) - 2 clamped to [-127,127];
+//              code = E2M1(k * 2^-X); amax == 0 -> scale byte 0, codes +0
+//
+// Structure (persistent kernel, one CTA per SM, 256 threads):
+//   smem  W^T as bf16 [512 ch][128 o] (128 KB, loaded once per CTA)
+//         y tile   fp32 [512 ch][32 entries] (64 KB)
+//   phase 1  warp per entry: coalesced 128-bit loads of the token rows,
+//            compress/normalise/rotate in registers, write the 288-byte main
+//            entry, stage y' in smem.
+//   phase 2  each thread owns 4 outputs x 4 entries (16 independent fma
+//            chains); W^T row reads are contiguous across the warp, y reads
+//            are broadcasts.  This phase is FP32-ALU bound (65,536 fma per entry).
+//   phase 3  MXFP4 of k: 8 lanes form one 32-wide block.
+#include "params.cuh"
+
+namespace csa2 {
+
+constexpr int CW_THREADS = 256;
+constexpr int CW_TILE = 32;                       // entries per tile
+constexpr int CW_SMEM = D * DI * 2 + D * CW_TILE * 4;  // 131072 + 65536
+
+
+__global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint16_t* wt = reinterpret_cast<uint16_t*>(smem);                  // [512][128]
+  float* ytile = reinterpret_cast<float*>(smem + D * DI * 2);        // [512][32]
+  __shared__ int tile_valid[CW_TILE];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // W [128][512] -> W^T [512][128] in smem (once per CTA)
+  for (int i = tid; i < DI * D / 2; i += CW_THREADS) {
+    int o = i / (D / 2), ch2 = (i % (D / 2)) * 2;
+    uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p.w_idx) + i);
+    wt[(ch2 + 0) * DI + o] = (uint16_t)(v & 0xFFFFu);
+    wt[(ch2 + 1) * DI + o] = (uint16_t)(v >> 16);
+  }
+
+  const int64_t n_local = p.T / p.m;                   // entries per sequence
+  const int64_t tiles_per_seq = ceil_div(n_local, CW_TILE);
+  const int64_t n_tiles = tiles_per_seq * p.B;
+
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int b = (int)(tile / tiles_per_seq);
+    const int64_t j0 = (tile % tiles_per_seq) * CW_TILE;
+    const int64_t e0 = p.entry_start[b];
+    __syncthreads();   // previous tile's readers of ytile are done (and W^T is ready)
+
+    // ---------------- phase 1: warp per entry
+    for (int t = warp; t < CW_TILE; t += CW_THREADS / 32) {
+      const int64_t j = j0 + t;
+      const int64_t e = e0 + j;
+      bool valid = j < n_local;
+      if (valid && (e < 0 || e >= p.cap || e >= p.rope_P)) {
+        if (lane == 0) report(p.hdr, CSA2_ERR_BOUNDS, e);
+        valid = false;
+      }
+      if (lane == 0) tile_valid[t] = valid;
+      float y[16];
+      if (valid) {
+        const uint16_t* x0 = p.x + ((int64_t)b * p.T + j * p.m) * D + lane * 16;
+        uint4 a0 = __ldg(reinterpret_cast<const uint4*>(x0));
+        uint4 a1 = __ldg(reinterpret_cast<const uint4*>(x0) + 1);
+        uint32_t xa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float c[16];
+        if (p.m == 2) {
+          const uint16_t* x1 = x0 + D;
+          uint4 b0 = __ldg(reinterpret_cast<const uint4*>(x1));
+          uint4 b1 = __ldg(reinterpret_cast<const uint4*>(x1) + 1);
+          uint32_t xb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          const float4* w0v = reinterpret_cast<const float4*>(p.w0 + lane * 16);
+          const float4* w1v = reinterpret_cast<const float4*>(p.w1 + lane * 16);
+          float w0r[16], w1r[16];
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            float4 u = __ldg(w0v + q), v = __ldg(w1v + q);
+            w0r[4 * q] = u.x; w0r[4 * q + 1] = u.y; w0r[4 * q + 2] = u.z; w0r[4 * q + 3] = u.w;
+            w1r[4 * q] = v.x; w1r[4 * q + 1] = v.y; w1r[4 * q + 2] = v.z; w1r[4 * q + 3] = v.w;
+          }
+#pragma unroll
+          for (int k = 0; k < 16; k++) {
+            float a = bf16_bits_to_f32((xa[k / 2] >> (16 * (k & 1))) & 0xFFFFu);
+            float bb = bf16_bits_to_f32((xb[k / 2] >> (16 * (k & 1))) & 0xFFFFu);
+            float num = __fmaf_rn(w0r[k], a, __fmul_rn(w1r[k], bb));
+            float den = __fadd_rn(w0r[k], w1r[k]);
+            c[k] = __fdiv_rn(num, den);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; k++) c[k] = bf16_bits_to_f32((xa[k / 2] >> (16 * (k & 1))) & 0xFFFFu);
+        }
+        // RMSNorm
+        float ps = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; k++) ps = __fmaf_rn(c[k], c[k], ps);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ps = __fadd_rn(ps, __shfl_xor_sync(0xFFFFFFFFu, ps, off));
+        float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ps, 512.0f), 1e-6f)));
+#pragma unroll
+        for (int k = 0; k < 16; k++) y[k] = __fmul_rn(c[k], r);
+        // RoPE on channels 448..511 = lanes 28..31, pairs i = 8*(lane-28) + k/2
+        if (lane >= 28) {
+          const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + (e * 32 + (lane - 28) * 8) * 2);
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            float4 v = __ldg(cs + q);          // two pairs: (cos, sin, cos, sin)
+            float y0 = y[4 * q], y1 = y[4 * q + 1], y2 = y[4 * q + 2], y3 = y[4 * q + 3];
+            y[4 * q + 0] = __fmaf_rn(y0, v.x, -__fmul_rn(y1, v.y));
+            y[4 * q + 1] = __fmaf_rn(y0, v.y, __fmul_rn(y1, v.x));
+            y[4 * q + 2] = __fmaf_rn(y2, v.z, -__fmul_rn(y3, v.w));
+            y[4 * q + 3] = __fmaf_rn(y2, v.w, __fmul_rn(y3, v.z));
+          }
+        }
+        // main FP4: this lane's 16 channels are exactly one scale group
+        float amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; k++) amax = fmaxf(amax, fabsf(y[k]));
+        uint32_t sb = e4m3_byte(__fdiv_rn(amax, 6.0f));
+        float s = e4m3_value(sb);
+        uint32_t packed[2] = {0u, 0u};
+        if (s != 0.0f) {
+#pragma unroll
+          for (int k = 0; k < 8; k++) {
+            uint32_t byte = e2m1x2(__fdiv_rn(y[2 * k], s), __fdiv_rn(y[2 * k + 1], s));
+            packed[k / 4] |= byte << (8 * (k % 4));
+          }
+        }
+        uint8_t* ent = p.main_kv + ((int64_t)b * p.cap + e) * MAIN_BYTES;
+        *reinterpret_cast<uint2*>(ent + lane * 8) = make_uint2(packed[0], packed[1]);
+        ent[256 + lane] = (uint8_t)sb;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; k++) y[k] = 0.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < 16; k++) ytile[(lane * 16 + k) * CW_TILE + t] = y[k];
+    }
+    __syncthreads();
+
+    // ---------------- phase 2: k = W y', 4 outputs x 4 entries per thread
+    const int og = tid & 31;        // outputs 4*og .. 4*og+3
+    const int eg = tid >> 5;        // entries 4*eg .. 4*eg+3
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; a++)
+#pragma unroll
+      for (int bq = 0; bq < 4; bq++) acc[a][bq] = 0.0f;
+#pragma unroll 4
+    for (int ch = 0; ch < D; ch++) {
+      uint2 wv = *reinterpret_cast<const uint2*>(wt + ch * DI + og * 4);
+      float4 yv = *reinterpret_cast<const float4*>(ytile + ch * CW_TILE + eg * 4);
+      float wf[4] = {__uint_as_float(wv.x << 16), __uint_as_float(wv.x & 0xFFFF0000u),
+                     __uint_as_float(wv.y << 16), __uint_as_float(wv.y & 0xFFFF0000u)};
+      float yf[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+      for (int a = 0; a < 4; a++)
+#pragma unroll
+        for (int bq = 0; bq < 4; bq++) acc[a][bq] = __fmaf_rn(yf[bq], wf[a], acc[a][bq]);
+    }
+
+    // ---------------- phase 3: MXFP4 (8 lanes = one 32-wide block of outputs)
+#pragma unroll
+    for (int bq = 0; bq < 4; bq++) {
+      const int t = eg * 4 + bq;
+      const int64_t j = j0 + t;
+      float amax = fmaxf(fmaxf(fabsf(acc[0][bq]), fabsf(acc[1][bq])), fmaxf(fabsf(acc[2][bq]), fabsf(acc[3][bq])));
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      if (!tile_valid[t]) continue;     // uniform across the warp
+      const int64_t e = e0 + j;
+      uint32_t scale_byte, codes = 0;
+      if (amax == 0.0f) {
+        scale_byte = 0;
+      } else {
+        int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;   // floor(log2 amax) for normals
+        int X = ex - 2;
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+        scale_byte = (uint32_t)(X + 127);
+        float inv = __uint_as_float((uint32_t)(127 - X) << 23);      // 2^-X, exact
+        uint32_t lo = e2m1x2(__fmul_rn(acc[0][bq], inv), __fmul_rn(acc[1][bq], inv));
+        uint32_t hi = e2m1x2(__fmul_rn(acc[2][bq], inv), __fmul_rn(acc[3][bq], inv));
+        codes = lo | (hi << 8);
+      }
+      uint8_t* cdst = p.idx_codes + ((int64_t)b * p.cap + e) * IDX_CODE_BYTES;
+      *reinterpret_cast<uint16_t*>(cdst + og * 2) = (uint16_t)codes;
+      if ((og & 7) == 0) p.idx_scales[((int64_t)b * p.cap + e) * IDX_SCALE_BYTES + (og >> 3)] = (uint8_t)scale_byte;
+    }
+  }
+}
+
+cudaError_t launch_cache_write(const CwParams& p, cudaStream_t stream, int num_sms) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(cache_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CW_SMEM);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  int64_t n_local = p.T / p.m;
+  int64_t n_tiles = ceil_div(n_local, CW_TILE) * p.B;
+  if (n_tiles == 0) return cudaSuccess;
+  int grid = (int)(n_tiles < num_sms ? n_tiles : num_sms);
+  cache_write_kernel<<<grid, CW_THREADS, CW_SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

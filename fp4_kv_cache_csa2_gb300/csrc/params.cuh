@@ -1,0 +1,73 @@
+// Launch parameters and launcher declarations shared by the CSA2 translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace csa2 {
+
+struct CwParams {
+  uint8_t* main_kv;
+  uint8_t* idx_codes;
+  uint8_t* idx_scales;
+  int64_t cap;
+  int m;
+  const uint16_t* x;        // [B][T][512]
+  int B, T;
+  const int64_t* entry_start;
+  const float* w0;
+  const float* w1;
+  const float* rope_cs;     // [P][32][2]
+  int64_t rope_P;
+  const uint16_t* w_idx;    // [128][512]
+  WsHeader* hdr;
+};
+
+struct IsParams {
+  const uint8_t* idx_codes;
+  const uint8_t* idx_scales;
+  int64_t cap;
+  const int32_t* n_entries;
+  int m;
+  const uint16_t* q_idx;      // [B][Q][32][128]
+  const float* w_head;        // [B][Q][32]
+  const int64_t* q_pos;       // [B][Q]
+  const int32_t* pool;        // [B][Q][M] or null
+  int M;
+  float* scores;              // [B][Q][max_n] or [B][Q][M*8]
+  int B, Q;
+  int64_t max_n;
+  int64_t entries_per_cta;    // set by the launcher
+  WsHeader* hdr;
+};
+
+struct AttnParams {
+  const uint8_t* main_kv;
+  int64_t cap;
+  const uint16_t* q;          // [BQ][64][512]
+  const int32_t* sel;         // [BQ][K]
+  int K;
+  const uint16_t* swa;        // [B][S][512]
+  const int64_t* swa_base;    // [B]
+  int S;
+  const int64_t* q_pos;       // [BQ]
+  float scale;
+  uint16_t* out;              // [BQ][64][512]
+  int Q, n_chunks;            // n_chunks set by the launcher
+  float* opart;               // [BQ][n_chunks][64][512]
+  float* mpart;               // [BQ][n_chunks][64]
+  float* lpart;               // [BQ][n_chunks][64]
+  WsHeader* hdr;
+};
+
+cudaError_t launch_cache_write(const CwParams& p, cudaStream_t stream, int num_sms);
+cudaError_t launch_index_score(IsParams p, cudaStream_t stream);
+cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m,
+                              int B, int Q, int64_t max_n, int M, int32_t* pool_blocks, uint32_t* gkeys,
+                              cudaStream_t stream);
+cudaError_t launch_select_topk(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m,
+                               const int32_t* pool, int M, int K, int32_t* sel, int B, int Q, int64_t max_n,
+                               cudaStream_t stream);
+cudaError_t launch_attention(AttnParams p, int B, float* partials, cudaStream_t stream);
+size_t attn_partials_bytes(int64_t BQ, int K);
+
+}  // namespace csa2

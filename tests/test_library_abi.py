@@ -1,0 +1,74 @@
+"""CPU-side checks of the boundary: the library builds, loads without a GPU and
+exports every function include/csa2.h declares; the binding fails loudly when
+the library is missing."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa2.h")
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa2_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from fp4_kv_cache_csa2_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_layer_calls():
+    names = declared_functions()
+    for call in ("csa2_compress_quantize", "csa2_index_score", "csa2_block_topk", "csa2_select_topk",
+                 "csa2_sparse_swa_attn", "csa2_decode", "csa2_sync_status", "csa2_status_string"):
+        assert call in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol(lib_path):
+    import fp4_kv_cache_csa2_gb300 as csa2
+    assert sorted(csa2.exported_symbols()) == declared_functions()
+
+
+def test_host_only_calls_without_gpu(lib_path):
+    import fp4_kv_cache_csa2_gb300 as csa2
+    lib = csa2.load(lib_path)
+    assert lib.csa2_layout_version() == 1
+    assert lib.csa2_status_string(6) == b"CSA2_ERR_BOUNDS"
+    assert lib.csa2_attn_workspace_size(1, 1, 512) > 256
+    assert lib.csa2_block_topk_workspace_size(2, 3, 100) == 256 + 512    # 2*3*13*4 = 312 bytes -> 512
+    # argument validation happens before any CUDA call
+    assert lib.csa2_index_score(None, None, None, None, None, 0, None, 1, 1, 10, None, 0, None) == 1
+
+
+def test_rope_table_matches_oracle_bit_for_bit(lib_path):
+    """The library's table builder and the oracle's are separate restatements of
+    cos/sin(p * theta^(-2i/64)); their binary32 tables agree."""
+    import numpy as np
+    import fp4_kv_cache_csa2_gb300 as csa2
+    import oracle
+    got = csa2.rope_table(70000).numpy()
+    want = oracle.rope_table(70000)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import fp4_kv_cache_csa2_gb300 as csa2
+    saved = csa2._lib
+    csa2._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            csa2.load(str(tmp_path / "libcsa2.so"))
+    finally:
+        csa2._lib = saved
