@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark of the CSA2 global-attention layer on one GB300.
+
+Default workload (the headline metric): decode at 1,048,576 cached entries per
+sequence, batch 16, one 4-layer decoder block = a Reindex layer (own index
+queries score only the 2048-block candidate pool, top-512) followed by three
+Reuse layers (attention only, same selection and cache, fresh queries).  The
+pool comes from a Full source-layer scan done before timing.
+
+Cold-L2 layers: real models run MoE between layers, so a layer's cache reads
+come from HBM.  The bench keeps R independent batches (instances, each with its
+own 5.97 GB cache copy) and software-pipelines them: step s runs the Reindex
+layer of instance s, Reuse-1 of instance s-d, Reuse-2 of s-2d and Reuse-3 of
+s-3d, so roughly d steps (d * 44 MB > L2) pass between two layers touching
+the same instance.  One step = four layer calls of batch 16 = 64
+query-token-layers.
+
+Other workloads (``--workload``): ``full`` (decode Full, m=1, 64 x 131,072),
+``cachewrite`` (4 source layers x 2^20 tokens), ``prefill`` (8192-token chunk
+on a 131,072-token prefix, m=2).
+
+``--impl reference`` times the CPU oracle (the checker, not a product path) on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode query-tokens/s/layer at 1M ctx; % of HBM roofline"
+UNIT = "query-token-layers/s"
+
+# algorithmic bytes (per query token) of the 1M Reindex + 3 Reuse chain
+IDX_ENTRY, MAIN_ENTRY = 68, 288
+K_SEL, M_BLK, WIN, D, H, HI, DI = 512, 2048, 128, 512, 64, 32, 128
+ATTN_BYTES = K_SEL * MAIN_ENTRY + WIN * D * 2 + H * D * 2 + H * D * 2          # 409,600
+REINDEX_BYTES = M_BLK * 8 * IDX_ENTRY + M_BLK * 4 + HI * DI * 2 + HI * 4 + K_SEL * 4 + ATTN_BYTES
+REUSE_BYTES = K_SEL * 4 + ATTN_BYTES                                             # 411,648
+CHAIN_BYTES = REINDEX_BYTES + 3 * REUSE_BYTES                                    # 2,777,216
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace('.', '').isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace('.', '').isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in self.samples:
+            for name, v in zip(names, s[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ decode 1M
+class Decode1M:
+    """Reindex + 3 Reuse at 1,048,576 entries, batch 16, R pipelined instances."""
+
+    def __init__(self, csa2, torch, B=16, N=1 << 20, d=3, seed=3):
+        import synth
+        self.csa2, self.torch = csa2, torch
+        self.B, self.N, self.d = B, N, d
+        self.R = 3 * d + 1
+        dev = "cuda"
+        self.stream = torch.cuda.current_stream()
+        t0 = time.time()
+        # ---- instance 0's cache from seeded N(0,1) latents through the cache write (m = 1)
+        base = csa2.Cache(B, N, 1, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        w_idx = synth.torch_normal(seed + 1, (DI, D), torch.float32, dev).mul_(1 / math.sqrt(D)).to(torch.bfloat16)
+        rope = csa2.rope_table(N).to(dev)
+        ws_cw = csa2.Workspace(1 << 16, device=dev)
+        chunk = 1 << 17
+        ones = torch.ones(D, device=dev)
+        for b in range(B):
+            for c0 in range(0, N, chunk):
+                x = torch.randn((1, chunk, D), generator=g, device=dev).to(torch.bfloat16)
+                start = torch.tensor([c0], dtype=torch.int64, device=dev)
+                cache_b = _SubCache(base, b)
+                csa2.compress_quantize(cache_b, x.view(torch.int16), start, ones, ones, rope, w_idx.view(torch.int16),
+                                       ws_cw)
+        base.n_entries.fill_(N)
+        del rope
+        torch.cuda.synchronize()
+        assert ws_cw.sync_status()[0] == 0
+        self.setup_cache_s = time.time() - t0
+        # ---- candidate pool: one untimed Full source-layer scan of instance 0 (own index queries)
+        M, K = M_BLK, K_SEL
+        self.q_pos = torch.full((B, 1), N - 1, dtype=torch.int64, device=dev)
+        self.swa_base = torch.full((B,), N - WIN, dtype=torch.int64, device=dev)
+        full_q_idx = synth.torch_normal(seed + 2, (B, 1, HI, DI), torch.bfloat16, dev)
+        full_w = synth.torch_normal(seed + 3, (B, 1, HI), torch.float32, dev)
+        full_q = synth.torch_normal(seed + 4, (B, 1, H, D), torch.bfloat16, dev)
+        full_swa = synth.torch_swa_rows(seed + 5, (B, WIN), dev)
+        self.pool = torch.empty((B, 1, M), dtype=torch.int32, device=dev)
+        sel0 = torch.empty((B, 1, K), dtype=torch.int32, device=dev)
+        out0 = torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev)
+        ws_full = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_FULL, B, 1, N, M, K), device=dev)
+        t1 = time.time()
+        csa2.decode(csa2.MODE_FULL, base, q_pos=self.q_pos, q=full_q.view(torch.int16), swa=full_swa.view(torch.int16),
+                    swa_base_pos=self.swa_base, scale=1 / math.sqrt(D), sel=sel0, out=out0.view(torch.int16),
+                    ws=ws_full, M=M, max_n=N, q_idx=full_q_idx.view(torch.int16), w_head=full_w,
+                    pool_blocks=self.pool)
+        torch.cuda.synchronize()
+        self.full_scan_ms = (time.time() - t1) * 1e3
+        assert ws_full.sync_status()[0] == 0
+        del ws_full
+        # ---- R instances: cache copies at distinct addresses, own queries per layer
+        self.caches = [base] + [_clone_cache(base) for _ in range(self.R - 1)]
+        self.inst = []
+        for r in range(self.R):
+            s = seed + 100 * (r + 1)
+            inst = {
+                "q_idx": synth.torch_normal(s + 1, (B, 1, HI, DI), torch.bfloat16, dev),
+                "w_head": synth.torch_normal(s + 2, (B, 1, HI), torch.float32, dev),
+                "q": [synth.torch_normal(s + 10 + l, (B, 1, H, D), torch.bfloat16, dev) for l in range(4)],
+                "swa": [synth.torch_swa_rows(s + 20 + l, (B, WIN), dev) for l in range(4)],
+                "out": [torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev) for l in range(4)],
+                "sel": torch.empty((B, 1, K), dtype=torch.int32, device=dev),
+            }
+            self.inst.append(inst)
+        self.ws = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REINDEX, B, 1, N, M, K), device=dev)
+        for r in range(self.R):          # every instance starts with a published selection
+            self.layer(0, r)
+        torch.cuda.synchronize()
+        assert self.ws.sync_status()[0] == 0
+        self.setup_s = time.time() - t0
+
+    def layer(self, layer: int, r: int):
+        csa2, inst, torch = self.csa2, self.inst[r], self.torch
+        mode = csa2.MODE_REINDEX if layer == 0 else csa2.MODE_REUSE
+        csa2.decode(mode, self.caches[r], q_pos=self.q_pos, q=inst["q"][layer].view(torch.int16),
+                    swa=inst["swa"][layer].view(torch.int16), swa_base_pos=self.swa_base, scale=1 / math.sqrt(D),
+                    sel=inst["sel"], out=inst["out"][layer].view(torch.int16), ws=self.ws, M=M_BLK, max_n=self.N,
+                    q_idx=inst["q_idx"].view(torch.int16), w_head=inst["w_head"], pool_blocks=self.pool)
+
+    def step(self, s: int, events=None):
+        """Reindex(s), Reuse1(s-d), Reuse2(s-2d), Reuse3(s-3d) over instances mod R."""
+        for layer in range(4):
+            r = (s - layer * self.d) % self.R
+            if events is not None:
+                events[layer][0].record()
+            self.layer(layer, r)
+            if events is not None:
+                events[layer][1].record()
+
+    def prologue(self):
+        for s in range(3 * self.d):
+            self.step(s)
+
+
+class _SubCache:
+    """View of one sequence of a Cache as a batch-1 cache (for chunked writes)."""
+
+    def __init__(self, cache, b):
+        self.main_kv = cache.main_kv[b:b + 1]
+        self.idx_codes = cache.idx_codes[b:b + 1]
+        self.idx_scales = cache.idx_scales[b:b + 1]
+        self.n_entries = cache.n_entries[b:b + 1]
+        self.cap, self.m, self.B = cache.cap, cache.m, 1
+
+    def struct(self):
+        from fp4_kv_cache_csa2_gb300 import CacheStruct
+        return CacheStruct(self.main_kv.data_ptr(), self.idx_codes.data_ptr(), self.idx_scales.data_ptr(),
+                           self.cap, self.n_entries.data_ptr(), self.m)
+
+
+def _clone_cache(c):
+    import fp4_kv_cache_csa2_gb300 as csa2
+    n = csa2.Cache.__new__(csa2.Cache)
+    n.B, n.cap, n.m = c.B, c.cap, c.m
+    n.main_kv = c.main_kv.clone()
+    n.idx_codes = c.idx_codes.clone()
+    n.idx_scales = c.idx_scales.clone()
+    n.n_entries = c.n_entries.clone()
+    return n
+
+
+def run_decode1m(args, torch, csa2):
+    rank, world, local = dist_info()
+    w = Decode1M(csa2, torch, d=args.pipeline_distance)
+    w.prologue()
+    for s in range(args.warmup):
+        w.step(3 * w.d + s)
+    torch.cuda.synchronize()
+    n_steps = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
+          for _ in range(n_steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0 = 3 * w.d + args.warmup
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("timed")
+        start.record()
+        for i in range(n_steps):
+            w.step(s0 + i, ev[i])
+        stop.record()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    barrier(world)
+    total_ms = max_over_ranks(start.elapsed_time(stop), world)
+    layer_ms = [statistics.mean(ev[i][l][0].elapsed_time(ev[i][l][1]) for i in range(n_steps)) for l in range(4)]
+    st, detail = w.ws.sync_status()
+    assert st == 0, f"device status {st} ({detail})"
+
+    ms_step = total_ms / n_steps
+    qtl_per_step = w.B * 4
+    value = qtl_per_step * world / (ms_step / 1e3)
+    hbm, bf16, which = peaks()
+    bytes_step = w.B * CHAIN_BYTES
+    # dominant layer call by time: Reuse calls are 3 of 4
+    reuse_ms = statistics.mean(layer_ms[1:])
+    reindex_ms = layer_ms[0]
+    dom_is_reuse = 3 * reuse_ms >= reindex_ms
+    dom_ms = reuse_ms if dom_is_reuse else reindex_ms
+    dom_bytes = w.B * (REUSE_BYTES if dom_is_reuse else REINDEX_BYTES)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    e2e = run_decode1m_e2e(args, torch, csa2, w)
+    return {
+        "value": value, "ms_per_step": ms_step, "dtype": "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+        "config": {"workload": "decode Reindex + 3 Reuse, 1,048,576 entries/seq, batch 16 per layer call",
+                   "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
+                   "l2": f"inputs larger than L2: {w.R} pipelined instances x 5.97 GB, layer distance {w.d} steps",
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "csa2_decode(REUSE) (attention)" if dom_is_reuse else "csa2_decode(REINDEX)",
+                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                     "peak_source": which},
+        "step_hbm": {"algorithmic_bytes": bytes_step, "GB_s": bytes_step / (ms_step / 1e3) / 1e9,
+                     "frac": bytes_step / (ms_step / 1e3) / 1e9 / hbm},
+        "layer_ms": {"reindex": reindex_ms, "reuse": layer_ms[1:]},
+        "full_scan_1m_ms_untimed_setup": w.full_scan_ms,
+        "clocks": clk.summary(),
+        "gpu_launches": n_steps * (4 + 3 * 2),
+        "e2e": e2e,
+    }
+
+
+def run_decode1m_e2e(args, torch, csa2, w):
+    """Same pipeline through the public API with per-step host<->device copies:
+    H2D from pinned host memory of each layer's queries, the Reindex layer's
+    index queries and head weights, and one new window row per sequence per
+    layer; D2H of each layer's output."""
+    B = w.B
+    host_q = [torch.empty((B, 1, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    host_row = [torch.empty((B, D), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    host_qidx = torch.empty((B, 1, HI, DI), dtype=torch.bfloat16).pin_memory()
+    host_w = torch.empty((B, 1, HI), dtype=torch.float32).pin_memory()
+    host_out = [torch.empty((B, 1, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    for t in host_q + host_row:
+        t.normal_()
+    host_qidx.normal_()
+    host_w.normal_()
+    h2d = 4 * host_q[0].nbytes + 4 * host_row[0].nbytes + host_qidx.nbytes + host_w.nbytes
+    d2h = 4 * host_out[0].nbytes
+
+    def step(s):
+        for layer in range(4):
+            r = (s - layer * w.d) % w.R
+            inst = w.inst[r]
+            inst["q"][layer].copy_(host_q[layer], non_blocking=True)
+            inst["swa"][layer][:, WIN - 1].copy_(host_row[layer], non_blocking=True)
+            if layer == 0:
+                inst["q_idx"].copy_(host_qidx, non_blocking=True)
+                inst["w_head"].copy_(host_w, non_blocking=True)
+            w.layer(layer, r)
+            host_out[layer].copy_(inst["out"][layer], non_blocking=True)
+
+    s0 = 100000
+    for i in range(args.warmup):
+        step(s0 + i)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(args.steps):
+        step(s0 + args.warmup + i)
+    stop.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / args.steps
+    return {"value": B * 4 / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+class OracleChain:
+    """Oracle (binary64 numpy + C cache write) on the per-query work of the
+    decode step: Reindex (score a 16,384-entry pool, top-512, attention) and
+    three Reuse attentions.  The pool's entries are written by the oracle's own
+    cache write during set-up (untimed); entry ids are compacted so the pool is
+    blocks 0..2047, which leaves the per-query work unchanged."""
+
+    def __init__(self, seed: int = 9, n_query_sets: int = 8):
+        import numpy as np
+        import oracle
+        import synth
+        self.oracle = oracle
+        g = synth.rng(seed)
+        self.n = M_BLK * 8
+        x = synth.latents(g, self.n)
+        w0, w1 = synth.compressor_weights(g)
+        W = synth.index_projection(g)
+        self.main, self.codes, self.scales = oracle.compress_quantize(x, 1, w0, w1, W)
+        self.swa = synth.swa_rows(g, WIN)
+        self.pool = np.arange(M_BLK, dtype=np.int32)
+        self.qs = [(synth.index_queries(g), synth.head_weights(g), [synth.main_queries(g) for _ in range(4)])
+                   for _ in range(n_query_sets)]
+
+    def run(self, n_queries: int) -> tuple[float, float]:
+        o = self.oracle
+        common = dict(t=self.n - 1, m=1, n_entries=self.n, main_kv=self.main, idx_codes=self.codes,
+                      idx_scales=self.scales, swa=self.swa, swa_base=self.n - WIN, scale=1 / math.sqrt(D),
+                      M=M_BLK, K=K_SEL)
+        t0 = time.perf_counter()
+        for i in range(n_queries):
+            q_idx, wh, q4 = self.qs[i % len(self.qs)]
+            _, sel, _ = o.decode_query(o.REINDEX, q=q4[0], q_idx=q_idx, w_head=wh, pool_blocks=self.pool, **common)
+            for layer in range(1, 4):
+                o.decode_query(o.REUSE, q=q4[layer], sel=sel, **common)
+        dt = time.perf_counter() - t0
+        return n_queries * 4 / dt, dt
+
+
+def oracle_threads() -> int:
+    try:
+        import numpy as np
+        cfg = np.show_config(mode="dicts")
+        _ = cfg
+    except Exception:
+        pass
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return None
+    per_step = 8
+    chain = OracleChain()
+    for _ in range(max(args.warmup, 0)):
+        chain.run(1)
+    dt = 0.0
+    for _ in range(args.steps):
+        dt += chain.run(per_step)[1]
+    v = per_step * 4 * args.steps / dt
+    sample = f"{per_step} query tokens per step: Reindex over a 16,384-entry pool + 3 Reuse attentions (oracle)"
+    return {"metric": METRIC, "value": v, "unit": UNIT, "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": "decode Reindex + 3 Reuse, 1,048,576 entries/seq, "
+                                                        "batch 16 per layer call"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode1m", choices=["decode1m"])
+    ap.add_argument("--pipeline-distance", type=int, default=3)
+    ap.add_argument("--cpu-sample-queries", type=int, default=384)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        res = run_reference(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import fp4_kv_cache_csa2_gb300 as csa2
+    csa2.load()
+    res = run_decode1m(args, torch, csa2)
+    if rank == 0:
+        cpu_v, cpu_dt = OracleChain().run(args.cpu_sample_queries)
+        line = {"metric": METRIC, "value": res.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": res.pop("dtype"), "data": "synthetic"}
+        line.update(res)
+        line["cpu_baseline"] = {"value": cpu_v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                                "sample": f"{args.cpu_sample_queries} query tokens x (Reindex over a 16,384-entry "
+                                          f"pool + 3 Reuse attentions), {cpu_dt:.1f} s"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
