@@ -114,6 +114,7 @@ class Cache:
 
     def __init__(self, B: int, cap: int, m: int, device="cuda"):
         import torch
+        cap = -(-int(cap) // BLOCK) * BLOCK        # the library needs cap % 8 == 0
         self.B, self.cap, self.m = B, cap, m
         self.main_kv = torch.zeros((B, cap, MAIN_ENTRY_BYTES), dtype=torch.uint8, device=device)
         self.idx_codes = torch.zeros((B, cap, INDEX_CODE_BYTES), dtype=torch.uint8, device=device)

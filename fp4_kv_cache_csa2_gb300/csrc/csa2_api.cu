@@ -33,7 +33,7 @@ int num_sms() {
 
 csa2_status check_cache(const csa2_cache* c) {
   if (!c || !c->main_kv || !c->idx_codes || !c->idx_scales || !c->n_entries) return CSA2_ERR_INVALID_ARG;
-  if (c->cap < 0) return CSA2_ERR_INVALID_ARG;
+  if (c->cap < 0 || (c->cap % BLK) != 0) return CSA2_ERR_INVALID_ARG;
   if (c->m != 1 && c->m != 2) return CSA2_ERR_UNSUPPORTED;
   if (!aligned16(c->main_kv) || !aligned16(c->idx_codes) || !aligned16(c->idx_scales)) return CSA2_ERR_INVALID_ARG;
   return CSA2_OK;

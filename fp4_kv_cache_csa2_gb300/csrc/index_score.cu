@@ -1,154 +1,357 @@
 // (b) Lightning-indexer scores  s(t,j) = sum_h w_h * ReLU(q_h . k_j)
-// over 32 index heads x 128 dims, with MXFP4 queries and keys.
+// over 32 index heads x 128 dims, with MXFP4 queries and keys, on the
+// 5th-generation tensor cores (tcgen05, kind::mxf4 block-scaled MMA).
 //
 // Sources: "DeepSeek-V4.1 Flash: 把 KV Cache 压缩推到极致" §2.3.4 (the Full layer
 // scores every causally visible main-KV position; Reindex layers score only the
 // candidate pool), §2.4.4 (FP4 indexer Q and K); "4. 层维度(下):CSA2 与每 token
-// 890 字节" §4.4 (index K is OCP MXFP4: E2M1 + one E8M0 scale per 32).
+// 890 字节" §4.4 (index K is OCP MXFP4: E2M1 + one E8M0 scale per 32), §4.7.
 //
-// This is the CUDA-core formulation: one thread scores one entry at a time,
-// the dequantised query (32 x 128 binary32) sits in shared memory and is read
-// by broadcast.  Each CTA owns one query and a slice of its entries.
+// One CTA scores a run of 128-entry tiles of one query:
+//   warp 0      TMA producer: index-K codes (SW64 K-major, 64 B per entry) by a
+//               2-D tensor map, the 4-byte E8M0 words by 1-D bulk copies, into a
+//               ring of shared-memory stages (mbarrier expect-tx).  In pool mode
+//               each of the 16 candidate blocks of a tile is one 8-row box.
+//   warp 1      TMEM owner and MMA issuer: per tile two M=128 N=32 K=64
+//               block-scaled MMAs into one of two TMEM accumulators.
+//   warps 2..5  per tile: copy the 128 scale words into TMEM (row m -> lane m,
+//               column base + m/32), then the epilogue of the previous tile:
+//               32 head dot products from TMEM -> ReLU -> weighted sum -> score.
+// The query is quantised once per CTA (the B operand, 2 KB, and its scales).
+// Products of E2M1 values scaled by powers of two are exact; the accumulation
+// is fp32.  Every mbarrier wait is bounded and reports CSA2_ERR_TIMEOUT.
+#include <cudaTypedefs.h>
+
 #include "params.cuh"
+#include "tc.cuh"
 
 namespace csa2 {
 
-constexpr int IS_THREADS = 256;
+constexpr int IS_THREADS = 192;
+constexpr int IS_STAGES = 6;
+constexpr int IS_TILE = 128;
+constexpr int IS_CODES = IS_TILE * IDX_CODE_BYTES;         // 8192
+constexpr int IS_STAGE_BYTES = IS_CODES + 1024;            // codes + 512 B scales, 1 KB aligned stride
+constexpr int IS_POOL_MAX = CSA2_MAX_M;
+constexpr int IS_TMEM_COLS = 128;
+constexpr int IS_ACC_COL = 0;                               // two accumulators of 32 columns
+constexpr int IS_SFA_COL = 64;                              // 4 columns per stage
+constexpr int IS_SFB_COL = 96;
 
+struct IsSmem {
+  uint8_t stage[IS_STAGES][IS_STAGE_BYTES];
+  uint8_t qcodes[HI * IDX_CODE_BYTES];      // 2 KB, SW64
+  int32_t pool[IS_POOL_MAX];
+  float w[HI];
+  uint32_t sfb[HI];                          // query scale words (head n -> lane n of every quarter)
+  uint64_t full[IS_STAGES], empty[IS_STAGES], sf_full[IS_STAGES];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+constexpr size_t IS_SMEM = sizeof(IsSmem) + 1024;
 
-// Quantise one query (32 heads x 128 dims, bf16) to MXFP4 and store the exact
-// dequantised values in smem.  Warp w handles heads w, w+8, ...; lane owns 4 dims.
-__device__ __forceinline__ void load_query_mxfp4(const uint16_t* q, float* qs, int tid) {
-  const int lane = tid & 31, warp = tid >> 5;
-  for (int h = warp; h < HI; h += IS_THREADS / 32) {
-    uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + h * DI) + lane);
-    float v[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
-                  bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-    for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    float out[4] = {0.f, 0.f, 0.f, 0.f};
-    if (amax != 0.0f) {
-      int X = (int)((__float_as_uint(amax) >> 23) & 255u) - 127 - 2;
-      if (X < -127) X = -127;
-      if (X > 127) X = 127;
-      float inv = __uint_as_float((uint32_t)(127 - X) << 23);
-      float sc = e8m0_value((uint32_t)(X + 127));
-      uint32_t lo = e2m1x2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv));
-      uint32_t hi = e2m1x2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
-      out[0] = e2m1_value(lo & 15u) * sc;
-      out[1] = e2m1_value(lo >> 4) * sc;
-      out[2] = e2m1_value(hi & 15u) * sc;
-      out[3] = e2m1_value(hi >> 4) * sc;
-    }
-    *reinterpret_cast<float4*>(qs + h * DI + lane * 4) = make_float4(out[0], out[1], out[2], out[3]);
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, IsSmem& sm, WsHeader* hdr) {
+  if (sm.abort_flag) return false;
+  for (int round = 0; round < 64; round++) {
+    if (tc::bar_wait(bar, parity, 1u << 16)) return true;
+    if (sm.abort_flag) return false;
   }
+  sm.abort_flag = 1;
+  report(hdr, CSA2_ERR_TIMEOUT, 1);
+  return false;
 }
 
-// Score of one entry against the query held in smem.
-__device__ __forceinline__ float score_entry(const uint8_t* codes, const uint8_t* scales,
-                                             const float* qs, const float* ws) {
-  float dot[HI];
-#pragma unroll
-  for (int h = 0; h < HI; h++) dot[h] = 0.0f;
-  uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(scales));
-#pragma unroll 1
-  for (int blk = 0; blk < 4; blk++) {
-    uint4 c = __ldg(reinterpret_cast<const uint4*>(codes) + blk);
-    float s = e8m0_value((sc4 >> (8 * blk)) & 255u);
-    uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    float k[32];
-#pragma unroll
-    for (int i = 0; i < 32; i++) k[i] = e2m1_value((cw[i / 8] >> (4 * (i % 8))) & 15u) * s;
-#pragma unroll
-    for (int h = 0; h < HI; h++) {
-      const float4* qh = reinterpret_cast<const float4*>(qs + h * DI + blk * 32);
-      float acc = dot[h];
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        float4 qv = qh[i];
-        acc = fmaf(qv.x, k[4 * i], acc);
-        acc = fmaf(qv.y, k[4 * i + 1], acc);
-        acc = fmaf(qv.z, k[4 * i + 2], acc);
-        acc = fmaf(qv.w, k[4 * i + 3], acc);
-      }
-      dot[h] = acc;
-    }
-  }
-  float s = 0.0f;
-#pragma unroll
-  for (int h = 0; h < HI; h++) s = fmaf(ws[h], fmaxf(dot[h], 0.0f), s);
-  return s;
-}
+__global__ void __launch_bounds__(IS_THREADS, 1)
+index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
+                      const __grid_constant__ CUtensorMap map_block) {
+  extern __shared__ unsigned char smem_raw[];
+  IsSmem& sm = *reinterpret_cast<IsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bq = blockIdx.y, b = bq / p.Q;
+  const bool pool_mode = p.pool != nullptr;
 
-__global__ void __launch_bounds__(IS_THREADS) index_score_kernel(IsParams p) {
-  __shared__ __align__(16) float qs[HI * DI];
-  __shared__ float ws[HI];
-  const int bq = blockIdx.y;
-  const int b = bq / p.Q;
-  const int tid = threadIdx.x;
-  load_query_mxfp4(p.q_idx + (int64_t)bq * HI * DI, qs, tid);
-  if (tid < HI) ws[tid] = p.w_head[(int64_t)bq * HI + tid];
-  __syncthreads();
-
-  const int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[b]);
-  const uint8_t* codes = p.idx_codes + (int64_t)b * p.cap * IDX_CODE_BYTES;
-  const uint8_t* scales = p.idx_scales + (int64_t)b * p.cap * IDX_SCALE_BYTES;
+  // ---- this CTA's tile range
+  int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[b]);
   if (nv > p.cap) {
-    if (tid == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
-    return;
+    if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
+    nv = p.cap;
   }
-
-  if (p.pool == nullptr) {
-    if (nv > p.max_n) {           // the score row is too short for the visible entries
-      if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
-    }
-    const int64_t j0 = (int64_t)blockIdx.x * p.entries_per_cta;
-    int64_t j1 = j0 + p.entries_per_cta;
-    if (j1 > nv) j1 = nv;
-    if (j1 > p.max_n) j1 = p.max_n;
-    float* out = p.scores + (int64_t)bq * p.max_n;
-    for (int64_t j = j0 + tid; j < j1; j += IS_THREADS)
-      out[j] = score_entry(codes + j * IDX_CODE_BYTES, scales + j * IDX_SCALE_BYTES, qs, ws);
+  int64_t n_units;                         // entries (full) or pool slots (pool)
+  if (pool_mode) {
+    n_units = (int64_t)p.M * BLK;
   } else {
-    // pool mode: CTA x handles pool slots [x*epc, (x+1)*epc) * 8 entries
-    const int32_t* blocks = p.pool + (int64_t)bq * p.M;
-    const int64_t s0 = (int64_t)blockIdx.x * p.entries_per_cta * BLK;
-    int64_t s1 = s0 + p.entries_per_cta * BLK;
-    if (s1 > (int64_t)p.M * BLK) s1 = (int64_t)p.M * BLK;
-    float* out = p.scores + (int64_t)bq * p.M * BLK;
-    for (int64_t s = s0 + tid; s < s1; s += IS_THREADS) {
-      int32_t blk = blocks[s / BLK];
-      int64_t j = (int64_t)blk * BLK + (s % BLK);
-      float v = -INFINITY;
-      if (blk >= 0) {
-        if ((int64_t)blk * BLK >= p.cap) {
-          report(p.hdr, CSA2_ERR_BOUNDS, blk);
-        } else if (j < nv) {
-          v = score_entry(codes + j * IDX_CODE_BYTES, scales + j * IDX_SCALE_BYTES, qs, ws);
+    if (nv > p.max_n) {
+      if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
+      nv = p.max_n;
+    }
+    n_units = nv;
+  }
+  const int64_t n_tiles = ceil_div(n_units, IS_TILE);
+  const int64_t t0 = (int64_t)blockIdx.x * p.entries_per_cta;
+  int64_t t1 = t0 + p.entries_per_cta;
+  if (t1 > n_tiles) t1 = n_tiles;
+  const int n = (int)(t1 > t0 ? t1 - t0 : 0);
+  if (n == 0) return;
+
+  // ---- set-up
+  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, IS_TMEM_COLS);
+  if (tid == 0) {
+    for (int s = 0; s < IS_STAGES; s++) {
+      tc::bar_init(&sm.full[s], 1);
+      tc::bar_init(&sm.empty[s], 1);
+      tc::bar_init(&sm.sf_full[s], 4);
+    }
+    for (int i = 0; i < 2; i++) {
+      tc::bar_init(&sm.acc_full[i], 1);
+      tc::bar_init(&sm.acc_empty[i], 4);
+    }
+    sm.abort_flag = 0;
+    tc::bar_init_fence();
+  }
+  if (tid < HI) sm.w[tid] = p.w_head[(int64_t)bq * HI + tid];
+  if (pool_mode) {
+    const int32_t* pool = p.pool + (int64_t)bq * p.M;
+    for (int i = tid; i < p.M; i += IS_THREADS) sm.pool[i] = pool[i];
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensormap(&map_tile);
+    tc::prefetch_tensormap(&map_block);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  // ---- quantise the query (B operand); its scale words go to TMEM lanes
+  // 32q + n of every lane quarter q (the MMA reads B scales from the quarter of
+  // the A row it is computing)
+  if (warp == 4) {
+    const uint16_t* qh = p.q_idx + ((int64_t)bq * HI + lane) * DI;
+    uint32_t sfw = 0;
+#pragma unroll 1
+    for (int kb = 0; kb < 4; kb++) {
+      float v[32];
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(qh + kb * 32) + c);
+        uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          v[c * 8 + 2 * e] = bf16_bits_to_f32(w4[e] & 0xFFFFu);
+          v[c * 8 + 2 * e + 1] = bf16_bits_to_f32(w4[e] >> 16);
         }
       }
-      out[s] = v;
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(v[i]));
+      uint32_t sb = 0, packed[4] = {0u, 0u, 0u, 0u};
+      if (amax != 0.0f) {
+        int X = (int)((__float_as_uint(amax) >> 23) & 255u) - 127 - 2;
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+        sb = (uint32_t)(X + 127);
+        const float inv = __uint_as_float((uint32_t)(127 - X) << 23);
+#pragma unroll
+        for (int k = 0; k < 16; k++)
+          packed[k / 4] |= e2m1x2(__fmul_rn(v[2 * k], inv), __fmul_rn(v[2 * k + 1], inv)) << (8 * (k % 4));
+      }
+      sfw |= sb << (8 * kb);
+      const int phys = lane * 64 + ((kb ^ ((lane >> 1) & 3)) * 16);      // SW64 swizzle of row `lane`
+      *reinterpret_cast<uint4*>(sm.qcodes + phys) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+    sm.sfb[lane] = sfw;
+  }
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  if (warp >= 2) {
+    tc::tmem_st_x1(tmem + ((uint32_t)((warp & 3) * 32) << 16) + IS_SFB_COL, sm.sfb[lane]);
+    tc::tmem_wait_st();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  const int64_t row_base = (int64_t)b * p.cap;
+  const int64_t rows_total = (int64_t)p.B * p.cap;
+
+  if (warp == 0) {
+    // ================= TMA producer
+    int issued = 0;
+    for (int i = 0; i < n; i++) {
+      const int s = i % IS_STAGES;
+      if (i >= IS_STAGES && !wait_or_abort(&sm.empty[s], ((i / IS_STAGES) - 1) & 1, sm, p.hdr)) break;
+      uint8_t* codes = sm.stage[s];
+      uint8_t* scl = sm.stage[s] + IS_CODES;
+      const int64_t t = t0 + i;
+      if (!pool_mode) {
+        if (lane == 0) {
+          const int64_t row0 = row_base + t * IS_TILE;
+          int64_t rows = rows_total - row0;
+          if (rows > IS_TILE) rows = IS_TILE;
+          const uint32_t sbytes = (uint32_t)rows * IDX_SCALE_BYTES;     // cap % 8 == 0 -> multiple of 16
+          tc::bar_arrive_expect_tx(&sm.full[s], IS_CODES + sbytes);
+          tc::tma_load_2d(codes, &map_tile, 0, (int32_t)row0, &sm.full[s]);
+          tc::bulk_load(scl, p.idx_scales + row0 * IDX_SCALE_BYTES, sbytes, &sm.full[s]);
+        }
+      } else {
+        int32_t blk = -1;
+        if (lane < 16) {
+          const int64_t pi = t * 16 + lane;
+          if (pi < p.M) blk = sm.pool[pi];
+          if (blk >= 0 && (int64_t)blk * BLK >= p.cap) blk = -1;      // reported by the epilogue
+        }
+        const unsigned vmask = __ballot_sync(0xFFFFFFFFu, blk >= 0);
+        if (lane == 0) tc::bar_arrive_expect_tx(&sm.full[s], (uint32_t)__popc(vmask) * (512u + 32u));
+        __syncwarp();
+        if (blk >= 0) {
+          const int64_t row0 = row_base + (int64_t)blk * BLK;
+          tc::tma_load_2d(codes + lane * 512, &map_block, 0, (int32_t)row0, &sm.full[s]);
+          tc::bulk_load(scl + lane * 32, p.idx_scales + row0 * IDX_SCALE_BYTES, 32, &sm.full[s]);
+        }
+      }
+      issued = i + 1;
+    }
+    if (sm.abort_flag && lane == 0) {
+      // drain copies still in flight before the CTA exits
+      for (int i = issued - 1; i >= 0 && i >= issued - IS_STAGES; i--)
+        tc::bar_wait(&sm.full[i % IS_STAGES], (i / IS_STAGES) & 1, 1u << 20);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer
+    if (lane == 0) {
+      const uint64_t bdesc = tc::smem_desc(tc::smem_u32(sm.qcodes), 16, 512, tc::SW_64B);
+      constexpr uint32_t id0 = tc::idesc_mxf4(IS_TILE, HI, 0, 0);
+      constexpr uint32_t id1 = tc::idesc_mxf4(IS_TILE, HI, 2, 2);
+      for (int i = 0; i < n; i++) {
+        const int s = i % IS_STAGES, buf = i & 1;
+        if (!wait_or_abort(&sm.sf_full[s], (i / IS_STAGES) & 1, sm, p.hdr)) break;
+        if (i >= 2 && !wait_or_abort(&sm.acc_empty[buf], ((i >> 1) - 1) & 1, sm, p.hdr)) break;
+        tc::fence_after_sync();
+        const uint64_t adesc = tc::smem_desc(tc::smem_u32(sm.stage[s]), 16, 512, tc::SW_64B);
+        const uint32_t d = tmem + IS_ACC_COL + buf * 32;
+        const uint32_t sfa = tmem + IS_SFA_COL + s * 4;
+        tc::mma_mxf4(d, adesc, bdesc, id0, sfa, tmem + IS_SFB_COL, 0);
+        tc::mma_mxf4(d, adesc + 2, bdesc + 2, id1, sfa, tmem + IS_SFB_COL, 1);   // next 32 bytes of K
+        tc::commit(&sm.empty[s]);
+        tc::commit(&sm.acc_full[buf]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= scale copy into TMEM + epilogue (warps 2..5)
+    const int q = warp & 3;                   // TMEM lane quarter of this warp
+    const int m = q * 32 + lane;              // tile row owned by this thread
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    float* out_row = p.scores + (pool_mode ? (int64_t)bq * p.M * BLK : (int64_t)bq * p.max_n);
+    for (int i = 0; i <= n; i++) {
+      if (i < n) {
+        const int s = i % IS_STAGES;
+        if (!wait_or_abort(&sm.full[s], (i / IS_STAGES) & 1, sm, p.hdr)) break;
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(sm.stage[s] + IS_CODES + m * 4);
+        tc::tmem_st_x1(tmem + lane_off + IS_SFA_COL + s * 4 + q, word);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::bar_arrive(&sm.sf_full[s]);
+      }
+      if (i >= 1) {
+        const int j = i - 1, buf = j & 1;
+        if (!wait_or_abort(&sm.acc_full[buf], (j >> 1) & 1, sm, p.hdr)) break;
+        tc::fence_after_sync();
+        float v[32];
+        tc::tmem_ld_x32(tmem + lane_off + IS_ACC_COL + buf * 32, v);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::bar_arrive(&sm.acc_empty[buf]);
+        float sc = 0.0f;
+#pragma unroll
+        for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(v[h], 0.0f), sc);
+        const int64_t u = (t0 + j) * IS_TILE + m;
+        if (!pool_mode) {
+          if (u < n_units) out_row[u] = sc;
+        } else if (u < n_units) {
+          const int32_t blk = sm.pool[u / BLK];
+          const int64_t e = (int64_t)blk * BLK + (u % BLK);
+          float val = -INFINITY;
+          if (blk >= 0) {
+            if ((int64_t)blk * BLK >= p.cap) {
+              if ((u % BLK) == 0) report(p.hdr, CSA2_ERR_BOUNDS, blk);
+            } else if (e < nv) {
+              val = sc;
+            }
+          }
+          out_row[u] = val;
+        }
+      }
     }
   }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, IS_TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows][64] with SW64 boxes of `box_rows` rows.
+static bool encode_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {64, rows};
+  cuuint64_t strides[1] = {64};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   if (p.B == 0 || p.Q == 0) return cudaSuccess;
-  int gx;
-  if (p.pool == nullptr) {
-    // slice so that a query's entries spread over enough CTAs to fill the GPU
-    int64_t per = 2048;
-    gx = (int)ceil_div(p.max_n, per);
-    if (gx < 1) gx = 1;
-    p.entries_per_cta = per;
-  } else {
-    int64_t per_blocks = 256;   // 2048 entries per CTA
-    gx = (int)ceil_div(p.M, per_blocks);
-    p.entries_per_cta = per_blocks;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)IS_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
   }
-  dim3 grid(gx, p.B * p.Q);
-  index_score_kernel<<<grid, IS_THREADS, 0, stream>>>(p);
+  int num_sms = 148;
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  const uint64_t rows = (uint64_t)p.B * (uint64_t)p.cap;
+  if (rows == 0) return cudaSuccess;
+  CUtensorMap map_tile, map_block;
+  if (!encode_rows64(&map_tile, p.idx_codes, rows, IS_TILE) || !encode_rows64(&map_block, p.idx_codes, rows, BLK))
+    return cudaErrorInvalidValue;
+  const int64_t units = p.pool ? (int64_t)p.M * BLK : p.max_n;
+  const int64_t tiles = ceil_div(units, IS_TILE);
+  if (tiles == 0) return cudaSuccess;
+  const int64_t BQ = (int64_t)p.B * p.Q;
+  // aim at ~3 CTAs per SM over the whole launch, at least 2 tiles per CTA
+  int64_t split = ceil_div(3 * (int64_t)num_sms, BQ);
+  if (split > ceil_div(tiles, 2)) split = ceil_div(tiles, 2);
+  if (split < 1) split = 1;
+  const int64_t per = ceil_div(tiles, split);
+  p.entries_per_cta = per;     // tiles per CTA
+  dim3 grid((unsigned)ceil_div(tiles, per), (unsigned)BQ);
+  index_score_tc_kernel<<<grid, IS_THREADS, IS_SMEM, stream>>>(p, map_tile, map_block);
   return cudaGetLastError();
 }
 

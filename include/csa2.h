@@ -87,7 +87,9 @@ typedef enum {
  *               nibble of byte k; bytes 256..287 one E4M3 scale per 16 channels.
  *   idx_codes   [B][cap][64]:  index K, E2M1 codes, dim 2k in the low nibble.
  *   idx_scales  [B][cap][4]:   index K, one E8M0 scale (2^(byte-127)) per 32 dims.
- *   cap         entries per sequence.
+ *   cap         entries per sequence, a multiple of 8 (the candidate block size),
+ *               so that every sequence and every block starts 16-byte aligned in
+ *               all three arrays.
  *   n_entries   device [B]: entries valid per sequence (maintained by the caller).
  *   m           compression ratio of the source layer: 2 (Encoder) or 1 (Decoder).
  * All three arrays need 16-byte aligned base pointers.

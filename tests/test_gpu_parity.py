@@ -327,12 +327,12 @@ def synth_bf16(bits):
 def test_attention_out_of_range_selection_reports_bounds(csa2):
     case = cases.make_case(B=1, T=100, m=1, Q=1, M=4, K=4, seed=701)
     L = GpuLayer(csa2, case)
-    sel = np.array([[[3, 100, 7, -1]]], np.int32)                 # 100 >= cap
+    sel = np.array([[[3, 200, 7, -1]]], np.int32)                 # 200 >= cap (104)
     out = torch.empty((1, 1, 64, 512), dtype=torch.int16, device=DEV)
     ws = csa2.Workspace(csa2.attn_workspace_size(1, 1, 4), device=DEV)
     csa2.sparse_swa_attn(L.cache, L.q, dev(sel), L.swa, L.swa_base, L.q_pos, case.scale, out, ws)
     st, detail = ws.sync_status()
-    assert st == 6 and detail == 100
+    assert st == 6 and detail == 200
     main, _, _ = cases.oracle_cache(case)
     cases.check_attention(bf16_to_f32(out)[0, 0],
                           _oracle_attention(case, main, 0, 0, np.array([3, -1, 7, -1])))
