@@ -200,6 +200,110 @@ __device__ void radix_select_block(const Keys& keys, const Ids& ids, int64_t n, 
   for (int64_t i = n_sel + tid; i < K; i += SEL_THREADS) out[i] = -1;
 }
 
+// Same selection for n <= SEL_SMEM_KEYS keys staged once in shared memory
+// (key 0 marks a position outside the domain: no finite score maps to 0).
+// Histograms are private per warp (plain shared atomics), summed per pass.
+constexpr int SEL_SMEM_KEYS = 16384;
+constexpr int SEL_DYN_SMEM = SEL_SMEM_KEYS * 4 + (SEL_THREADS / 32) * 256 * 4;
+
+template <class Keys, class Ids>
+__device__ void radix_select_smem(const Keys& keys, const Ids& ids, int n, int K, int32_t* out, ScanSmem& sm,
+                                  uint32_t* sk, uint32_t* whist) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  long long cnt = 0;
+  for (int i = tid; i < n; i += SEL_THREADS) {
+    uint32_t k;
+    const bool ok = keys.get(i, k);
+    sk[i] = ok ? k : 0u;
+    cnt += ok ? 1 : 0;
+  }
+  long long n_valid;
+  block_exclusive_scan(cnt, sm, &n_valid);      // also orders the smem key writes
+  uint32_t thr = 0;
+  long long take_eq = 0;
+  if (n_valid > K) {
+    uint32_t prefix = 0, mask = 0;
+    long long remaining = K;
+    uint32_t* myh = whist + warp * 256;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = lane; i < 256; i += 32) myh[i] = 0;
+      __syncwarp();
+      for (int i = tid; i < n; i += SEL_THREADS) {
+        const uint32_t k = sk[i];
+        if (k != 0u && (k & mask) == prefix) atomicAdd(&myh[(k >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid < 256) {
+        uint32_t tot = 0;
+#pragma unroll 8
+        for (int w = 0; w < SEL_THREADS / 32; w++) tot += whist[w * 256 + tid];
+        sm.hist[tid] = tot;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t c[8];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; q++) { c[q] = sm.hist[255 - 8 * lane - q]; sum += c[q]; }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const uint32_t excl = incl - sum;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, (long long)incl >= remaining);
+        const int owner = __ffs(hit) - 1;
+        if (lane == owner) {
+          long long cum = excl;
+          int d = 255 - 8 * lane;
+#pragma unroll
+          for (int q = 0; q < 8; q++) {
+            if (cum + c[q] >= remaining) { d = 255 - 8 * lane - q; break; }
+            cum += c[q];
+          }
+          sm.bcast[0] = d;
+          sm.bcast[1] = remaining - cum;
+        }
+      }
+      __syncthreads();
+      prefix |= (uint32_t)sm.bcast[0] << shift;
+      mask |= 255u << shift;
+      remaining = sm.bcast[1];
+      __syncthreads();
+    }
+    thr = prefix;
+    take_eq = remaining;
+  }
+  const bool all = n_valid <= K;
+  const int chunk = (n + SEL_THREADS - 1) / SEL_THREADS;
+  const int i0 = tid * chunk;
+  const int i1 = (i0 + chunk < n) ? i0 + chunk : n;
+  long long gt = 0, eq = 0;
+  for (int i = i0; i < i1; i++) {
+    const uint32_t k = sk[i];
+    if (k == 0u) continue;
+    if (all || k > thr) gt++;
+    else if (k == thr) eq++;
+  }
+  long long eq_total;
+  const long long eq_before = block_exclusive_scan(eq, sm, &eq_total);
+  long long mine_eq = take_eq - eq_before;
+  if (mine_eq < 0) mine_eq = 0;
+  if (mine_eq > eq) mine_eq = eq;
+  long long n_sel;
+  long long off = block_exclusive_scan(gt + mine_eq, sm, &n_sel);
+  long long used_eq = 0;
+  for (int i = i0; i < i1; i++) {
+    const uint32_t k = sk[i];
+    if (k == 0u) continue;
+    bool take = all || k > thr;
+    if (!take && k == thr && used_eq < mine_eq) { take = true; used_eq++; }
+    if (take) out[off++] = (int32_t)ids(i);
+  }
+  for (long long i = n_sel + tid; i < K; i += SEL_THREADS) out[i] = -1;
+}
+
 // ------------------------------------------------------------------ kernels
 struct BlockTopParams {
   const uint32_t* gkeys;
@@ -212,12 +316,17 @@ struct BlockTopParams {
 
 __global__ void __launch_bounds__(SEL_THREADS) block_topm_kernel(BlockTopParams p) {
   __shared__ ScanSmem sm;
+  extern __shared__ uint32_t dyn[];
   const int bq = blockIdx.x;
   int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[bq / p.Q]);
   if (nv > p.nb_max * BLK) nv = p.nb_max * BLK;
   const int64_t nb = ceil_div(nv, BLK);
   RawKeys keys{p.gkeys + (int64_t)bq * p.nb_max};
-  radix_select_block(keys, IdentityIds{}, nb, p.M, p.pool_blocks + (int64_t)bq * p.M, sm);
+  int32_t* out = p.pool_blocks + (int64_t)bq * p.M;
+  if (nb <= SEL_SMEM_KEYS)
+    radix_select_smem(keys, IdentityIds{}, (int)nb, p.M, out, sm, dyn, dyn + SEL_SMEM_KEYS);
+  else
+    radix_select_block(keys, IdentityIds{}, nb, p.M, out, sm);
 }
 
 struct SelectParams {
@@ -232,18 +341,34 @@ struct SelectParams {
 
 __global__ void __launch_bounds__(SEL_THREADS) select_topk_kernel(SelectParams p) {
   __shared__ ScanSmem sm;
+  extern __shared__ uint32_t dyn[];
   const int bq = blockIdx.x;
   int32_t* out = p.sel + (int64_t)bq * p.K;
   if (p.pool == nullptr) {
     int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[bq / p.Q]);
     if (nv > p.max_n) nv = p.max_n;
     FullKeys keys{p.scores + (int64_t)bq * p.max_n};
-    radix_select_block(keys, IdentityIds{}, nv, p.K, out, sm);
+    if (nv <= SEL_SMEM_KEYS)
+      radix_select_smem(keys, IdentityIds{}, (int)nv, p.K, out, sm, dyn, dyn + SEL_SMEM_KEYS);
+    else
+      radix_select_block(keys, IdentityIds{}, nv, p.K, out, sm);
   } else {
     PoolKeys keys{p.scores + (int64_t)bq * p.M * BLK};
     PoolIds ids{p.pool + (int64_t)bq * p.M};
-    radix_select_block(keys, ids, (int64_t)p.M * BLK, p.K, out, sm);
+    radix_select_smem(keys, ids, p.M * BLK, p.K, out, sm, dyn, dyn + SEL_SMEM_KEYS);
   }
+}
+
+static cudaError_t set_select_smem() {
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev == dev) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_DYN_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(block_topm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_DYN_SMEM);
+  if (e == cudaSuccess) attr_dev = dev;
+  return e;
 }
 
 cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m,
@@ -256,8 +381,10 @@ cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const i
     dim3 grid((unsigned)ceil_div(nb_max, 256), B * Q);
     block_max_kernel<<<grid, 256, 0, stream>>>(bp);
   }
+  cudaError_t e = set_select_smem();
+  if (e != cudaSuccess) return e;
   BlockTopParams tp{gkeys, q_pos, n_entries, m, Q, M, nb_max, pool_blocks};
-  block_topm_kernel<<<B * Q, SEL_THREADS, 0, stream>>>(tp);
+  block_topm_kernel<<<B * Q, SEL_THREADS, SEL_DYN_SMEM, stream>>>(tp);
   return cudaGetLastError();
 }
 
@@ -265,8 +392,10 @@ cudaError_t launch_select_topk(const float* scores, const int64_t* q_pos, const 
                                const int32_t* pool, int M, int K, int32_t* sel, int B, int Q, int64_t max_n,
                                cudaStream_t stream) {
   if (B == 0 || Q == 0) return cudaSuccess;
+  cudaError_t e = set_select_smem();
+  if (e != cudaSuccess) return e;
   SelectParams sp{scores, q_pos, n_entries, pool, m, Q, M, K, max_n, sel};
-  select_topk_kernel<<<B * Q, SEL_THREADS, 0, stream>>>(sp);
+  select_topk_kernel<<<B * Q, SEL_THREADS, SEL_DYN_SMEM, stream>>>(sp);
   return cudaGetLastError();
 }
 

@@ -46,7 +46,7 @@ def test_host_only_calls_without_gpu(lib_path):
     lib = csa2.load(lib_path)
     assert lib.csa2_layout_version() == 1
     assert lib.csa2_status_string(6) == b"CSA2_ERR_BOUNDS"
-    assert lib.csa2_attn_workspace_size(1, 1, 512) > 256
+    assert lib.csa2_attn_workspace_size(1, 1, 512) >= 256
     assert lib.csa2_block_topk_workspace_size(2, 3, 100) == 256 + 512    # 2*3*13*4 = 312 bytes -> 512
     # argument validation happens before any CUDA call
     assert lib.csa2_index_score(None, None, None, None, None, 0, None, 1, 1, 10, None, 0, None) == 1
