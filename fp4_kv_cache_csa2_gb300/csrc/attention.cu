@@ -1,4 +1,5 @@
-// (c) Joint sparse + SWA attention over the shared 512-d latent (K = V).
+// (c) Joint sparse + SWA attention over the shared 512-d latent (K = V), on
+// the 5th-generation tensor cores.
 //
 // Sources: "DeepSeek-V4.1 Flash: 把 KV Cache 压缩推到极致" §3.3.2 (the readout
 // concatenates the SWA KV with the selected main-KV entries into one sparse
@@ -7,23 +8,29 @@
 // more precise format before attention: FP4 saves storage, it does not feed
 // the matrix multiply); "4. 层维度(下):CSA2 与每 token 890 字节" §4.5.
 //
-// One thread-block cluster of 8 CTAs per query token.  The query's key list (K
-// selected slots, then the 128 window positions) is cut into 8 equal slices;
-// CTA r of the cluster
-//   1. receives Q (64 heads x 512, bf16) by bulk copies multicast to the whole
-//      cluster (CTA r issues rows 8r..8r+7 for all 8 CTAs), bulk-copies its
-//      slice's 288-byte FP4 entries and 1 KB window rows (one mbarrier, one
-//      round trip), and dequantises the entries to bf16 in shared memory
-//      through a byte -> bf16x2 table and an exact bf16x2 multiply by the
-//      group scale (E2M1 x E4M3 has at most 6 significant bits),
-//   2. computes S = Q K^T with bf16 tensor-core MMAs (fp32 accumulate),
-//   3. exchanges per-head row maxima with the other 7 CTAs through distributed
-//      shared memory, forms P = exp(S - max) and O_r = P V,
-//   4. after a cluster barrier, owns output dims [64r, 64r+64): it sums that slice
-//      of the 8 partial O's and the 8 partial row sums over DSMEM, normalises and
-//      stores bf16.
-// Nothing leaves the cluster except the final output.
+// One thread-block cluster of C CTAs per query token, 128 keys per CTA: CTAs
+// 0..C-2 take the K selected slots in runs of 128, CTA C-1 the 128 window
+// positions.  In every CTA:
+//   * keys land in shared memory as bf16 [128 keys][512] in 8 SW128 column
+//     chunks of 64 dims: window rows by 2-D TMA straight from the bf16 window,
+//     selected FP4 entries by bulk copies into a staging buffer followed by an
+//     exact dequantisation (E2M1 x E4M3 has at most 6 significant bits);
+//   * Q (64 heads x 512) streams through a 4-stage TMA ring;
+//   * S^T = K Q^T is one M=128 (keys) x N=64 (heads) x K=512 tcgen05 bf16 MMA
+//     chain into TMEM;
+//   * row maxima are exchanged over distributed shared memory, P = exp(S - max)
+//     is written as the K-major bf16 B operand of the second product;
+//   * O^T = V^T P^T reuses the same key buffer as an MN-major A operand:
+//     4 tiles of M=128 dims x N=64 heads x K=128 keys;
+//   * row sums are exchanged; every CTA writes its share O_c / L of each 128-dim
+//     tile as fp16 (relative rounding 2^-11, four times finer than the bf16
+//     output) and bulk-copies the tiles it does not own into the owner's
+//     receive slots over DSMEM; the owner adds the C shares in fp32, rounds to
+//     bf16 and stores.
+// All mbarrier waits are bounded; a timeout reports CSA2_ERR_TIMEOUT.
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
 #include "params.cuh"
 #include "tc.cuh"
@@ -33,41 +40,36 @@ namespace cg = cooperative_groups;
 namespace csa2 {
 
 constexpr int AT_THREADS = 256;
-constexpr int AT_CLUSTER = 8;
-constexpr int AT_MAX_KPC = 80;              // keys per CTA at K = 512
-constexpr int AT_ROW = D + 8;               // padded smem row (bf16 elements): conflict-free ldmatrix
-constexpr int AT_PROW = AT_MAX_KPC + 8;
-constexpr int AT_Q_BYTES = H * AT_ROW * 2;              // 66,560
-constexpr int AT_K_BYTES = AT_MAX_KPC * AT_ROW * 2;     // 83,200
-constexpr int AT_P_BYTES = H * AT_PROW * 2;             // 11,264
-constexpr int AT_STG_BYTES = AT_MAX_KPC * MAIN_BYTES;   // 23,040: FP4 entries as loaded
-constexpr int AT_RED_BYTES = 3 * H * 4 + AT_MAX_KPC * 4 + 256 * 4 + 16;
-constexpr int AT_SMEM = AT_Q_BYTES + AT_K_BYTES + AT_P_BYTES + AT_STG_BYTES + AT_RED_BYTES;
-static_assert(AT_Q_BYTES + AT_K_BYTES >= H * D * 4, "partial O must fit over Q and K");
+constexpr int AT_KEYS = 128;                  // keys per CTA (one M = 128 tile)
+constexpr int AT_QSTAGES = 6;
+constexpr int AT_CHUNK_BYTES = AT_KEYS * 128;            // [128 keys][64 dims] bf16 = 16 KB
+constexpr int AT_OFF_K = 0;                              // 8 chunks, 128 KB
+constexpr int AT_OFF_Q = 8 * AT_CHUNK_BYTES;             // 6 stages x 8 KB
+constexpr int AT_OFF_SCR = AT_OFF_Q + AT_QSTAGES * 8192; // FP4 staging | S^T transposed | P
+constexpr int AT_SCR_BYTES = AT_KEYS * MAIN_BYTES;       // 36,864
+constexpr int AT_ST_ROW = AT_KEYS + 1;                   // padded fp32 row of S^T transposed
+constexpr int AT_OFF_SMALL = AT_OFF_SCR + AT_SCR_BYTES;
+constexpr int AT_SHARE_BYTES = 128 * H * 2;             // one O^T tile share in fp16: 16 KB
+constexpr int AT_OFF_RECV = AT_OFF_Q;                    // 4 receive slots over the dead Q ring + scratch
+constexpr int AT_TMEM_COLS = 512;                        // S^T: 64 cols, O^T: 4 x 64 cols
 
-using tc::smem_u32;
-
-__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r0), "=r"(r1) : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+struct AtSmall {
+  int kvalid[AT_KEYS];
+  float loc_max[H];
+  float loc_sum[H];
+  float inv_l[H];
+  float gmax[H];
+  uint32_t lut[256];
+  uint64_t bar_kv, bar_s, bar_o, bar_red;
+  uint64_t bar_q[AT_QSTAGES], bar_qe[AT_QSTAGES];
+  uint64_t bar_chunk[8];                 // chunk c of the keys is in shared memory (bf16, SW128)
+  uint32_t tmem_base;
+  int err;
+};
+constexpr int AT_SMEM = AT_OFF_SMALL + (int)sizeof(AtSmall) + 1024;
+static_assert(AT_ST_ROW * H * 4 <= AT_SCR_BYTES, "S^T scratch must fit");
+static_assert(4 * AT_SHARE_BYTES <= 8 * AT_CHUNK_BYTES, "O^T shares must fit over the keys");
+static_assert(4 * AT_SHARE_BYTES <= AT_QSTAGES * 8192 + AT_SCR_BYTES, "receive slots must fit");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -75,266 +77,405 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// keys per CTA: the slot list split 8 ways, rounded up to a multiple of 16
-__host__ __device__ __forceinline__ int attn_kpc(int K) {
-  int per = (K + WIN + AT_CLUSTER - 1) / AT_CLUSTER;
-  return (per + 15) / 16 * 16;
+// byte offset of (row, byte) in a 1 KB-aligned SW128 region of 128-byte rows
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte) {
+  return row * 128u + ((((byte >> 4) ^ (row & 7u)) << 4) | (byte & 15u));
 }
 
-__global__ void __cluster_dims__(AT_CLUSTER, 1, 1) __launch_bounds__(AT_THREADS, 1)
-attn_cluster_kernel(AttnParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem + AT_Q_BYTES);
-  uint16_t* Ps = reinterpret_cast<uint16_t*>(smem + AT_Q_BYTES + AT_K_BYTES);
-  uint8_t* stg = smem + AT_Q_BYTES + AT_K_BYTES + AT_P_BYTES;
-  float* red = reinterpret_cast<float*>(stg + AT_STG_BYTES);
-  float* loc_max = red;              // [64] this CTA's row maxima (read by the cluster)
-  float* loc_sum = red + H;          // [64] this CTA's row sums   (read by the cluster)
-  float* half_max = red + 2 * H;     // [64] per warp-half scratch
-  int* kvalid = reinterpret_cast<int*>(red + 3 * H);              // [80] 0 none, 1 entry, 2 window row
-  uint32_t* lut = reinterpret_cast<uint32_t*>(kvalid + AT_MAX_KPC); // [256] byte -> two bf16 E2M1 values
-  uint64_t* bar = reinterpret_cast<uint64_t*>(lut + 256);
-  float* Opart = reinterpret_cast<float*>(smem);   // [64][512] fp32, reuses Q and K after the MMAs
+__device__ __forceinline__ bool at_wait(uint64_t* bar, uint32_t parity, AtSmall& sm, WsHeader* hdr, int where) {
+  if (tc::bar_wait(bar, parity)) return true;
+  if (atomicExch(&sm.err, 1) == 0) report(hdr, CSA2_ERR_TIMEOUT, where);
+  return false;
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_swa,
+               int C) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* kbuf = smem + AT_OFF_K;
+  unsigned char* qbuf = smem + AT_OFF_Q;
+  unsigned char* scr = smem + AT_OFF_SCR;
+  AtSmall& sm = *reinterpret_cast<AtSmall*>(smem + AT_OFF_SMALL);
+  float* st = reinterpret_cast<float*>(scr);                 // S^T transposed: [64 heads][129] fp32
+  __half* ostage = reinterpret_cast<__half*>(kbuf);          // 4 tiles x [128 dims][64 heads] fp16 shares
+  __half* orecv = reinterpret_cast<__half*>(smem + AT_OFF_RECV); // up to 4 received shares
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const int bq = blockIdx.x / AT_CLUSTER;
+  const int bq = blockIdx.x / C;
   const int b = bq / p.Q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t = p.q_pos[bq];
-  const int kpc = attn_kpc(p.K);
-  const int slot0 = rank * kpc;
+  const bool window_cta = rank == C - 1;
+  const int slot0 = rank * AT_KEYS;
 
+  // ---------------- set-up
+  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, AT_TMEM_COLS);
   if (tid == 0) {
-    tc::bar_init(bar, 1);
+    tc::bar_init(&sm.bar_kv, 1);
+    tc::bar_init(&sm.bar_s, 1);
+    tc::bar_init(&sm.bar_o, 1);
+    tc::bar_init(&sm.bar_red, 1);
+    for (int i = 0; i < AT_QSTAGES; i++) {
+      tc::bar_init(&sm.bar_q[i], 1);
+      tc::bar_init(&sm.bar_qe[i], 1);
+    }
+    for (int i = 0; i < 8; i++) tc::bar_init(&sm.bar_chunk[i], 1);
+    sm.err = 0;
     tc::bar_init_fence();
   }
-  {
-    const uint32_t c = (uint32_t)tid;           // tid < 256: one table entry per thread
-    lut[c] = pack_bf16x2(e2m1_value(c & 15u), e2m1_value(c >> 4));
-  }
-  cluster.sync();                                              // #0: every CTA's barrier is initialised
-
-  // ---- one warp issues every copy of this CTA; the others zero empty key rows
-  if (warp == 0) {
-    uint32_t bytes = 0;
-    for (int s = lane; s < kpc; s += 32) {
-      const int gs = slot0 + s;
-      int kind = 0;
+  sm.lut[tid] = pack_bf16x2(e2m1_value(tid & 15u), e2m1_value((uint32_t)tid >> 4));
+  if (tid < AT_KEYS) {                       // which keys of this CTA exist
+    int kind = 0;
+    if (!window_cta) {
+      const int gs = slot0 + tid;
       if (gs < p.K) {
         const int32_t id = p.sel[(int64_t)bq * p.K + gs];
-        if (id >= 0 && id < p.cap) {
-          kind = 1;
-          bytes += MAIN_BYTES;
-        } else if (id >= p.cap) {
-          report(p.hdr, CSA2_ERR_BOUNDS, id);
+        if (id >= 0 && id < p.cap) kind = 1;
+        else if (id >= p.cap) report(p.hdr, CSA2_ERR_BOUNDS, id);
+      }
+    } else {
+      const int64_t pos = t - (WIN - 1) + tid;
+      if (pos >= 0) {
+        const int64_t row = pos - p.swa_base[b];
+        if (row >= 0 && row < p.S) kind = 2;
+        else report(p.hdr, CSA2_ERR_BOUNDS, pos);
+      }
+    }
+    sm.kvalid[tid] = kind;
+  }
+  tc::fence_before_sync();
+  cluster.sync();                                          // #0: barriers initialised cluster-wide
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  // ---------------- producer: keys and the Q ring
+  if (warp == 0) {
+    if (window_cta) {
+      if (lane == 0) {
+        if (p.S > 0) {       // rows outside this sequence's window are masked (kvalid == 0) but finite
+          tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * AT_CHUNK_BYTES);
+          const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
+          for (int c = 0; c < 8; c++) tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.bar_kv);
+        } else {
+          tc::bar_arrive_expect_tx(&sm.bar_kv, 0u);
         }
-      } else if (gs < p.K + WIN) {
-        const int64_t pos = t - (WIN - 1) + (gs - p.K);
-        if (pos >= 0) {
-          const int64_t row = pos - p.swa_base[b];
-          if (row >= 0 && row < p.S) {
-            kind = 2;
-            bytes += D * 2;
+      }
+    }
+    if (lane == 0) {
+      for (int c = 0; c < 8; c++) {
+        const int s = c % AT_QSTAGES;
+        if (c >= AT_QSTAGES && !at_wait(&sm.bar_qe[s], ((c / AT_QSTAGES) - 1) & 1, sm, p.hdr, 10)) break;
+        tc::bar_arrive_expect_tx(&sm.bar_q[s], 8192u);
+        tc::tma_load_2d(qbuf + s * 8192, &map_q, c * 64, bq * H, &sm.bar_q[s]);
+      }
+    }
+  }
+
+  // ---------------- warps 1..7: keys ready -> dequantise the selected FP4 entries
+  // (warp 0 keeps feeding the Q ring and is not part of this barrier)
+  if (warp > 0) {
+    if (!window_cta) {              // 16-byte asynchronous copies of the selected FP4 entries
+      for (int i = tid - 32; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS - 32) {
+        const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
+        if (sm.kvalid[s] == 1) {
+          const int32_t id = p.sel[(int64_t)bq * p.K + slot0 + s];
+          const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES + part * 16;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                       :: "r"(tc::smem_u32(scr + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
+        }
+      }
+      asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" :: "r"(AT_THREADS - 32) : "memory");
+    } else {
+      at_wait(&sm.bar_kv, 0, sm, p.hdr, 11);
+    }
+    if (!window_cta) {
+      // warp w dequantises chunk w-1 (warp 7 also chunk 7) and publishes it on its
+      // own mbarrier, so the MMAs of chunk c start as soon as c is ready
+      for (int c = warp - 1; c < 8; c += (warp == 7 ? 1 : 8)) {
+        unsigned char* rowp = kbuf + c * AT_CHUNK_BYTES;
+        for (int s = lane; s < AT_KEYS; s += 32) {
+          if (sm.kvalid[s] == 1) {
+            const unsigned char* ent = scr + s * MAIN_BYTES;
+            const uint4 c0 = *reinterpret_cast<const uint4*>(ent + c * 32);
+            const uint4 c1 = *reinterpret_cast<const uint4*>(ent + c * 32 + 16);
+            const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(ent + 256 + c * 4);
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int g = 0; g < 4; g++) {                      // 16 channels per E4M3 scale
+              const float sc = e4m3_value((sc4 >> (8 * g)) & 255u);
+              const uint32_t sc2 = pack_bf16x2(sc, sc);
+              uint32_t o[8];
+#pragma unroll
+              for (int k = 0; k < 8; k++) {
+                const uint32_t byte = (cw[2 * g + (k >> 2)] >> (8 * (k & 3))) & 255u;
+                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(sm.lut[byte]), "r"(sc2));
+              }
+              *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u + 16u)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
           } else {
-            report(p.hdr, CSA2_ERR_BOUNDS, pos);
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+              *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)u * 16u)) = make_uint4(0, 0, 0, 0);
           }
         }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::bar_arrive(&sm.bar_chunk[c]);
       }
-      kvalid[s] = kind;
+    } else {
+      if (p.S == 0) {                                          // no window rows supplied: zero keys
+        for (int i = tid - 32; i < 8 * AT_CHUNK_BYTES / 16; i += AT_THREADS - 32)
+          reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async_smem();
+        asm volatile("bar.sync 1, %0;" :: "r"(AT_THREADS - 32) : "memory");
+      }
+      if (warp == 1 && lane == 0)
+        for (int c = 0; c < 8; c++) tc::bar_arrive(&sm.bar_chunk[c]);
     }
+
+    // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims)
+    if (warp == 1 && lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
+      for (int c = 0; c < 8; c++) {
+        const int s = c % AT_QSTAGES;
+        if (!at_wait(&sm.bar_chunk[c], 0, sm, p.hdr, 16)) break;
+        if (!at_wait(&sm.bar_q[s], (c / AT_QSTAGES) & 1, sm, p.hdr, 12)) break;
+        tc::fence_after_sync();
+        const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + s * 8192);
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) bytes += __shfl_xor_sync(0xFFFFFFFFu, bytes, off);
-    if (lane == 0) tc::bar_arrive_expect_tx(bar, (uint32_t)(H * D * 2) + bytes);
+        for (int ks = 0; ks < 4; ks++)
+          tc::mma_bf16(tmem, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
+                       tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c | ks) ? 1u : 0u);
+        tc::commit(&sm.bar_qe[s]);
+      }
+      tc::commit(&sm.bar_s);
+    }
     __syncwarp();
-    // Q rows 8*rank .. 8*rank+7, multicast to all 8 CTAs at the same smem offset
-    if (lane < 8) {
-      const int r = rank * 8 + lane;
-      tc::bulk_load_multicast(Qs + r * AT_ROW, p.q + ((int64_t)bq * H + r) * D, D * 2, bar, 0xFFu);
-    }
-    for (int s = lane; s < kpc; s += 32) {
-      const int gs = slot0 + s;
-      if (kvalid[s] == 1) {
-        const int32_t id = p.sel[(int64_t)bq * p.K + gs];
-        tc::bulk_load(stg + s * MAIN_BYTES, p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES, MAIN_BYTES, bar);
-      } else if (kvalid[s] == 2) {
-        const int64_t row = t - (WIN - 1) + (gs - p.K) - p.swa_base[b];
-        tc::bulk_load(Ks + s * AT_ROW, p.swa + ((int64_t)b * p.S + row) * D, D * 2, bar);
-      }
-    }
   }
-  __syncthreads();                                             // kvalid visible
-  for (int idx = tid; idx < kpc * 64; idx += AT_THREADS) {    // zero rows of empty slots
-    const int s = idx >> 6;
-    if (kvalid[s] == 0) reinterpret_cast<uint4*>(Ks + s * AT_ROW)[idx & 63] = make_uint4(0, 0, 0, 0);
-  }
-  bool ok = tc::bar_wait(bar, 0);
-  if (!ok) report(p.hdr, CSA2_ERR_TIMEOUT, 2);
-  // ---- dequantise the FP4 entries: 8 code bytes = 16 channels = one E4M3 scale group
-  for (int idx = tid; idx < kpc * 32; idx += AT_THREADS) {
-    const int s = idx >> 5, grp = idx & 31;
-    if (kvalid[s] != 1) continue;
-    const uint8_t* ent = stg + s * MAIN_BYTES;
-    const uint2 cb = *reinterpret_cast<const uint2*>(ent + grp * 8);
-    const float sc = e4m3_value(ent[256 + grp]);
-    const uint32_t sc2 = pack_bf16x2(sc, sc);
-    uint32_t o[8];
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-      const uint32_t byte = ((k < 4 ? cb.x : cb.y) >> (8 * (k & 3))) & 255u;
-      const uint32_t v = lut[byte];
-      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(v), "r"(sc2));
-    }
-    uint4* d4 = reinterpret_cast<uint4*>(Ks + s * AT_ROW + grp * 16);
-    d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
-  }
-  __syncthreads();
 
-  // ---- S = Q K^T : warp -> heads 16*(warp%4), key half warp/4 (NTH n8-tiles)
-  const int mh = warp & 3, kh = warp >> 2;
-  const int nth = kpc / 16;                 // n8 tiles per half
-  const int g = lane >> 2;
-  float sacc[5][4];
-#pragma unroll
-  for (int j = 0; j < 5; j++)
-#pragma unroll
-    for (int e = 0; e < 4; e++) sacc[j][e] = 0.f;
+  // ---------------- S^T from TMEM -> scaled, masked, transposed into smem
+  at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
+  tc::fence_after_sync();
   {
-    const uint16_t* a_base = Qs + (16 * mh + (lane & 15)) * AT_ROW + (lane >> 4) * 8;
-    const uint16_t* b_base = Ks + (kh * nth * 8 + (lane & 7)) * AT_ROW + ((lane >> 3) & 1) * 8;
-#pragma unroll 2
-    for (int ks = 0; ks < D / 16; ks++) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(a0, a1, a2, a3, a_base + ks * 16);
+    const int q4 = warp & 3, half = warp >> 2;
+    const int m = q4 * 32 + lane;                   // key row
+    float v[32];
+    tc::tmem_ld_x32(tmem + ((uint32_t)(q4 * 32) << 16) + half * 32, v);
+    const bool valid = sm.kvalid[m] != 0;
 #pragma unroll
-      for (int j = 0; j < 5; j++) {
-        if (j < nth) {
-          uint32_t b0, b1;
-          ldsm_x2(b0, b1, b_base + j * 8 * AT_ROW + ks * 16);
-          mma_bf16(sacc[j], a0, a1, a2, a3, b0, b1);
-        }
-      }
-    }
-  }
-  // ---- row maxima over this CTA's keys, exchanged across the cluster
-  float rmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-  for (int j = 0; j < 5; j++)
-#pragma unroll
-    for (int e = 0; e < 4; e++) {
-      const int key = kh * nth * 8 + 8 * j + 2 * (lane & 3) + (e & 1);
-      const float v = (j < nth && kvalid[key] != 0) ? sacc[j][e] * p.scale : -INFINITY;
-      sacc[j][e] = v;
-      rmax[e >> 1] = fmaxf(rmax[e >> 1], v);
-    }
-#pragma unroll
-  for (int r = 0; r < 2; r++) {
-    rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xFFFFFFFFu, rmax[r], 1));
-    rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xFFFFFFFFu, rmax[r], 2));
-  }
-  if (kh == 1 && (lane & 3) == 0) {
-    half_max[16 * mh + g] = rmax[0];
-    half_max[16 * mh + g + 8] = rmax[1];
+    for (int j = 0; j < 32; j++) st[(half * 32 + j) * AT_ST_ROW + m] = valid ? v[j] * p.scale : -INFINITY;
   }
   __syncthreads();
-  if (kh == 0 && (lane & 3) == 0) {
-    loc_max[16 * mh + g] = fmaxf(rmax[0], half_max[16 * mh + g]);
-    loc_max[16 * mh + g + 8] = fmaxf(rmax[1], half_max[16 * mh + g + 8]);
+  // row maxima of this CTA (warp w: heads 8w .. 8w+7)
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int h = warp * 8 + i;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; j++) mx = fmaxf(mx, st[h * AT_ST_ROW + lane + 32 * j]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    if (lane == 0) sm.loc_max[h] = mx;
   }
-  cluster.sync();                                              // #1: maxima visible
-  float gmax[2];
-#pragma unroll
-  for (int r = 0; r < 2; r++) {
-    const int h = 16 * mh + g + 8 * r;
-    float mm = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < AT_CLUSTER; c++) mm = fmaxf(mm, cluster.map_shared_rank(loc_max, c)[h]);
-    gmax[r] = (mm == -INFINITY) ? 0.f : mm;
-  }
-  // ---- P = exp(S - max) (bf16) and this CTA's row sums
-  float rsum[2] = {0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 5; j++) {
-    if (j < nth) {
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        pv[e] = (sacc[j][e] == -INFINITY) ? 0.f : __expf(sacc[j][e] - gmax[e >> 1]);
-        rsum[e >> 1] += pv[e];
-      }
-      const int key = kh * nth * 8 + 8 * j + 2 * (lane & 3);
-      *reinterpret_cast<uint32_t*>(Ps + (16 * mh + g) * AT_PROW + key) = pack_bf16x2(pv[0], pv[1]);
-      *reinterpret_cast<uint32_t*>(Ps + (16 * mh + g + 8) * AT_PROW + key) = pack_bf16x2(pv[2], pv[3]);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < 2; r++) {
-    rsum[r] += __shfl_xor_sync(0xFFFFFFFFu, rsum[r], 1);
-    rsum[r] += __shfl_xor_sync(0xFFFFFFFFu, rsum[r], 2);
-  }
-  if (kh == 1 && (lane & 3) == 0) {
-    half_max[16 * mh + g] = rsum[0];            // reuse as half-sum scratch
-    half_max[16 * mh + g + 8] = rsum[1];
+  cluster.sync();                                          // #1: maxima visible
+  if (tid < H) {
+    float gm = -INFINITY;
+    for (int c = 0; c < C; c++) gm = fmaxf(gm, cluster.map_shared_rank(sm.loc_max, c)[tid]);
+    sm.gmax[tid] = (gm == -INFINITY) ? 0.f : gm;
   }
   __syncthreads();
-  if (kh == 0 && (lane & 3) == 0) {
-    loc_sum[16 * mh + g] = rsum[0] + half_max[16 * mh + g];
-    loc_sum[16 * mh + g + 8] = rsum[1] + half_max[16 * mh + g + 8];
+  float pv[8][4];
+  float lsum[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int h = warp * 8 + i;
+    const float gm = sm.gmax[h];
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {                 // keys 2*lane, 2*lane+1, 64+2*lane, 65+2*lane
+      const int k = (j >> 1) * 64 + 2 * lane + (j & 1);
+      const float s_ = st[h * AT_ST_ROW + k];
+      const float e = (s_ == -INFINITY) ? 0.f : __expf(s_ - gm);
+      pv[i][j] = e;
+      sum += e;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+    lsum[i] = sum;
   }
+  __syncthreads();                                         // every read of S^T is done: P overwrites it
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int h = warp * 8 + i;
+    if (lane == 0) sm.loc_sum[h] = lsum[i];
+#pragma unroll
+    for (int blk = 0; blk < 2; blk++)
+      *reinterpret_cast<uint32_t*>(scr + blk * 8192 + sw128((uint32_t)h, (uint32_t)(4 * lane))) =
+          pack_bf16x2(pv[i][2 * blk], pv[i][2 * blk + 1]);
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
 
-  // ---- O_r = P V : warp -> heads 16*(warp%4), dims 256*(warp/4)
-  const int dh = warp >> 2;
-  float oacc[32][4];
+  // ---------------- O^T = V^T P^T  (4 tiles of M = 128 dims, N = 64 heads, K = 128 keys)
+  if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc_o = tc::idesc_bf16(128, H, 1, 0);
+    const uint32_t kb = tc::smem_u32(kbuf), pb = tc::smem_u32(scr);
+    for (int tile = 0; tile < 4; tile++) {
 #pragma unroll
-  for (int j = 0; j < 32; j++)
-#pragma unroll
-    for (int e = 0; e < 4; e++) oacc[j][e] = 0.f;
-  {
-    const uint16_t* a_base = Ps + (16 * mh + (lane & 15)) * AT_PROW + (lane >> 4) * 8;
-    const int mi = lane >> 3;
-    const uint16_t* b_base = Ks + ((mi & 1) * 8 + (lane & 7)) * AT_ROW + 256 * dh + (mi >> 1) * 8;
-    for (int ks = 0; ks < kpc / 16; ks++) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(a0, a1, a2, a3, a_base + ks * 16);
-#pragma unroll
-      for (int jp = 0; jp < 16; jp++) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(b0, b1, b2, b3, b_base + ks * 16 * AT_ROW + jp * 16);
-        mma_bf16(oacc[2 * jp], a0, a1, a2, a3, b0, b1);
-        mma_bf16(oacc[2 * jp + 1], a0, a1, a2, a3, b2, b3);
+      for (int ks = 0; ks < AT_KEYS / 16; ks++) {
+        const uint64_t ad = tc::smem_desc(kb + (2 * tile) * AT_CHUNK_BYTES + ks * 2048, AT_CHUNK_BYTES, 1024,
+                                          tc::SW_128B);
+        const uint64_t bd = tc::smem_desc(pb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, tc::SW_128B);
+        tc::mma_bf16(tmem + 64 + tile * 64, ad, bd, idesc_o, ks ? 1u : 0u);
       }
     }
+    tc::commit(&sm.bar_o);
   }
-  __syncthreads();                                           // all reads of Q and K done
-#pragma unroll
-  for (int j = 0; j < 32; j++) {
-    const int col = 256 * dh + 8 * j + 2 * (lane & 3);
-    *reinterpret_cast<float2*>(Opart + (16 * mh + g) * D + col) = make_float2(oacc[j][0], oacc[j][1]);
-    *reinterpret_cast<float2*>(Opart + (16 * mh + g + 8) * D + col) = make_float2(oacc[j][2], oacc[j][3]);
-  }
-  cluster.sync();                                              // #2: partial O and sums visible
-
-  // ---- reduce this CTA's 64-dim slice over the cluster, normalise, store bf16
-  uint16_t* out = p.out + (int64_t)bq * H * D;
-  for (int idx = tid; idx < H * 16; idx += AT_THREADS) {
-    const int h = idx >> 4, d4 = idx & 15;
-    const int col = rank * 64 + d4 * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncwarp();
+  cluster.sync();                                          // #2: row sums visible
+  if (tid < H) {
     float L = 0.f;
-#pragma unroll
-    for (int c = 0; c < AT_CLUSTER; c++) {
-      const float* rem = cluster.map_shared_rank(Opart, c);
-      const float4 v = *reinterpret_cast<const float4*>(rem + h * D + col);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      L += cluster.map_shared_rank(loc_sum, c)[h];
-    }
-    const float inv = (L > 0.f) ? 1.0f / L : 0.f;
-    *reinterpret_cast<uint2*>(out + h * D + col) =
-        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    for (int c = 0; c < C; c++) L += cluster.map_shared_rank(sm.loc_sum, c)[tid];
+    sm.inv_l[tid] = (L > 0.f) ? 1.0f / L : 0.f;
   }
-  cluster.sync();                                              // #3: remote reads finished
+  __syncthreads();
+  at_wait(&sm.bar_o, 0, sm, p.hdr, 14);
+  tc::fence_after_sync();
+  // this CTA's share O_c / L per tile as fp16 [dim][head], 16-byte units swizzled by dim
+  {
+    const int q4 = warp & 3, half = warp >> 2;
+    uint32_t ta[4][32];
+#pragma unroll
+    for (int tile = 0; tile < 4; tile++) {       // issue all four TMEM loads, then wait once
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                   "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                   : "=r"(ta[tile][0]), "=r"(ta[tile][1]), "=r"(ta[tile][2]), "=r"(ta[tile][3]), "=r"(ta[tile][4]),
+                     "=r"(ta[tile][5]), "=r"(ta[tile][6]), "=r"(ta[tile][7]), "=r"(ta[tile][8]), "=r"(ta[tile][9]),
+                     "=r"(ta[tile][10]), "=r"(ta[tile][11]), "=r"(ta[tile][12]), "=r"(ta[tile][13]), "=r"(ta[tile][14]),
+                     "=r"(ta[tile][15]), "=r"(ta[tile][16]), "=r"(ta[tile][17]), "=r"(ta[tile][18]), "=r"(ta[tile][19]),
+                     "=r"(ta[tile][20]), "=r"(ta[tile][21]), "=r"(ta[tile][22]), "=r"(ta[tile][23]), "=r"(ta[tile][24]),
+                     "=r"(ta[tile][25]), "=r"(ta[tile][26]), "=r"(ta[tile][27]), "=r"(ta[tile][28]), "=r"(ta[tile][29]),
+                     "=r"(ta[tile][30]), "=r"(ta[tile][31])
+                   : "r"(tmem + ((uint32_t)(q4 * 32) << 16) + 64 + tile * 64 + half * 32) : "memory");
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    const int d = q4 * 32 + lane;                 // dim row inside a tile
+#pragma unroll
+    for (int tile = 0; tile < 4; tile++) {
+      __half* row = ostage + tile * (128 * H) + d * H;
+#pragma unroll
+      for (int u = 0; u < 4; u++) {               // 16-byte units = 8 heads: half*32 + 8u .. +7
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int j = 8 * u + 2 * e;
+          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * sm.inv_l[half * 32 + j],
+                                               __uint_as_float(ta[tile][j + 1]) * sm.inv_l[half * 32 + j + 1]);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        const int unit = (half * 4 + u) ^ (d & 7);
+        *reinterpret_cast<uint4*>(row + unit * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+  tc::fence_proxy_async_smem();
+  cluster.sync();                                          // #3: every share staged, receive slots free
+
+  // ---------------- cluster reduction: tile t is owned by CTA t % C; the others send
+  // their fp16 share into the owner's slot (j * (C - 1) + sender index)
+  int owned = 0;
+  for (int tile = rank; tile < 4; tile += C) owned++;
+  if (tid == 0) {
+    if (owned) tc::bar_arrive_expect_tx(&sm.bar_red, (uint32_t)(owned * (C - 1) * AT_SHARE_BYTES));
+    for (int tile = 0; tile < 4; tile++) {
+      const int owner = tile % C;
+      if (owner == rank) continue;
+      const int j = tile / C;
+      const int slot = j * (C - 1) + (rank < owner ? rank : rank - 1);
+      const uint32_t src = tc::smem_u32(ostage + tile * (128 * H));
+      uint32_t dst, rbar;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(tc::smem_u32(orecv + slot * (128 * H))), "r"(owner));
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(tc::smem_u32(&sm.bar_red)), "r"(owner));
+      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                   :: "r"(dst), "r"(src), "r"(AT_SHARE_BYTES), "r"(rbar) : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
+  if (owned) {
+    at_wait(&sm.bar_red, 0, sm, p.hdr, 15);
+    uint16_t* out = p.out + (int64_t)bq * H * D;
+    int j = 0;
+    for (int tile = rank; tile < 4; tile += C, j++) {
+      // thread: dim d (consecutive lanes -> coalesced bf16 stores per head row), 8-head unit u
+      for (int task = tid; task < 128 * 8; task += AT_THREADS) {
+        const int d = task & 127, u = task >> 7;
+        const int off = d * H + ((u ^ (d & 7)) << 3);
+        float acc[8];
+        {
+          const uint4 v = *reinterpret_cast<const uint4*>(ostage + tile * (128 * H) + off);
+          const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const float2 f = __half22float2(h2[e]);
+            acc[2 * e] = f.x;
+            acc[2 * e + 1] = f.y;
+          }
+        }
+        for (int r = 0; r < C - 1; r++) {
+          const uint4 v = *reinterpret_cast<const uint4*>(orecv + (j * (C - 1) + r) * (128 * H) + off);
+          const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const float2 f = __half22float2(h2[e]);
+            acc[2 * e] += f.x;
+            acc[2 * e + 1] += f.y;
+          }
+        }
+        uint16_t* o = out + (u * 8) * D + tile * 128 + d;
+#pragma unroll
+        for (int e = 0; e < 8; e++) o[e * D] = (uint16_t)(pack_bf16x2(acc[e], 0.f) & 0xFFFFu);
+      }
+    }
+  }
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  tc::fence_before_sync();
+  cluster.sync();                                          // #4: all remote traffic finished
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, AT_TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows][512] with SW128 boxes of 64 columns x box_rows rows.
+static bool encode_bf16_rows512(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = at_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t attn_partials_bytes(int64_t, int) { return 0; }
@@ -346,12 +487,28 @@ cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
     if (e != cudaSuccess) return e;
     attr_dev = dev;
   }
-  attn_cluster_kernel<<<(unsigned)(BQ * AT_CLUSTER), AT_THREADS, AT_SMEM, stream>>>(p);
-  return cudaGetLastError();
+  CUtensorMap map_q, map_swa;
+  if (!encode_bf16_rows512(&map_q, p.q, (uint64_t)BQ * H, 64)) return cudaErrorInvalidValue;
+  const uint64_t swa_rows = (uint64_t)B * (uint64_t)(p.S > 0 ? p.S : 1);
+  if (!encode_bf16_rows512(&map_swa, p.swa, swa_rows, AT_KEYS)) return cudaErrorInvalidValue;
+  const int C = (p.K + AT_KEYS - 1) / AT_KEYS + 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(BQ * C));
+  cfg.blockDim = dim3(AT_THREADS);
+  cfg.dynamicSmemBytes = AT_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, map_q, map_swa, C);
 }
 
 }  // namespace csa2
