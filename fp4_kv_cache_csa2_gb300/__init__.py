@@ -61,6 +61,7 @@ _SIGNATURES = {
                               _P, _SZ, _P]),
     "csa2_block_topk_workspace_size": (_SZ, [_I, _I, _I64]),
     "csa2_block_topk": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I, _I, _I64, _I, _P, _P, _SZ, _P]),
+    "csa2_block_topk_static": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I, _I, _I64, _I, _P, _P]),
     "csa2_select_topk": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _P, _I, _I, _P, _I, _I, _I64,
                               _P, _SZ, _P]),
     "csa2_attn_workspace_size": (_SZ, [_I, _I, _I]),
@@ -184,6 +185,15 @@ def block_topk(cache: Cache, scores, q_pos, max_n: int, M: int, pool_blocks, ws:
     _check("csa2_block_topk", load().csa2_block_topk(
         ctypes.byref(c), _ptr(scores), _ptr(q_pos), B, Q, max_n, M, _ptr(pool_blocks), ws.ptr,
         ws.nbytes, _stream(stream)))
+
+
+def block_topk_static(cache: Cache, scores, q_pos, max_n: int, M: int, pool_blocks, stream=None) -> int:
+    """Candidate blocks without a workspace (library-held 4 MiB scratch); returns
+    the status code (CSA2_ERR_WORKSPACE = 3 when the request exceeds the scratch)."""
+    B, Q = q_pos.shape
+    c = cache.struct()
+    return load().csa2_block_topk_static(ctypes.byref(c), _ptr(scores), _ptr(q_pos), B, Q, max_n, M,
+                                         _ptr(pool_blocks), _stream(stream))
 
 
 def select_topk(cache: Cache, scores, q_pos, K: int, sel, max_n: int, ws: Workspace,

@@ -12,6 +12,8 @@
 // warp-aggregated shared-memory histograms), followed by an order-preserving
 // compaction that keeps every key above the threshold and the lowest-index
 // keys equal to it.  Output ids are ascending and padded with -1.
+#include <mutex>
+
 #include "params.cuh"
 
 namespace csa2 {
@@ -399,4 +401,57 @@ cudaError_t launch_select_topk(const float* scores, const int64_t* q_pos, const 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ fixed-scratch variant
+// csa2_block_topk_static keeps its block-maximum keys in this file-scope device
+// array instead of a caller-provided workspace.  4 MiB = 2^20 keys, enough for
+// B * Q * ceil(max_n / 8) <= 1,048,576 (for example 64 queries over 131,072
+// entries).  Every GPU that loads the library holds the array until the process
+// exits.
+constexpr size_t STATIC_BLOCK_KEYS = (size_t)1 << 20;
+__device__ __align__(256) uint32_t g_static_block_keys[STATIC_BLOCK_KEYS];
+
+// Device address of the array for the current device, looked up once per device
+// with that device current (host code may not use the symbol itself).
+static uint32_t* static_block_keys(cudaError_t* err) {
+  static std::mutex mu;
+  static uint32_t* ptrs[128] = {nullptr};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 128) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_static_block_keys);
+    if (*err != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
 }  // namespace csa2
+
+extern "C" csa2_status csa2_block_topk_static(const csa2_cache* cache, const float* scores, const int64_t* q_pos,
+                                              int B, int Q, int64_t max_n, int M, int32_t* pool_blocks,
+                                              void* stream) {
+  using namespace csa2;
+  if (!cache || !cache->main_kv || !cache->idx_codes || !cache->idx_scales || !cache->n_entries)
+    return CSA2_ERR_INVALID_ARG;
+  if (cache->cap < 0 || (cache->cap % BLK) != 0) return CSA2_ERR_INVALID_ARG;
+  if (cache->m != 1 && cache->m != 2) return CSA2_ERR_UNSUPPORTED;
+  if (B < 0 || Q < 0 || max_n < 0) return CSA2_ERR_INVALID_ARG;
+  if (M < 1 || M > CSA2_MAX_M) return CSA2_ERR_UNSUPPORTED;
+  if ((uint64_t)B * (uint64_t)Q * (uint64_t)ceil_div(max_n, BLK) > STATIC_BLOCK_KEYS) return CSA2_ERR_WORKSPACE;
+  if (B == 0 || Q == 0) return CSA2_OK;
+  if (!scores || !q_pos || !pool_blocks) return CSA2_ERR_INVALID_ARG;
+  cudaError_t err = cudaSuccess;
+  uint32_t* keys = static_block_keys(&err);
+  if (!keys) return CSA2_ERR_CUDA;
+  // every key the selection reads is written first by the block-max pass, so the
+  // array needs no clearing between calls
+  return launch_block_topk(scores, q_pos, cache->n_entries, cache->m, B, Q, max_n, M, pool_blocks, keys,
+                           (cudaStream_t)stream) == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}

@@ -193,6 +193,31 @@ csa2_status csa2_block_topk(const csa2_cache *cache, const float *scores, const 
                             void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Same result as csa2_block_topk, for callers that cannot allocate device
+ * memory: for example a plugin running inside a host engine that owns every
+ * byte of the GPU through its own allocator, or a latency-critical path where
+ * a cudaMalloc (which may synchronise the device) is not allowed.  The pages
+ * describe no such call; it exists only for this reason.
+ *   - No workspace: the per-block maxima live in a 4 MiB array inside the
+ *     library, so B * Q * ceil(max_n / 8) must not exceed 1,048,576 (e.g. 64
+ *     queries over 131,072 entries).  Larger requests return
+ *     CSA2_ERR_WORKSPACE before anything is enqueued.
+ *   - The library allocates nothing here and calls no allocating routine; the
+ *     array is loaded with the library and stays on every GPU that used it
+ *     until the process exits.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the previous call's contents
+ *     (nothing in it needs to start at zero).  Calls that may overlap on the
+ *     GPU (different streams without ordering, other threads, other processes
+ *     sharing the context) race on it: serialise them.
+ * Arguments and outputs are those of csa2_block_topk; device-side errors are
+ * not reported (there is no status word), argument errors are returned.
+ */
+csa2_status csa2_block_topk_static(const csa2_cache *cache, const float *scores, const int64_t *q_pos,
+                                   int B, int Q, int64_t max_n, int M, int32_t *pool_blocks, void *stream);
+
+/*
  * (b) Top-K entries by (score desc, entry id asc).  [zartbot §2.3.4: the Full
  * layer takes its own top-K over every visible entry; Reindex layers choose
  * inside the candidate pool]
