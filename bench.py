@@ -74,7 +74,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
@@ -257,31 +257,59 @@ def _clone_cache(c):
     return n
 
 
+def _capture(torch, fn):
+    """CUDA graph of the launches `fn` enqueues (the library calls only enqueue)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _graph_ms(torch, graph, reps):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def run_decode1m(args, torch, csa2):
     rank, world, local = dist_info()
     w = Decode1M(csa2, torch, d=args.pipeline_distance)
     w.prologue()
+    torch.cuda.synchronize()
+    # one graph per pipeline phase: step s only depends on s mod R
+    s_base = 3 * w.d
+    graphs = [_capture(torch, lambda i=i: w.step(s_base + i)) for i in range(w.R)]
     for s in range(args.warmup):
-        w.step(3 * w.d + s)
+        graphs[s % w.R].replay()
     torch.cuda.synchronize()
     n_steps = args.steps
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
-          for _ in range(n_steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0 = 3 * w.d + args.warmup
+    s0 = args.warmup
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         torch.cuda.nvtx.range_push("timed")
         start.record()
         for i in range(n_steps):
-            w.step(s0 + i, ev[i])
+            graphs[(s0 + i) % w.R].replay()
         stop.record()
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
     barrier(world)
     total_ms = max_over_ranks(start.elapsed_time(stop), world)
-    layer_ms = [statistics.mean(ev[i][l][0].elapsed_time(ev[i][l][1]) for i in range(n_steps)) for l in range(4)]
+    st, detail = w.ws.sync_status()
+    assert st == 0, f"device status {st} ({detail})"
+    # per-layer-call durations, same pipeline (cold instances), timed by layer type
+    reindex_g = _capture(torch, lambda: [w.layer(0, r) for r in range(w.R)])
+    reuse_g = _capture(torch, lambda: [w.layer(1 + (r % 3), r) for r in range(w.R)])
+    reindex_ms = _graph_ms(torch, reindex_g, 20) / w.R
+    reuse_ms = _graph_ms(torch, reuse_g, 20) / w.R
     st, detail = w.ws.sync_status()
     assert st == 0, f"device status {st} ({detail})"
 
@@ -290,10 +318,7 @@ def run_decode1m(args, torch, csa2):
     value = qtl_per_step * world / (ms_step / 1e3)
     hbm, bf16, which = peaks()
     bytes_step = w.B * CHAIN_BYTES
-    # dominant layer call by time: Reuse calls are 3 of 4
-    reuse_ms = statistics.mean(layer_ms[1:])
-    reindex_ms = layer_ms[0]
-    dom_is_reuse = 3 * reuse_ms >= reindex_ms
+    dom_is_reuse = 3 * reuse_ms >= reindex_ms          # Reuse calls are 3 of the 4 layers
     dom_ms = reuse_ms if dom_is_reuse else reindex_ms
     dom_bytes = w.B * (REUSE_BYTES if dom_is_reuse else REINDEX_BYTES)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -303,18 +328,19 @@ def run_decode1m(args, torch, csa2):
         "config": {"workload": "decode Reindex + 3 Reuse, 1,048,576 entries/seq, batch 16 per layer call",
                    "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                    "l2": f"inputs larger than L2: {w.R} pipelined instances x 5.97 GB, layer distance {w.d} steps",
+                   "launch": "one CUDA graph per pipeline phase (4 layer calls)",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": None,
-                     "kernel": "csa2_decode(REUSE) (attention)" if dom_is_reuse else "csa2_decode(REINDEX)",
+                     "kernel": "attn_tc_kernel (Reuse layer)" if dom_is_reuse else "Reindex layer",
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
                      "peak_source": which},
         "step_hbm": {"algorithmic_bytes": bytes_step, "GB_s": bytes_step / (ms_step / 1e3) / 1e9,
                      "frac": bytes_step / (ms_step / 1e3) / 1e9 / hbm},
-        "layer_ms": {"reindex": reindex_ms, "reuse": layer_ms[1:]},
+        "layer_ms": {"reindex": reindex_ms, "reuse": reuse_ms},
         "full_scan_1m_ms_untimed_setup": w.full_scan_ms,
         "clocks": clk.summary(),
-        "gpu_launches": n_steps * (4 + 3 * 2),
+        "gpu_launches": n_steps * (3 + 3),
         "e2e": e2e,
     }
 
@@ -440,7 +466,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode1m", choices=["decode1m"])

@@ -51,6 +51,9 @@ constexpr int AT_ST_ROW = AT_KEYS + 1;                   // padded fp32 row of S
 constexpr int AT_OFF_SMALL = AT_OFF_SCR + AT_SCR_BYTES;
 constexpr int AT_SHARE_BYTES = 128 * H * 2;             // one O^T tile share in fp16: 16 KB
 constexpr int AT_OFF_RECV = AT_OFF_Q;                    // 4 receive slots over the dead Q ring + scratch
+// Shares are O_c / 128 (exact power-of-two scaling): |share| <= the largest |key|
+// value, far inside the fp16 range.
+constexpr float AT_SHARE_DIV = 128.0f;
 constexpr int AT_TMEM_COLS = 512;                        // S^T: 64 cols, O^T: 4 x 64 cols
 
 struct AtSmall {
@@ -146,116 +149,105 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     sm.kvalid[tid] = kind;
   }
   tc::fence_before_sync();
-  cluster.sync();                                          // #0: barriers initialised cluster-wide
+  __syncthreads();                       // local barriers and key flags visible (no remote access yet)
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
-  // ---------------- producer: keys and the Q ring
-  if (warp == 0) {
+  // ---------------- initial copies: window rows (window CTA) and Q chunks 0..5
+  if (tid == 0) {
     if (window_cta) {
-      if (lane == 0) {
-        if (p.S > 0) {       // rows outside this sequence's window are masked (kvalid == 0) but finite
-          tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * AT_CHUNK_BYTES);
-          const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
-          for (int c = 0; c < 8; c++) tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.bar_kv);
-        } else {
-          tc::bar_arrive_expect_tx(&sm.bar_kv, 0u);
-        }
+      if (p.S > 0) {         // rows outside this sequence's window are masked (kvalid == 0) but finite
+        tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * AT_CHUNK_BYTES);
+        const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
+        for (int c = 0; c < 8; c++) tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.bar_kv);
+      } else {
+        tc::bar_arrive_expect_tx(&sm.bar_kv, 0u);
       }
     }
-    if (lane == 0) {
-      for (int c = 0; c < 8; c++) {
-        const int s = c % AT_QSTAGES;
-        if (c >= AT_QSTAGES && !at_wait(&sm.bar_qe[s], ((c / AT_QSTAGES) - 1) & 1, sm, p.hdr, 10)) break;
-        tc::bar_arrive_expect_tx(&sm.bar_q[s], 8192u);
-        tc::tma_load_2d(qbuf + s * 8192, &map_q, c * 64, bq * H, &sm.bar_q[s]);
-      }
+    for (int c = 0; c < AT_QSTAGES; c++) {
+      tc::bar_arrive_expect_tx(&sm.bar_q[c], 8192u);
+      tc::tma_load_2d(qbuf + c * 8192, &map_q, c * 64, bq * H, &sm.bar_q[c]);
     }
   }
 
-  // ---------------- warps 1..7: keys ready -> dequantise the selected FP4 entries
-  // (warp 0 keeps feeding the Q ring and is not part of this barrier)
-  if (warp > 0) {
-    if (!window_cta) {              // 16-byte asynchronous copies of the selected FP4 entries
-      for (int i = tid - 32; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS - 32) {
-        const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
-        if (sm.kvalid[s] == 1) {
-          const int32_t id = p.sel[(int64_t)bq * p.K + slot0 + s];
-          const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES + part * 16;
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                       :: "r"(tc::smem_u32(scr + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
-        }
+  // ---------------- keys: FP4 entries by 16-byte asynchronous copies, then warp w
+  // dequantises 64-dim chunk w and publishes it on its own mbarrier
+  if (!window_cta) {
+    for (int i = tid; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS) {
+      const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
+      if (sm.kvalid[s] == 1) {
+        const int32_t id = p.sel[(int64_t)bq * p.K + slot0 + s];
+        const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES + part * 16;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                     :: "r"(tc::smem_u32(scr + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
       }
-      asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-      asm volatile("bar.sync 1, %0;" :: "r"(AT_THREADS - 32) : "memory");
-    } else {
-      at_wait(&sm.bar_kv, 0, sm, p.hdr, 11);
     }
-    if (!window_cta) {
-      // warp w dequantises chunk w-1 (warp 7 also chunk 7) and publishes it on its
-      // own mbarrier, so the MMAs of chunk c start as soon as c is ready
-      for (int c = warp - 1; c < 8; c += (warp == 7 ? 1 : 8)) {
-        unsigned char* rowp = kbuf + c * AT_CHUNK_BYTES;
-        for (int s = lane; s < AT_KEYS; s += 32) {
-          if (sm.kvalid[s] == 1) {
-            const unsigned char* ent = scr + s * MAIN_BYTES;
-            const uint4 c0 = *reinterpret_cast<const uint4*>(ent + c * 32);
-            const uint4 c1 = *reinterpret_cast<const uint4*>(ent + c * 32 + 16);
-            const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(ent + 256 + c * 4);
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int c = warp;
+    unsigned char* rowp = kbuf + c * AT_CHUNK_BYTES;
+    for (int s = lane; s < AT_KEYS; s += 32) {
+      if (sm.kvalid[s] == 1) {
+        const unsigned char* ent = scr + s * MAIN_BYTES;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(ent + c * 32);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(ent + c * 32 + 16);
+        const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(ent + 256 + c * 4);
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-            for (int g = 0; g < 4; g++) {                      // 16 channels per E4M3 scale
-              const float sc = e4m3_value((sc4 >> (8 * g)) & 255u);
-              const uint32_t sc2 = pack_bf16x2(sc, sc);
-              uint32_t o[8];
+        for (int g = 0; g < 4; g++) {                      // 16 channels per E4M3 scale
+          const float sc = e4m3_value((sc4 >> (8 * g)) & 255u);
+          const uint32_t sc2 = pack_bf16x2(sc, sc);
+          uint32_t o[8];
 #pragma unroll
-              for (int k = 0; k < 8; k++) {
-                const uint32_t byte = (cw[2 * g + (k >> 2)] >> (8 * (k & 3))) & 255u;
-                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(sm.lut[byte]), "r"(sc2));
-              }
-              *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u + 16u)) = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 8; u++)
-              *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)u * 16u)) = make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 8; k++) {
+            const uint32_t byte = (cw[2 * g + (k >> 2)] >> (8 * (k & 3))) & 255u;
+            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(sm.lut[byte]), "r"(sc2));
           }
+          *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u + 16u)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::bar_arrive(&sm.bar_chunk[c]);
-      }
-    } else {
-      if (p.S == 0) {                                          // no window rows supplied: zero keys
-        for (int i = tid - 32; i < 8 * AT_CHUNK_BYTES / 16; i += AT_THREADS - 32)
-          reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0, 0, 0, 0);
-        tc::fence_proxy_async_smem();
-        asm volatile("bar.sync 1, %0;" :: "r"(AT_THREADS - 32) : "memory");
-      }
-      if (warp == 1 && lane == 0)
-        for (int c = 0; c < 8; c++) tc::bar_arrive(&sm.bar_chunk[c]);
-    }
-
-    // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims)
-    if (warp == 1 && lane == 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
-      for (int c = 0; c < 8; c++) {
-        const int s = c % AT_QSTAGES;
-        if (!at_wait(&sm.bar_chunk[c], 0, sm, p.hdr, 16)) break;
-        if (!at_wait(&sm.bar_q[s], (c / AT_QSTAGES) & 1, sm, p.hdr, 12)) break;
-        tc::fence_after_sync();
-        const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + s * 8192);
+      } else {
 #pragma unroll
-        for (int ks = 0; ks < 4; ks++)
-          tc::mma_bf16(tmem, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
-                       tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c | ks) ? 1u : 0u);
-        tc::commit(&sm.bar_qe[s]);
+        for (int u = 0; u < 8; u++)
+          *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)u * 16u)) = make_uint4(0, 0, 0, 0);
       }
-      tc::commit(&sm.bar_s);
     }
+    tc::fence_proxy_async_smem();
     __syncwarp();
+    if (lane == 0) tc::bar_arrive(&sm.bar_chunk[c]);
+  } else if (p.S == 0) {                                   // no window rows supplied: zero keys
+    for (int i = tid; i < 8 * AT_CHUNK_BYTES / 16; i += AT_THREADS)
+      reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0, 0, 0, 0);
+    tc::fence_proxy_async_smem();
+    __syncthreads();
   }
+
+  // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims); the
+  // issuing thread also refills Q stages 0 and 1 with chunks 6 and 7
+  if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
+    if (window_cta) at_wait(&sm.bar_kv, 0, sm, p.hdr, 11);
+    for (int c = 0; c < 8; c++) {
+      const int s = c % AT_QSTAGES;
+      if (!window_cta && !at_wait(&sm.bar_chunk[c], 0, sm, p.hdr, 16)) break;
+      if (!at_wait(&sm.bar_q[s], (c / AT_QSTAGES) & 1, sm, p.hdr, 12)) break;
+      tc::fence_after_sync();
+      const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + s * 8192);
+#pragma unroll
+      for (int ks = 0; ks < 4; ks++)
+        tc::mma_bf16(tmem, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
+                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c | ks) ? 1u : 0u);
+      tc::commit(&sm.bar_qe[s]);
+      if (c == 2 || c == 3) {              // stage c-2 is free once chunk c-2's MMAs finished
+        const int r = c - 2;
+        if (!at_wait(&sm.bar_qe[r], 0, sm, p.hdr, 10)) break;
+        tc::bar_arrive_expect_tx(&sm.bar_q[r], 8192u);
+        tc::tma_load_2d(qbuf + r * 8192, &map_q, (r + AT_QSTAGES) * 64, bq * H, &sm.bar_q[r]);
+      }
+    }
+    tc::commit(&sm.bar_s);
+  }
+  __syncwarp();
 
   // ---------------- S^T from TMEM -> scaled, masked, transposed into smem
   at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
@@ -338,13 +330,6 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::commit(&sm.bar_o);
   }
   __syncwarp();
-  cluster.sync();                                          // #2: row sums visible
-  if (tid < H) {
-    float L = 0.f;
-    for (int c = 0; c < C; c++) L += cluster.map_shared_rank(sm.loc_sum, c)[tid];
-    sm.inv_l[tid] = (L > 0.f) ? 1.0f / L : 0.f;
-  }
-  __syncthreads();
   at_wait(&sm.bar_o, 0, sm, p.hdr, 14);
   tc::fence_after_sync();
   // this CTA's share O_c / L per tile as fp16 [dim][head], 16-byte units swizzled by dim
@@ -375,8 +360,8 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int j = 8 * u + 2 * e;
-          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * sm.inv_l[half * 32 + j],
-                                               __uint_as_float(ta[tile][j + 1]) * sm.inv_l[half * 32 + j + 1]);
+          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * (1.0f / AT_SHARE_DIV),
+                                               __uint_as_float(ta[tile][j + 1]) * (1.0f / AT_SHARE_DIV));
           w[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
         const int unit = (half * 4 + u) ^ (d & 7);
@@ -385,7 +370,15 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
   }
   tc::fence_proxy_async_smem();
-  cluster.sync();                                          // #3: every share staged, receive slots free
+  cluster.sync();                                          // #2: shares staged, receive slots free, sums visible
+  if (tid < H) {
+    float L = 0.f;
+    for (int c = 0; c < C; c++) L += cluster.map_shared_rank(sm.loc_sum, c)[tid];
+    sm.inv_l[tid] = (L > 0.f) ? AT_SHARE_DIV / L : 0.f;
+  }
+  __syncthreads();
+  // no remote shared-memory reads after this point: let the cluster go ahead
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // ---------------- cluster reduction: tile t is owned by CTA t % C; the others send
   // their fp16 share into the owner's slot (j * (C - 1) + sender index)
@@ -439,13 +432,14 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
         }
         uint16_t* o = out + (u * 8) * D + tile * 128 + d;
 #pragma unroll
-        for (int e = 0; e < 8; e++) o[e * D] = (uint16_t)(pack_bf16x2(acc[e], 0.f) & 0xFFFFu);
+        for (int e = 0; e < 8; e++)
+          o[e * D] = (uint16_t)(pack_bf16x2(acc[e] * sm.inv_l[u * 8 + e], 0.f) & 0xFFFFu);
       }
     }
   }
   if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   tc::fence_before_sync();
-  cluster.sync();                                          // #4: all remote traffic finished
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every CTA done reading ours
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, AT_TMEM_COLS);
