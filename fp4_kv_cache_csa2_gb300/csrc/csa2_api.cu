@@ -322,12 +322,24 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
                                       a->B, a->Q, a->max_n, s));
     if (st != CSA2_OK) return st;
   } else if (a->mode == CSA2_MODE_REINDEX) {
-    float* scores = reinterpret_cast<float*>(cur);
-    st = do_index_score(cache, a->q_idx, a->w_head, a->q_pos, a->pool_blocks, a->M, scores, a->B, a->Q,
-                        a->max_n, hdr, s);
-    if (st != CSA2_OK) return st;
-    st = from_cuda(launch_select_topk(scores, a->q_pos, cache->n_entries, cache->m, a->pool_blocks, a->M, a->K,
-                                      a->sel, a->B, a->Q, a->max_n, s));
+    IsParams ip{};
+    ip.idx_codes = cache->idx_codes;
+    ip.idx_scales = cache->idx_scales;
+    ip.cap = cache->cap;
+    ip.n_entries = cache->n_entries;
+    ip.m = cache->m;
+    ip.q_idx = a->q_idx;
+    ip.w_head = a->w_head;
+    ip.q_pos = a->q_pos;
+    ip.pool = a->pool_blocks;
+    ip.M = a->M;
+    ip.B = a->B;
+    ip.Q = a->Q;
+    ip.max_n = a->max_n;
+    ip.sel = a->sel;
+    ip.K = a->K;
+    ip.hdr = hdr;
+    st = from_cuda(launch_reindex_select(ip, s));
     if (st != CSA2_OK) return st;
   }
   return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out, a->B,

@@ -37,6 +37,8 @@ struct IsParams {
   int B, Q;
   int64_t max_n;
   int64_t entries_per_cta;    // set by the launcher
+  int32_t* sel;               // fused Reindex: [B][Q][K] output
+  int K;
   WsHeader* hdr;
 };
 
@@ -61,6 +63,7 @@ struct AttnParams {
 
 cudaError_t launch_cache_write(const CwParams& p, cudaStream_t stream, int num_sms);
 cudaError_t launch_index_score(IsParams p, cudaStream_t stream);
+cudaError_t launch_reindex_select(IsParams p, cudaStream_t stream);
 cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m,
                               int B, int Q, int64_t max_n, int M, int32_t* pool_blocks, uint32_t* gkeys,
                               cudaStream_t stream);

@@ -230,9 +230,13 @@ __device__ void radix_select_smem(const Keys& keys, const Ids& ids, int n, int K
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = lane; i < 256; i += 32) myh[i] = 0;
       __syncwarp();
-      for (int i = tid; i < n; i += SEL_THREADS) {
-        const uint32_t k = sk[i];
-        if (k != 0u && (k & mask) == prefix) atomicAdd(&myh[(k >> shift) & 255u], 1u);
+      for (int base = 0; base < n; base += SEL_THREADS) {     // uniform trip count for match_any
+        const int i = base + tid;
+        const uint32_t k = (i < n) ? sk[i] : 0u;
+        const bool ok = k != 0u && (k & mask) == prefix;
+        const uint32_t digit = ok ? ((k >> shift) & 255u) : 256u;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, digit);
+        if (ok && lane == __ffs(peers) - 1) atomicAdd(&myh[digit], (uint32_t)__popc(peers));
       }
       __syncthreads();
       if (tid < 256) {

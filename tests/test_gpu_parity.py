@@ -412,3 +412,66 @@ def test_decode_reindex_with_all_blocks_equals_full_selection(csa2):
     csa2.decode(csa2.MODE_REINDEX, L.cache, sel=sel2, out=out2, pool_blocks=pool, **common)
     assert torch.equal(sel, sel2)
     assert torch.equal(out, out2)
+
+
+def test_decode_reindex_cluster_select_ties_and_short_pool(csa2):
+    """Reindex selection is one radix select across the 8 CTAs that each score an
+    eighth of the pool.  Query 0: every block in the pool, and eight blocks spread
+    over all eight eighths carry copies of one index-key row, so 65 entries have
+    bit-identical scores and K cuts through them: the lowest ids must win (score
+    desc, id asc).  Its last pooled entry is not yet visible.  Query 1: a pool of
+    30 blocks (240 entries) padded with -1 and K > 240, so every pooled entry is
+    chosen in ascending order and the tail of sel is -1."""
+    T, M = 4096, 512
+    case = cases.make_case(B=1, T=T, m=1, Q=2, M=M, K=1, seed=911)
+    L = GpuLayer(csa2, case)
+    main, codes, scales = cases.oracle_cache(case)
+    codes, scales = codes.copy(), scales.copy()
+    s0 = _oracle_scores(case, codes, scales, 0, 0, np.arange(T))
+    X = int(np.argsort(-s0, kind="stable")[350])
+    tie_blocks = [5, 70, 140, 200, 260, 330, 400, 470]          # one in each CTA's eighth (64 blocks)
+    for blk in tie_blocks:
+        codes[0, 8 * blk:8 * blk + 8] = codes[0, X]
+        scales[0, 8 * blk:8 * blk + 8] = scales[0, X]
+    L.cache.idx_codes[0, :T].copy_(torch.from_numpy(codes[0]))
+    L.cache.idx_scales[0, :T].copy_(torch.from_numpy(scales[0]))
+    tied = np.sort(np.concatenate([[X], *[np.arange(8 * b, 8 * b + 8) for b in tie_blocks]]))
+    nv0 = oracle.visible_entries(case.q_pos[0, 0], 1, T)
+    assert nv0 == T - 1
+    s0 = np.full(T, -np.inf)
+    s0[:nv0] = _oracle_scores(case, codes, scales, 0, 0, np.arange(nv0))
+    v = s0[X]
+    n_greater = int(np.sum(s0 > v))
+    K = n_greater + 32
+    assert 240 < K <= 512 and n_greater + len(tied) > K
+
+    g = np.random.default_rng(5)
+    pool = np.full((1, 2, M), -1, np.int32)
+    pool[0, 0] = np.arange(M)
+    pool[0, 1, :30] = np.sort(g.choice(M, 30, replace=False))
+    sel = torch.empty((1, 2, K), dtype=torch.int32, device=DEV)
+    out = torch.empty((1, 2, 64, 512), dtype=torch.int16, device=DEV)
+    ws = csa2.Workspace(csa2.decode_workspace_size(1, 1, 2, T, M, K), device=DEV)
+    csa2.decode(csa2.MODE_REINDEX, L.cache, q_pos=L.q_pos, q=L.q, swa=L.swa, swa_base_pos=L.swa_base,
+                scale=case.scale, sel=sel, out=out, ws=ws, M=M, max_n=T, q_idx=L.q_idx, w_head=L.w_head,
+                pool_blocks=dev(pool))
+    assert ws.sync_status()[0] == 0
+    got, got_out = host(sel), bf16_to_f32(out)
+
+    # query 0: exact top-K by (score desc, id asc); ties inside the tie group go to the lowest ids
+    want0 = oracle.select_topk(s0, oracle.pool_entries(pool[0, 0], nv0), K)
+    cases.assert_set_within_tie_window(got[0, 0], want0, lambda j: s0[j], what="reindex ties")
+    assert np.all(np.diff(got[0, 0]) > 0) and got[0, 0].max() < nv0
+    taken = np.isin(tied, got[0, 0])
+    assert 0 < taken.sum() < len(tied)
+    assert np.all(taken[:taken.sum()]), "tied entries must be taken in ascending id order"
+    cases.check_attention(got_out[0, 0], _oracle_attention(case, main, 0, 0, got[0, 0]), "reindex ties")
+
+    # query 1: fewer pooled entries than K
+    nv1 = oracle.visible_entries(case.q_pos[0, 1], 1, T)
+    dom1 = oracle.pool_entries(pool[0, 1], nv1)
+    assert len(dom1) == 240
+    want1 = np.full(K, -1, np.int32)
+    want1[:240] = dom1
+    np.testing.assert_array_equal(got[0, 1], want1)
+    cases.check_attention(got_out[0, 1], _oracle_attention(case, main, 0, 1, got[0, 1]), "reindex short pool")
