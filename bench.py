@@ -15,16 +15,20 @@ s-3d, so roughly d steps (d * 44 MB > L2) pass between two layers touching
 the same instance.  One step = four layer calls of batch 16 = 64
 query-token-layers.
 
-Other workloads (``--workload``): ``full`` (decode Full, m=1, 64 x 131,072),
-``cachewrite`` (4 source layers x 2^20 tokens), ``prefill`` (8192-token chunk
-on a 131,072-token prefix, m=2).
+``--seq-len`` shrinks the cache (the same step on fewer entries; used for
+small profiler captures), ``--cpu-sample-queries 0`` skips the CPU oracle leg.
 
 ``--impl reference`` times the CPU oracle (the checker, not a product path) on
 a bounded sample of the same workload.
+
+The roofline's ``traffic`` (DRAM bytes per launch of the dominant kernel) is
+read from the ncu summary under ``profiles/`` and reported only while the
+kernel's source file still has the hash recorded beside the figure.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -57,6 +61,23 @@ def peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from profiles/traffic.txt, or None when
+    absent or when the kernel's source changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 4 and parts[0] == kernel and not line.startswith("#"):
+                    src = os.path.join(ROOT, "fp4_kv_cache_csa2_gb300", "csrc", parts[2])
+                    with open(src, "rb") as g:
+                        if hashlib.sha256(g.read()).hexdigest()[:16] == parts[3]:
+                            return float(parts[1])
+    except OSError:
+        pass
+    return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -151,7 +172,7 @@ class Decode1M:
         w_idx = synth.torch_normal(seed + 1, (DI, D), torch.float32, dev).mul_(1 / math.sqrt(D)).to(torch.bfloat16)
         rope = csa2.rope_table(N).to(dev)
         ws_cw = csa2.Workspace(1 << 16, device=dev)
-        chunk = 1 << 17
+        chunk = min(1 << 17, N)
         ones = torch.ones(D, device=dev)
         for b in range(B):
             for c0 in range(0, N, chunk):
@@ -279,7 +300,7 @@ def _graph_ms(torch, graph, reps):
 
 def run_decode1m(args, torch, csa2):
     rank, world, local = dist_info()
-    w = Decode1M(csa2, torch, d=args.pipeline_distance)
+    w = Decode1M(csa2, torch, N=args.seq_len, d=args.pipeline_distance)
     w.prologue()
     torch.cuda.synchronize()
     # one graph per pipeline phase: step s only depends on s mod R
@@ -322,17 +343,20 @@ def run_decode1m(args, torch, csa2):
     dom_ms = reuse_ms if dom_is_reuse else reindex_ms
     dom_bytes = w.B * (REUSE_BYTES if dom_is_reuse else REINDEX_BYTES)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    dom_kernel = "attn_tc_kernel" if dom_is_reuse else "index_score_tc_kernel<true>"
+    traffic = ncu_traffic(dom_kernel) if w.N == 1 << 20 else None
     e2e = run_decode1m_e2e(args, torch, csa2, w)
     return {
         "value": value, "ms_per_step": ms_step, "dtype": "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
-        "config": {"workload": "decode Reindex + 3 Reuse, 1,048,576 entries/seq, batch 16 per layer call",
+        "config": {"workload": f"decode Reindex + 3 Reuse, {w.N:,} entries/seq, batch 16 per layer call",
                    "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
-                   "l2": f"inputs larger than L2: {w.R} pipelined instances x 5.97 GB, layer distance {w.d} steps",
+                   "l2": f"inputs larger than L2: {w.R} pipelined instances x "
+                         f"{w.B * w.N * (MAIN_ENTRY + IDX_ENTRY) / 1e9:.2f} GB, layer distance {w.d} steps",
                    "launch": "one CUDA graph per pipeline phase (4 layer calls)",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
-                     "kernel": "attn_tc_kernel (Reuse layer)" if dom_is_reuse else "Reindex layer",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": dom_kernel + (" (Reuse layer)" if dom_is_reuse else " (Reindex layer)"),
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
                      "peak_source": which},
         "step_hbm": {"algorithmic_bytes": bytes_step, "GB_s": bytes_step / (ms_step / 1e3) / 1e9,
@@ -340,7 +364,8 @@ def run_decode1m(args, torch, csa2):
         "layer_ms": {"reindex": reindex_ms, "reuse": reuse_ms},
         "full_scan_1m_ms_untimed_setup": w.full_scan_ms,
         "clocks": clk.summary(),
-        "gpu_launches": n_steps * (3 + 3),
+        # Reindex layer: fused score + select kernel and attention; Reuse: attention
+        "gpu_launches": n_steps * (2 + 3),
         "e2e": e2e,
     }
 
@@ -470,6 +495,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode1m", choices=["decode1m"])
+    ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
     args = ap.parse_args()
@@ -491,14 +517,16 @@ def main():
     csa2.load()
     res = run_decode1m(args, torch, csa2)
     if rank == 0:
-        cpu_v, cpu_dt = OracleChain().run(args.cpu_sample_queries)
         line = {"metric": METRIC, "value": res.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": res.pop("dtype"), "data": "synthetic"}
         line.update(res)
-        line["cpu_baseline"] = {"value": cpu_v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
-                                "sample": f"{args.cpu_sample_queries} query tokens x (Reindex over a 16,384-entry "
-                                          f"pool + 3 Reuse attentions), {cpu_dt:.1f} s"}
+        line["cpu_baseline"] = None
+        if args.cpu_sample_queries > 0:
+            cpu_v, cpu_dt = OracleChain().run(args.cpu_sample_queries)
+            line["cpu_baseline"] = {"value": cpu_v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                                    "sample": f"{args.cpu_sample_queries} query tokens x (Reindex over a 16,384-"
+                                              f"entry pool + 3 Reuse attentions), {cpu_dt:.1f} s"}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
