@@ -11,22 +11,31 @@
 // One thread-block cluster of C CTAs per query token, 128 keys per CTA: CTAs
 // 0..C-2 take the K selected slots in runs of 128, CTA C-1 the 128 window
 // positions.  In every CTA:
+//   * Q (64 heads x 512, bf16) lands by TMA in 8 SW128 column chunks;
 //   * keys land in shared memory as bf16 [128 keys][512] in 8 SW128 column
-//     chunks of 64 dims: window rows by 2-D TMA straight from the bf16 window,
-//     selected FP4 entries by bulk copies into a staging buffer followed by an
-//     exact dequantisation (E2M1 x E4M3 has at most 6 significant bits);
-//   * Q (64 heads x 512) streams through a 4-stage TMA ring;
+//     chunks of 64 dims: window rows by 2-D TMA straight from the bf16 window;
+//     selected FP4 entries by 16-byte asynchronous copies into a staging
+//     buffer (consecutive threads take consecutive pieces of an entry), from
+//     there into registers, two lanes per entry, after which Q chunks 4..7 are
+//     loaded over the staging buffer; every warp then dequantises its 16 keys
+//     exactly, chunk by chunk (E2M1 -> bf16 by byte permutes, times the E4M3
+//     scale; the product has at most 6 significant bits);
 //   * S^T = K Q^T is one M=128 (keys) x N=64 (heads) x K=512 tcgen05 bf16 MMA
-//     chain into TMEM;
-//   * row maxima are exchanged over distributed shared memory, P = exp(S - max)
-//     is written as the K-major bf16 B operand of the second product;
-//   * O^T = V^T P^T reuses the same key buffer as an MN-major A operand:
-//     4 tiles of M=128 dims x N=64 heads x K=128 keys;
-//   * row sums are exchanged; every CTA writes its share O_c / L of each 128-dim
-//     tile as fp16 (relative rounding 2^-11, four times finer than the bf16
-//     output) and bulk-copies the tiles it does not own into the owner's
-//     receive slots over DSMEM; the owner adds the C shares in fp32, rounds to
-//     bf16 and stores.
+//     chain into TMEM, issued chunk by chunk as the dequantisation finishes;
+//   * softmax over this CTA's keys with its own row maxima m_c, straight from
+//     TMEM (thread = key, 32 heads in registers; per-warp column maxima and
+//     sums by transpose-reductions over the lanes): P = exp(S - m_c) becomes
+//     the MN-major bf16 B operand [key][head] of the second product, L_c = sum P;
+//   * O^T = V^T P^T reuses the key buffer as an MN-major A operand: 4 tiles of
+//     M=128 dims x N=64 heads x K=128 keys;
+//   * every CTA stages its normalised share O_c / L_c of each 128-dim tile in
+//     fp16 (a convex combination of key vectors, relative rounding 2^-11) and
+//     bulk-copies the tiles it does not own, each followed by its (m_c, L_c)
+//     rows, into the owner's receive slots over distributed shared memory; the
+//     owner weights the C shares by L_c exp(m_c - M) / sum_c' L_c' exp(m_c' - M),
+//     M = max_c m_c, in fp32, rounds to bf16 and stores.  A split cluster
+//     barrier (arrive once the receive slots are dead, wait before sending)
+//     orders the exchange; no CTA reads another's shared memory.
 // All mbarrier waits are bounded; a timeout reports CSA2_ERR_TIMEOUT.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
@@ -41,43 +50,69 @@ namespace csa2 {
 
 constexpr int AT_THREADS = 256;
 constexpr int AT_KEYS = 128;                  // keys per CTA (one M = 128 tile)
-constexpr int AT_QSTAGES = 6;
+constexpr int AT_MAXC = CSA2_MAX_K / AT_KEYS + 1;
 constexpr int AT_CHUNK_BYTES = AT_KEYS * 128;            // [128 keys][64 dims] bf16 = 16 KB
-constexpr int AT_OFF_K = 0;                              // 8 chunks, 128 KB
-constexpr int AT_OFF_Q = 8 * AT_CHUNK_BYTES;             // 6 stages x 8 KB
-constexpr int AT_OFF_SCR = AT_OFF_Q + AT_QSTAGES * 8192; // FP4 staging | S^T transposed | P
-constexpr int AT_SCR_BYTES = AT_KEYS * MAIN_BYTES;       // 36,864
-constexpr int AT_ST_ROW = AT_KEYS + 1;                   // padded fp32 row of S^T transposed
-constexpr int AT_OFF_SMALL = AT_OFF_SCR + AT_SCR_BYTES;
+constexpr int AT_QCHUNK_BYTES = H * 128;                 // [64 heads][64 dims] bf16 = 8 KB
+constexpr int AT_OFF_K = 0;                              // 8 key chunks, 128 KB
+constexpr int AT_OFF_Q = 8 * AT_CHUNK_BYTES;             // Q chunks 0..3, 32 KB; 4..7 follow over the staging
+constexpr int AT_OFF_STAGE = AT_OFF_Q + 4 * AT_QCHUNK_BYTES;   // FP4 staging [128][288], then Q chunks 4..7
+constexpr int AT_STAGE_BYTES = AT_KEYS * MAIN_BYTES;     // 36,864
+constexpr int AT_OFF_P = AT_OFF_Q;                       // after S: P^T [128 keys][64 heads] bf16 SW128, 16 KB
+constexpr int AT_OFF_SMALL = AT_OFF_STAGE + AT_STAGE_BYTES;
 constexpr int AT_SHARE_BYTES = 128 * H * 2;             // one O^T tile share in fp16: 16 KB
-constexpr int AT_OFF_RECV = AT_OFF_Q;                    // 4 receive slots over the dead Q ring + scratch
-// Shares are O_c / 128 (exact power-of-two scaling): |share| <= the largest |key|
-// value, far inside the fp16 range.
-constexpr float AT_SHARE_DIV = 128.0f;
+constexpr int AT_OFF_RECV = AT_OFF_Q;                    // after O: 4 receive slots over the Q region
 constexpr int AT_TMEM_COLS = 512;                        // S^T: 64 cols, O^T: 4 x 64 cols
 
 struct AtSmall {
   int kvalid[AT_KEYS];
-  float loc_max[H];
-  float loc_sum[H];
+  int32_t kid[AT_KEYS];
+  alignas(16) float ml[2 * H];           // this CTA's row maxima m_c, then row sums L_c (sent to the owners)
+  alignas(16) float recv_ml[4][2 * H];   // (m, L) rows received with each share
   float inv_l[H];
-  float gmax[H];
-  uint32_t lut[256];
+  float red[4][H];                       // per-warp column maxima / sums (warp w & 3, head)
+  float wgt[AT_MAXC][H];                 // combination weight of each CTA's share, per head
   uint64_t bar_kv, bar_s, bar_o, bar_red;
-  uint64_t bar_q[AT_QSTAGES], bar_qe[AT_QSTAGES];
+  uint64_t bar_q[8];
   uint64_t bar_chunk[8];                 // chunk c of the keys is in shared memory (bf16, SW128)
   uint32_t tmem_base;
   int err;
 };
 constexpr int AT_SMEM = AT_OFF_SMALL + (int)sizeof(AtSmall) + 1024;
-static_assert(AT_ST_ROW * H * 4 <= AT_SCR_BYTES, "S^T scratch must fit");
+static_assert(4 * AT_QCHUNK_BYTES <= AT_STAGE_BYTES, "Q chunks 4..7 must fit over the staging");
+static_assert(AT_OFF_STAGE % 1024 == 0, "SW128 destinations are 1 KB aligned");
 static_assert(4 * AT_SHARE_BYTES <= 8 * AT_CHUNK_BYTES, "O^T shares must fit over the keys");
-static_assert(4 * AT_SHARE_BYTES <= AT_QSTAGES * 8192 + AT_SCR_BYTES, "receive slots must fit");
+static_assert(4 * AT_SHARE_BYTES <= 8 * AT_QCHUNK_BYTES, "receive slots must fit over Q");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
   return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Eight E2M1 codes (element k in bits 4k..4k+3 of w) -> four bf16x2 words
+// (element 2i in the low half of word i).  The bf16 patterns of the eight
+// magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are looked up byte-wise (high bytes
+// 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80 C0) and each code's
+// sign bit becomes bit 15 of its half.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t out[4]) {
+  const uint32_t mag = w & 0x77777777u;
+  uint32_t h0 = prmt(0x3F3F3F00u, 0x40404040u, mag);
+  uint32_t h1 = prmt(0x3F3F3F00u, 0x40404040u, mag >> 16);
+  const uint32_t l0 = prmt(0xC0800000u, 0xC0804000u, mag);
+  const uint32_t l1 = prmt(0xC0800000u, 0xC0804000u, mag >> 16);
+  const uint32_t a = w << 4;                  // byte j, bit 7: sign of element 2j (w's byte j: element 2j+1)
+  h0 |= prmt(a, w, 0x5140u) & 0x80808080u;    // byte k, bit 7: sign of element k (k = 0..3)
+  h1 |= prmt(a, w, 0x7362u) & 0x80808080u;    // elements 4..7
+  out[0] = prmt(l0, h0, 0x5140u);
+  out[1] = prmt(l0, h0, 0x7362u);
+  out[2] = prmt(l1, h1, 0x5140u);
+  out[3] = prmt(l1, h1, 0x7362u);
 }
 
 // byte offset of (row, byte) in a 1 KB-aligned SW128 region of 128-byte rows
@@ -98,9 +133,9 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* kbuf = smem + AT_OFF_K;
   unsigned char* qbuf = smem + AT_OFF_Q;
-  unsigned char* scr = smem + AT_OFF_SCR;
+  unsigned char* pbuf = smem + AT_OFF_P;
+  unsigned char* stage = smem + AT_OFF_STAGE;
   AtSmall& sm = *reinterpret_cast<AtSmall*>(smem + AT_OFF_SMALL);
-  float* st = reinterpret_cast<float*>(scr);                 // S^T transposed: [64 heads][129] fp32
   __half* ostage = reinterpret_cast<__half*>(kbuf);          // 4 tiles x [128 dims][64 heads] fp16 shares
   __half* orecv = reinterpret_cast<__half*>(smem + AT_OFF_RECV); // up to 4 received shares
 
@@ -120,21 +155,20 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::bar_init(&sm.bar_s, 1);
     tc::bar_init(&sm.bar_o, 1);
     tc::bar_init(&sm.bar_red, 1);
-    for (int i = 0; i < AT_QSTAGES; i++) {
+    for (int i = 0; i < 8; i++) {
       tc::bar_init(&sm.bar_q[i], 1);
-      tc::bar_init(&sm.bar_qe[i], 1);
+      tc::bar_init(&sm.bar_chunk[i], AT_THREADS / 32);
     }
-    for (int i = 0; i < 8; i++) tc::bar_init(&sm.bar_chunk[i], 1);
     sm.err = 0;
     tc::bar_init_fence();
   }
-  sm.lut[tid] = pack_bf16x2(e2m1_value(tid & 15u), e2m1_value((uint32_t)tid >> 4));
   if (tid < AT_KEYS) {                       // which keys of this CTA exist
     int kind = 0;
+    int32_t id = 0;
     if (!window_cta) {
       const int gs = slot0 + tid;
       if (gs < p.K) {
-        const int32_t id = p.sel[(int64_t)bq * p.K + gs];
+        id = p.sel[(int64_t)bq * p.K + gs];
         if (id >= 0 && id < p.cap) kind = 1;
         else if (id >= p.cap) report(p.hdr, CSA2_ERR_BOUNDS, id);
       }
@@ -147,13 +181,14 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
       }
     }
     sm.kvalid[tid] = kind;
+    sm.kid[tid] = kind == 1 ? id : 0;
   }
   tc::fence_before_sync();
   __syncthreads();                       // local barriers and key flags visible (no remote access yet)
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
-  // ---------------- initial copies: window rows (window CTA) and Q chunks 0..5
+  // ---------------- copies: window rows (window CTA) and all of Q
   if (tid == 0) {
     if (window_cta) {
       if (p.S > 0) {         // rows outside this sequence's window are masked (kvalid == 0) but finite
@@ -164,57 +199,72 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
         tc::bar_arrive_expect_tx(&sm.bar_kv, 0u);
       }
     }
-    for (int c = 0; c < AT_QSTAGES; c++) {
-      tc::bar_arrive_expect_tx(&sm.bar_q[c], 8192u);
-      tc::tma_load_2d(qbuf + c * 8192, &map_q, c * 64, bq * H, &sm.bar_q[c]);
+    for (int c = 0; c < (window_cta ? 8 : 4); c++) {     // chunks 4..7 land over the staging buffer
+      tc::bar_arrive_expect_tx(&sm.bar_q[c], (uint32_t)AT_QCHUNK_BYTES);
+      tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q[c]);
     }
   }
 
-  // ---------------- keys: FP4 entries by 16-byte asynchronous copies, then warp w
-  // dequantises 64-dim chunk w and publishes it on its own mbarrier
+  // ---------------- keys: FP4 entries by 16-byte asynchronous copies into the
+  // staging buffer; lanes 2k and 2k+1 of warp w then take the halves of entry
+  // 16w + k (128 code bytes = dims 256h .. 256h+255, and their 16 scale bytes)
+  // into registers, the staging buffer receives Q chunks 4..7, and chunk by
+  // chunk every warp dequantises its 16 keys and arrives on that chunk's
+  // mbarrier (8 arrivals complete it)
   if (!window_cta) {
     for (int i = tid; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS) {
       const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
       if (sm.kvalid[s] == 1) {
-        const int32_t id = p.sel[(int64_t)bq * p.K + slot0 + s];
-        const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES + part * 16;
+        const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + sm.kid[s]) * MAIN_BYTES + part * 16;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                     :: "r"(tc::smem_u32(scr + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
+                     :: "r"(tc::smem_u32(stage + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
       }
     }
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    const int c = warp;
-    unsigned char* rowp = kbuf + c * AT_CHUNK_BYTES;
-    for (int s = lane; s < AT_KEYS; s += 32) {
-      if (sm.kvalid[s] == 1) {
-        const unsigned char* ent = scr + s * MAIN_BYTES;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(ent + c * 32);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(ent + c * 32 + 16);
-        const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(ent + 256 + c * 4);
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const int s = warp * 16 + (lane >> 1), hf = lane & 1;
+    uint4 code[8], scl = make_uint4(0u, 0u, 0u, 0u);     // masked keys: +0 codes, scale 0 -> zero rows
 #pragma unroll
-        for (int g = 0; g < 4; g++) {                      // 16 channels per E4M3 scale
-          const float sc = e4m3_value((sc4 >> (8 * g)) & 255u);
-          const uint32_t sc2 = pack_bf16x2(sc, sc);
-          uint32_t o[8];
+    for (int k = 0; k < 8; k++) code[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (sm.kvalid[s] == 1) {
+      const uint4* ent = reinterpret_cast<const uint4*>(stage + s * MAIN_BYTES);
 #pragma unroll
-          for (int k = 0; k < 8; k++) {
-            const uint32_t byte = (cw[2 * g + (k >> 2)] >> (8 * (k & 3))) & 255u;
-            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(sm.lut[byte]), "r"(sc2));
-          }
-          *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u + 16u)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; u++)
-          *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)u * 16u)) = make_uint4(0, 0, 0, 0);
-      }
+      for (int k = 0; k < 8; k++) code[k] = ent[hf * 8 + k];
+      scl = ent[16 + hf];
     }
     tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::bar_arrive(&sm.bar_chunk[c]);
+    __syncthreads();                                       // the staging buffer is free
+    if (tid == 0) {
+      for (int c = 4; c < 8; c++) {
+        tc::bar_arrive_expect_tx(&sm.bar_q[c], (uint32_t)AT_QCHUNK_BYTES);
+        tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q[c]);
+      }
+    }
+    const uint32_t scw[4] = {scl.x, scl.y, scl.z, scl.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      unsigned char* rowp = kbuf + (4 * hf + i) * AT_CHUNK_BYTES;
+      const uint32_t cw[8] = {code[2 * i].x, code[2 * i].y, code[2 * i].z, code[2 * i].w,
+                              code[2 * i + 1].x, code[2 * i + 1].y, code[2 * i + 1].z, code[2 * i + 1].w};
+#pragma unroll
+      for (int g = 0; g < 4; g++) {                      // 16 channels per E4M3 scale
+        const float sc = e4m3_value((scw[i] >> (8 * g)) & 255u);
+        const uint32_t sc2 = pack_bf16x2(sc, sc);
+        uint32_t o[8];
+        e2m1x8_to_bf16(cw[2 * g], o);
+        e2m1x8_to_bf16(cw[2 * g + 1], o + 4);
+#pragma unroll
+        for (int k = 0; k < 8; k++) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(o[k]), "r"(sc2));
+        *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u + 16u)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {                                   // chunks i (lanes h = 0) and 4 + i (h = 1)
+        tc::bar_arrive(&sm.bar_chunk[i]);
+        tc::bar_arrive(&sm.bar_chunk[4 + i]);
+      }
+    }
   } else if (p.S == 0) {                                   // no window rows supplied: zero keys
     for (int i = tid; i < 8 * AT_CHUNK_BYTES / 16; i += AT_THREADS)
       reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0, 0, 0, 0);
@@ -222,108 +272,101 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     __syncthreads();
   }
 
-  // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims); the
-  // issuing thread also refills Q stages 0 and 1 with chunks 6 and 7
+  // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims)
   if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
     if (window_cta) at_wait(&sm.bar_kv, 0, sm, p.hdr, 11);
-    for (int c = 0; c < 8; c++) {
-      const int s = c % AT_QSTAGES;
+    for (int cc = 0; cc < 8; cc++) {                     // Q chunks 4..7 arrive last
+      const int c = cc;
       if (!window_cta && !at_wait(&sm.bar_chunk[c], 0, sm, p.hdr, 16)) break;
-      if (!at_wait(&sm.bar_q[s], (c / AT_QSTAGES) & 1, sm, p.hdr, 12)) break;
+      if (!at_wait(&sm.bar_q[c], 0, sm, p.hdr, 12)) break;
       tc::fence_after_sync();
-      const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + s * 8192);
+      const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + c * AT_QCHUNK_BYTES);
 #pragma unroll
       for (int ks = 0; ks < 4; ks++)
         tc::mma_bf16(tmem, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
-                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c | ks) ? 1u : 0u);
-      tc::commit(&sm.bar_qe[s]);
-      if (c == 2 || c == 3) {              // stage c-2 is free once chunk c-2's MMAs finished
-        const int r = c - 2;
-        if (!at_wait(&sm.bar_qe[r], 0, sm, p.hdr, 10)) break;
-        tc::bar_arrive_expect_tx(&sm.bar_q[r], 8192u);
-        tc::tma_load_2d(qbuf + r * 8192, &map_q, (r + AT_QSTAGES) * 64, bq * H, &sm.bar_q[r]);
-      }
+                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (cc | ks) ? 1u : 0u);
     }
     tc::commit(&sm.bar_s);
   }
   __syncwarp();
 
-  // ---------------- S^T from TMEM -> scaled, masked, transposed into smem
+  // ---------------- softmax straight from TMEM: warp w holds keys 32(w&3) .. +31 (one
+  // per lane) and heads 32(w>>2) .. +31 (one per register)
   at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
   tc::fence_after_sync();
   {
     const int q4 = warp & 3, half = warp >> 2;
     const int m = q4 * 32 + lane;                   // key row
-    float v[32];
-    tc::tmem_ld_x32(tmem + ((uint32_t)(q4 * 32) << 16) + half * 32, v);
+    const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + half * 32;
     const bool valid = sm.kvalid[m] != 0;
+    float v[32], r[32];
+    tc::tmem_ld_x32(taddr, v);
 #pragma unroll
-    for (int j = 0; j < 32; j++) st[(half * 32 + j) * AT_ST_ROW + m] = valid ? v[j] * p.scale : -INFINITY;
-  }
-  __syncthreads();
-  // row maxima of this CTA (warp w: heads 8w .. 8w+7)
+    for (int j = 0; j < 32; j++) r[j] = v[j] = valid ? v[j] * p.scale : -INFINITY;
+    // transpose-reduction: afterwards lane l holds the maximum of column l over the warp's keys
 #pragma unroll
-  for (int i = 0; i < 8; i++) {
-    const int h = warp * 8 + i;
-    float mx = -INFINITY;
+    for (int k = 16; k >= 1; k >>= 1) {
+      const bool upper = (lane & k) != 0;
 #pragma unroll
-    for (int j = 0; j < 4; j++) mx = fmaxf(mx, st[h * AT_ST_ROW + lane + 32 * j]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-    if (lane == 0) sm.loc_max[h] = mx;
-  }
-  cluster.sync();                                          // #1: maxima visible
-  if (tid < H) {
-    float gm = -INFINITY;
-    for (int c = 0; c < C; c++) gm = fmaxf(gm, cluster.map_shared_rank(sm.loc_max, c)[tid]);
-    sm.gmax[tid] = (gm == -INFINITY) ? 0.f : gm;
-  }
-  __syncthreads();
-  float pv[8][4];
-  float lsum[8];
-#pragma unroll
-  for (int i = 0; i < 8; i++) {
-    const int h = warp * 8 + i;
-    const float gm = sm.gmax[h];
-    float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; j++) {                 // keys 2*lane, 2*lane+1, 64+2*lane, 65+2*lane
-      const int k = (j >> 1) * 64 + 2 * lane + (j & 1);
-      const float s_ = st[h * AT_ST_ROW + k];
-      const float e = (s_ == -INFINITY) ? 0.f : __expf(s_ - gm);
-      pv[i][j] = e;
-      sum += e;
+      for (int i = 0; i < k; i++) {
+        const float send = upper ? r[i] : r[i + k];
+        const float keep = upper ? r[i + k] : r[i];
+        r[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, k));
+      }
     }
+    sm.red[q4][half * 32 + lane] = r[0];
+    __syncthreads();
+    float mx[32];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-    lsum[i] = sum;
+    for (int j = 0; j < 32; j++) {
+      const int h = half * 32 + j;
+      mx[j] = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]), fmaxf(sm.red[2][h], sm.red[3][h]));
+    }
+    if (tid < H) sm.ml[tid] = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
+    __syncthreads();                                 // every thread has read the maxima
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 32; j++) {
+      r[j] = (v[j] == -INFINITY) ? 0.f : __expf(v[j] - mx[j]);
+      if (j & 1) pk[j >> 1] = pack_bf16x2(r[j - 1], r[j]);
+    }
+    // P^T row m (heads 32 half .. +31 = 16-byte units 4 half .. 4 half + 3), SW128
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+      *reinterpret_cast<uint4*>(pbuf + sw128((uint32_t)m, (uint32_t)(half * 64 + u * 16))) =
+          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+    tc::fence_proxy_async_smem();                    // P^T is read by the tensor cores
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) {
+      const bool upper = (lane & k) != 0;
+#pragma unroll
+      for (int i = 0; i < k; i++) {
+        const float send = upper ? r[i] : r[i + k];
+        const float keep = upper ? r[i + k] : r[i];
+        r[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, k);
+      }
+    }
+    sm.red[q4][half * 32 + lane] = r[0];
+    tc::fence_before_sync();
+    __syncthreads();                                 // P^T complete, every warp's column sums visible
+    tc::fence_after_sync();
+    if (tid < H) {
+      const float sum = sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
+      sm.ml[H + tid] = sum;
+      sm.inv_l[tid] = sum > 0.f ? 1.0f / sum : 0.f;
+    }
   }
-  __syncthreads();                                         // every read of S^T is done: P overwrites it
-#pragma unroll
-  for (int i = 0; i < 8; i++) {
-    const int h = warp * 8 + i;
-    if (lane == 0) sm.loc_sum[h] = lsum[i];
-#pragma unroll
-    for (int blk = 0; blk < 2; blk++)
-      *reinterpret_cast<uint32_t*>(scr + blk * 8192 + sw128((uint32_t)h, (uint32_t)(4 * lane))) =
-          pack_bf16x2(pv[i][2 * blk], pv[i][2 * blk + 1]);
-  }
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-
   // ---------------- O^T = V^T P^T  (4 tiles of M = 128 dims, N = 64 heads, K = 128 keys)
   if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc_o = tc::idesc_bf16(128, H, 1, 0);
-    const uint32_t kb = tc::smem_u32(kbuf), pb = tc::smem_u32(scr);
+    constexpr uint32_t idesc_o = tc::idesc_bf16(128, H, 1, 1);
+    const uint32_t kb = tc::smem_u32(kbuf), pb = tc::smem_u32(pbuf);
     for (int tile = 0; tile < 4; tile++) {
 #pragma unroll
       for (int ks = 0; ks < AT_KEYS / 16; ks++) {
         const uint64_t ad = tc::smem_desc(kb + (2 * tile) * AT_CHUNK_BYTES + ks * 2048, AT_CHUNK_BYTES, 1024,
                                           tc::SW_128B);
-        const uint64_t bd = tc::smem_desc(pb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, tc::SW_128B);
+        const uint64_t bd = tc::smem_desc(pb + ks * 2048, 8192, 1024, tc::SW_128B);
         tc::mma_bf16(tmem + 64 + tile * 64, ad, bd, idesc_o, ks ? 1u : 0u);
       }
     }
@@ -331,8 +374,11 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   }
   __syncwarp();
   at_wait(&sm.bar_o, 0, sm, p.hdr, 14);
+  __syncthreads();                                         // 1 / L_c visible to every thread
   tc::fence_after_sync();
-  // this CTA's share O_c / L per tile as fp16 [dim][head], 16-byte units swizzled by dim
+  // S^T and P are dead, so this CTA's receive slots (over them) are free
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  // this CTA's share O_c / L_c per tile as fp16 [dim][head], 16-byte units swizzled by dim
   {
     const int q4 = warp & 3, half = warp >> 2;
     uint32_t ta[4][32];
@@ -360,8 +406,9 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int j = 8 * u + 2 * e;
-          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * (1.0f / AT_SHARE_DIV),
-                                               __uint_as_float(ta[tile][j + 1]) * (1.0f / AT_SHARE_DIV));
+          const int h = half * 32 + j;
+          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * sm.inv_l[h],
+                                               __uint_as_float(ta[tile][j + 1]) * sm.inv_l[h + 1]);
           w[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
         const int unit = (half * 4 + u) ^ (d & 7);
@@ -370,38 +417,59 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
   }
   tc::fence_proxy_async_smem();
-  cluster.sync();                                          // #2: shares staged, receive slots free, sums visible
-  if (tid < H) {
-    float L = 0.f;
-    for (int c = 0; c < C; c++) L += cluster.map_shared_rank(sm.loc_sum, c)[tid];
-    sm.inv_l[tid] = (L > 0.f) ? AT_SHARE_DIV / L : 0.f;
-  }
   __syncthreads();
-  // no remote shared-memory reads after this point: let the cluster go ahead
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every owner's slots are free
 
   // ---------------- cluster reduction: tile t is owned by CTA t % C; the others send
-  // their fp16 share into the owner's slot (j * (C - 1) + sender index)
+  // their fp16 share and (m, L) rows into the owner's slot (j * (C - 1) + sender index)
   int owned = 0;
   for (int tile = rank; tile < 4; tile += C) owned++;
   if (tid == 0) {
-    if (owned) tc::bar_arrive_expect_tx(&sm.bar_red, (uint32_t)(owned * (C - 1) * AT_SHARE_BYTES));
+    if (owned) tc::bar_arrive_expect_tx(&sm.bar_red, (uint32_t)(owned * (C - 1) * (AT_SHARE_BYTES + 2 * H * 4)));
     for (int tile = 0; tile < 4; tile++) {
       const int owner = tile % C;
       if (owner == rank) continue;
       const int j = tile / C;
       const int slot = j * (C - 1) + (rank < owner ? rank : rank - 1);
-      const uint32_t src = tc::smem_u32(ostage + tile * (128 * H));
-      uint32_t dst, rbar;
+      uint32_t dst, dml, rbar;
       asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(tc::smem_u32(orecv + slot * (128 * H))), "r"(owner));
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dml) : "r"(tc::smem_u32(sm.recv_ml[slot])), "r"(owner));
       asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(tc::smem_u32(&sm.bar_red)), "r"(owner));
       asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                   :: "r"(dst), "r"(src), "r"(AT_SHARE_BYTES), "r"(rbar) : "memory");
+                   :: "r"(dst), "r"(tc::smem_u32(ostage + tile * (128 * H))), "r"(AT_SHARE_BYTES), "r"(rbar) : "memory");
+      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                   :: "r"(dml), "r"(tc::smem_u32(sm.ml)), "r"(2 * H * 4), "r"(rbar) : "memory");
     }
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   }
   if (owned) {
     at_wait(&sm.bar_red, 0, sm, p.hdr, 15);
+    if (tid < H) {                             // weight of each CTA's share for head tid
+      float mc[AT_MAXC], lc[AT_MAXC];
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < AT_MAXC; c++) {
+        if (c >= C) break;
+        const float* src = c == rank ? sm.ml : sm.recv_ml[c < rank ? c : c - 1];
+        mc[c] = src[tid];
+        lc[c] = src[H + tid];
+        if (lc[c] > 0.f) M = fmaxf(M, mc[c]);
+      }
+      float den = 0.f;
+#pragma unroll
+      for (int c = 0; c < AT_MAXC; c++) {
+        if (c >= C) break;
+        lc[c] = lc[c] > 0.f ? lc[c] * __expf(mc[c] - M) : 0.f;
+        den += lc[c];
+      }
+      const float inv = den > 0.f ? 1.0f / den : 0.f;
+#pragma unroll
+      for (int c = 0; c < AT_MAXC; c++) {
+        if (c >= C) break;
+        sm.wgt[c][tid] = lc[c] * inv;
+      }
+    }
+    __syncthreads();
     uint16_t* out = p.out + (int64_t)bq * H * D;
     int j = 0;
     for (int tile = rank; tile < 4; tile += C, j++) {
@@ -416,30 +484,31 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const float2 f = __half22float2(h2[e]);
-            acc[2 * e] = f.x;
-            acc[2 * e + 1] = f.y;
+            acc[2 * e] = f.x * sm.wgt[rank][u * 8 + 2 * e];
+            acc[2 * e + 1] = f.y * sm.wgt[rank][u * 8 + 2 * e + 1];
           }
         }
         for (int r = 0; r < C - 1; r++) {
+          const int sender = r < rank ? r : r + 1;
           const uint4 v = *reinterpret_cast<const uint4*>(orecv + (j * (C - 1) + r) * (128 * H) + off);
           const __half2* h2 = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const float2 f = __half22float2(h2[e]);
-            acc[2 * e] += f.x;
-            acc[2 * e + 1] += f.y;
+            acc[2 * e] = fmaf(f.x, sm.wgt[sender][u * 8 + 2 * e], acc[2 * e]);
+            acc[2 * e + 1] = fmaf(f.y, sm.wgt[sender][u * 8 + 2 * e + 1], acc[2 * e + 1]);
           }
         }
         uint16_t* o = out + (u * 8) * D + tile * 128 + d;
 #pragma unroll
-        for (int e = 0; e < 8; e++)
-          o[e * D] = (uint16_t)(pack_bf16x2(acc[e] * sm.inv_l[u * 8 + e], 0.f) & 0xFFFFu);
+        for (int e = 0; e < 8; e++) o[e * D] = (uint16_t)(pack_bf16x2(acc[e], 0.f) & 0xFFFFu);
       }
     }
   }
   if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   tc::fence_before_sync();
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every CTA done reading ours
+  // no CTA leaves while a share it sent may still be read, or one it owns still arrive
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, AT_TMEM_COLS);
