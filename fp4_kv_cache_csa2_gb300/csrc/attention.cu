@@ -18,10 +18,12 @@
 //     buffer (consecutive threads take consecutive pieces of an entry), from
 //     there into registers, two lanes per entry, after which Q chunks 4..7 are
 //     loaded over the staging buffer; every warp then dequantises its 16 keys
-//     exactly, chunk by chunk (E2M1 -> bf16 by byte permutes, times the E4M3
-//     scale; the product has at most 6 significant bits);
+//     exactly (E2M1 -> bf16 by byte permutes, times the E4M3 scale; the
+//     product has at most 6 significant bits);
 //   * S^T = K Q^T is one M=128 (keys) x N=64 (heads) x K=512 tcgen05 bf16 MMA
-//     chain into TMEM, issued chunk by chunk as the dequantisation finishes;
+//     chain into TMEM, issued back to back once keys and Q are in place (an
+//     mbarrier wait between MMAs of the issuing thread costs more than the
+//     overlap with the dequantisation would gain);
 //   * softmax over this CTA's keys with its own row maxima m_c, straight from
 //     TMEM (thread = key, 32 heads in registers; per-warp column maxima and
 //     sums by transpose-reductions over the lanes): P = exp(S - m_c) becomes
@@ -73,7 +75,7 @@ struct AtSmall {
   float wgt[AT_MAXC][H];                 // combination weight of each CTA's share, per head
   uint64_t bar_kv, bar_s, bar_o, bar_red;
   uint64_t bar_q[8];
-  uint64_t bar_chunk[8];                 // chunk c of the keys is in shared memory (bf16, SW128)
+  uint64_t bar_keys;                     // every warp's dequantised keys are in shared memory
   uint32_t tmem_base;
   int err;
 };
@@ -126,6 +128,7 @@ __device__ __forceinline__ bool at_wait(uint64_t* bar, uint32_t parity, AtSmall&
   return false;
 }
 
+
 __global__ void __launch_bounds__(AT_THREADS, 1)
 attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_swa,
                int C) {
@@ -155,10 +158,8 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::bar_init(&sm.bar_s, 1);
     tc::bar_init(&sm.bar_o, 1);
     tc::bar_init(&sm.bar_red, 1);
-    for (int i = 0; i < 8; i++) {
-      tc::bar_init(&sm.bar_q[i], 1);
-      tc::bar_init(&sm.bar_chunk[i], AT_THREADS / 32);
-    }
+    for (int i = 0; i < 8; i++) tc::bar_init(&sm.bar_q[i], 1);
+    tc::bar_init(&sm.bar_keys, AT_THREADS / 32);
     sm.err = 0;
     tc::bar_init_fence();
   }
@@ -208,9 +209,8 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   // ---------------- keys: FP4 entries by 16-byte asynchronous copies into the
   // staging buffer; lanes 2k and 2k+1 of warp w then take the halves of entry
   // 16w + k (128 code bytes = dims 256h .. 256h+255, and their 16 scale bytes)
-  // into registers, the staging buffer receives Q chunks 4..7, and chunk by
-  // chunk every warp dequantises its 16 keys and arrives on that chunk's
-  // mbarrier (8 arrivals complete it)
+  // into registers, the staging buffer receives Q chunks 4..7, and every warp
+  // dequantises its 16 keys and arrives on bar_keys (8 arrivals complete it)
   if (!window_cta) {
     for (int i = tid; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS) {
       const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
@@ -258,13 +258,10 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
         *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u + 16u)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {                                   // chunks i (lanes h = 0) and 4 + i (h = 1)
-        tc::bar_arrive(&sm.bar_chunk[i]);
-        tc::bar_arrive(&sm.bar_chunk[4 + i]);
-      }
     }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(&sm.bar_keys);
   } else if (p.S == 0) {                                   // no window rows supplied: zero keys
     for (int i = tid; i < 8 * AT_CHUNK_BYTES / 16; i += AT_THREADS)
       reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0, 0, 0, 0);
@@ -275,17 +272,15 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims)
   if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
-    if (window_cta) at_wait(&sm.bar_kv, 0, sm, p.hdr, 11);
-    for (int cc = 0; cc < 8; cc++) {                     // Q chunks 4..7 arrive last
-      const int c = cc;
-      if (!window_cta && !at_wait(&sm.bar_chunk[c], 0, sm, p.hdr, 16)) break;
-      if (!at_wait(&sm.bar_q[c], 0, sm, p.hdr, 12)) break;
-      tc::fence_after_sync();
+    bool ok = at_wait(window_cta ? &sm.bar_kv : &sm.bar_keys, 0, sm, p.hdr, window_cta ? 11 : 16);
+    for (int c = 0; c < 8 && ok; c++) ok = at_wait(&sm.bar_q[c], 0, sm, p.hdr, 12);
+    tc::fence_after_sync();
+    for (int c = 0; c < 8 && ok; c++) {
       const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + c * AT_QCHUNK_BYTES);
 #pragma unroll
       for (int ks = 0; ks < 4; ks++)
         tc::mma_bf16(tmem, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
-                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (cc | ks) ? 1u : 0u);
+                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c | ks) ? 1u : 0u);
     }
     tc::commit(&sm.bar_s);
   }

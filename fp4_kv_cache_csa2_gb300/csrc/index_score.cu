@@ -423,25 +423,31 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
           tc::bulk_load(scl, p.idx_scales + row0 * IDX_SCALE_BYTES, sbytes, &sm.full[s]);
         }
       } else {
-        // 16 candidate blocks of 8 entries; lanes 2b and 2b+1 copy block b: four
-        // 64-byte code rows each into the SW64 layout and 16 of its 32 bytes of
-        // scale words.  Each lane's arrival fires once its own copies have landed.
-        const int sb = lane >> 1, half = lane & 1;
-        const int64_t pi = t * 16 + sb;
-        const int32_t blk = (pi < p.M) ? sm.pool[pi] : -1;
-        if (blk >= 0 && (int64_t)blk * BLK < p.cap) {                   // otherwise reported by the epilogue
-          const int64_t row0 = row_base + (int64_t)blk * BLK;
-          const uint8_t* src = p.idx_codes + (row0 + half * 4) * IDX_CODE_BYTES;
-#pragma unroll
-          for (int k = 0; k < 16; k++) {
-            const int trow = sb * BLK + half * 4 + (k >> 2), c = k & 3;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                         :: "r"(tc::smem_u32(codes + trow * 64 + ((c ^ ((trow >> 1) & 3)) * 16))), "l"(src + k * 16)
-                         : "memory");
-          }
+        // 16 candidate blocks of 8 entries.  One warp instruction copies one whole
+        // block (512 contiguous code bytes, 16 per lane: entry l/4, 16-byte chunk
+        // l%4) into the SW64 layout, so each instruction touches 4 cache lines;
+        // lanes 2b and 2b+1 then copy block b's 32 bytes of scale words.  Each
+        // lane's arrival fires once its own copies have landed.
+        const int64_t pl = t * 16 + (lane & 15);
+        int32_t my_blk = (pl < p.M) ? sm.pool[pl] : -1;
+        if (my_blk >= 0 && (int64_t)my_blk * BLK >= p.cap) my_blk = -1;   // reported by the epilogue
+        const int r = lane >> 2, c = lane & 3;
+#pragma unroll 4
+        for (int sb = 0; sb < 16; sb++) {
+          const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, sb);
+          if (blk < 0) continue;
+          const int trow = sb * BLK + r;
+          const uint8_t* src = p.idx_codes + (row_base + (int64_t)blk * BLK) * IDX_CODE_BYTES + lane * 16;
           asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                       :: "r"(tc::smem_u32(scl + sb * 32 + half * 16)),
-                          "l"(p.idx_scales + row0 * IDX_SCALE_BYTES + half * 16) : "memory");
+                       :: "r"(tc::smem_u32(codes + trow * 64 + ((c ^ ((trow >> 1) & 3)) * 16))), "l"(src) : "memory");
+        }
+        {
+          const int sb = lane >> 1, half = lane & 1;
+          const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, sb);
+          if (blk >= 0)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                         :: "r"(tc::smem_u32(scl + sb * 32 + half * 16)),
+                            "l"(p.idx_scales + (row_base + (int64_t)blk * BLK) * IDX_SCALE_BYTES + half * 16) : "memory");
         }
         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(tc::smem_u32(&sm.full[s])) : "memory");
       }
