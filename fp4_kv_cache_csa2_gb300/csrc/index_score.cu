@@ -11,8 +11,9 @@
 //   warp 0      producer: full scans load 128-entry tiles of index-K codes
 //               (SW64 K-major, 64 B per entry) with a 2-D tensor map and the
 //               4-byte E8M0 words with 1-D bulk copies (mbarrier expect-tx); pool
-//               scans gather the 16 candidate blocks of a tile with cp.async, two
-//               lanes per 8-entry block, into the same layout.  6-stage ring.
+//               scans gather the 16 candidate blocks of a tile with cp.async,
+//               one 512-byte block per warp instruction, into the same layout.
+//               6-stage ring.
 //   warp 1      TMEM owner and MMA issuer: per tile two M=128 N=32 K=64
 //               block-scaled MMAs into one of two TMEM accumulators.
 //   warps 2..5  per tile: copy the 128 scale words into TMEM (row m -> lane m,
@@ -21,18 +22,10 @@
 // The query is quantised once per CTA (the B operand, 2 KB, and its scales).
 // Products of E2M1 values scaled by powers of two are exact; the accumulation
 // is fp32.  Every mbarrier wait is bounded and reports CSA2_ERR_TIMEOUT.
-//
-// Fused Reindex variant (REINDEX_SELECT = true): one cluster of 8 CTAs per
-// query scores the candidate pool (each CTA a contiguous eighth of it) into
-// shared memory as order-preserving keys, then the cluster runs one exact radix
-// select over all of them: four 8-bit digit passes, each CTA publishing its
-// digit histogram in shared memory and every CTA summing the eight histograms
-// over distributed shared memory, so that all CTAs agree on the threshold
-// without a second kernel; a last exchange of per-CTA counts places every
-// CTA's chosen entries in the output in pool-slot order.
 #include <cstddef>
 #include <cudaTypedefs.h>
 
+#include "index_query.cuh"
 #include "params.cuh"
 #include "tc.cuh"
 
@@ -63,217 +56,6 @@ struct IsSmem {
 };
 constexpr size_t IS_SMEM = sizeof(IsSmem) + 1024;
 
-constexpr int FUSE_CL = 8;                                   // CTAs per query in the fused Reindex kernel
-constexpr int FUSE_SLOTS = CSA2_MAX_M * BLK / FUSE_CL;       // pool slots per CTA at most (2048)
-constexpr int IS_WARPS = IS_THREADS / 32;
-
-struct alignas(128) FuseSmem {
-  uint32_t keys[FUSE_SLOTS];                 // this CTA's slot keys; 0 = outside the search domain
-  uint32_t hist[2][256];                     // this CTA's digit histogram (double buffered), read by the cluster
-  uint32_t whist[IS_WARPS][256];
-  int32_t cnt[2];                            // this CTA's (above threshold, equal to it) counts, read by the cluster
-  int32_t wsum[IS_WARPS];
-  int32_t bcast[4];
-};
-// FuseSmem starts at the first 128-byte boundary after IsSmem (16-byte
-// distributed-shared-memory loads read its histograms).
-constexpr size_t FUSE_OFF = (sizeof(IsSmem) + 127) / 128 * 128;
-constexpr size_t FUSE_SMEM = FUSE_OFF + sizeof(FuseSmem) + 1024;
-static_assert(offsetof(FuseSmem, hist) % 16 == 0, "histograms are read 16 bytes at a time");
-
-// Exclusive prefix sum over the CTA (IS_THREADS threads); *total receives the sum.
-__device__ int cta_exclusive_scan(int v, FuseSmem& fs, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) fs.wsum[warp] = x;
-  __syncthreads();
-  int base = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < IS_WARPS; w++) {
-    const int ws = fs.wsum[w];
-    base += (w < warp) ? ws : 0;
-    tot += ws;
-  }
-  __syncthreads();
-  *total = tot;
-  return base + x - v;
-}
-
-// Four consecutive words of CTA `rank`'s copy of the shared variable at `local`.
-__device__ __forceinline__ uint4 cluster_ld4(const uint32_t* local, int rank) {
-  uint32_t a;
-  uint4 v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(tc::smem_u32(local)), "r"(rank));
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
-// Top-K over the keys of every CTA of the cluster (key 0 = not a candidate) by
-// (key desc, slot asc), where CTA r's keys[0..n) are slots that follow those of
-// CTAs 0..r-1.  Exact radix select over four 8-bit digits: every CTA builds its
-// histogram of the digit (per-warp, warp-aggregated with match_any), the
-// cluster sums the eight histograms, and every CTA derives the same digit of
-// the threshold and the same number of ties still to take.  Then each CTA
-// counts its keys above the threshold and equal to it, the counts are
-// exchanged, and CTA r calls out(i, rank) for its chosen keys, ranks following
-// those of CTAs 0..r-1 (ties taken in slot order).  Returns the cluster total.
-template <class Out>
-__device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, FuseSmem& fs, Out out) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int remaining = K;
-  for (int pass = 0; pass < 4; pass++) {
-    const int shift = 24 - 8 * pass, buf = pass & 1;
-    for (int i = lane; i < 256; i += 32) fs.whist[warp][i] = 0;
-    __syncwarp();
-    for (int base = 0; base < n; base += IS_THREADS) {     // uniform trip count for match_any
-      const int i = base + tid;
-      const uint32_t k = (i < n) ? keys[i] : 0u;
-      const bool ok = k != 0u && (k & mask) == prefix;
-      const uint32_t digit = ok ? ((k >> shift) & 255u) : 256u;
-      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, digit);
-      if (ok && lane == __ffs(peers) - 1) atomicAdd(&fs.whist[warp][digit], (uint32_t)__popc(peers));
-    }
-    __syncthreads();
-    for (int i = tid; i < 256; i += IS_THREADS) {
-      uint32_t t = 0;
-#pragma unroll
-      for (int w = 0; w < IS_WARPS; w++) t += fs.whist[w][i];
-      fs.hist[buf][i] = t;
-    }
-    // every CTA's histogram of this pass is final; the other buffer was read by
-    // all CTAs before they arrived here
-    cluster_arrive();
-    cluster_wait();
-    if (tid < 64) {
-      uint4 t = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int r = 0; r < FUSE_CL; r++) {
-        const uint4 v = cluster_ld4(&fs.hist[buf][4 * tid], r);
-        t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
-      }
-      // the cluster-wide histogram replaces this CTA's per-warp one (warp 0 row)
-      *reinterpret_cast<uint4*>(&fs.whist[0][4 * tid]) = t;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t c[8], sum = 0;
-#pragma unroll
-      for (int q = 0; q < 8; q++) { c[q] = fs.whist[0][255 - 8 * lane - q]; sum += c[q]; }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      if (total <= (uint32_t)remaining && pass == 0) {
-        if (lane == 0) fs.bcast[0] = -1;                   // at most K candidates: take them all
-      } else {
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= (uint32_t)remaining);
-        const int owner = __ffs(hit) - 1;
-        if (lane == owner) {
-          int cum = (int)(incl - sum);
-          int d = 255 - 8 * lane;
-#pragma unroll
-          for (int q = 0; q < 8; q++) {
-            if (cum + (int)c[q] >= remaining) { d = 255 - 8 * lane - q; break; }
-            cum += (int)c[q];
-          }
-          fs.bcast[0] = d;
-          fs.bcast[1] = remaining - cum;
-        }
-      }
-    }
-    __syncthreads();
-    const int d = fs.bcast[0];
-    if (d < 0) {                                           // threshold 0: every valid key is above it
-      prefix = 0;
-      remaining = 0;
-      break;
-    }
-    prefix |= (uint32_t)d << shift;
-    mask |= 255u << shift;
-    remaining = fs.bcast[1];
-  }
-  const uint32_t thr = prefix;
-  const int take_eq = remaining;                           // keys equal to thr still to take, in slot order
-
-  const int chunk = (n + IS_THREADS - 1) / IS_THREADS;
-  const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
-  int gt = 0, eq = 0;
-  for (int i = i0; i < i1; i++) {
-    const uint32_t k = keys[i];
-    if (k == 0u) continue;
-    if (k > thr) gt++;
-    else if (k == thr) eq++;
-  }
-  int gt_tot, eq_tot;
-  const int gt_before = cta_exclusive_scan(gt, fs, &gt_tot);
-  const int eq_before = cta_exclusive_scan(eq, fs, &eq_tot);
-  if (tid == 0) {
-    fs.cnt[0] = gt_tot;
-    fs.cnt[1] = eq_tot;
-  }
-  cluster_arrive();
-  cluster_wait();
-  if (warp == 0) {
-    // lane r < 8 holds CTA r's counts; ties go to the lowest CTAs first
-    int g = 0, e = 0;
-    if (lane < FUSE_CL) {
-      uint32_t a;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(tc::smem_u32(&fs.cnt[0])), "r"(lane));
-      asm volatile("ld.shared::cluster.v2.s32 {%0, %1}, [%2];" : "=r"(g), "=r"(e) : "r"(a) : "memory");
-    }
-    int e_incl = e;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, e_incl, off);
-      if (lane >= off) e_incl += y;
-    }
-    const int budget = max(0, take_eq - (e_incl - e));     // ties this CTA may still take
-    const int taken = min(e, budget);
-    int t_incl = g + taken;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, t_incl, off);
-      if (lane >= off) t_incl += y;
-    }
-    const int my_base = __shfl_sync(0xFFFFFFFFu, t_incl - g - taken, crank);
-    const int my_budget = __shfl_sync(0xFFFFFFFFu, budget, crank);
-    const int total = __shfl_sync(0xFFFFFFFFu, t_incl, 31);
-    if (lane == 0) {
-      fs.bcast[0] = my_base;
-      fs.bcast[1] = my_budget;
-      fs.bcast[2] = total;
-    }
-  }
-  cluster_arrive();                                        // this CTA is done reading the others
-  __syncthreads();
-  const int my_base = fs.bcast[0], my_budget = fs.bcast[1], total = fs.bcast[2];
-  const int mine_eq = max(0, min(eq, my_budget - eq_before));
-  int r = my_base + gt_before + min(eq_before, my_budget);
-  int used = 0;
-  for (int i = i0; i < i1; i++) {
-    const uint32_t k = keys[i];
-    if (k == 0u) continue;
-    bool take = k > thr;
-    if (!take && k == thr && used < mine_eq) { take = true; used++; }
-    if (take) out(i, r++);
-  }
-  cluster_wait();                                          // no CTA leaves while others read its counts
-  return total;
-}
-
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, IsSmem& sm, WsHeader* hdr) {
   if (sm.abort_flag) return false;
   for (int round = 0; round < 64; round++) {
@@ -285,18 +67,16 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Is
   return false;
 }
 
-template <bool REINDEX_SELECT>
 __global__ void __launch_bounds__(IS_THREADS, 1)
 index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
                       const __grid_constant__ CUtensorMap map_block) {
   extern __shared__ unsigned char smem_raw[];
   IsSmem& sm = *reinterpret_cast<IsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  FuseSmem& fs = *reinterpret_cast<FuseSmem*>(reinterpret_cast<unsigned char*>(&sm) + FUSE_OFF);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bq = REINDEX_SELECT ? (int)(blockIdx.x / FUSE_CL) : (int)blockIdx.y;
-  const int crank = REINDEX_SELECT ? (int)(blockIdx.x % FUSE_CL) : (int)blockIdx.x;   // slice of the query
+  const int bq = (int)blockIdx.y;
+  const int crank = (int)blockIdx.x;         // slice of the query
   const int b = bq / p.Q;
-  const bool pool_mode = REINDEX_SELECT || p.pool != nullptr;
+  const bool pool_mode = p.pool != nullptr;
 
   // ---- this CTA's tile range
   int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[b]);
@@ -319,8 +99,7 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
   int64_t t1 = t0 + p.entries_per_cta;
   if (t1 > n_tiles) t1 = n_tiles;
   const int n = (int)(t1 > t0 ? t1 - t0 : 0);
-  if (n == 0 && !REINDEX_SELECT) return;     // the fused kernel still joins its cluster
-  if (n > 0) {
+  if (n == 0) return;
 
   // ---- set-up
   if (warp == 1) tc::tmem_alloc(&sm.tmem_base, IS_TMEM_COLS);
@@ -354,42 +133,7 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
   // ---- quantise the query (B operand); its scale words go to TMEM lanes
   // 32q + n of every lane quarter q (the MMA reads B scales from the quarter of
   // the A row it is computing)
-  if (warp == 4) {
-    const uint16_t* qh = p.q_idx + ((int64_t)bq * HI + lane) * DI;
-    uint32_t sfw = 0;
-#pragma unroll 1
-    for (int kb = 0; kb < 4; kb++) {
-      float v[32];
-#pragma unroll
-      for (int c = 0; c < 4; c++) {
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(qh + kb * 32) + c);
-        uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          v[c * 8 + 2 * e] = bf16_bits_to_f32(w4[e] & 0xFFFFu);
-          v[c * 8 + 2 * e + 1] = bf16_bits_to_f32(w4[e] >> 16);
-        }
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(v[i]));
-      uint32_t sb = 0, packed[4] = {0u, 0u, 0u, 0u};
-      if (amax != 0.0f) {
-        int X = (int)((__float_as_uint(amax) >> 23) & 255u) - 127 - 2;
-        if (X < -127) X = -127;
-        if (X > 127) X = 127;
-        sb = (uint32_t)(X + 127);
-        const float inv = __uint_as_float((uint32_t)(127 - X) << 23);
-#pragma unroll
-        for (int k = 0; k < 16; k++)
-          packed[k / 4] |= e2m1x2(__fmul_rn(v[2 * k], inv), __fmul_rn(v[2 * k + 1], inv)) << (8 * (k % 4));
-      }
-      sfw |= sb << (8 * kb);
-      const int phys = lane * 64 + ((kb ^ ((lane >> 1) & 3)) * 16);      // SW64 swizzle of row `lane`
-      *reinterpret_cast<uint4*>(sm.qcodes + phys) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    }
-    sm.sfb[lane] = sfw;
-  }
+  if (warp == 4) quantize_index_query_warp(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
   tc::fence_proxy_async_smem();
   __syncthreads();
   if (warp >= 2) {
@@ -524,8 +268,7 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
               }
             }
           }
-          if (REINDEX_SELECT) fs.keys[j * IS_TILE + m] = ok ? float_key(sc) : 0u;
-          else if (u < n_units) out_row[u] = ok ? sc : -INFINITY;
+          if (u < n_units) out_row[u] = ok ? sc : -INFINITY;
         }
       }
     }
@@ -536,20 +279,6 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, IS_TMEM_COLS);
-  }
-  }  // n > 0
-
-  if constexpr (REINDEX_SELECT) {
-    // ---- exact top-K over the whole pool, across the cluster
-    const int64_t slot_base = t0 * IS_TILE;
-    int32_t* sel = p.sel + (int64_t)bq * p.K;
-    __syncthreads();
-    const int ns = cluster_select(fs.keys, n * IS_TILE, p.K, crank, fs, [&](int i, int r) {
-      const int64_t u = slot_base + i;
-      sel[r] = sm.pool[u / BLK] * BLK + (int)(u % BLK);
-    });
-    if (crank == FUSE_CL - 1)
-      for (int i = ns + tid; i < p.K; i += IS_THREADS) sel[i] = -1;
   }
 }
 
@@ -585,11 +314,8 @@ static cudaError_t set_is_attrs() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev == dev) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)IS_SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(index_score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)FUSE_SMEM);
   if (e == cudaSuccess) attr_dev = dev;
   return e;
 }
@@ -618,36 +344,9 @@ cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   const int64_t per = ceil_div(tiles, split);
   p.entries_per_cta = per;     // tiles per CTA
   dim3 grid((unsigned)ceil_div(tiles, per), (unsigned)BQ);
-  index_score_tc_kernel<false><<<grid, IS_THREADS, IS_SMEM, stream>>>(p, map_tile, map_block);
+  index_score_tc_kernel<<<grid, IS_THREADS, IS_SMEM, stream>>>(p, map_tile, map_block);
   return cudaGetLastError();
 }
 
 // Reindex: score the pool of every query and publish its top-K in one launch.
-cudaError_t launch_reindex_select(IsParams p, cudaStream_t stream) {
-  if (p.B == 0 || p.Q == 0) return cudaSuccess;
-  cudaError_t e = set_is_attrs();
-  if (e != cudaSuccess) return e;
-  const uint64_t rows = (uint64_t)p.B * (uint64_t)p.cap;
-  if (rows == 0) return cudaErrorInvalidValue;
-  CUtensorMap map_tile, map_block;
-  if (!encode_rows64(&map_tile, p.idx_codes, rows, IS_TILE) || !encode_rows64(&map_block, p.idx_codes, rows, BLK))
-    return cudaErrorInvalidValue;
-  const int64_t tiles = ceil_div((int64_t)p.M * BLK, IS_TILE);
-  p.entries_per_cta = ceil_div(tiles, FUSE_CL);     // tiles per CTA (<= 16)
-  const int64_t BQ = (int64_t)p.B * p.Q;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(BQ * FUSE_CL));
-  cfg.blockDim = dim3(IS_THREADS);
-  cfg.dynamicSmemBytes = FUSE_SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = FUSE_CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, index_score_tc_kernel<true>, p, map_tile, map_block);
-}
-
 }  // namespace csa2

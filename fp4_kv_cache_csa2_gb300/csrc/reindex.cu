@@ -1,0 +1,438 @@
+// (b) Fused Reindex layer: the lightning-indexer scores of the candidate pool
+// and the exact top-K over them, in one kernel with one thread-block cluster
+// per query token.
+//
+// Sources: "DeepSeek-V4.1 Flash: 把 KV Cache 压缩推到极致" §2.3.4 (a Reindex layer
+// scores only the entries of the candidate blocks its source layer chose and
+// keeps its own top-512), §2.4.4 (FP4 indexer Q and K); "4. 层维度(下):CSA2 与
+// 每 token 890 字节" §4.4 (index K is OCP MXFP4), §4.7 (hierarchical sparse
+// indexing).
+//
+// A cluster of 6 CTAs (256 threads each, one per SM) takes one query: six is
+// the largest cluster size for which 16 such clusters are resident at once on
+// 152 SMs.  CTA r scores a contiguous sixth of the pool slots (at most 22
+// tiles of 128 = 16 blocks of 8 entries each) in bulk-synchronous phases, with
+// no per-tile hand-offs:
+//   1. every warp copies whole tiles (one 512-byte block of index codes per
+//      warp instruction, into the SW64 K-major layout, plus the blocks' scale
+//      words) with cp.async; one warp also quantises the query to MXFP4;
+//   2. warps 0..3 store the E8M0 scale words of every tile (A operand) and of
+//      the query (B operand, replicated to every lane quarter) in TMEM;
+//   3. one thread issues the block-scaled MMAs (M = 128 entries, N = 32 heads,
+//      K = 128 as two K = 64 halves) for up to 8 tiles at a time into 8 TMEM
+//      accumulators; all warps then read them back (lane = entry, column =
+//      head) and form s = sum_h w_h ReLU(q_h . k), kept as an order-preserving
+//      key per pool slot (0 for slots outside the search domain);
+//   4. the cluster runs one exact radix select over all slot keys: four 8-bit
+//      digit passes, each CTA publishing its digit histogram in shared memory
+//      and every CTA summing the six histograms over distributed shared
+//      memory, so that all agree on the threshold; a last exchange of per-CTA
+//      counts places every CTA's chosen entries in pool-slot order.
+// Products of E2M1 values scaled by powers of two are exact; the accumulation
+// is fp32.  Ties go to the lower pool slot (= lower entry for an ascending
+// pool).  The MMA wait is bounded and reports CSA2_ERR_TIMEOUT.
+#include <cstddef>
+
+#include "index_query.cuh"
+#include "params.cuh"
+#include "tc.cuh"
+
+namespace csa2 {
+
+constexpr int RX_THREADS = 256;
+constexpr int RX_WARPS = RX_THREADS / 32;
+constexpr int RX_CL = 6;                                        // CTAs per query
+constexpr int RX_TILE = 128;                                    // pool slots per tile
+constexpr int RX_MAX_TILES = (CSA2_MAX_M * BLK / RX_TILE + RX_CL - 1) / RX_CL;   // 22
+constexpr int RX_ROUNDS = (RX_MAX_TILES + 7) / 8;
+constexpr int RX_CODES = RX_TILE * IDX_CODE_BYTES;              // 8192
+constexpr int RX_TILE_BYTES = RX_CODES + 1024;                  // codes + 512 B scale words, 1 KB stride
+constexpr int RX_ROUND = 8;                                     // TMEM accumulators per MMA round
+constexpr int RX_TMEM_COLS = 512;
+constexpr int RX_ACC_COL = 0;                                   // 8 accumulators of 32 columns
+constexpr int RX_SFA_COL = RX_ROUND * HI;                       // 4 columns per tile
+constexpr int RX_SFB_COL = RX_SFA_COL + 4 * RX_MAX_TILES;
+static_assert(RX_SFB_COL + 4 <= RX_TMEM_COLS, "TMEM columns");
+
+struct RxSmem {
+  uint8_t tile[RX_MAX_TILES][RX_TILE_BYTES];   // SW64 codes, then 128 scale words
+  uint8_t qcodes[HI * IDX_CODE_BYTES];          // 2 KB, SW64
+  int32_t pool[RX_MAX_TILES * 16];              // this CTA's blocks (-1: none)
+  float w[HI];
+  uint32_t sfb[HI];
+  uint32_t keys[RX_MAX_TILES * RX_TILE];        // slot keys; 0 = outside the search domain
+  alignas(16) uint32_t hist[2][256];            // this CTA's digit histogram (double buffered), read by the cluster
+  uint32_t whist[RX_WARPS][256];
+  alignas(8) int32_t cnt[2];                    // this CTA's (above threshold, equal to it) counts, read by the cluster
+  int32_t wsum[RX_WARPS];
+  int32_t bcast[4];
+  uint64_t mma_done[RX_ROUNDS];
+  uint32_t tmem_base;
+};
+constexpr size_t RX_SMEM = sizeof(RxSmem) + 1024;
+static_assert(RX_SMEM <= 227 * 1024, "shared memory");
+
+// Exclusive prefix sum over the CTA (RX_THREADS threads); *total receives the sum.
+__device__ int cta_exclusive_scan(int v, RxSmem& fs, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) fs.wsum[warp] = x;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < RX_WARPS; w++) {
+    const int ws = fs.wsum[w];
+    base += (w < warp) ? ws : 0;
+    tot += ws;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + x - v;
+}
+
+// Four consecutive words of CTA `rank`'s copy of the shared variable at `local`.
+__device__ __forceinline__ uint4 cluster_ld4(const uint32_t* local, int rank) {
+  uint32_t a;
+  uint4 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(tc::smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Top-K over the keys of every CTA of the cluster (key 0 = not a candidate) by
+// (key desc, slot asc), where CTA r's keys[0..n) are slots that follow those of
+// CTAs 0..r-1.  Exact radix select over four 8-bit digits: every CTA builds its
+// histogram of the digit (per-warp, warp-aggregated with match_any), the
+// cluster sums the eight histograms, and every CTA derives the same digit of
+// the threshold and the same number of ties still to take.  Then each CTA
+// counts its keys above the threshold and equal to it, the counts are
+// exchanged, and CTA r calls out(i, rank) for its chosen keys, ranks following
+// those of CTAs 0..r-1 (ties taken in slot order).  Returns the cluster total.
+template <class Out>
+__device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxSmem& fs, Out out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = K;
+  for (int pass = 0; pass < 4; pass++) {
+    const int shift = 24 - 8 * pass, buf = pass & 1;
+    for (int i = lane; i < 256; i += 32) fs.whist[warp][i] = 0;
+    __syncwarp();
+    for (int base = 0; base < n; base += RX_THREADS) {     // uniform trip count for match_any
+      const int i = base + tid;
+      const uint32_t k = (i < n) ? keys[i] : 0u;
+      const bool ok = k != 0u && (k & mask) == prefix;
+      const uint32_t digit = ok ? ((k >> shift) & 255u) : 256u;
+      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, digit);
+      if (ok && lane == __ffs(peers) - 1) atomicAdd(&fs.whist[warp][digit], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    for (int i = tid; i < 256; i += RX_THREADS) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < RX_WARPS; w++) t += fs.whist[w][i];
+      fs.hist[buf][i] = t;
+    }
+    // every CTA's histogram of this pass is final; the other buffer was read by
+    // all CTAs before they arrived here
+    cluster_arrive();
+    cluster_wait();
+    if (tid < 64) {
+      uint4 t = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int r = 0; r < RX_CL; r++) {
+        const uint4 v = cluster_ld4(&fs.hist[buf][4 * tid], r);
+        t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+      }
+      // the cluster-wide histogram replaces this CTA's per-warp one (warp 0 row)
+      *reinterpret_cast<uint4*>(&fs.whist[0][4 * tid]) = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; q++) { c[q] = fs.whist[0][255 - 8 * lane - q]; sum += c[q]; }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      if (total <= (uint32_t)remaining && pass == 0) {
+        if (lane == 0) fs.bcast[0] = -1;                   // at most K candidates: take them all
+      } else {
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= (uint32_t)remaining);
+        const int owner = __ffs(hit) - 1;
+        if (lane == owner) {
+          int cum = (int)(incl - sum);
+          int d = 255 - 8 * lane;
+#pragma unroll
+          for (int q = 0; q < 8; q++) {
+            if (cum + (int)c[q] >= remaining) { d = 255 - 8 * lane - q; break; }
+            cum += (int)c[q];
+          }
+          fs.bcast[0] = d;
+          fs.bcast[1] = remaining - cum;
+        }
+      }
+    }
+    __syncthreads();
+    const int d = fs.bcast[0];
+    if (d < 0) {                                           // threshold 0: every valid key is above it
+      prefix = 0;
+      remaining = 0;
+      break;
+    }
+    prefix |= (uint32_t)d << shift;
+    mask |= 255u << shift;
+    remaining = fs.bcast[1];
+  }
+  const uint32_t thr = prefix;
+  const int take_eq = remaining;                           // keys equal to thr still to take, in slot order
+
+  const int chunk = (n + RX_THREADS - 1) / RX_THREADS;
+  const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
+  int gt = 0, eq = 0;
+  for (int i = i0; i < i1; i++) {
+    const uint32_t k = keys[i];
+    if (k == 0u) continue;
+    if (k > thr) gt++;
+    else if (k == thr) eq++;
+  }
+  int gt_tot, eq_tot;
+  const int gt_before = cta_exclusive_scan(gt, fs, &gt_tot);
+  const int eq_before = cta_exclusive_scan(eq, fs, &eq_tot);
+  if (tid == 0) {
+    fs.cnt[0] = gt_tot;
+    fs.cnt[1] = eq_tot;
+  }
+  cluster_arrive();
+  cluster_wait();
+  if (warp == 0) {
+    // lane r < 8 holds CTA r's counts; ties go to the lowest CTAs first
+    int g = 0, e = 0;
+    if (lane < RX_CL) {
+      uint32_t a;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(tc::smem_u32(&fs.cnt[0])), "r"(lane));
+      asm volatile("ld.shared::cluster.v2.s32 {%0, %1}, [%2];" : "=r"(g), "=r"(e) : "r"(a) : "memory");
+    }
+    int e_incl = e;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, e_incl, off);
+      if (lane >= off) e_incl += y;
+    }
+    const int budget = max(0, take_eq - (e_incl - e));     // ties this CTA may still take
+    const int taken = min(e, budget);
+    int t_incl = g + taken;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, t_incl, off);
+      if (lane >= off) t_incl += y;
+    }
+    const int my_base = __shfl_sync(0xFFFFFFFFu, t_incl - g - taken, crank);
+    const int my_budget = __shfl_sync(0xFFFFFFFFu, budget, crank);
+    const int total = __shfl_sync(0xFFFFFFFFu, t_incl, 31);
+    if (lane == 0) {
+      fs.bcast[0] = my_base;
+      fs.bcast[1] = my_budget;
+      fs.bcast[2] = total;
+    }
+  }
+  cluster_arrive();                                        // this CTA is done reading the others
+  __syncthreads();
+  const int my_base = fs.bcast[0], my_budget = fs.bcast[1], total = fs.bcast[2];
+  const int mine_eq = max(0, min(eq, my_budget - eq_before));
+  int r = my_base + gt_before + min(eq_before, my_budget);
+  int used = 0;
+  for (int i = i0; i < i1; i++) {
+    const uint32_t k = keys[i];
+    if (k == 0u) continue;
+    bool take = k > thr;
+    if (!take && k == thr && used < mine_eq) { take = true; used++; }
+    if (take) out(i, r++);
+  }
+  cluster_wait();                                          // no CTA leaves while others read its counts
+  return total;
+}
+
+__global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  RxSmem& sm = *reinterpret_cast<RxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bq = (int)(blockIdx.x / RX_CL), crank = (int)(blockIdx.x % RX_CL);
+  const int b = bq / p.Q;
+
+  int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[b]);
+  if (nv > p.cap) {
+    if (tid == 0 && crank == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
+    nv = p.cap;
+  }
+  const int64_t n_slots = (int64_t)p.M * BLK;
+  const int64_t t0 = (int64_t)crank * p.entries_per_cta;          // first tile of this CTA
+  int64_t t1 = t0 + p.entries_per_cta;
+  const int64_t n_tiles = ceil_div(n_slots, RX_TILE);
+  if (t1 > n_tiles) t1 = n_tiles;
+  const int n = (int)(t1 > t0 ? t1 - t0 : 0);                    // <= RX_MAX_TILES (host)
+  const int64_t row_base = (int64_t)b * p.cap;
+
+  // ---- set-up: TMEM, barriers, head weights, this CTA's pool blocks
+  if (warp == 0) tc::tmem_alloc(&sm.tmem_base, RX_TMEM_COLS);
+  if (tid == 0) {
+    for (int r = 0; r < RX_ROUNDS; r++) tc::bar_init(&sm.mma_done[r], 1);
+    tc::bar_init_fence();
+  }
+  if (tid < HI) sm.w[tid] = p.w_head[(int64_t)bq * HI + tid];
+  for (int i = tid; i < n * 16; i += RX_THREADS) {
+    const int64_t pi = t0 * 16 + i;
+    int32_t blk = pi < p.M ? p.pool[(int64_t)bq * p.M + pi] : -1;
+    if (blk >= 0 && (int64_t)blk * BLK >= p.cap) {
+      report(p.hdr, CSA2_ERR_BOUNDS, blk);
+      blk = -1;
+    }
+    sm.pool[i] = blk;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  // ---- 1. copies: warp w takes tiles w, w + 8, w + 16; one warp instruction per block
+  for (int i = warp; i < n; i += RX_WARPS) {
+    uint8_t* codes = sm.tile[i];
+    const int32_t my_blk = sm.pool[i * 16 + (lane & 15)];
+    const int r = lane >> 2, c = lane & 3;                      // entry of the block, 16-byte chunk
+#pragma unroll 4
+    for (int sb = 0; sb < 16; sb++) {
+      const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, sb);
+      if (blk < 0) continue;
+      const int trow = sb * BLK + r;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                   :: "r"(tc::smem_u32(codes + trow * 64 + ((c ^ ((trow >> 1) & 3)) * 16))),
+                      "l"(p.idx_codes + (row_base + (int64_t)blk * BLK) * IDX_CODE_BYTES + lane * 16) : "memory");
+    }
+    const int sb = lane >> 1, half = lane & 1;                  // scale words: 32 bytes per block
+    const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, sb);
+    if (blk >= 0)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                   :: "r"(tc::smem_u32(codes + RX_CODES + sb * 32 + half * 16)),
+                      "l"(p.idx_scales + (row_base + (int64_t)blk * BLK) * IDX_SCALE_BYTES + half * 16) : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  if (warp == RX_WARPS - 1) quantize_index_query_warp(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  tc::fence_proxy_async_smem();                                 // copies and query codes feed the tensor cores
+  __syncthreads();
+
+  // ---- 2. scale words to TMEM: tile row m -> lane m, column base + m / 32;
+  // the query's words to lane 32 q + head of every quarter q
+  if (warp < 4) {
+    const int m = warp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    for (int i = 0; i < n; i++)
+      tc::tmem_st_x1(tmem + lane_off + RX_SFA_COL + i * 4 + warp,
+                     *reinterpret_cast<const uint32_t*>(sm.tile[i] + RX_CODES + m * 4));
+    tc::tmem_st_x1(tmem + lane_off + RX_SFB_COL, sm.sfb[lane]);
+    tc::tmem_wait_st();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  // ---- 3. MMAs in rounds of 8 tiles, then the scores of the round as keys
+  const int q4 = warp & 3;                                      // TMEM lane quarter of this warp
+  const int m = q4 * 32 + lane;                                 // tile row = slot within the tile
+  const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+  bool ok_all = true;
+  for (int r0 = 0, round = 0; r0 < n; r0 += RX_ROUND, round++) {
+    const int rn = min(RX_ROUND, n - r0);
+    if (tid == 0) {
+      const uint64_t bdesc = tc::smem_desc(tc::smem_u32(sm.qcodes), 16, 512, tc::SW_64B);
+      constexpr uint32_t id0 = tc::idesc_mxf4(RX_TILE, HI, 0, 0);
+      constexpr uint32_t id1 = tc::idesc_mxf4(RX_TILE, HI, 2, 2);
+      for (int j = 0; j < rn; j++) {
+        const int i = r0 + j;
+        const uint64_t adesc = tc::smem_desc(tc::smem_u32(sm.tile[i]), 16, 512, tc::SW_64B);
+        const uint32_t d = tmem + RX_ACC_COL + j * HI, sfa = tmem + RX_SFA_COL + i * 4;
+        tc::mma_mxf4(d, adesc, bdesc, id0, sfa, tmem + RX_SFB_COL, 0);
+        tc::mma_mxf4(d, adesc + 2, bdesc + 2, id1, sfa, tmem + RX_SFB_COL, 1);   // next 32 bytes of K
+      }
+      tc::commit(&sm.mma_done[round]);
+    }
+    __syncwarp();
+    if (!tc::bar_wait(&sm.mma_done[round], 0)) {
+      if (lane == 0) report(p.hdr, CSA2_ERR_TIMEOUT, 2);
+      ok_all = false;
+    }
+    tc::fence_after_sync();
+    if (ok_all) {
+      for (int j = warp >> 2; j < rn; j += 2) {                 // warps 0..3: even slots, 4..7: odd slots
+        float v[32];
+        tc::tmem_ld_x32(tmem + lane_off + RX_ACC_COL + j * HI, v);
+        float sc = 0.0f;
+#pragma unroll
+        for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(v[h], 0.0f), sc);
+        const int u = (r0 + j) * RX_TILE + m;                   // slot within this CTA
+        const int32_t blk = sm.pool[u / BLK];
+        const int64_t e = (int64_t)blk * BLK + (u % BLK);
+        const bool ok = blk >= 0 && e < nv && t0 * RX_TILE + u < n_slots;
+        sm.keys[u] = ok ? float_key(sc) : 0u;
+      }
+    } else {
+      for (int j = warp >> 2; j < rn; j += 2) sm.keys[(r0 + j) * RX_TILE + m] = 0u;
+    }
+    tc::fence_before_sync();
+    __syncthreads();                                            // accumulators free for the next round
+    tc::fence_after_sync();
+  }
+  if (warp == 0) tc::tmem_dealloc(tmem, RX_TMEM_COLS);
+
+  // ---- 4. exact top-K over the whole pool, across the cluster
+  int32_t* sel = p.sel + (int64_t)bq * p.K;
+  const int ns = cluster_select(sm.keys, n * RX_TILE, p.K, crank, sm, [&](int i, int r) {
+    sel[r] = sm.pool[i / BLK] * BLK + (i % BLK);
+  });
+  if (crank == RX_CL - 1)
+    for (int i = ns + tid; i < p.K; i += RX_THREADS) sel[i] = -1;
+}
+
+cudaError_t launch_reindex_select(IsParams p, cudaStream_t stream) {
+  if (p.B == 0 || p.Q == 0) return cudaSuccess;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(reindex_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)RX_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
+  const int64_t tiles = ceil_div((int64_t)p.M * BLK, RX_TILE);
+  p.entries_per_cta = ceil_div(tiles, RX_CL);     // tiles per CTA (<= 22)
+  if (p.entries_per_cta > RX_MAX_TILES) return cudaErrorInvalidValue;
+  const int64_t BQ = (int64_t)p.B * p.Q;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(BQ * RX_CL));
+  cfg.blockDim = dim3(RX_THREADS);
+  cfg.dynamicSmemBytes = RX_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = RX_CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reindex_select_kernel, p);
+}
+
+}  // namespace csa2
