@@ -24,10 +24,11 @@
 //      head) and form s = sum_h w_h ReLU(q_h . k), kept as an order-preserving
 //      key per pool slot (0 for slots outside the search domain);
 //   4. the cluster runs one exact radix select over all slot keys: four 8-bit
-//      digit passes, each CTA publishing its digit histogram in shared memory
-//      and every CTA summing the six histograms over distributed shared
-//      memory, so that all agree on the threshold; a last exchange of per-CTA
-//      counts places every CTA's chosen entries in pool-slot order.
+//      digit passes, each CTA pushing its digit histogram into every CTA's
+//      shared memory before one cluster barrier, so that all derive the same
+//      threshold digit from the same data; the same histograms give every
+//      CTA's count above and at the threshold, which places every CTA's
+//      chosen entries in pool-slot order without a further exchange.
 // Products of E2M1 values scaled by powers of two are exact; the accumulation
 // is fp32.  Ties go to the lower pool slot (= lower entry for an ascending
 // pool).  The MMA wait is bounded and reports CSA2_ERR_TIMEOUT.
@@ -46,7 +47,7 @@ constexpr int RX_TILE = 128;                                    // pool slots pe
 constexpr int RX_MAX_TILES = (CSA2_MAX_M * BLK / RX_TILE + RX_CL - 1) / RX_CL;   // 22
 constexpr int RX_ROUNDS = (RX_MAX_TILES + 7) / 8;
 constexpr int RX_CODES = RX_TILE * IDX_CODE_BYTES;              // 8192
-constexpr int RX_TILE_BYTES = RX_CODES + 1024;                  // codes + 512 B scale words, 1 KB stride
+constexpr int RX_TILE_BYTES = RX_CODES + 512;                   // codes + 512 B scale words (SW64 atoms: 512 B aligned)
 constexpr int RX_ROUND = 8;                                     // TMEM accumulators per MMA round
 constexpr int RX_TMEM_COLS = 512;
 constexpr int RX_ACC_COL = 0;                                   // 8 accumulators of 32 columns
@@ -61,11 +62,13 @@ struct RxSmem {
   float w[HI];
   uint32_t sfb[HI];
   uint32_t keys[RX_MAX_TILES * RX_TILE];        // slot keys; 0 = outside the search domain
-  alignas(16) uint32_t hist[2][256];            // this CTA's digit histogram (double buffered), read by the cluster
-  uint32_t whist[RX_WARPS][256];
-  alignas(8) int32_t cnt[2];                    // this CTA's (above threshold, equal to it) counts, read by the cluster
+  uint32_t hist[256];                           // this CTA's digit histogram of the current pass
+  alignas(16) uint32_t rows[2][RX_CL][256];     // every CTA's histogram, pushed by its owner (double buffered)
+  int32_t gt_all[RX_CL];                       // every CTA's keys above the threshold (same in all CTAs)
+  int32_t eq_all[RX_CL];                       // every CTA's keys equal to it
   int32_t wsum[RX_WARPS];
   int32_t bcast[4];
+  uint32_t suf[257];                            // cluster-wide suffix sums of the current histogram
   uint64_t mma_done[RX_ROUNDS];
   uint32_t tmem_base;
 };
@@ -95,98 +98,115 @@ __device__ int cta_exclusive_scan(int v, RxSmem& fs, int* total) {
   return base + x - v;
 }
 
-// Four consecutive words of CTA `rank`'s copy of the shared variable at `local`.
-__device__ __forceinline__ uint4 cluster_ld4(const uint32_t* local, int rank) {
-  uint32_t a;
-  uint4 v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(tc::smem_u32(local)), "r"(rank));
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Top-K over the keys of every CTA of the cluster (key 0 = not a candidate) by
 // (key desc, slot asc), where CTA r's keys[0..n) are slots that follow those of
-// CTAs 0..r-1.  Exact radix select over four 8-bit digits: every CTA builds its
-// histogram of the digit (per-warp, warp-aggregated with match_any), the
-// cluster sums the eight histograms, and every CTA derives the same digit of
-// the threshold and the same number of ties still to take.  Then each CTA
-// counts its keys above the threshold and equal to it, the counts are
-// exchanged, and CTA r calls out(i, rank) for its chosen keys, ranks following
-// those of CTAs 0..r-1 (ties taken in slot order).  Returns the cluster total.
+// CTAs 0..r-1.  Exact radix select over four 8-bit digits.  In every pass each
+// CTA builds the histogram of the digit over its keys that match the prefix
+// chosen so far (warp-aggregated with match_any in the first pass, where most
+// keys share a digit) and stores it into row crank of every CTA's row array;
+// after one cluster barrier every CTA holds all histograms, turns each row
+// into suffix sums (keys with a digit >= b), and finds the same threshold
+// digit and the same number of ties still to take.  The suffix sums also give,
+// for every CTA, its keys above the threshold digit, and after the last digit
+// its keys equal to the threshold, so the output offsets need no further
+// exchange.  CTA r calls out(i, rank) for its chosen keys (ties in slot order,
+// ranks after those of CTAs 0..r-1) and the function returns the cluster
+// total.  Each thread keeps its contiguous chunk of keys in registers.
 template <class Out>
 __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxSmem& fs, Out out) {
+  constexpr int KPT = (RX_MAX_TILES * RX_TILE + RX_THREADS - 1) / RX_THREADS;   // keys per thread
+  static_assert(RX_THREADS == 256, "one histogram bin per thread");
+  static_assert(RX_CL <= RX_WARPS, "one warp per CTA row");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunk = (n + RX_THREADS - 1) / RX_THREADS;                         // <= KPT
+  const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
+  uint32_t kr[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; j++) kr[j] = (i0 + j < i1) ? keys[i0 + j] : 0u;
+  if (tid < RX_CL) {
+    fs.gt_all[tid] = 0;
+    fs.eq_all[tid] = 0;
+  }
+  fs.hist[tid] = 0;
+  __syncthreads();
+  cluster_wait();                                          // (arrived at set-up) every CTA runs: rows may be pushed
+
   uint32_t prefix = 0, mask = 0;
   int remaining = K;
   for (int pass = 0; pass < 4; pass++) {
     const int shift = 24 - 8 * pass, buf = pass & 1;
-    for (int i = lane; i < 256; i += 32) fs.whist[warp][i] = 0;
-    __syncwarp();
-    for (int base = 0; base < n; base += RX_THREADS) {     // uniform trip count for match_any
-      const int i = base + tid;
-      const uint32_t k = (i < n) ? keys[i] : 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; j++) {
+      const uint32_t k = kr[j];
       const bool ok = k != 0u && (k & mask) == prefix;
-      const uint32_t digit = ok ? ((k >> shift) & 255u) : 256u;
-      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, digit);
-      if (ok && lane == __ffs(peers) - 1) atomicAdd(&fs.whist[warp][digit], (uint32_t)__popc(peers));
+      const uint32_t digit = (k >> shift) & 255u;
+      if (pass == 0) {                                     // few distinct digits: aggregate per warp
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, ok ? digit : 256u);
+        if (ok && lane == __ffs(peers) - 1) atomicAdd(&fs.hist[digit], (uint32_t)__popc(peers));
+      } else if (ok) {
+        atomicAdd(&fs.hist[digit], 1u);
+      }
     }
     __syncthreads();
-    for (int i = tid; i < 256; i += RX_THREADS) {
-      uint32_t t = 0;
-#pragma unroll
-      for (int w = 0; w < RX_WARPS; w++) t += fs.whist[w][i];
-      fs.hist[buf][i] = t;
-    }
-    // every CTA's histogram of this pass is final; the other buffer was read by
-    // all CTAs before they arrived here
-    cluster_arrive();
-    cluster_wait();
-    if (tid < 64) {
-      uint4 t = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < 64) {                                        // push this CTA's histogram to every CTA
+      const uint4 v = *reinterpret_cast<const uint4*>(&fs.hist[4 * tid]);
+      const uint32_t local = tc::smem_u32(&fs.rows[buf][crank][4 * tid]);
 #pragma unroll
       for (int r = 0; r < RX_CL; r++) {
-        const uint4 v = cluster_ld4(&fs.hist[buf][4 * tid], r);
-        t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+        uint32_t a;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(r));
+        asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
       }
-      // the cluster-wide histogram replaces this CTA's per-warp one (warp 0 row)
-      *reinterpret_cast<uint4*>(&fs.whist[0][4 * tid]) = t;
     }
-    __syncthreads();
-    if (warp == 0) {
+    // every CTA's histogram of this pass has landed everywhere; the other row
+    // buffer was read by all CTAs before they arrived here
+    cluster_arrive();
+    cluster_wait();
+    fs.hist[tid] = 0;                                      // for the next pass (pushed already)
+    if (warp < RX_CL) {                                    // row `warp` -> suffix sums, in place
+      uint32_t* row = fs.rows[buf][warp];
       uint32_t c[8], sum = 0;
 #pragma unroll
-      for (int q = 0; q < 8; q++) { c[q] = fs.whist[0][255 - 8 * lane - q]; sum += c[q]; }
-      uint32_t incl = sum;
+      for (int q = 0; q < 8; q++) { c[q] = row[255 - 8 * lane - q]; sum += c[q]; }
+      uint32_t incl = sum;                                 // bins 255 .. 255 - 8 lane - 7
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
         if (lane >= off) incl += y;
       }
-      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      if (total <= (uint32_t)remaining && pass == 0) {
-        if (lane == 0) fs.bcast[0] = -1;                   // at most K candidates: take them all
-      } else {
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= (uint32_t)remaining);
-        const int owner = __ffs(hit) - 1;
-        if (lane == owner) {
-          int cum = (int)(incl - sum);
-          int d = 255 - 8 * lane;
+      uint32_t run = incl - sum;
 #pragma unroll
-          for (int q = 0; q < 8; q++) {
-            if (cum + (int)c[q] >= remaining) { d = 255 - 8 * lane - q; break; }
-            cum += (int)c[q];
-          }
-          fs.bcast[0] = d;
-          fs.bcast[1] = remaining - cum;
-        }
+      for (int q = 0; q < 8; q++) { run += c[q]; row[255 - 8 * lane - q] = run; }
+    }
+    __syncthreads();
+    {
+      uint32_t t = 0;
+#pragma unroll
+      for (int r = 0; r < RX_CL; r++) t += fs.rows[buf][r][tid];
+      fs.suf[tid] = t;                                     // cluster keys with digit >= tid
+      if (tid == 0) fs.suf[256] = 0u;
+    }
+    __syncthreads();
+    if (pass == 0 && fs.suf[0] <= (uint32_t)remaining) {
+      if (tid == 0) fs.bcast[0] = -1;                      // at most K candidates: take them all
+    } else {
+      const uint32_t here = fs.suf[tid], above = fs.suf[tid + 1];
+      if (here >= (uint32_t)remaining && above < (uint32_t)remaining) {
+        fs.bcast[0] = tid;                                 // the digit of the K-th largest key
+        fs.bcast[1] = remaining - (int)above;
       }
     }
     __syncthreads();
     const int d = fs.bcast[0];
+    if (tid < RX_CL) {
+      const uint32_t* row = fs.rows[buf][tid];
+      fs.gt_all[tid] += (int)(d < 0 ? row[0] : (d < 255 ? row[d + 1] : 0u));
+      if (pass == 3) fs.eq_all[tid] = (int)(row[d] - (d < 255 ? row[d + 1] : 0u));
+    }
     if (d < 0) {                                           // threshold 0: every valid key is above it
       prefix = 0;
       remaining = 0;
@@ -195,36 +215,14 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
     prefix |= (uint32_t)d << shift;
     mask |= 255u << shift;
     remaining = fs.bcast[1];
+    __syncthreads();                                       // bcast read before the next pass writes it
   }
   const uint32_t thr = prefix;
   const int take_eq = remaining;                           // keys equal to thr still to take, in slot order
-
-  const int chunk = (n + RX_THREADS - 1) / RX_THREADS;
-  const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
-  int gt = 0, eq = 0;
-  for (int i = i0; i < i1; i++) {
-    const uint32_t k = keys[i];
-    if (k == 0u) continue;
-    if (k > thr) gt++;
-    else if (k == thr) eq++;
-  }
-  int gt_tot, eq_tot;
-  const int gt_before = cta_exclusive_scan(gt, fs, &gt_tot);
-  const int eq_before = cta_exclusive_scan(eq, fs, &eq_tot);
-  if (tid == 0) {
-    fs.cnt[0] = gt_tot;
-    fs.cnt[1] = eq_tot;
-  }
-  cluster_arrive();
-  cluster_wait();
+  __syncthreads();
   if (warp == 0) {
-    // lane r < 8 holds CTA r's counts; ties go to the lowest CTAs first
-    int g = 0, e = 0;
-    if (lane < RX_CL) {
-      uint32_t a;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(tc::smem_u32(&fs.cnt[0])), "r"(lane));
-      asm volatile("ld.shared::cluster.v2.s32 {%0, %1}, [%2];" : "=r"(g), "=r"(e) : "r"(a) : "memory");
-    }
+    // lane r < RX_CL: CTA r's counts; ties go to the lowest CTAs first
+    const int g = lane < RX_CL ? fs.gt_all[lane] : 0, e = lane < RX_CL ? fs.eq_all[lane] : 0;
     int e_incl = e;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -248,21 +246,30 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
       fs.bcast[2] = total;
     }
   }
-  cluster_arrive();                                        // this CTA is done reading the others
-  __syncthreads();
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; j++) {
+    const uint32_t k = kr[j];
+    if (k == 0u) continue;
+    if (k > thr) gt++;
+    else if (k == thr) eq++;
+  }
+  int gt_tot, eq_tot;
+  const int gt_before = cta_exclusive_scan(gt, fs, &gt_tot);    // (its barriers also publish bcast)
+  const int eq_before = cta_exclusive_scan(eq, fs, &eq_tot);
   const int my_base = fs.bcast[0], my_budget = fs.bcast[1], total = fs.bcast[2];
   const int mine_eq = max(0, min(eq, my_budget - eq_before));
   int r = my_base + gt_before + min(eq_before, my_budget);
   int used = 0;
-  for (int i = i0; i < i1; i++) {
-    const uint32_t k = keys[i];
+#pragma unroll
+  for (int j = 0; j < KPT; j++) {
+    const uint32_t k = kr[j];
     if (k == 0u) continue;
     bool take = k > thr;
     if (!take && k == thr && used < mine_eq) { take = true; used++; }
-    if (take) out(i, r++);
+    if (take) out(i0 + j, r++);
   }
-  cluster_wait();                                          // no CTA leaves while others read its counts
-  return total;
+  return total;                    // the last push preceded the last cluster barrier
 }
 
 __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams p) {
@@ -305,6 +312,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
+  cluster_arrive();                                             // waited for before the first histogram push
 
   // ---- 1. copies: warp w takes tiles w, w + 8, w + 16; one warp instruction per block
   for (int i = warp; i < n; i += RX_WARPS) {
