@@ -37,7 +37,8 @@
 //     owner weights the C shares by L_c exp(m_c - M) / sum_c' L_c' exp(m_c' - M),
 //     M = max_c m_c, in fp32, rounds to bf16 and stores.  A split cluster
 //     barrier (arrive once the receive slots are dead, wait before sending)
-//     orders the exchange; no CTA reads another's shared memory.
+//     orders the exchange; no CTA reads another's shared memory, and the
+//     owners' byte counts make a closing cluster barrier unnecessary.
 // All mbarrier waits are bounded; a timeout reports CSA2_ERR_TIMEOUT.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
@@ -500,10 +501,12 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
       }
     }
   }
+  // A sender's shares stay in place until its copies have read them; an owner
+  // has received every byte sent to it (bar_red) before it gets here, so no
+  // cross-CTA access remains and no final cluster barrier is needed.
   if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   tc::fence_before_sync();
-  // no CTA leaves while a share it sent may still be read, or one it owns still arrive
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, AT_TMEM_COLS);

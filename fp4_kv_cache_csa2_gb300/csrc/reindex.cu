@@ -98,6 +98,18 @@ __device__ int cta_exclusive_scan(int v, RxSmem& fs, int* total) {
   return base + x - v;
 }
 
+// 32 consecutive 32-bit TMEM columns of this thread's lane, without waiting.
+__device__ __forceinline__ void tmem_ld_x32_nowait(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                 "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                 "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                 "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr) : "memory");
+}
+
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
@@ -383,12 +395,22 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
     tc::fence_after_sync();
     if (ok_all) {
-      for (int j = warp >> 2; j < rn; j += 2) {                 // warps 0..3: even slots, 4..7: odd slots
-        float v[32];
-        tc::tmem_ld_x32(tmem + lane_off + RX_ACC_COL + j * HI, v);
+      // warps 0..3 take accumulators 0, 2, 4, 6 and warps 4..7 take 1, 3, 5, 7:
+      // all four TMEM loads are issued before one wait
+      uint32_t acc[4][32];
+#pragma unroll
+      for (int jj = 0; jj < 4; jj++) {
+        const int j = (warp >> 2) + 2 * jj;
+        if (j < rn) tmem_ld_x32_nowait(tmem + lane_off + RX_ACC_COL + j * HI, acc[jj]);
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+      for (int jj = 0; jj < 4; jj++) {
+        const int j = (warp >> 2) + 2 * jj;
+        if (j >= rn) break;
         float sc = 0.0f;
 #pragma unroll
-        for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(v[h], 0.0f), sc);
+        for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(__uint_as_float(acc[jj][h]), 0.0f), sc);
         const int u = (r0 + j) * RX_TILE + m;                   // slot within this CTA
         const int32_t blk = sm.pool[u / BLK];
         const int64_t e = (int64_t)blk * BLK + (u % BLK);
