@@ -75,7 +75,7 @@ struct AtSmall {
   float red[4][H];                       // per-warp column maxima / sums (warp w & 3, head)
   float wgt[AT_MAXC][H];                 // combination weight of each CTA's share, per head
   uint64_t bar_kv, bar_s, bar_o, bar_red;
-  uint64_t bar_q[8];
+  uint64_t bar_q;                        // all of Q landed (chunks 0..3 and 4..7: two arrivals)
   uint64_t bar_keys;                     // every warp's dequantised keys are in shared memory
   uint32_t tmem_base;
   int err;
@@ -159,7 +159,7 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::bar_init(&sm.bar_s, 1);
     tc::bar_init(&sm.bar_o, 1);
     tc::bar_init(&sm.bar_red, 1);
-    for (int i = 0; i < 8; i++) tc::bar_init(&sm.bar_q[i], 1);
+    tc::bar_init(&sm.bar_q, 2);
     tc::bar_init(&sm.bar_keys, AT_THREADS / 32);
     sm.err = 0;
     tc::bar_init_fence();
@@ -201,9 +201,13 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
         tc::bar_arrive_expect_tx(&sm.bar_kv, 0u);
       }
     }
-    for (int c = 0; c < (window_cta ? 8 : 4); c++) {     // chunks 4..7 land over the staging buffer
-      tc::bar_arrive_expect_tx(&sm.bar_q[c], (uint32_t)AT_QCHUNK_BYTES);
-      tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q[c]);
+    // chunks 0..3 now; 4..7 land over the staging buffer once it is free (at
+    // once in the window CTA, which stages nothing)
+    tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
+    for (int c = 0; c < 4; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
+    if (window_cta) {
+      tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
+      for (int c = 4; c < 8; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
     }
   }
 
@@ -236,10 +240,8 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::fence_proxy_async_smem();
     __syncthreads();                                       // the staging buffer is free
     if (tid == 0) {
-      for (int c = 4; c < 8; c++) {
-        tc::bar_arrive_expect_tx(&sm.bar_q[c], (uint32_t)AT_QCHUNK_BYTES);
-        tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q[c]);
-      }
+      tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
+      for (int c = 4; c < 8; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
     }
     const uint32_t scw[4] = {scl.x, scl.y, scl.z, scl.w};
 #pragma unroll
@@ -274,7 +276,7 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
     bool ok = at_wait(window_cta ? &sm.bar_kv : &sm.bar_keys, 0, sm, p.hdr, window_cta ? 11 : 16);
-    for (int c = 0; c < 8 && ok; c++) ok = at_wait(&sm.bar_q[c], 0, sm, p.hdr, 12);
+    if (ok) ok = at_wait(&sm.bar_q, 0, sm, p.hdr, 12);
     tc::fence_after_sync();
     for (int c = 0; c < 8 && ok; c++) {
       const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + c * AT_QCHUNK_BYTES);
