@@ -148,7 +148,6 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   const int bq = blockIdx.x / C;
   const int b = bq / p.Q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t t = p.q_pos[bq];
   const bool window_cta = rank == C - 1;
   const int slot0 = rank * AT_KEYS;
 
@@ -164,6 +163,15 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     sm.err = 0;
     tc::bar_init_fence();
   }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensormap(&map_q);
+    tc::prefetch_tensormap(&map_swa);
+  }
+  // everything above reads no input: with programmatic dependent launch it
+  // overlaps the previous kernel, which may have produced q, sel or the window
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t t = p.q_pos[bq];
   if (tid < AT_KEYS) {                       // which keys of this CTA exist
     int kind = 0;
     int32_t id = 0;
@@ -564,13 +572,15 @@ cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
   cfg.blockDim = dim3(AT_THREADS);
   cfg.dynamicSmemBytes = AT_SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // set-up overlaps the previous kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, map_q, map_swa, C);
 }
 

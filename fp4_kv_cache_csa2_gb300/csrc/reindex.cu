@@ -291,6 +291,16 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   const int bq = (int)(blockIdx.x / RX_CL), crank = (int)(blockIdx.x % RX_CL);
   const int b = bq / p.Q;
 
+  // ---- set-up: TMEM, barriers, head weights, this CTA's pool blocks
+  if (warp == 0) tc::tmem_alloc(&sm.tmem_base, RX_TMEM_COLS);
+  if (tid == 0) {
+    for (int r = 0; r < RX_ROUNDS; r++) tc::bar_init(&sm.mma_done[r], 1);
+    tc::bar_init_fence();
+  }
+  // everything above reads no input: with programmatic dependent launch it
+  // overlaps the previous kernel, which may have produced the pool or the queries
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[b]);
   if (nv > p.cap) {
     if (tid == 0 && crank == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
@@ -304,12 +314,6 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   const int n = (int)(t1 > t0 ? t1 - t0 : 0);                    // <= RX_MAX_TILES (host)
   const int64_t row_base = (int64_t)b * p.cap;
 
-  // ---- set-up: TMEM, barriers, head weights, this CTA's pool blocks
-  if (warp == 0) tc::tmem_alloc(&sm.tmem_base, RX_TMEM_COLS);
-  if (tid == 0) {
-    for (int r = 0; r < RX_ROUNDS; r++) tc::bar_init(&sm.mma_done[r], 1);
-    tc::bar_init_fence();
-  }
   if (tid < HI) sm.w[tid] = p.w_head[(int64_t)bq * HI + tid];
   for (int i = tid; i < n * 16; i += RX_THREADS) {
     const int64_t pi = t0 * 16 + i;
@@ -455,13 +459,15 @@ cudaError_t launch_reindex_select(IsParams p, cudaStream_t stream) {
   cfg.blockDim = dim3(RX_THREADS);
   cfg.dynamicSmemBytes = RX_SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = RX_CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // set-up overlaps the previous kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, reindex_select_kernel, p);
 }
 
