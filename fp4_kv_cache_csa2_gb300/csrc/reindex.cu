@@ -19,8 +19,8 @@
 //   2. warps 0..3 store the E8M0 scale words of every tile (A operand) and of
 //      the query (B operand, replicated to every lane quarter) in TMEM;
 //   3. one thread issues the block-scaled MMAs (M = 128 entries, N = 32 heads,
-//      K = 128 as two K = 64 halves) for up to 8 tiles at a time into 8 TMEM
-//      accumulators; all warps then read them back (lane = entry, column =
+//      K = 128 as two K = 64 halves) for up to 13 tiles at a time into 13
+//      TMEM accumulators; all warps then read them back (lane = entry, column =
 //      head) and form s = sum_h w_h ReLU(q_h . k), kept as an order-preserving
 //      key per pool slot (0 for slots outside the search domain);
 //   4. the cluster runs one exact radix select over all slot keys: four 8-bit
@@ -45,12 +45,12 @@ constexpr int RX_WARPS = RX_THREADS / 32;
 constexpr int RX_CL = 6;                                        // CTAs per query
 constexpr int RX_TILE = 128;                                    // pool slots per tile
 constexpr int RX_MAX_TILES = (CSA2_MAX_M * BLK / RX_TILE + RX_CL - 1) / RX_CL;   // 22
-constexpr int RX_ROUNDS = (RX_MAX_TILES + 7) / 8;
+constexpr int RX_ROUND = 13;                                    // TMEM accumulators per MMA round
+constexpr int RX_ROUNDS = (RX_MAX_TILES + RX_ROUND - 1) / RX_ROUND;
 constexpr int RX_CODES = RX_TILE * IDX_CODE_BYTES;              // 8192
 constexpr int RX_TILE_BYTES = RX_CODES + 512;                   // codes + 512 B scale words (SW64 atoms: 512 B aligned)
-constexpr int RX_ROUND = 8;                                     // TMEM accumulators per MMA round
 constexpr int RX_TMEM_COLS = 512;
-constexpr int RX_ACC_COL = 0;                                   // 8 accumulators of 32 columns
+constexpr int RX_ACC_COL = 0;                                   // RX_ROUND accumulators of 32 columns
 constexpr int RX_SFA_COL = RX_ROUND * HI;                       // 4 columns per tile
 constexpr int RX_SFB_COL = RX_SFA_COL + 4 * RX_MAX_TILES;
 static_assert(RX_SFB_COL + 4 <= RX_TMEM_COLS, "TMEM columns");
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   __syncthreads();
   tc::fence_after_sync();
 
-  // ---- 3. MMAs in rounds of 8 tiles, then the scores of the round as keys
+  // ---- 3. MMAs in rounds of RX_ROUND tiles, then the scores of the round as keys
   const int q4 = warp & 3;                                      // TMEM lane quarter of this warp
   const int m = q4 * 32 + lane;                                 // tile row = slot within the tile
   const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -399,27 +399,29 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
     tc::fence_after_sync();
     if (ok_all) {
-      // warps 0..3 take accumulators 0, 2, 4, 6 and warps 4..7 take 1, 3, 5, 7:
-      // all four TMEM loads are issued before one wait
-      uint32_t acc[4][32];
+      // warps 0..3 take the even accumulators and warps 4..7 the odd ones,
+      // four TMEM loads in flight per batch
+      for (int jb = warp >> 2; jb < rn; jb += 8) {
+        uint32_t acc[4][32];
 #pragma unroll
-      for (int jj = 0; jj < 4; jj++) {
-        const int j = (warp >> 2) + 2 * jj;
-        if (j < rn) tmem_ld_x32_nowait(tmem + lane_off + RX_ACC_COL + j * HI, acc[jj]);
-      }
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        for (int jj = 0; jj < 4; jj++) {
+          const int j = jb + 2 * jj;
+          if (j < rn) tmem_ld_x32_nowait(tmem + lane_off + RX_ACC_COL + j * HI, acc[jj]);
+        }
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int jj = 0; jj < 4; jj++) {
-        const int j = (warp >> 2) + 2 * jj;
-        if (j >= rn) break;
-        float sc = 0.0f;
+        for (int jj = 0; jj < 4; jj++) {
+          const int j = jb + 2 * jj;
+          if (j >= rn) break;
+          float sc = 0.0f;
 #pragma unroll
-        for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(__uint_as_float(acc[jj][h]), 0.0f), sc);
-        const int u = (r0 + j) * RX_TILE + m;                   // slot within this CTA
-        const int32_t blk = sm.pool[u / BLK];
-        const int64_t e = (int64_t)blk * BLK + (u % BLK);
-        const bool ok = blk >= 0 && e < nv && t0 * RX_TILE + u < n_slots;
-        sm.keys[u] = ok ? float_key(sc) : 0u;
+          for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(__uint_as_float(acc[jj][h]), 0.0f), sc);
+          const int u = (r0 + j) * RX_TILE + m;                 // slot within this CTA
+          const int32_t blk = sm.pool[u / BLK];
+          const int64_t e = (int64_t)blk * BLK + (u % BLK);
+          const bool ok = blk >= 0 && e < nv && t0 * RX_TILE + u < n_slots;
+          sm.keys[u] = ok ? float_key(sc) : 0u;
+        }
       }
     } else {
       for (int j = warp >> 2; j < rn; j += 2) sm.keys[(r0 + j) * RX_TILE + m] = 0u;
