@@ -178,7 +178,7 @@ class Decode1M:
             for c0 in range(0, N, chunk):
                 x = torch.randn((1, chunk, D), generator=g, device=dev).to(torch.bfloat16)
                 start = torch.tensor([c0], dtype=torch.int64, device=dev)
-                cache_b = _SubCache(base, b)
+                cache_b = base.sequence(b)
                 csa2.compress_quantize(cache_b, x.view(torch.int16), start, ones, ones, rope, w_idx.view(torch.int16),
                                        ws_cw)
         base.n_entries.fill_(N)
@@ -249,22 +249,6 @@ class Decode1M:
     def prologue(self):
         for s in range(3 * self.d):
             self.step(s)
-
-
-class _SubCache:
-    """View of one sequence of a Cache as a batch-1 cache (for chunked writes)."""
-
-    def __init__(self, cache, b):
-        self.main_kv = cache.main_kv[b:b + 1]
-        self.idx_codes = cache.idx_codes[b:b + 1]
-        self.idx_scales = cache.idx_scales[b:b + 1]
-        self.n_entries = cache.n_entries[b:b + 1]
-        self.cap, self.m, self.B = cache.cap, cache.m, 1
-
-    def struct(self):
-        from fp4_kv_cache_csa2_gb300 import CacheStruct
-        return CacheStruct(self.main_kv.data_ptr(), self.idx_codes.data_ptr(), self.idx_scales.data_ptr(),
-                           self.cap, self.n_entries.data_ptr(), self.m)
 
 
 def _clone_cache(c):

@@ -126,6 +126,17 @@ class Cache:
         return CacheStruct(self.main_kv.data_ptr(), self.idx_codes.data_ptr(),
                            self.idx_scales.data_ptr(), self.cap, self.n_entries.data_ptr(), self.m)
 
+    def sequence(self, b: int) -> "Cache":
+        """Sequence b as a batch-1 cache sharing this cache's memory (for writing
+        one sequence, or one chunk of it, at a time)."""
+        v = Cache.__new__(Cache)
+        v.B, v.cap, v.m = 1, self.cap, self.m
+        v.main_kv = self.main_kv[b:b + 1]
+        v.idx_codes = self.idx_codes[b:b + 1]
+        v.idx_scales = self.idx_scales[b:b + 1]
+        v.n_entries = self.n_entries[b:b + 1]
+        return v
+
 
 class Workspace:
     """Device scratch with the status header, initialised on creation."""
