@@ -82,6 +82,7 @@ struct AtSmall {
 };
 constexpr int AT_SMEM = AT_OFF_SMALL + (int)sizeof(AtSmall) + 1024;
 static_assert(4 * AT_QCHUNK_BYTES <= AT_STAGE_BYTES, "Q chunks 4..7 must fit over the staging");
+static_assert(AT_THREADS / 32 * 8 == H, "the combine gives every warp one 8-head unit");
 static_assert(AT_OFF_STAGE % 1024 == 0, "SW128 destinations are 1 KB aligned");
 static_assert(4 * AT_SHARE_BYTES <= 8 * AT_CHUNK_BYTES, "O^T shares must fit over the keys");
 static_assert(4 * AT_SHARE_BYTES <= 8 * AT_QCHUNK_BYTES, "receive slots must fit over Q");
@@ -323,14 +324,15 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
     sm.red[q4][half * 32 + lane] = r[0];
     __syncthreads();
+    // lane l combines the four warps' maxima of head 32 half + l, then every
+    // lane gets all 32 by shuffles
+    const int hl = half * 32 + lane;
+    const float mlane = fmaxf(fmaxf(sm.red[0][hl], sm.red[1][hl]), fmaxf(sm.red[2][hl], sm.red[3][hl]));
     float mx[32];
 #pragma unroll
-    for (int j = 0; j < 32; j++) {
-      const int h = half * 32 + j;
-      mx[j] = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]), fmaxf(sm.red[2][h], sm.red[3][h]));
-    }
-    if (tid < H) sm.ml[tid] = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
-    __syncthreads();                                 // every thread has read the maxima
+    for (int j = 0; j < 32; j++) mx[j] = __shfl_sync(0xFFFFFFFFu, mlane, j);
+    if (q4 == 0) sm.ml[hl] = mlane;
+    __syncthreads();                                 // every thread has read the per-warp maxima
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 32; j++) {
@@ -477,11 +479,24 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
     __syncthreads();
     uint16_t* out = p.out + (int64_t)bq * H * D;
+    // thread: 8-head unit u = warp (heads 8u .. 8u+7), dims lane + 32k of the tile
+    // (consecutive lanes -> coalesced bf16 stores per head row); its 8 x C
+    // weights are loaded once
+    const int u = warp;
+    float wself[8], wr[AT_MAXC - 1][8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) wself[e] = sm.wgt[rank][u * 8 + e];
+#pragma unroll
+    for (int r = 0; r < AT_MAXC - 1; r++) {
+      const int sender = r < rank ? r : r + 1;
+#pragma unroll
+      for (int e = 0; e < 8; e++) wr[r][e] = (r < C - 1) ? sm.wgt[sender][u * 8 + e] : 0.f;
+    }
     int j = 0;
     for (int tile = rank; tile < 4; tile += C, j++) {
-      // thread: dim d (consecutive lanes -> coalesced bf16 stores per head row), 8-head unit u
-      for (int task = tid; task < 128 * 8; task += AT_THREADS) {
-        const int d = task & 127, u = task >> 7;
+#pragma unroll 2
+      for (int k = 0; k < 4; k++) {
+        const int d = lane + 32 * k;
         const int off = d * H + ((u ^ (d & 7)) << 3);
         float acc[8];
         {
@@ -490,19 +505,20 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const float2 f = __half22float2(h2[e]);
-            acc[2 * e] = f.x * sm.wgt[rank][u * 8 + 2 * e];
-            acc[2 * e + 1] = f.y * sm.wgt[rank][u * 8 + 2 * e + 1];
+            acc[2 * e] = f.x * wself[2 * e];
+            acc[2 * e + 1] = f.y * wself[2 * e + 1];
           }
         }
-        for (int r = 0; r < C - 1; r++) {
-          const int sender = r < rank ? r : r + 1;
+#pragma unroll
+        for (int r = 0; r < AT_MAXC - 1; r++) {
+          if (r >= C - 1) break;
           const uint4 v = *reinterpret_cast<const uint4*>(orecv + (j * (C - 1) + r) * (128 * H) + off);
           const __half2* h2 = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const float2 f = __half22float2(h2[e]);
-            acc[2 * e] = fmaf(f.x, sm.wgt[sender][u * 8 + 2 * e], acc[2 * e]);
-            acc[2 * e + 1] = fmaf(f.y, sm.wgt[sender][u * 8 + 2 * e + 1], acc[2 * e + 1]);
+            acc[2 * e] = fmaf(f.x, wr[r][2 * e], acc[2 * e]);
+            acc[2 * e + 1] = fmaf(f.y, wr[r][2 * e + 1], acc[2 * e + 1]);
           }
         }
         uint16_t* o = out + (u * 8) * D + tile * 128 + d;
