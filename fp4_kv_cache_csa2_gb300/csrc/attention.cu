@@ -389,6 +389,9 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   // this CTA's share O_c / L_c per tile as fp16 [dim][head], 16-byte units swizzled by dim
   {
     const int q4 = warp & 3, half = warp >> 2;
+    float il[32];                                 // 1 / L_c of this thread's 32 heads, in registers
+#pragma unroll
+    for (int j = 0; j < 32; j++) il[j] = sm.inv_l[half * 32 + j];
     uint32_t ta[4][32];
 #pragma unroll
     for (int tile = 0; tile < 4; tile++) {       // issue all four TMEM loads, then wait once
@@ -414,9 +417,8 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int j = 8 * u + 2 * e;
-          const int h = half * 32 + j;
-          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * sm.inv_l[h],
-                                               __uint_as_float(ta[tile][j + 1]) * sm.inv_l[h + 1]);
+          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * il[j],
+                                               __uint_as_float(ta[tile][j + 1]) * il[j + 1]);
           w[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
         const int unit = (half * 4 + u) ^ (d & 7);
