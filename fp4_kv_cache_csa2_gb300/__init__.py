@@ -62,6 +62,7 @@ _SIGNATURES = {
     "csa2_block_topk_workspace_size": (_SZ, [_I, _I, _I64]),
     "csa2_block_topk": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I, _I, _I64, _I, _P, _P, _SZ, _P]),
     "csa2_block_topk_static": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I, _I, _I64, _I, _P, _P]),
+    "csa2_select_topk_workspace_size": (_SZ, [_I, _I, _I64]),
     "csa2_select_topk": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _P, _I, _I, _P, _I, _I, _I64,
                               _P, _SZ, _P]),
     "csa2_attn_workspace_size": (_SZ, [_I, _I, _I]),
@@ -205,6 +206,10 @@ def block_topk_static(cache: Cache, scores, q_pos, max_n: int, M: int, pool_bloc
     c = cache.struct()
     return load().csa2_block_topk_static(ctypes.byref(c), _ptr(scores), _ptr(q_pos), B, Q, max_n, M,
                                          _ptr(pool_blocks), _stream(stream))
+
+
+def select_topk_workspace_size(B: int, Q: int, max_n: int) -> int:
+    return load().csa2_select_topk_workspace_size(B, Q, max_n)
 
 
 def select_topk(cache: Cache, scores, q_pos, K: int, sel, max_n: int, ws: Workspace,

@@ -55,6 +55,15 @@ size_t gkeys_bytes(int B, int Q, int64_t max_n) {
   return align256((size_t)B * Q * (size_t)ceil_div(max_n, BLK) * sizeof(uint32_t));
 }
 
+bool long_rows(int64_t max_n) { return max_n > ROW_SELECT_MIN_KEYS; }
+
+// scratch of the Full selections: per-row histograms and lists for long rows,
+// block-maximum keys otherwise
+size_t select_scratch_bytes(int B, int Q, int64_t max_n, bool blocks) {
+  if (long_rows(max_n)) return align256(row_select_bytes((int64_t)B * Q));
+  return blocks ? gkeys_bytes(B, Q, max_n) : 0;
+}
+
 csa2_status check_q(int B, int Q) {
   if (B < 0 || Q < 0) return CSA2_ERR_INVALID_ARG;
   return CSA2_OK;
@@ -219,7 +228,7 @@ csa2_status csa2_index_score(const csa2_cache* cache, const uint16_t* q_idx, con
 
 size_t csa2_block_topk_workspace_size(int B, int Q, int64_t max_n) {
   if (B < 0 || Q < 0 || max_n < 0) return 0;
-  return HDR + gkeys_bytes(B, Q, max_n);
+  return HDR + select_scratch_bytes(B, Q, max_n, true);
 }
 
 csa2_status csa2_block_topk(const csa2_cache* cache, const float* scores, const int64_t* q_pos, int B, int Q,
@@ -232,8 +241,16 @@ csa2_status csa2_block_topk(const csa2_cache* cache, const float* scores, const 
   if ((st = check_ws(ws, ws_bytes, csa2_block_topk_workspace_size(B, Q, max_n))) != CSA2_OK) return st;
   if (B == 0 || Q == 0) return CSA2_OK;
   if (!scores || !q_pos || !pool_blocks) return CSA2_ERR_INVALID_ARG;
+  if (long_rows(max_n))
+    return from_cuda(launch_row_select(scores, q_pos, cache->n_entries, cache->m, B, Q, max_n, 0, nullptr, M,
+                                       pool_blocks, scratch(ws), (cudaStream_t)stream));
   return from_cuda(launch_block_topk(scores, q_pos, cache->n_entries, cache->m, B, Q, max_n, M, pool_blocks,
                                      reinterpret_cast<uint32_t*>(scratch(ws)), (cudaStream_t)stream));
+}
+
+size_t csa2_select_topk_workspace_size(int B, int Q, int64_t max_n) {
+  if (B < 0 || Q < 0 || max_n < 0) return 0;
+  return HDR + select_scratch_bytes(B, Q, max_n, false);
 }
 
 csa2_status csa2_select_topk(const csa2_cache* cache, const float* scores, const int64_t* q_pos,
@@ -245,9 +262,13 @@ csa2_status csa2_select_topk(const csa2_cache* cache, const float* scores, const
   if (max_n < 0) return CSA2_ERR_INVALID_ARG;
   if (K < 1 || K > CSA2_MAX_K) return CSA2_ERR_UNSUPPORTED;
   if (pool_blocks && (M < 1 || M > CSA2_MAX_M)) return CSA2_ERR_UNSUPPORTED;
-  if ((st = check_ws(ws, ws_bytes, HDR)) != CSA2_OK) return st;
+  const size_t need = pool_blocks ? HDR : csa2_select_topk_workspace_size(B, Q, max_n);
+  if ((st = check_ws(ws, ws_bytes, need)) != CSA2_OK) return st;
   if (B == 0 || Q == 0) return CSA2_OK;
   if (!scores || !q_pos || !sel) return CSA2_ERR_INVALID_ARG;
+  if (!pool_blocks && long_rows(max_n))
+    return from_cuda(launch_row_select(scores, q_pos, cache->n_entries, cache->m, B, Q, max_n, K, sel, 0, nullptr,
+                                       scratch(ws), (cudaStream_t)stream));
   return from_cuda(launch_select_topk(scores, q_pos, cache->n_entries, cache->m, pool_blocks, M, K, sel, B, Q,
                                       max_n, (cudaStream_t)stream));
 }
@@ -278,7 +299,7 @@ size_t csa2_decode_workspace_size(csa2_mode mode, int B, int Q, int64_t max_n, i
   if (B < 0 || Q < 0 || max_n < 0 || M < 0 || K < 0) return 0;
   size_t need = HDR + align256(attn_partials_bytes((int64_t)B * Q, K));
   if (mode == CSA2_MODE_FULL) {
-    need += align256((size_t)B * Q * max_n * sizeof(float)) + gkeys_bytes(B, Q, max_n);
+    need += align256((size_t)B * Q * max_n * sizeof(float)) + select_scratch_bytes(B, Q, max_n, true);
   } else if (mode == CSA2_MODE_REINDEX) {
     need += align256((size_t)B * Q * M * BLK * sizeof(float));
   }
@@ -315,6 +336,13 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
     uint32_t* gkeys = reinterpret_cast<uint32_t*>(cur);
     st = do_index_score(cache, a->q_idx, a->w_head, a->q_pos, nullptr, a->M, scores, a->B, a->Q, a->max_n, hdr, s);
     if (st != CSA2_OK) return st;
+    if (long_rows(a->max_n)) {
+      st = from_cuda(launch_row_select(scores, a->q_pos, cache->n_entries, cache->m, a->B, a->Q, a->max_n, a->K,
+                                       a->sel, a->M, a->pool_blocks, cur, s));
+      if (st != CSA2_OK) return st;
+      return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out,
+                          a->B, a->Q, part, hdr, s);
+    }
     st = from_cuda(launch_block_topk(scores, a->q_pos, cache->n_entries, cache->m, a->B, a->Q, a->max_n, a->M,
                                      a->pool_blocks, gkeys, s));
     if (st != CSA2_OK) return st;

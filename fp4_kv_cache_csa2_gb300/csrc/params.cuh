@@ -70,6 +70,13 @@ cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const i
 cudaError_t launch_select_topk(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m,
                                const int32_t* pool, int M, int K, int32_t* sel, int B, int Q, int64_t max_n,
                                cudaStream_t stream);
+// Full rows longer than ROW_SELECT_MIN_KEYS entries are selected by the
+// multi-CTA histogram/filter path, with row_select_bytes(B*Q) of scratch.
+constexpr int64_t ROW_SELECT_MIN_KEYS = 16384;
+size_t row_select_bytes(int64_t BQ);
+cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m, int B,
+                              int Q, int64_t max_n, int K, int32_t* sel, int M, int32_t* pool, void* scratch,
+                              cudaStream_t stream);
 cudaError_t launch_attention(AttnParams p, int B, float* partials, cudaStream_t stream);
 size_t attn_partials_bytes(int64_t BQ, int K);
 

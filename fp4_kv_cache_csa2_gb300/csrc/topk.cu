@@ -206,6 +206,7 @@ __device__ void radix_select_block(const Keys& keys, const Ids& ids, int64_t n, 
 // (key 0 marks a position outside the domain: no finite score maps to 0).
 // Histograms are private per warp (plain shared atomics), summed per pass.
 constexpr int SEL_SMEM_KEYS = 16384;
+static_assert(SEL_SMEM_KEYS == ROW_SELECT_MIN_KEYS, "long rows start where the staged path ends");
 constexpr int SEL_DYN_SMEM = SEL_SMEM_KEYS * 4 + (SEL_THREADS / 32) * 256 * 4;
 
 template <class Keys, class Ids>
@@ -402,6 +403,432 @@ cudaError_t launch_select_topk(const float* scores, const int64_t* q_pos, const 
   if (e != cudaSuccess) return e;
   SelectParams sp{scores, q_pos, n_entries, pool, m, Q, M, K, max_n, sel};
   select_topk_kernel<<<B * Q, SEL_THREADS, SEL_DYN_SMEM, stream>>>(sp);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------ multi-CTA selection on long rows
+// A Full row holds one score per visible entry (up to the whole cache: 2^20
+// and more), so one CTA per row leaves most of the GPU idle and reads the row
+// five times.  Rows longer than SEL_SMEM_KEYS keys take three launches instead:
+//   scan 1  many CTAs per row histogram the top 12 bits of every key (entry
+//           keys for the top-K, block-maximum keys for the top-M, from the
+//           same read of the scores) into a per-row histogram in global
+//           memory; the row's last CTA finds the threshold bin b1 (the bin
+//           holding the K-th largest key) and the count above it;
+//   scan 2  the same CTAs read the row again and append every key above b1
+//           to the row's list of sure picks, and every key inside b1 to a
+//           candidate list as a (key, ~id) composite;
+//   resolve one CTA per row and kind finishes the exact selection among the
+//           candidates (8-bit digit passes over the 52 bits the composites do
+//           not share, stopping as soon as the threshold bin is taken whole),
+//           sorts the K ids and writes them.
+// Composites order by key and then by the lower id, so the result is the
+// (score desc, id asc) top-K.  A threshold bin with more than RS_CAP keys
+// (scores bunched far from zero, or massive ties) sends its row to the
+// single-CTA radix select, which is exact for any input.
+constexpr int RS_BITS = 12;
+constexpr int RS_BINS = 1 << RS_BITS;
+constexpr int RS_SHIFT = 32 - RS_BITS;
+constexpr int RS_CAP = 8192;                     // candidates kept per row and kind
+constexpr int RS_THREADS = 512;
+constexpr int RS_WARPS = RS_THREADS / 32;
+constexpr int RS_TILE = 256;                     // entries per warp tile: 8 coalesced loads
+constexpr int64_t RS_CHUNK = (int64_t)RS_WARPS * RS_TILE * 4;   // 16,384 entries per CTA
+constexpr int RS_MAX_OUT = CSA2_MAX_M;           // >= CSA2_MAX_K
+static_assert(RS_CHUNK % (RS_WARPS * RS_TILE) == 0 && 32 % BLK == 0, "warp tiles hold whole blocks");
+
+struct RsRow {                                   // zeroed before every selection
+  uint32_t hist[RS_BINS];
+  uint32_t n_gt, n_eq, done, b1, above, pad[11];
+};
+
+size_t row_select_bytes(int64_t BQ) {
+  const size_t per = sizeof(RsRow) + RS_MAX_OUT * sizeof(int32_t) + RS_CAP * sizeof(unsigned long long);
+  return (size_t)(2 * BQ) * per + 3 * 256;
+}
+
+struct RsParams {
+  const float* scores;      // [BQ][max_n]
+  const int64_t* q_pos;
+  const int32_t* n_entries;
+  int m, Q, K, M;           // K = 0: no entry selection; M = 0: no block selection
+  int64_t max_n;
+  int chunks;               // scan CTAs per row
+  int32_t* sel;             // [BQ][K]
+  int32_t* pool;            // [BQ][M]
+  RsRow* rows;              // [2][BQ]: entries, then blocks
+  int32_t* gt;              // [2][BQ][RS_MAX_OUT]
+  unsigned long long* cand; // [2][BQ][RS_CAP]
+  int64_t BQ;
+};
+
+// one block's max over 8 consecutive scores, with the newest visible block forced
+struct BlockScoreKeys {
+  const float* s;
+  int64_t nv;
+  __device__ bool get(int64_t r, uint32_t& k) const {
+    if (r == (nv - 1) / BLK) { k = float_key(INFINITY); return true; }
+    const int64_t e0 = r * BLK;
+    float g = -INFINITY;
+    for (int i = 0; i < BLK && e0 + i < nv; i++) g = fmaxf(g, s[e0 + i]);
+    k = float_key(g);
+    return true;
+  }
+};
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned r;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(r));
+  return r;
+}
+
+// warp-aggregated append of one 32- or 64-bit item per taking lane
+template <class T>
+__device__ __forceinline__ void warp_append(bool take, uint32_t* counter, T* list, uint32_t cap, T item) {
+  const unsigned ball = __ballot_sync(0xFFFFFFFFu, take);
+  if (ball == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(ball) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, (uint32_t)__popc(ball));
+  base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  const uint32_t at = base + (uint32_t)__popc(ball & lanemask_lt());
+  if (take && at < cap) list[at] = item;
+}
+
+// the K scores of one warp tile: lane l holds entries t0 + 32 i + l
+__device__ __forceinline__ void rs_load_tile(const float* s, int64_t t0, int64_t nv, float v[8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int64_t e = t0 + 32 * i + lane;
+    v[i] = e < nv ? __ldg(s + e) : -INFINITY;
+  }
+}
+
+// block maximum key of lanes 8b..8b+7 (valid in lanes with lane % 8 == 0)
+__device__ __forceinline__ uint32_t rs_block_key(float v, int64_t r, int64_t nb) {
+  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+  return r == nb - 1 ? float_key(INFINITY) : float_key(v);
+}
+
+struct RsRowInfo {
+  int64_t nv, nb;
+  bool do_e, do_b;
+};
+
+__device__ __forceinline__ RsRowInfo rs_row_info(const RsParams& p, int64_t bq) {
+  RsRowInfo r;
+  r.nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[bq / p.Q]);
+  if (r.nv > p.max_n) r.nv = p.max_n;
+  r.nb = ceil_div(r.nv, BLK);
+  r.do_e = p.K > 0 && r.nv > p.K;
+  r.do_b = p.M > 0 && r.nb > p.M;
+  return r;
+}
+
+// Threshold bin of a complete row histogram: the bin b1 holding the K-th
+// largest key, and the number of keys in higher bins.  Whole block (RS_THREADS).
+__device__ void rs_threshold(RsRow& row, int K, uint32_t* warp_sums) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int PER = RS_BINS / RS_THREADS;      // 8 bins per thread, descending
+  uint32_t h[PER], sum = 0;
+#pragma unroll
+  for (int q = 0; q < PER; q++) {
+    h[q] = __ldcg(&row.hist[RS_BINS - 1 - PER * tid - q]);
+    sum += h[q];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0;
+  for (int w = 0; w < warp; w++) before += warp_sums[w];
+  const uint32_t excl = before + incl - sum;
+  if (excl < (uint32_t)K && excl + sum >= (uint32_t)K) {
+    uint32_t cum = excl;
+#pragma unroll
+    for (int q = 0; q < PER; q++) {
+      if (cum + h[q] >= (uint32_t)K) {
+        row.b1 = (uint32_t)(RS_BINS - 1 - PER * tid - q);
+        row.above = cum;
+        break;
+      }
+      cum += h[q];
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(RS_THREADS) rs_hist_kernel(RsParams p) {
+  extern __shared__ uint32_t rs_dyn[];
+  uint32_t* hist_e = rs_dyn;
+  uint32_t* hist_b = rs_dyn + RS_BINS;
+  __shared__ uint32_t warp_sums[RS_WARPS];
+  __shared__ int is_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bq = blockIdx.x / p.chunks;
+  const int64_t chunk = blockIdx.x % p.chunks;
+  const RsRowInfo ri = rs_row_info(p, bq);
+  if (!ri.do_e && !ri.do_b) return;
+  RsRow& row_e = p.rows[bq];
+  RsRow& row_b = p.rows[p.BQ + bq];
+  for (int i = tid; i < 2 * RS_BINS; i += RS_THREADS) rs_dyn[i] = 0;
+  __syncthreads();
+  const float* s = p.scores + bq * p.max_n;
+  const int64_t e_lo = chunk * RS_CHUNK;
+  const int64_t e_hi = e_lo + RS_CHUNK < ri.nv ? e_lo + RS_CHUNK : ri.nv;
+  for (int64_t t0 = e_lo + (int64_t)warp * RS_TILE; t0 < e_hi; t0 += (int64_t)RS_WARPS * RS_TILE) {
+    float v[8];
+    rs_load_tile(s, t0, ri.nv, v);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const int64_t e = t0 + 32 * i + lane;
+      if (ri.do_e && e < ri.nv) atomicAdd(&hist_e[float_key(v[i]) >> RS_SHIFT], 1u);
+      if (ri.do_b) {
+        const int64_t r = e / BLK;
+        const uint32_t k = rs_block_key(v[i], r, ri.nb);
+        if ((lane & 7) == 0 && r < ri.nb) atomicAdd(&hist_b[k >> RS_SHIFT], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < RS_BINS; b += RS_THREADS) {
+    if (ri.do_e && hist_e[b]) atomicAdd(&row_e.hist[b], hist_e[b]);
+    if (ri.do_b && hist_b[b]) atomicAdd(&row_b.hist[b], hist_b[b]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(&row_e.done, 1u) == (uint32_t)p.chunks - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  if (ri.do_e) rs_threshold(row_e, p.K, warp_sums);
+  if (ri.do_b) rs_threshold(row_b, p.M, warp_sums);
+}
+
+__global__ void __launch_bounds__(RS_THREADS) rs_filter_kernel(RsParams p) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bq = blockIdx.x / p.chunks;
+  const int64_t chunk = blockIdx.x % p.chunks;
+  const RsRowInfo ri = rs_row_info(p, bq);
+  if (!ri.do_e && !ri.do_b) return;
+  RsRow& row_e = p.rows[bq];
+  RsRow& row_b = p.rows[p.BQ + bq];
+  const uint32_t b1e = ri.do_e ? row_e.b1 : 0u, b1b = ri.do_b ? row_b.b1 : 0u;
+  const bool keep_e = ri.do_e && row_e.hist[b1e] <= (uint32_t)RS_CAP;
+  const bool keep_b = ri.do_b && row_b.hist[b1b] <= (uint32_t)RS_CAP;
+  int32_t* gt_e = p.gt + bq * RS_MAX_OUT;
+  int32_t* gt_b = p.gt + (p.BQ + bq) * RS_MAX_OUT;
+  unsigned long long* cd_e = p.cand + bq * RS_CAP;
+  unsigned long long* cd_b = p.cand + (p.BQ + bq) * RS_CAP;
+  const float* s = p.scores + bq * p.max_n;
+  const int64_t e_lo = chunk * RS_CHUNK;
+  const int64_t e_hi = e_lo + RS_CHUNK < ri.nv ? e_lo + RS_CHUNK : ri.nv;
+  for (int64_t t0 = e_lo + (int64_t)warp * RS_TILE; t0 < e_hi; t0 += (int64_t)RS_WARPS * RS_TILE) {
+    float v[8];
+    rs_load_tile(s, t0, ri.nv, v);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const int64_t e = t0 + 32 * i + lane;
+      if (ri.do_e) {
+        const uint32_t k = float_key(v[i]);
+        const uint32_t d = k >> RS_SHIFT;
+        const bool ok = e < ri.nv;
+        warp_append<int32_t>(ok && d > b1e, &row_e.n_gt, gt_e, (uint32_t)p.K, (int32_t)e);
+        warp_append<unsigned long long>(keep_e && ok && d == b1e, &row_e.n_eq, cd_e, (uint32_t)RS_CAP,
+                                        ((unsigned long long)k << 32) | (uint32_t)~(uint32_t)e);
+      }
+      if (ri.do_b) {
+        const int64_t r = e / BLK;
+        const uint32_t k = rs_block_key(v[i], r, ri.nb);
+        const uint32_t d = k >> RS_SHIFT;
+        const bool ok = (lane & 7) == 0 && r < ri.nb;
+        warp_append<int32_t>(ok && d > b1b, &row_b.n_gt, gt_b, (uint32_t)p.M, (int32_t)r);
+        warp_append<unsigned long long>(keep_b && ok && d == b1b, &row_b.n_eq, cd_b, (uint32_t)RS_CAP,
+                                        ((unsigned long long)k << 32) | (uint32_t)~(uint32_t)r);
+      }
+    }
+  }
+}
+
+constexpr int RS_RESOLVE_SMEM = RS_CAP * 8 + (SEL_THREADS / 32) * 256 * 4 + RS_MAX_OUT * 4;
+
+__global__ void __launch_bounds__(SEL_THREADS) rs_resolve_kernel(RsParams p) {
+  __shared__ ScanSmem sm;
+  __shared__ uint32_t n_taken;
+  __shared__ uint32_t bc[3];
+  extern __shared__ __align__(16) unsigned char rs_res_dyn[];
+  unsigned long long* cs = reinterpret_cast<unsigned long long*>(rs_res_dyn);
+  uint32_t* whist = reinterpret_cast<uint32_t*>(rs_res_dyn + RS_CAP * 8);
+  int32_t* ids = reinterpret_cast<int32_t*>(rs_res_dyn + RS_CAP * 8 + (SEL_THREADS / 32) * 256 * 4);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t bq = blockIdx.x;
+  const int kind = blockIdx.y;                   // 0: entries (top-K), 1: blocks (top-M)
+  const int KK = kind ? p.M : p.K;
+  if (KK <= 0) return;
+  const RsRowInfo ri = rs_row_info(p, bq);
+  const int64_t n = kind ? ri.nb : ri.nv;
+  int32_t* out = kind ? p.pool + bq * p.M : p.sel + bq * p.K;
+  if (n <= KK) {
+    for (int i = tid; i < KK; i += SEL_THREADS) out[i] = i < n ? i : -1;
+    return;
+  }
+  const float* s = p.scores + bq * p.max_n;
+  const RsRow& row = p.rows[kind * p.BQ + bq];
+  const uint32_t above = row.above;
+  const uint32_t n_eq = row.hist[row.b1];
+  if (n_eq > (uint32_t)RS_CAP) {                 // bunched threshold bin: exact single-CTA select
+    if (kind) radix_select_block(BlockScoreKeys{s, ri.nv}, IdentityIds{}, n, KK, out, sm);
+    else radix_select_block(FullKeys{s}, IdentityIds{}, n, KK, out, sm);
+    return;
+  }
+  const int32_t* gt = p.gt + (kind * p.BQ + bq) * RS_MAX_OUT;
+  const unsigned long long* cd = p.cand + (kind * p.BQ + bq) * RS_CAP;
+  for (uint32_t i = tid; i < above; i += SEL_THREADS) ids[i] = gt[i];
+  for (uint32_t i = tid; i < n_eq; i += SEL_THREADS) cs[i] = cd[i] << RS_BITS;   // drop the shared bin bits
+  if (tid == 0) n_taken = 0;
+  __syncthreads();
+  // Candidates are unique 64-bit values (bits 63..12 = low key bits, ~id);
+  // keep the `rem` largest with digit passes from the top.
+  uint32_t rem = (uint32_t)KK - above;
+  unsigned long long prefix = 0, mask = 0;
+  if (rem < n_eq) {
+    uint32_t* myh = whist + warp * 256;
+    for (int shift = 56; shift >= 8; shift -= 8) {
+      for (int i = lane; i < 256; i += 32) myh[i] = 0;
+      __syncwarp();
+      for (uint32_t base = 0; base < n_eq; base += SEL_THREADS) {
+        const uint32_t i = base + tid;
+        const unsigned long long c = i < n_eq ? cs[i] : 0ull;
+        const bool ok = i < n_eq && (c & mask) == prefix;
+        const uint32_t digit = ok ? (uint32_t)(c >> shift) & 255u : 256u;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, digit);
+        if (ok && lane == __ffs(peers) - 1) atomicAdd(&myh[digit], (uint32_t)__popc(peers));
+      }
+      __syncthreads();
+      if (tid < 256) {
+        uint32_t tot = 0;
+#pragma unroll 8
+        for (int w = 0; w < SEL_THREADS / 32; w++) tot += whist[w * 256 + tid];
+        sm.hist[tid] = tot;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; q++) { c[q] = sm.hist[255 - 8 * lane - q]; sum += c[q]; }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const uint32_t excl = incl - sum;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= rem);
+        if (lane == __ffs(hit) - 1) {
+          uint32_t cum = excl;
+          int d = 255 - 8 * lane;
+#pragma unroll
+          for (int q = 0; q < 8; q++) {
+            if (cum + c[q] >= rem) { d = 255 - 8 * lane - q; break; }
+            cum += c[q];
+          }
+          bc[0] = (uint32_t)d;
+          bc[1] = rem - cum;                     // still needed from bin d
+          bc[2] = sm.hist[d];
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)bc[0] << shift;
+      mask |= 255ull << shift;
+      rem = bc[1];
+      const bool whole = bc[2] == rem;           // the rest of the bin is taken whole
+      __syncthreads();
+      if (whole) break;
+    }
+  }
+  for (uint32_t base = 0; base < n_eq; base += SEL_THREADS) {
+    const uint32_t i = base + tid;
+    if (i < n_eq && (cs[i] & mask) >= prefix) {
+      const uint32_t at = above + atomicAdd(&n_taken, 1u);
+      if (at < (uint32_t)KK) ids[at] = (int32_t)~(uint32_t)(cs[i] >> RS_BITS);
+    }
+  }
+  // bitonic sort of the KK ids, ascending
+  int P = 1;
+  while (P < KK) P <<= 1;
+  __syncthreads();
+  for (int i = KK + tid; i < P; i += SEL_THREADS) ids[i] = 0x7FFFFFFF;
+  __syncthreads();
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int t = tid; t < P / 2; t += SEL_THREADS) {
+        const int i = (t / j) * 2 * j + (t % j);
+        const int l = i + j;
+        const int32_t a = ids[i], b = ids[l];
+        if ((a > b) == ((i & k) == 0)) { ids[i] = b; ids[l] = a; }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < KK; i += SEL_THREADS) out[i] = ids[i];
+}
+
+// Full-row selection of the entry top-K (K > 0) and/or the block top-M
+// (M > 0) of every row, with `scratch` (row_select_bytes(B*Q), 256-byte
+// aligned) as per-row histograms and lists.
+cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m, int B,
+                              int Q, int64_t max_n, int K, int32_t* sel, int M, int32_t* pool, void* scratch,
+                              cudaStream_t stream) {
+  const int64_t BQ = (int64_t)B * Q;
+  if (BQ == 0) return cudaSuccess;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(rs_resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         RS_RESOLVE_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(rs_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               2 * RS_BINS * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  unsigned char* cur = static_cast<unsigned char*>(scratch);
+  RsParams p{};
+  p.scores = scores;
+  p.q_pos = q_pos;
+  p.n_entries = n_entries;
+  p.m = m;
+  p.Q = Q;
+  p.K = sel ? K : 0;
+  p.M = pool ? M : 0;
+  p.max_n = max_n;
+  p.chunks = (int)(max_n > 0 ? ceil_div(max_n, RS_CHUNK) : 1);
+  p.sel = sel;
+  p.pool = pool;
+  p.BQ = BQ;
+  const size_t rows_bytes = (size_t)(2 * BQ) * sizeof(RsRow);
+  p.rows = reinterpret_cast<RsRow*>(cur);
+  cur += up(rows_bytes);
+  p.gt = reinterpret_cast<int32_t*>(cur);
+  cur += up((size_t)(2 * BQ) * RS_MAX_OUT * sizeof(int32_t));
+  p.cand = reinterpret_cast<unsigned long long*>(cur);
+  cudaError_t e = cudaMemsetAsync(p.rows, 0, rows_bytes, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t scan_ctas = BQ * p.chunks;
+  if (scan_ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  rs_hist_kernel<<<(unsigned)scan_ctas, RS_THREADS, 2 * RS_BINS * sizeof(uint32_t), stream>>>(p);
+  rs_filter_kernel<<<(unsigned)scan_ctas, RS_THREADS, 0, stream>>>(p);
+  rs_resolve_kernel<<<dim3((unsigned)BQ, 2), SEL_THREADS, RS_RESOLVE_SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 

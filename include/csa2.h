@@ -185,7 +185,8 @@ csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx,
  * the lower block id.  [dilfish §4.7; zartbot §2.3.4]
  *   scores       float [B][Q][max_n] in the layout of csa2_index_score(NULL pool).
  *   pool_blocks  out int32 [B][Q][M]: chosen block ids ascending, -1 padded.
- * Workspace: csa2_block_topk_workspace_size.
+ * Workspace: csa2_block_topk_workspace_size (per-row histograms and lists
+ * when max_n > 16384, the per-block maxima otherwise).
  */
 size_t csa2_block_topk_workspace_size(int B, int Q, int64_t max_n);
 csa2_status csa2_block_topk(const csa2_cache *cache, const float *scores, const int64_t *q_pos,
@@ -225,8 +226,10 @@ csa2_status csa2_block_topk_static(const csa2_cache *cache, const float *scores,
  *                [B][Q][max_n] layout.  Otherwise choose inside the pool,
  *                scores in the [B][Q][M*8] pool layout of csa2_index_score.
  *   sel          out int32 [B][Q][K]: entry ids ascending, -1 padded.
- * Needs only the workspace header.
+ * Workspace: the header in pool mode; csa2_select_topk_workspace_size(B, Q,
+ * max_n) without a pool (per-row histograms and lists when max_n > 16384).
  */
+size_t csa2_select_topk_workspace_size(int B, int Q, int64_t max_n);
 csa2_status csa2_select_topk(const csa2_cache *cache, const float *scores,
                              const int64_t *q_pos, const int32_t *pool_blocks, int M, int K,
                              int32_t *sel, int B, int Q, int64_t max_n, void *ws,

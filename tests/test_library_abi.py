@@ -48,6 +48,11 @@ def test_host_only_calls_without_gpu(lib_path):
     assert lib.csa2_status_string(6) == b"CSA2_ERR_BOUNDS"
     assert lib.csa2_attn_workspace_size(1, 1, 512) >= 256
     assert lib.csa2_block_topk_workspace_size(2, 3, 100) == 256 + 512    # 2*3*13*4 = 312 bytes -> 512
+    assert lib.csa2_select_topk_workspace_size(2, 3, 16384) == 256       # short rows: header only
+    # long rows: per row and kind a 4096-bin histogram + 16 counters, 2048 sure picks, 8192 candidates
+    per = 2 * 6 * (4096 * 4 + 64 + 2048 * 4 + 8192 * 8)
+    assert lib.csa2_select_topk_workspace_size(2, 3, 16385) >= 256 + per
+    assert lib.csa2_block_topk_workspace_size(2, 3, 1 << 20) == lib.csa2_select_topk_workspace_size(2, 3, 1 << 20)
     # argument validation happens before any CUDA call
     assert lib.csa2_index_score(None, None, None, None, None, 0, None, 1, 1, 10, None, 0, None) == 1
 
