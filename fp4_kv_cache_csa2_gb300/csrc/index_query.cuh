@@ -52,4 +52,29 @@ __device__ __forceinline__ void quantize_index_query_warp(const uint16_t* q_head
   sfb[lane] = sfw;
 }
 
+// Head weights of one query as 16 packed (even head, odd head) pairs.
+__device__ __forceinline__ void pack_head_weights(const float* w, unsigned long long* w2) {
+#pragma unroll
+  for (int i = 0; i < HI / 2; i++)
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w2[i]) : "f"(w[2 * i]), "f"(w[2 * i + 1]));
+}
+
+// s = sum_h w_h * max(v_h, 0) over the 32 head dot products of one entry, as
+// two binary32 chains (even heads and odd heads, each in head order, each term
+// one fused multiply-add) added at the end.  Every indexer kernel uses this
+// one order, so an entry's score does not depend on which kernel computed it.
+__device__ __forceinline__ float index_head_sum(const float* v, const unsigned long long* w2) {
+  unsigned long long acc;
+  asm("mov.b64 %0, 0;" : "=l"(acc));
+#pragma unroll
+  for (int i = 0; i < HI / 2; i++) {
+    unsigned long long x;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(fmaxf(v[2 * i], 0.0f)), "f"(fmaxf(v[2 * i + 1], 0.0f)));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(x), "l"(w2[i]));
+  }
+  float even, odd;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(even), "=f"(odd) : "l"(acc));
+  return __fadd_rn(even, odd);
+}
+
 }  // namespace csa2

@@ -7,19 +7,31 @@
 // candidate pool), §2.4.4 (FP4 indexer Q and K); "4. 层维度(下):CSA2 与每 token
 // 890 字节" §4.4 (index K is OCP MXFP4: E2M1 + one E8M0 scale per 32), §4.7.
 //
-// One CTA scores a run of 128-entry tiles of one query:
+// One CTA scores a run of 128-entry tiles for a group of NQ queries of one
+// sequence (NQ = 1 for decode and pool scans; NQ = 4 when a sequence brings many
+// queries, as a prefill chunk does, so that every tile of keys loaded feeds a
+// 128-column MMA instead of a 32-column one):
 //   warp 0      producer: full scans load 128-entry tiles of index-K codes
-//               (SW64 K-major, 64 B per entry) with a 2-D tensor map and the
-//               4-byte E8M0 words with 1-D bulk copies (mbarrier expect-tx); pool
-//               scans gather the 16 candidate blocks of a tile with cp.async,
-//               one 512-byte block per warp instruction, into the same layout.
+//               (SW64 K-major, 64 B per entry) with a 3-D tensor map that puts
+//               slot 4g + q of the tile in row 32q + g, and the 4-byte E8M0
+//               words with 1-D bulk copies (mbarrier expect-tx); pool scans
+//               gather the 16 candidate blocks of a tile with cp.async, one
+//               512-byte block per warp instruction, into the same rows.
 //               6-stage ring.
-//   warp 1      TMEM owner and MMA issuer: per tile two M=128 N=32 K=64
-//               block-scaled MMAs into one of two TMEM accumulators.
-//   warps 2..5  per tile: copy the 128 scale words into TMEM (row m -> lane m,
-//               column base + m/32), then the epilogue of the previous tile:
-//               32 head dot products from TMEM -> ReLU -> weighted sum -> score.
-// The query is quantised once per CTA (the B operand, 2 KB, and its scales).
+//   warp 1..I   MMA issuers (I = 2 for NQ = 1, 3 for NQ = 4; warp 1 owns
+//               TMEM): issuer k takes every I-th tile into its own TMEM
+//               accumulator: one tcgen05.cp of the tile's 512 bytes of scale
+//               words into TMEM (with that row order, 16 contiguous bytes per
+//               lane of every lane quarter: row 32q + g reads word q), then two
+//               M=128 N=32*NQ K=64 block-scaled MMAs.  A single issuer is bound
+//               by its own wait latencies, not by the tensor core.
+//   warp I+1    publisher: turns the TMA completions (mbarriers) into shared
+//               words the issuers poll.
+//   the rest    4*NQ epilogue warps, one per (TMEM lane quarter, query): 32 head
+//               dot products from TMEM -> ReLU -> weighted sum -> score.
+// The queries are quantised once per CTA (the B operand, 2 KB per query, and
+// its scale words: head n of query j -> lane n of every lane quarter, column
+// base + j).
 // Products of E2M1 values scaled by powers of two are exact; the accumulation
 // is fp32.  Every mbarrier wait is bounded and reports CSA2_ERR_TIMEOUT.
 #include <cstddef>
@@ -32,31 +44,77 @@
 
 namespace csa2 {
 
-constexpr int IS_THREADS = 192;
 constexpr int IS_STAGES = 6;
 constexpr int IS_TILE = 128;
 constexpr int IS_CODES = IS_TILE * IDX_CODE_BYTES;         // 8192
 constexpr int IS_STAGE_BYTES = IS_CODES + 1024;            // codes + 512 B scales, 1 KB aligned stride
 constexpr int IS_POOL_MAX = CSA2_MAX_M;
-constexpr int IS_TMEM_COLS = 128;
-constexpr int IS_ACC_COL = 0;                               // two accumulators of 32 columns
-constexpr int IS_SFA_COL = 64;                              // 4 columns per stage
-constexpr int IS_SFB_COL = 96;
+constexpr int IS_GROUP = 4;                                 // queries per CTA for many-query sequences
 
+// Warp roles: 0 producer; 1..ISSUERS MMA issuers (issuer k takes tiles
+// i = k mod ISSUERS into accumulator k); ISSUERS+1 publisher; then 4*NQ
+// epilogue warps, one per (TMEM lane quarter, query).
+template <int NQ>
+struct IsCfg {
+  static constexpr int N = NQ * HI;                         // MMA N: query heads
+  static constexpr int ISSUERS = NQ == 1 ? 2 : 3;           // = accumulators
+  static constexpr int PUB_WARP = 1 + ISSUERS;
+  static constexpr int EPI0 = PUB_WARP + 1;                 // first epilogue warp
+  static constexpr int EPI_WARPS = 4 * NQ;
+  static constexpr int THREADS = 32 * (EPI0 + EPI_WARPS);
+  static constexpr int ACC_COL = 0;                         // ISSUERS accumulators of N columns
+  static constexpr int SFA_COL = ISSUERS * N;               // 4 columns per stage
+  static constexpr int SFB_COL = SFA_COL + 4 * IS_STAGES;   // NQ columns
+  static constexpr int TMEM_COLS = NQ == 1 ? 128 : 512;
+  static constexpr int MIN_CTAS = NQ == 1 ? 3 : 1;         // resident CTAs per SM (one issue chain each)
+  static_assert(SFB_COL % 8 == 0 && SFB_COL + NQ <= TMEM_COLS, "TMEM columns");
+};
+
+template <int NQ>
 struct IsSmem {
   uint8_t stage[IS_STAGES][IS_STAGE_BYTES];
-  uint8_t qcodes[HI * IDX_CODE_BYTES];      // 2 KB, SW64
+  uint8_t qcodes[NQ * HI * IDX_CODE_BYTES];  // 2 KB per query, SW64
   int32_t pool[IS_POOL_MAX];
-  float w[HI];
-  uint32_t sfb[HI];                          // query scale words (head n -> lane n of every quarter)
-  uint64_t full[IS_STAGES], empty[IS_STAGES], sf_full[IS_STAGES];
-  uint64_t acc_full[2], acc_empty[2];
+  float w[NQ * HI];
+  uint32_t sfb[NQ * HI];                     // query scale words
+  uint64_t full[IS_STAGES], empty[IS_STAGES];
+  uint64_t acc_full[4];
+  uint32_t ready[IS_STAGES];                 // tile i + 1 once tile i sits in stage i % IS_STAGES
+  uint32_t acc_free[4];                      // epilogue warps done reading accumulator k, cumulative
   uint32_t tmem_base;
   volatile int abort_flag;
 };
-constexpr size_t IS_SMEM = sizeof(IsSmem) + 1024;
+template <int NQ>
+constexpr size_t is_smem_bytes() { return sizeof(IsSmem<NQ>) + 1024; }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, IsSmem& sm, WsHeader* hdr) {
+// Shared-memory row of tile slot u: slot 4g + q sits in row 32q + g, so that
+// the 16 bytes of scale words of slots 4g..4g+3 (contiguous as they arrive) are
+// the words lane g of every TMEM lane quarter needs: row 32q + g takes word q.
+__device__ __forceinline__ int is_tile_row(int u) { return 32 * (u & 3) + (u >> 2); }
+
+// Bounded spin until the shared word reaches `target` (acquire); false on
+// abort or timeout (which sets the abort flag and reports CSA2_ERR_TIMEOUT).
+// The issuers poll plain words: after a thread has MMAs in flight, its
+// mbarrier waits return markedly later than the barrier completes.
+template <class Sm>
+__device__ __forceinline__ bool poll_at_least(const uint32_t* word, uint32_t target, Sm& sm, WsHeader* hdr) {
+  for (uint32_t it = 0; it < (1u << 26); it++) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(tc::smem_u32(word)) : "memory");
+    if ((int32_t)(v - target) >= 0) return true;
+    if (sm.abort_flag) return false;
+  }
+  sm.abort_flag = 1;
+  report(hdr, CSA2_ERR_TIMEOUT, 1);
+  return false;
+}
+
+__device__ __forceinline__ void publish_word(uint32_t* word, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" :: "r"(tc::smem_u32(word)), "r"(v) : "memory");
+}
+
+template <class Sm>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm& sm, WsHeader* hdr) {
   if (sm.abort_flag) return false;
   for (int round = 0; round < 64; round++) {
     if (tc::bar_wait(bar, parity, 1u << 16)) return true;
@@ -67,33 +125,44 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Is
   return false;
 }
 
-__global__ void __launch_bounds__(IS_THREADS, 1)
-index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
-                      const __grid_constant__ CUtensorMap map_block) {
+template <int NQ>
+__global__ void __launch_bounds__(IsCfg<NQ>::THREADS, IsCfg<NQ>::MIN_CTAS)
+index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) {
+  using C = IsCfg<NQ>;
   extern __shared__ unsigned char smem_raw[];
-  IsSmem& sm = *reinterpret_cast<IsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  IsSmem<NQ>& sm =
+      *reinterpret_cast<IsSmem<NQ>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bq = (int)blockIdx.y;
-  const int crank = (int)blockIdx.x;         // slice of the query
-  const int b = bq / p.Q;
-  const bool pool_mode = p.pool != nullptr;
+  const int groups = (p.Q + NQ - 1) / NQ;    // query groups per sequence
+  const int b = (int)blockIdx.y / groups;
+  const int qf = ((int)blockIdx.y % groups) * NQ;
+  const int nq = p.Q - qf < NQ ? p.Q - qf : NQ;   // queries in this group
+  const int64_t bq0 = (int64_t)b * p.Q + qf;
+  const int crank = (int)blockIdx.x;         // slice of the group's tiles
+  const bool pool_mode = p.pool != nullptr;  // (NQ == 1 only)
 
-  // ---- this CTA's tile range
-  int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[b]);
-  if (nv > p.cap) {
-    if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
-    nv = p.cap;
-  }
-  int64_t n_units;                         // entries (full) or pool slots (pool)
-  if (pool_mode) {
-    n_units = (int64_t)p.M * BLK;
-  } else {
-    if (nv > p.max_n) {
-      if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
-      nv = p.max_n;
+  // ---- visible entries of each query; this CTA's tile range
+  int64_t nvq[NQ];
+  int64_t n_units = 0;                       // entries (full) or pool slots (pool)
+#pragma unroll
+  for (int j = 0; j < NQ; j++) {
+    int64_t v = 0;
+    if (j < nq) {
+      v = visible_entries(p.q_pos[bq0 + j], p.m, p.n_entries[b]);
+      if (v > p.cap) {
+        if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, v);
+        v = p.cap;
+      }
+      if (!pool_mode && v > p.max_n) {
+        if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, v);
+        v = p.max_n;
+      }
     }
-    n_units = nv;
+    nvq[j] = v;
+    if (v > n_units) n_units = v;
   }
+  if (pool_mode) n_units = (int64_t)p.M * BLK;
+  const int64_t nv = nvq[0];
   const int64_t n_tiles = ceil_div(n_units, IS_TILE);
   const int64_t t0 = (int64_t)crank * p.entries_per_cta;
   int64_t t1 = t0 + p.entries_per_cta;
@@ -102,42 +171,52 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
   if (n == 0) return;
 
   // ---- set-up
-  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, IS_TMEM_COLS);
+  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, C::TMEM_COLS);
   if (tid == 0) {
     for (int s = 0; s < IS_STAGES; s++) {
-      tc::bar_init(&sm.full[s], pool_mode ? 32 : 1);
+      tc::bar_init(&sm.full[s], 1);
       tc::bar_init(&sm.empty[s], 1);
-      tc::bar_init(&sm.sf_full[s], 4);
     }
-    for (int i = 0; i < 2; i++) {
-      tc::bar_init(&sm.acc_full[i], 1);
-      tc::bar_init(&sm.acc_empty[i], 4);
+    for (int k = 0; k < 4; k++) {
+      tc::bar_init(&sm.acc_full[k], 1);
+      sm.acc_free[k] = 0;
     }
+    for (int s = 0; s < IS_STAGES; s++) sm.ready[s] = 0;
     sm.abort_flag = 0;
     tc::bar_init_fence();
   }
-  if (tid < HI) sm.w[tid] = p.w_head[(int64_t)bq * HI + tid];
+  for (int i = tid; i < NQ * HI; i += C::THREADS)
+    sm.w[i] = i < nq * HI ? p.w_head[bq0 * HI + i] : 0.0f;
   if (pool_mode) {
-    const int32_t* pool = p.pool + (int64_t)bq * p.M;
-    for (int i = tid; i < p.M; i += IS_THREADS) sm.pool[i] = pool[i];
+    const int32_t* pool = p.pool + bq0 * p.M;
+    for (int i = tid; i < p.M; i += C::THREADS) sm.pool[i] = pool[i];
   }
-  if (warp == 0 && lane == 0) {
-    tc::prefetch_tensormap(&map_tile);
-    tc::prefetch_tensormap(&map_block);
-  }
+  if (warp == 0 && lane == 0) tc::prefetch_tensormap(&map_tile);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
-  // ---- quantise the query (B operand); its scale words go to TMEM lanes
-  // 32q + n of every lane quarter q (the MMA reads B scales from the quarter of
-  // the A row it is computing)
-  if (warp == 4) quantize_index_query_warp(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
+  // ---- quantise the queries (B operand); the scale word of head n of query j
+  // goes to TMEM lane 32q + n, column SFB_COL + j, of every lane quarter q (the
+  // MMA reads B scales from the quarter of the A row it is computing)
+  if (warp >= C::EPI0 && warp < C::EPI0 + NQ) {
+    const int j = warp - C::EPI0;
+    if (j < nq) {
+      quantize_index_query_warp(p.q_idx + (bq0 + j) * HI * DI, sm.qcodes + j * HI * IDX_CODE_BYTES,
+                                sm.sfb + j * HI);
+    } else {                                  // missing query of a partial group: zero codes, scores unused
+      for (int i = lane; i < HI * IDX_CODE_BYTES / 16; i += 32)
+        reinterpret_cast<uint4*>(sm.qcodes + j * HI * IDX_CODE_BYTES)[i] = make_uint4(0u, 0u, 0u, 0u);
+      sm.sfb[j * HI + lane] = 0u;
+    }
+  }
   tc::fence_proxy_async_smem();
   __syncthreads();
-  if (warp >= 2) {
-    tc::tmem_st_x1(tmem + ((uint32_t)((warp & 3) * 32) << 16) + IS_SFB_COL, sm.sfb[lane]);
+  if (warp >= C::EPI0 && warp < C::EPI0 + 4) {
+#pragma unroll
+    for (int j = 0; j < NQ; j++)
+      tc::tmem_st_x1(tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::SFB_COL + j, sm.sfb[j * HI + lane]);
     tc::tmem_wait_st();
   }
   tc::fence_before_sync();
@@ -148,31 +227,46 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
   const int64_t rows_total = (int64_t)p.B * p.cap;
 
   if (warp == 0) {
-    // ================= TMA producer
+    // ================= producer
     int issued = 0;
-    for (int i = 0; i < n; i++) {
-      const int s = i % IS_STAGES;
-      if (i >= IS_STAGES && !wait_or_abort(&sm.empty[s], ((i / IS_STAGES) - 1) & 1, sm, p.hdr)) break;
-      uint8_t* codes = sm.stage[s];
-      uint8_t* scl = sm.stage[s] + IS_CODES;
-      const int64_t t = t0 + i;
-      if (!pool_mode) {
-        if (lane == 0) {
-          const int64_t row0 = row_base + t * IS_TILE;
+    if (!pool_mode) {
+      if (lane == 0) {
+        for (int i = 0; i < n; i++) {
+          const int s = i % IS_STAGES;
+          if (i >= IS_STAGES && !wait_or_abort(&sm.empty[s], ((i / IS_STAGES) - 1) & 1, sm, p.hdr)) break;
+          const int64_t row0 = row_base + (t0 + i) * IS_TILE;
           int64_t rows = rows_total - row0;
           if (rows > IS_TILE) rows = IS_TILE;
           const uint32_t sbytes = (uint32_t)rows * IDX_SCALE_BYTES;     // cap % 8 == 0 -> multiple of 16
           tc::bar_arrive_expect_tx(&sm.full[s], IS_CODES + sbytes);
-          tc::tma_load_2d(codes, &map_tile, 0, (int32_t)row0, &sm.full[s]);
-          tc::bulk_load(scl, p.idx_scales + row0 * IDX_SCALE_BYTES, sbytes, &sm.full[s]);
+          tc::tma_load_3d(sm.stage[s], &map_tile, 0, (int32_t)(row0 / 4), 0, &sm.full[s]);
+          tc::bulk_load(sm.stage[s] + IS_CODES, p.idx_scales + row0 * IDX_SCALE_BYTES, sbytes, &sm.full[s]);
+          issued = i + 1;
         }
-      } else {
-        // 16 candidate blocks of 8 entries.  One warp instruction copies one whole
-        // block (512 contiguous code bytes, 16 per lane: entry l/4, 16-byte chunk
-        // l%4) into the SW64 layout, so each instruction touches 4 cache lines;
-        // lanes 2b and 2b+1 then copy block b's 32 bytes of scale words.  Each
-        // lane's arrival fires once its own copies have landed.
-        const int64_t pl = t * 16 + (lane & 15);
+        if (sm.abort_flag) {
+          // drain copies still in flight before the CTA exits
+          for (int i = issued - 1; i >= 0 && i >= issued - IS_STAGES; i--)
+            tc::bar_wait(&sm.full[i % IS_STAGES], (i / IS_STAGES) & 1, 1u << 20);
+        }
+      }
+    } else {
+      // 16 candidate blocks of 8 entries per tile.  One warp instruction copies
+      // one whole block (512 contiguous code bytes, 16 per lane: entry l/4,
+      // 16-byte chunk l%4) to the tile rows of its entries; lanes 2b and 2b+1
+      // copy block b's 32 bytes of scale words.  A tile is published two tiles
+      // later, once its copies have retired and been fenced for the tensor core.
+      constexpr int LAG = 2;
+      auto publish = [&](int i) {
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) publish_word(&sm.ready[i % IS_STAGES], (uint32_t)(i + 1));
+      };
+      for (int i = 0; i < n; i++) {
+        const int s = i % IS_STAGES;
+        if (i >= IS_STAGES && !wait_or_abort(&sm.empty[s], ((i / IS_STAGES) - 1) & 1, sm, p.hdr)) break;
+        uint8_t* codes = sm.stage[s];
+        uint8_t* scl = sm.stage[s] + IS_CODES;
+        const int64_t pl = (t0 + i) * 16 + (lane & 15);
         int32_t my_blk = (pl < p.M) ? sm.pool[pl] : -1;
         if (my_blk >= 0 && (int64_t)my_blk * BLK >= p.cap) my_blk = -1;   // reported by the epilogue
         const int r = lane >> 2, c = lane & 3;
@@ -180,7 +274,8 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
         for (int sb = 0; sb < 16; sb++) {
           const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, sb);
           if (blk < 0) continue;
-          const int trow = sb * BLK + r;
+          const int u = sb * BLK + r;                       // slot of the tile
+          const int trow = is_tile_row(u);
           const uint8_t* src = p.idx_codes + (row_base + (int64_t)blk * BLK) * IDX_CODE_BYTES + lane * 16;
           asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
                        :: "r"(tc::smem_u32(codes + trow * 64 + ((c ^ ((trow >> 1) & 3)) * 16))), "l"(src) : "memory");
@@ -193,83 +288,91 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
                          :: "r"(tc::smem_u32(scl + sb * 32 + half * 16)),
                             "l"(p.idx_scales + (row_base + (int64_t)blk * BLK) * IDX_SCALE_BYTES + half * 16) : "memory");
         }
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(tc::smem_u32(&sm.full[s])) : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (i >= LAG) {
+          asm volatile("cp.async.wait_group %0;" :: "n"(LAG) : "memory");
+          publish(i - LAG);
+        }
+        issued = i + 1;
       }
-      issued = i + 1;
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      for (int i = issued - LAG < 0 ? 0 : issued - LAG; i < issued; i++) publish(i);
     }
-    if (sm.abort_flag && lane == 0) {
-      // drain copies still in flight before the CTA exits
-      for (int i = issued - 1; i >= 0 && i >= issued - IS_STAGES; i--)
-        tc::bar_wait(&sm.full[i % IS_STAGES], (i / IS_STAGES) & 1, 1u << 20);
-    }
-  } else if (warp == 1) {
-    // ================= MMA issuer
+  } else if (warp <= C::ISSUERS) {
+    // ================= MMA issuer k: tiles k, k + ISSUERS, ... into accumulator k
+    const int k = warp - 1;
     if (lane == 0) {
       const uint64_t bdesc = tc::smem_desc(tc::smem_u32(sm.qcodes), 16, 512, tc::SW_64B);
-      constexpr uint32_t id0 = tc::idesc_mxf4(IS_TILE, HI, 0, 0);
-      constexpr uint32_t id1 = tc::idesc_mxf4(IS_TILE, HI, 2, 2);
-      for (int i = 0; i < n; i++) {
-        const int s = i % IS_STAGES, buf = i & 1;
-        if (!wait_or_abort(&sm.sf_full[s], (i / IS_STAGES) & 1, sm, p.hdr)) break;
-        if (i >= 2 && !wait_or_abort(&sm.acc_empty[buf], ((i >> 1) - 1) & 1, sm, p.hdr)) break;
+      constexpr uint32_t id0 = tc::idesc_mxf4(IS_TILE, C::N, 0, 0);
+      constexpr uint32_t id1 = tc::idesc_mxf4(IS_TILE, C::N, 2, 2);
+      const uint32_t d = tmem + C::ACC_COL + k * C::N;
+      for (int i = k, use = 0; i < n; i += C::ISSUERS, use++) {
+        const int s = i % IS_STAGES;
+        if (!poll_at_least(&sm.ready[s], (uint32_t)(i + 1), sm, p.hdr)) break;
+        if (use > 0 && !poll_at_least(&sm.acc_free[k], (uint32_t)(C::EPI_WARPS * use), sm, p.hdr)) break;
         tc::fence_after_sync();
+        const uint32_t sfa = tmem + C::SFA_COL + s * 4;
+        // 32 rows x 16 bytes (scale words 4g..4g+3) to lanes 32q + g of every quarter q
+        tc::tmem_cp_32x128b_warpx4(sfa, tc::smem_desc(tc::smem_u32(sm.stage[s] + IS_CODES), 128, 128, tc::SW_NONE));
         const uint64_t adesc = tc::smem_desc(tc::smem_u32(sm.stage[s]), 16, 512, tc::SW_64B);
-        const uint32_t d = tmem + IS_ACC_COL + buf * 32;
-        const uint32_t sfa = tmem + IS_SFA_COL + s * 4;
-        tc::mma_mxf4(d, adesc, bdesc, id0, sfa, tmem + IS_SFB_COL, 0);
-        tc::mma_mxf4(d, adesc + 2, bdesc + 2, id1, sfa, tmem + IS_SFB_COL, 1);   // next 32 bytes of K
+        tc::mma_mxf4(d, adesc, bdesc, id0, sfa, tmem + C::SFB_COL, 0);
+        tc::mma_mxf4(d, adesc + 2, bdesc + 2, id1, sfa, tmem + C::SFB_COL, 1);   // next 32 bytes of K
         tc::commit(&sm.empty[s]);
-        tc::commit(&sm.acc_full[buf]);
+        tc::commit(&sm.acc_full[k]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == C::PUB_WARP) {
+    // ================= publisher: TMA completions -> ready words for the issuers
+    if (!pool_mode && lane == 0) {
+      for (int i = 0; i < n; i++) {
+        if (!wait_or_abort(&sm.full[i % IS_STAGES], (i / IS_STAGES) & 1, sm, p.hdr)) break;
+        publish_word(&sm.ready[i % IS_STAGES], (uint32_t)(i + 1));
       }
     }
     __syncwarp();
   } else {
-    // ================= scale copy into TMEM + epilogue (warps 2..5)
-    const int q = warp & 3;                   // TMEM lane quarter of this warp
-    const int m = q * 32 + lane;              // tile row owned by this thread
+    // ================= epilogue: warp (lane quarter q, query jq); lane r of
+    // quarter q holds tile row 32q + r = slot 4r + q of the tile
+    const int q = warp & 3;
+    const int jq = (warp - C::EPI0) >> 2;
+    const int slot = 4 * lane + q;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    float* out_row = p.scores + (pool_mode ? (int64_t)bq * p.M * BLK : (int64_t)bq * p.max_n);
-    for (int i = 0; i <= n; i++) {
-      if (i < n) {
-        const int s = i % IS_STAGES;
-        if (!wait_or_abort(&sm.full[s], (i / IS_STAGES) & 1, sm, p.hdr)) break;
-        const uint32_t word = *reinterpret_cast<const uint32_t*>(sm.stage[s] + IS_CODES + m * 4);
-        tc::tmem_st_x1(tmem + lane_off + IS_SFA_COL + s * 4 + q, word);
-        tc::tmem_wait_st();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::bar_arrive(&sm.sf_full[s]);
-      }
-      if (i >= 1) {
-        const int j = i - 1, buf = j & 1;
-        if (!wait_or_abort(&sm.acc_full[buf], (j >> 1) & 1, sm, p.hdr)) break;
-        tc::fence_after_sync();
-        float v[32];
-        tc::tmem_ld_x32(tmem + lane_off + IS_ACC_COL + buf * 32, v);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::bar_arrive(&sm.acc_empty[buf]);
-        float sc = 0.0f;
+    int64_t nv_mine = nvq[0];
 #pragma unroll
-        for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(v[h], 0.0f), sc);
-        const int64_t u = (t0 + j) * IS_TILE + m;
-        if (!pool_mode) {
-          if (u < n_units) out_row[u] = sc;
-        } else {
-          bool ok = false;
-          if (u < n_units) {
-            const int32_t blk = sm.pool[u / BLK];
-            const int64_t e = (int64_t)blk * BLK + (u % BLK);
-            if (blk >= 0) {
-              if ((int64_t)blk * BLK >= p.cap) {
-                if ((u % BLK) == 0) report(p.hdr, CSA2_ERR_BOUNDS, blk);
-              } else if (e < nv) {
-                ok = true;
-              }
+    for (int j = 1; j < NQ; j++)
+      if (jq == j) nv_mine = nvq[j];
+    float* out_row = p.scores + (pool_mode ? bq0 * p.M * BLK : (bq0 + jq) * p.max_n);
+    unsigned long long w2[HI / 2];
+    pack_head_weights(sm.w + jq * HI, w2);
+    for (int j = 0; j < n; j++) {
+      const int k = j % C::ISSUERS;
+      if (!wait_or_abort(&sm.acc_full[k], (j / C::ISSUERS) & 1, sm, p.hdr)) break;
+      tc::fence_after_sync();
+      float v[32];
+      tc::tmem_ld_x32(tmem + lane_off + C::ACC_COL + k * C::N + jq * HI, v);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" :: "r"(tc::smem_u32(&sm.acc_free[k])) : "memory");
+      const float sc = index_head_sum(v, w2);
+      const int64_t u = (t0 + j) * IS_TILE + slot;
+      if (!pool_mode) {
+        if (u < nv_mine && jq < nq) out_row[u] = sc;
+      } else {
+        bool ok = false;
+        if (u < n_units) {
+          const int32_t blk = sm.pool[u / BLK];
+          const int64_t e = (int64_t)blk * BLK + (u % BLK);
+          if (blk >= 0) {
+            if ((int64_t)blk * BLK >= p.cap) {
+              if ((u % BLK) == 0) report(p.hdr, CSA2_ERR_BOUNDS, blk);
+            } else if (e < nv) {
+              ok = true;
             }
           }
-          if (u < n_units) out_row[u] = ok ? sc : -INFINITY;
         }
+        if (u < n_units) out_row[u] = ok ? sc : -INFINITY;
       }
     }
   }
@@ -278,7 +381,7 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile,
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, IS_TMEM_COLS);
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -295,15 +398,18 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D byte tensor [rows][64] with SW64 boxes of `box_rows` rows.
-static bool encode_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+// Index-code rows [rows][64 B] seen as [rows/4 groups g][4 members q][64 B], so
+// that one box of 32 groups x 4 members lands member-major: shared row 32q + g
+// holds entry 4g + q of the tile (the row order the scale-word copy needs), in
+// the SW64 layout.
+static bool encode_tile_rows(CUtensorMap* map, const void* base, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {64, rows};
-  cuuint64_t strides[1] = {64};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[3] = {64, rows / 4, 4};
+  cuuint64_t strides[2] = {4 * 64, 64};
+  cuuint32_t box[3] = {64, IS_TILE / 4, 4};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -314,8 +420,15 @@ static cudaError_t set_is_attrs() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev == dev) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)IS_SMEM);
+  static_assert(IsCfg<1>::MIN_CTAS * (is_smem_bytes<1>() + 1024) <= 228 * 1024, "resident CTAs");
+  cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)is_smem_bytes<1>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(index_score_tc_kernel<IS_GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)is_smem_bytes<IS_GROUP>());
   if (e == cudaSuccess) attr_dev = dev;
   return e;
 }
@@ -330,21 +443,30 @@ cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   const uint64_t rows = (uint64_t)p.B * (uint64_t)p.cap;
   if (rows == 0) return cudaSuccess;
-  CUtensorMap map_tile, map_block;
-  if (!encode_rows64(&map_tile, p.idx_codes, rows, IS_TILE) || !encode_rows64(&map_block, p.idx_codes, rows, BLK))
-    return cudaErrorInvalidValue;
+  CUtensorMap map_tile;
+  if (!encode_tile_rows(&map_tile, p.idx_codes, rows)) return cudaErrorInvalidValue;
   const int64_t units = p.pool ? (int64_t)p.M * BLK : p.max_n;
   const int64_t tiles = ceil_div(units, IS_TILE);
   if (tiles == 0) return cudaSuccess;
-  const int64_t BQ = (int64_t)p.B * p.Q;
-  // aim at ~3 CTAs per SM over the whole launch, at least 2 tiles per CTA
-  int64_t split = ceil_div(3 * (int64_t)num_sms, BQ);
+  // many queries per sequence (and no pool): groups of IS_GROUP queries share each key tile
+  const bool grouped = p.pool == nullptr && p.Q >= IS_GROUP;
+  const int nq = grouped ? IS_GROUP : 1;
+  const int64_t groups = (int64_t)p.B * ceil_div(p.Q, nq);
+  if (groups > 65535) return cudaErrorInvalidValue;
+  // one wave: as many CTAs as are resident at once (the launch bounds and the
+  // shared-memory carveout guarantee MIN_CTAS per SM), at least 2 tiles per CTA
+  const int64_t resident = (int64_t)(grouped ? IsCfg<IS_GROUP>::MIN_CTAS : IsCfg<1>::MIN_CTAS) * num_sms;
+  int64_t split = resident / groups;
   if (split > ceil_div(tiles, 2)) split = ceil_div(tiles, 2);
   if (split < 1) split = 1;
   const int64_t per = ceil_div(tiles, split);
   p.entries_per_cta = per;     // tiles per CTA
-  dim3 grid((unsigned)ceil_div(tiles, per), (unsigned)BQ);
-  index_score_tc_kernel<<<grid, IS_THREADS, IS_SMEM, stream>>>(p, map_tile, map_block);
+  dim3 grid((unsigned)ceil_div(tiles, per), (unsigned)groups);
+  if (grouped)
+    index_score_tc_kernel<IS_GROUP><<<grid, IsCfg<IS_GROUP>::THREADS, is_smem_bytes<IS_GROUP>(), stream>>>(
+        p, map_tile);
+  else
+    index_score_tc_kernel<1><<<grid, IsCfg<1>::THREADS, is_smem_bytes<1>(), stream>>>(p, map_tile);
   return cudaGetLastError();
 }
 

@@ -399,6 +399,8 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
     tc::fence_after_sync();
     if (ok_all) {
+      unsigned long long w2[HI / 2];
+      pack_head_weights(sm.w, w2);
       // warps 0..3 take the even accumulators and warps 4..7 the odd ones,
       // four TMEM loads in flight per batch
       for (int jb = warp >> 2; jb < rn; jb += 8) {
@@ -413,9 +415,10 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
         for (int jj = 0; jj < 4; jj++) {
           const int j = jb + 2 * jj;
           if (j >= rn) break;
-          float sc = 0.0f;
+          float v[32];
 #pragma unroll
-          for (int h = 0; h < HI; h++) sc = fmaf(sm.w[h], fmaxf(__uint_as_float(acc[jj][h]), 0.0f), sc);
+          for (int h = 0; h < HI; h++) v[h] = __uint_as_float(acc[jj][h]);
+          const float sc = index_head_sum(v, w2);
           const int u = (r0 + j) * RX_TILE + m;                 // slot within this CTA
           const int32_t blk = sm.pool[u / BLK];
           const int64_t e = (int64_t)blk * BLK + (u % BLK);

@@ -123,8 +123,10 @@ def _score_bound(case, codes, scales, b, qi, entries):
     return 1e-5 * (np.maximum(dots, 0) @ np.abs(case.w_head[b, qi].astype(np.float64))) + 1e-30
 
 
-@pytest.mark.parametrize("m,T,B,Q", [(1, 1000, 2, 3), (2, 2 * 2100, 1, 2)])
+@pytest.mark.parametrize("m,T,B,Q", [(1, 1000, 2, 3), (2, 2 * 2100, 1, 2), (1, 1000, 2, 6), (2, 2 * 1500, 1, 9)])
 def test_index_score_all_entries(csa2, m, T, B, Q):
+    """Every visible entry of every query; Q >= 4 runs the grouped kernel (four
+    queries share each key tile), with a partial last group for Q = 6 and 9."""
     case = cases.make_case(B=B, T=T, m=m, Q=Q, M=8, K=8, seed=200 + T)
     L = GpuLayer(csa2, case)
     max_n = case.n_entries + 3
@@ -140,6 +142,24 @@ def test_index_score_all_entries(csa2, m, T, B, Q):
             bound = _score_bound(case, codes, scales, b, qi, ent)
             assert np.all(np.abs(got[b, qi, :nv] - want) <= bound)
             assert np.all(np.isnan(got[b, qi, nv:]))             # invisible columns untouched
+    assert L.ws.sync_status()[0] == 0
+
+
+def test_index_score_grouped_equals_single_query_bit_for_bit(csa2):
+    """Scoring four queries per CTA and one query per CTA runs the same head sum
+    in the same order, so the scores agree bit for bit."""
+    case = cases.make_case(B=1, T=3000, m=1, Q=5, M=8, K=8, seed=251)
+    L = GpuLayer(csa2, case)
+    max_n = case.n_entries
+    grouped = torch.full((1, 5, max_n), float("nan"), device=DEV)
+    csa2.index_score(L.cache, L.q_idx, L.w_head, L.q_pos, grouped, max_n, L.ws)
+    single = torch.full((1, 5, max_n), float("nan"), device=DEV)
+    for qi in range(5):
+        csa2.index_score(L.cache, L.q_idx[:, qi:qi + 1].contiguous(), L.w_head[:, qi:qi + 1].contiguous(),
+                         L.q_pos[:, qi:qi + 1].contiguous(), single[:, qi:qi + 1], max_n, L.ws)
+    a, b = host(grouped), host(single)
+    assert np.array_equal(np.isnan(a), np.isnan(b))
+    assert np.array_equal(a.view(np.uint32)[~np.isnan(a)], b.view(np.uint32)[~np.isnan(b)])
     assert L.ws.sync_status()[0] == 0
 
 
