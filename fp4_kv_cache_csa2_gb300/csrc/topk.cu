@@ -430,12 +430,15 @@ constexpr int RS_BITS = 12;
 constexpr int RS_BINS = 1 << RS_BITS;
 constexpr int RS_SHIFT = 32 - RS_BITS;
 constexpr int RS_CAP = 8192;                     // candidates kept per row and kind
-constexpr int RS_THREADS = 512;
+constexpr int RS_THREADS = 256;
 constexpr int RS_WARPS = RS_THREADS / 32;
-constexpr int RS_TILE = 256;                     // entries per warp tile: 8 coalesced loads
-constexpr int64_t RS_CHUNK = (int64_t)RS_WARPS * RS_TILE * 4;   // 16,384 entries per CTA
+constexpr int RS_TILE = 512;                     // entries per warp tile: lane l holds 128 i + 4 l + c
+constexpr int RS_TILES = 2;                      // warp tiles loaded together
+constexpr int RS_BATCH = RS_WARPS * RS_TILE * RS_TILES;   // 8,192 entries: one batch of a scan CTA
+constexpr int RS_SCAN_CTAS_PER_SM = 4;           // resident scan CTAs per SM (launch bounds)
 constexpr int RS_MAX_OUT = CSA2_MAX_M;           // >= CSA2_MAX_K
-static_assert(RS_CHUNK % (RS_WARPS * RS_TILE) == 0 && 32 % BLK == 0, "warp tiles hold whole blocks");
+constexpr uint32_t RS_STAGE_EQ = 1024;           // threshold-bin candidates staged per scan CTA
+static_assert(BLK == 8, "a block is the 8 entries of two neighbouring lanes");
 
 struct RsRow {                                   // zeroed before every selection
   uint32_t hist[RS_BINS];
@@ -454,6 +457,7 @@ struct RsParams {
   int m, Q, K, M;           // K = 0: no entry selection; M = 0: no block selection
   int64_t max_n;
   int chunks;               // scan CTAs per row
+  int batches;              // batches of RS_BATCH entries per scan CTA
   int32_t* sel;             // [BQ][K]
   int32_t* pool;            // [BQ][M]
   RsRow* rows;              // [2][BQ]: entries, then blocks
@@ -496,34 +500,69 @@ __device__ __forceinline__ void warp_append(bool take, uint32_t* counter, T* lis
   if (take && at < cap) list[at] = item;
 }
 
-// the K scores of one warp tile: lane l holds entries t0 + 32 i + l
-__device__ __forceinline__ void rs_load_tile(const float* s, int64_t t0, int64_t nv, float v[8]) {
+// Warp-aggregated append into a CTA's shared-memory staging list of cap_s
+// items; items beyond it go straight to the global list.
+template <class T>
+__device__ __forceinline__ void stage_append(bool take, uint32_t* s_n, T* s_list, uint32_t cap_s, uint32_t* g_n,
+                                             T* g_list, uint32_t g_cap, T item) {
+  const unsigned ball = __ballot_sync(0xFFFFFFFFu, take);
+  if (ball == 0) return;
   const int lane = threadIdx.x & 31;
+  const int leader = __ffs(ball) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(s_n, (uint32_t)__popc(ball));
+  base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  const uint32_t at = base + (uint32_t)__popc(ball & lanemask_lt());
+  if (take && at < cap_s) s_list[at] = item;
+  warp_append<T>(take && at >= cap_s, g_n, g_list, g_cap, item);
+}
+
+// Scores of one warp tile of RS_TILE entries from t0 (a multiple of RS_TILE):
+// lane l holds entries t0 + 128 i + 4 l + c (i, c < 4), -inf past nv.  VEC:
+// the row is 16-byte aligned, so each group of four is one 16-byte load.
+template <bool VEC>
+__device__ __forceinline__ void rs_load_tile(const float* s, int t0, int nv, float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+  const bool full = t0 + RS_TILE <= nv;
 #pragma unroll
-  for (int i = 0; i < 8; i++) {
-    const int64_t e = t0 + 32 * i + lane;
-    v[i] = e < nv ? __ldg(s + e) : -INFINITY;
+  for (int i = 0; i < 4; i++) {
+    const int e = t0 + 128 * i + 4 * lane;
+    if (VEC && full) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(s + e));
+      v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; c++) v[4 * i + c] = e + c < nv ? __ldg(s + e + c) : -INFINITY;
+    }
   }
 }
 
-// block maximum key of lanes 8b..8b+7 (valid in lanes with lane % 8 == 0)
-__device__ __forceinline__ uint32_t rs_block_key(float v, int64_t r, int64_t nb) {
-  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
-  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
-  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
-  return r == nb - 1 ? float_key(INFINITY) : float_key(v);
+// Block keys of a loaded tile: block t0/8 + 16 i + l/2 is the 8 entries of
+// lanes l and l^1; its key (max, or +inf for the newest block nb - 1) is valid
+// in the even lane when the block exists.
+__device__ __forceinline__ void rs_block_keys(const float (&v)[16], int t0, int nb, uint32_t (&bk)[4], bool (&bok)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    float g = fmaxf(fmaxf(v[4 * i], v[4 * i + 1]), fmaxf(v[4 * i + 2], v[4 * i + 3]));
+    g = fmaxf(g, __shfl_xor_sync(0xFFFFFFFFu, g, 1));
+    const int r = t0 / BLK + 16 * i + (lane >> 1);
+    bk[i] = r == nb - 1 ? float_key(INFINITY) : float_key(g);
+    bok[i] = (lane & 1) == 0 && r < nb;
+  }
 }
 
 struct RsRowInfo {
-  int64_t nv, nb;
+  int nv, nb;                                    // < 2^31 (entry ids are int32)
   bool do_e, do_b;
 };
 
 __device__ __forceinline__ RsRowInfo rs_row_info(const RsParams& p, int64_t bq) {
   RsRowInfo r;
-  r.nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[bq / p.Q]);
-  if (r.nv > p.max_n) r.nv = p.max_n;
-  r.nb = ceil_div(r.nv, BLK);
+  int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[bq / p.Q]);
+  if (nv > p.max_n) nv = p.max_n;
+  r.nv = (int)nv;
+  r.nb = (int)ceil_div(nv, BLK);
   r.do_e = p.K > 0 && r.nv > p.K;
   r.do_b = p.M > 0 && r.nb > p.M;
   return r;
@@ -566,42 +605,71 @@ __device__ void rs_threshold(RsRow& row, int K, uint32_t* warp_sums) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(RS_THREADS) rs_hist_kernel(RsParams p) {
+template <bool VEC>
+__global__ void __launch_bounds__(RS_THREADS, RS_SCAN_CTAS_PER_SM) rs_hist_kernel(RsParams p) {
   extern __shared__ uint32_t rs_dyn[];
   uint32_t* hist_e = rs_dyn;
   uint32_t* hist_b = rs_dyn + RS_BINS;
   __shared__ uint32_t warp_sums[RS_WARPS];
   __shared__ int is_last;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t bq = blockIdx.x / p.chunks;
-  const int64_t chunk = blockIdx.x % p.chunks;
+  const int chunk = (int)(blockIdx.x % p.chunks);
   const RsRowInfo ri = rs_row_info(p, bq);
   if (!ri.do_e && !ri.do_b) return;
   RsRow& row_e = p.rows[bq];
   RsRow& row_b = p.rows[p.BQ + bq];
-  for (int i = tid; i < 2 * RS_BINS; i += RS_THREADS) rs_dyn[i] = 0;
+  for (int i = tid; i < 2 * RS_BINS / 4; i += RS_THREADS) reinterpret_cast<uint4*>(rs_dyn)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   const float* s = p.scores + bq * p.max_n;
-  const int64_t e_lo = chunk * RS_CHUNK;
-  const int64_t e_hi = e_lo + RS_CHUNK < ri.nv ? e_lo + RS_CHUNK : ri.nv;
-  for (int64_t t0 = e_lo + (int64_t)warp * RS_TILE; t0 < e_hi; t0 += (int64_t)RS_WARPS * RS_TILE) {
-    float v[8];
-    rs_load_tile(s, t0, ri.nv, v);
+  const int e_lo = chunk * p.batches * RS_BATCH;
+  for (int bt = 0; bt < p.batches; bt++) {
+  float v[RS_TILES][16];
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const int64_t e = t0 + 32 * i + lane;
-      if (ri.do_e && e < ri.nv) atomicAdd(&hist_e[float_key(v[i]) >> RS_SHIFT], 1u);
-      if (ri.do_b) {
-        const int64_t r = e / BLK;
-        const uint32_t k = rs_block_key(v[i], r, ri.nb);
-        if ((lane & 7) == 0 && r < ri.nb) atomicAdd(&hist_b[k >> RS_SHIFT], 1u);
-      }
+  for (int k = 0; k < RS_TILES; k++) {
+    const int t0 = e_lo + ((bt * RS_TILES + k) * RS_WARPS + warp) * RS_TILE;
+    if (t0 < ri.nv) rs_load_tile<VEC>(s, t0, ri.nv, v[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < RS_TILES; k++) {
+    const int t0 = e_lo + ((bt * RS_TILES + k) * RS_WARPS + warp) * RS_TILE;
+    if (t0 >= ri.nv) break;                      // warp-uniform
+    if (ri.do_e) {
+#pragma unroll
+      for (int j = 0; j < 16; j++)               // -inf past nv is counted in bin 0x007, then taken back
+        atomicAdd(&hist_e[float_key(v[k][j]) >> RS_SHIFT], 1u);
+    }
+    if (ri.do_b) {
+      uint32_t bk[4];
+      bool bok[4];
+      rs_block_keys(v[k], t0, ri.nb, bk, bok);
+#pragma unroll
+      for (int i = 0; i < 4; i++)
+        if (bok[i]) atomicAdd(&hist_b[bk[i] >> RS_SHIFT], 1u);
     }
   }
+  }
+  if (ri.do_e && e_lo + p.batches * RS_BATCH > ri.nv && e_lo < ri.nv) {
+    // the padding of the row's last tile went to the -inf bin
+    const int last_t0 = (ri.nv - 1) / RS_TILE * RS_TILE;
+    if (tid == 0) atomicSub(&hist_e[float_key(-INFINITY) >> RS_SHIFT], (uint32_t)(last_t0 + RS_TILE - ri.nv));
+  }
   __syncthreads();
-  for (int b = tid; b < RS_BINS; b += RS_THREADS) {
-    if (ri.do_e && hist_e[b]) atomicAdd(&row_e.hist[b], hist_e[b]);
-    if (ri.do_b && hist_b[b]) atomicAdd(&row_b.hist[b], hist_b[b]);
+  for (int b4 = tid; b4 < RS_BINS / 4; b4 += RS_THREADS) {
+    if (ri.do_e) {
+      const uint4 c = reinterpret_cast<const uint4*>(hist_e)[b4];
+      if (c.x) atomicAdd(&row_e.hist[4 * b4], c.x);
+      if (c.y) atomicAdd(&row_e.hist[4 * b4 + 1], c.y);
+      if (c.z) atomicAdd(&row_e.hist[4 * b4 + 2], c.z);
+      if (c.w) atomicAdd(&row_e.hist[4 * b4 + 3], c.w);
+    }
+    if (ri.do_b) {
+      const uint4 c = reinterpret_cast<const uint4*>(hist_b)[b4];
+      if (c.x) atomicAdd(&row_b.hist[4 * b4], c.x);
+      if (c.y) atomicAdd(&row_b.hist[4 * b4 + 1], c.y);
+      if (c.z) atomicAdd(&row_b.hist[4 * b4 + 2], c.z);
+      if (c.w) atomicAdd(&row_b.hist[4 * b4 + 3], c.w);
+    }
   }
   __threadfence();
   __syncthreads();
@@ -613,54 +681,104 @@ __global__ void __launch_bounds__(RS_THREADS) rs_hist_kernel(RsParams p) {
   if (ri.do_b) rs_threshold(row_b, p.M, warp_sums);
 }
 
-__global__ void __launch_bounds__(RS_THREADS) rs_filter_kernel(RsParams p) {
+template <bool VEC>
+__global__ void __launch_bounds__(RS_THREADS, RS_SCAN_CTAS_PER_SM) rs_filter_kernel(RsParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t bq = blockIdx.x / p.chunks;
-  const int64_t chunk = blockIdx.x % p.chunks;
+  const int chunk = (int)(blockIdx.x % p.chunks);
   const RsRowInfo ri = rs_row_info(p, bq);
   if (!ri.do_e && !ri.do_b) return;
   RsRow& row_e = p.rows[bq];
   RsRow& row_b = p.rows[p.BQ + bq];
-  const uint32_t b1e = ri.do_e ? row_e.b1 : 0u, b1b = ri.do_b ? row_b.b1 : 0u;
+  const uint32_t b1e = ri.do_e ? row_e.b1 : 0xFFFFFFFFu, b1b = ri.do_b ? row_b.b1 : 0xFFFFFFFFu;
   const bool keep_e = ri.do_e && row_e.hist[b1e] <= (uint32_t)RS_CAP;
   const bool keep_b = ri.do_b && row_b.hist[b1b] <= (uint32_t)RS_CAP;
   int32_t* gt_e = p.gt + bq * RS_MAX_OUT;
   int32_t* gt_b = p.gt + (p.BQ + bq) * RS_MAX_OUT;
   unsigned long long* cd_e = p.cand + bq * RS_CAP;
   unsigned long long* cd_b = p.cand + (p.BQ + bq) * RS_CAP;
+  // this CTA's picks are staged in shared memory and published with one
+  // global reservation per list at the end
+  constexpr uint32_t SE = RS_STAGE_EQ;
+  __shared__ int32_t s_gt_e[CSA2_MAX_K], s_gt_b[CSA2_MAX_M];
+  __shared__ unsigned long long s_eq_e[SE], s_eq_b[SE];
+  __shared__ uint32_t s_n[4], s_base[4];
+  if (tid < 4) s_n[tid] = 0;
+  __syncthreads();
   const float* s = p.scores + bq * p.max_n;
-  const int64_t e_lo = chunk * RS_CHUNK;
-  const int64_t e_hi = e_lo + RS_CHUNK < ri.nv ? e_lo + RS_CHUNK : ri.nv;
-  for (int64_t t0 = e_lo + (int64_t)warp * RS_TILE; t0 < e_hi; t0 += (int64_t)RS_WARPS * RS_TILE) {
-    float v[8];
-    rs_load_tile(s, t0, ri.nv, v);
+  const int e_lo = chunk * p.batches * RS_BATCH;
+  for (int bt = 0; bt < p.batches; bt++) {
+    float v[RS_TILES][16];
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const int64_t e = t0 + 32 * i + lane;
+    for (int k = 0; k < RS_TILES; k++) {
+      const int t0 = e_lo + ((bt * RS_TILES + k) * RS_WARPS + warp) * RS_TILE;
+      if (t0 < ri.nv) rs_load_tile<VEC>(s, t0, ri.nv, v[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < RS_TILES; k++) {
+      const int t0 = e_lo + ((bt * RS_TILES + k) * RS_WARPS + warp) * RS_TILE;
+      if (t0 >= ri.nv) break;                    // warp-uniform
       if (ri.do_e) {
-        const uint32_t k = float_key(v[i]);
-        const uint32_t d = k >> RS_SHIFT;
-        const bool ok = e < ri.nv;
-        warp_append<int32_t>(ok && d > b1e, &row_e.n_gt, gt_e, (uint32_t)p.K, (int32_t)e);
-        warp_append<unsigned long long>(keep_e && ok && d == b1e, &row_e.n_eq, cd_e, (uint32_t)RS_CAP,
-                                        ((unsigned long long)k << 32) | (uint32_t)~(uint32_t)e);
+        // keys in or above the threshold bin are rare: one vote per value slot,
+        // the appends only where some lane holds one
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+          const uint32_t key = float_key(v[k][j]);
+          const uint32_t d = key >> RS_SHIFT;
+          const int e = t0 + 128 * (j >> 2) + 4 * lane + (j & 3);
+          const bool ok = e < ri.nv;
+          if (__any_sync(0xFFFFFFFFu, ok && d >= b1e)) {
+            stage_append<int32_t>(ok && d > b1e, &s_n[0], s_gt_e, CSA2_MAX_K, &row_e.n_gt, gt_e, (uint32_t)p.K,
+                                  (int32_t)e);
+            if (keep_e)
+              stage_append<unsigned long long>(ok && d == b1e, &s_n[1], s_eq_e, SE, &row_e.n_eq, cd_e,
+                                               (uint32_t)RS_CAP,
+                                               ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)e);
+          }
+        }
       }
       if (ri.do_b) {
-        const int64_t r = e / BLK;
-        const uint32_t k = rs_block_key(v[i], r, ri.nb);
-        const uint32_t d = k >> RS_SHIFT;
-        const bool ok = (lane & 7) == 0 && r < ri.nb;
-        warp_append<int32_t>(ok && d > b1b, &row_b.n_gt, gt_b, (uint32_t)p.M, (int32_t)r);
-        warp_append<unsigned long long>(keep_b && ok && d == b1b, &row_b.n_eq, cd_b, (uint32_t)RS_CAP,
-                                        ((unsigned long long)k << 32) | (uint32_t)~(uint32_t)r);
+        uint32_t bk[4];
+        bool bok[4];
+        rs_block_keys(v[k], t0, ri.nb, bk, bok);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const uint32_t d = bk[i] >> RS_SHIFT;
+          if (__any_sync(0xFFFFFFFFu, bok[i] && d >= b1b)) {
+            const int r = t0 / BLK + 16 * i + (lane >> 1);
+            stage_append<int32_t>(bok[i] && d > b1b, &s_n[2], s_gt_b, CSA2_MAX_M, &row_b.n_gt, gt_b, (uint32_t)p.M,
+                                  (int32_t)r);
+            if (keep_b)
+              stage_append<unsigned long long>(bok[i] && d == b1b, &s_n[3], s_eq_b, SE, &row_b.n_eq, cd_b,
+                                               (uint32_t)RS_CAP,
+                                               ((unsigned long long)bk[i] << 32) | (uint32_t)~(uint32_t)r);
+          }
+        }
       }
     }
   }
+  __syncthreads();
+  if (tid < 4) {
+    const uint32_t cap_s = tid == 0 ? CSA2_MAX_K : tid == 2 ? CSA2_MAX_M : SE;
+    const uint32_t c = s_n[tid] < cap_s ? s_n[tid] : cap_s;
+    uint32_t* g_n = tid == 0 ? &row_e.n_gt : tid == 1 ? &row_e.n_eq : tid == 2 ? &row_b.n_gt : &row_b.n_eq;
+    s_base[tid] = c ? atomicAdd(g_n, c) : 0u;
+    s_n[tid] = c;
+  }
+  __syncthreads();
+  for (uint32_t i = tid; i < s_n[0]; i += RS_THREADS)
+    if (s_base[0] + i < (uint32_t)p.K) gt_e[s_base[0] + i] = s_gt_e[i];
+  for (uint32_t i = tid; i < s_n[1]; i += RS_THREADS)
+    if (s_base[1] + i < (uint32_t)RS_CAP) cd_e[s_base[1] + i] = s_eq_e[i];
+  for (uint32_t i = tid; i < s_n[2]; i += RS_THREADS)
+    if (s_base[2] + i < (uint32_t)p.M) gt_b[s_base[2] + i] = s_gt_b[i];
+  for (uint32_t i = tid; i < s_n[3]; i += RS_THREADS)
+    if (s_base[3] + i < (uint32_t)RS_CAP) cd_b[s_base[3] + i] = s_eq_b[i];
 }
 
 constexpr int RS_RESOLVE_SMEM = RS_CAP * 8 + (SEL_THREADS / 32) * 256 * 4 + RS_MAX_OUT * 4;
 
-__global__ void __launch_bounds__(SEL_THREADS) rs_resolve_kernel(RsParams p) {
+__global__ void __launch_bounds__(SEL_THREADS, 1) rs_resolve_kernel(RsParams p) {
   __shared__ ScanSmem sm;
   __shared__ uint32_t n_taken;
   __shared__ uint32_t bc[3];
@@ -761,10 +879,29 @@ __global__ void __launch_bounds__(SEL_THREADS) rs_resolve_kernel(RsParams p) {
       if (at < (uint32_t)KK) ids[at] = (int32_t)~(uint32_t)(cs[i] >> RS_BITS);
     }
   }
-  // bitonic sort of the KK ids, ascending
+  __syncthreads();
+  if (n <= RS_CAP * 64) {
+    // ascending order through a bitmap of the row (in the candidates' space,
+    // now free): one bit per chosen id, then a block-wide count of set bits
+    uint32_t* bm = reinterpret_cast<uint32_t*>(cs);
+    const int words = (int)((n + 31) / 32);
+    for (int i = tid; i < words; i += SEL_THREADS) bm[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < KK; i += SEL_THREADS) atomicOr(&bm[ids[i] >> 5], 1u << (ids[i] & 31));
+    __syncthreads();
+    const int per = (words + SEL_THREADS - 1) / SEL_THREADS;
+    const int w0 = tid * per, w1 = w0 + per < words ? w0 + per : words;
+    long long cnt = 0;
+    for (int w = w0; w < w1; w++) cnt += __popc(bm[w]);
+    long long total;
+    long long at = block_exclusive_scan(cnt, sm, &total);
+    for (int w = w0; w < w1; w++)
+      for (uint32_t x = bm[w]; x; x &= x - 1) out[at++] = w * 32 + __ffs(x) - 1;
+    return;
+  }
+  // longer rows: bitonic sort of the KK ids, ascending
   int P = 1;
   while (P < KK) P <<= 1;
-  __syncthreads();
   for (int i = KK + tid; i < P; i += SEL_THREADS) ids[i] = 0x7FFFFFFF;
   __syncthreads();
   for (int k = 2; k <= P; k <<= 1) {
@@ -789,6 +926,7 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
                               cudaStream_t stream) {
   const int64_t BQ = (int64_t)B * Q;
   if (BQ == 0) return cudaSuccess;
+  if (max_n > 0x7FFFFFFF - 2 * (int64_t)RS_BATCH) return cudaErrorInvalidValue;   // entry ids are int32
   static int attr_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -796,7 +934,10 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
     cudaError_t e = cudaFuncSetAttribute(rs_resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          RS_RESOLVE_SMEM);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(rs_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(rs_hist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               2 * RS_BINS * (int)sizeof(uint32_t));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(rs_hist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                2 * RS_BINS * (int)sizeof(uint32_t));
     if (e != cudaSuccess) return e;
     attr_dev = dev;
@@ -812,7 +953,15 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
   p.K = sel ? K : 0;
   p.M = pool ? M : 0;
   p.max_n = max_n;
-  p.chunks = (int)(max_n > 0 ? ceil_div(max_n, RS_CHUNK) : 1);
+  // one wave of scan CTAs where the rows allow it: batches per CTA from the total
+  int dev_sms = 148;
+  cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t row_batches = max_n > 0 ? ceil_div(max_n, RS_BATCH) : 1;
+  int64_t per = ceil_div(BQ * row_batches, (int64_t)RS_SCAN_CTAS_PER_SM * dev_sms);
+  if (per < 1) per = 1;
+  if (per > row_batches) per = row_batches;
+  p.batches = (int)per;
+  p.chunks = (int)ceil_div(row_batches, per);
   p.sel = sel;
   p.pool = pool;
   p.BQ = BQ;
@@ -826,8 +975,15 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
   if (e != cudaSuccess) return e;
   const int64_t scan_ctas = BQ * p.chunks;
   if (scan_ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  rs_hist_kernel<<<(unsigned)scan_ctas, RS_THREADS, 2 * RS_BINS * sizeof(uint32_t), stream>>>(p);
-  rs_filter_kernel<<<(unsigned)scan_ctas, RS_THREADS, 0, stream>>>(p);
+  // 16-byte loads when every row starts 16-byte aligned
+  const bool vec = (max_n % 4) == 0 && (reinterpret_cast<uintptr_t>(scores) & 15u) == 0;
+  if (vec) {
+    rs_hist_kernel<true><<<(unsigned)scan_ctas, RS_THREADS, 2 * RS_BINS * sizeof(uint32_t), stream>>>(p);
+    rs_filter_kernel<true><<<(unsigned)scan_ctas, RS_THREADS, 0, stream>>>(p);
+  } else {
+    rs_hist_kernel<false><<<(unsigned)scan_ctas, RS_THREADS, 2 * RS_BINS * sizeof(uint32_t), stream>>>(p);
+    rs_filter_kernel<false><<<(unsigned)scan_ctas, RS_THREADS, 0, stream>>>(p);
+  }
   rs_resolve_kernel<<<dim3((unsigned)BQ, 2), SEL_THREADS, RS_RESOLVE_SMEM, stream>>>(p);
   return cudaGetLastError();
 }
