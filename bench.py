@@ -439,6 +439,254 @@ def run_decode1m_e2e(args, torch, csa2, w):
             "placements and 4 layer calls"}
 
 
+# ------------------------------------------------------------------ other configurations
+# The remaining workload configurations, one JSON line each (--workload):
+#   full131k   decode Full mode on a decoder source layer (m=1): batch 64 x
+#              131,072 entries, one query per sequence at t = N-1
+#   prefill8k  prefill chunk on an encoder source layer (m=2): 8192 queries at
+#              t = 131,072..139,263 over 69,632 entries, causal
+#   cachewrite cache write of 4 source layers (3 at m=2, 1 at m=1) over
+#              1,048,576 tokens each
+FP4_PER_BF16 = 13.5 / 2.25          # nominal dense fp4 : bf16 tensor ratio
+FP32_FMA_PER_SM_CLK = 128           # fp32 FMA lanes per SM and clock
+
+
+def _weights(torch, seed):
+    import numpy as np
+    import synth
+    g = synth.rng(seed)
+    w0, w1 = synth.compressor_weights(g)
+    W = synth.index_projection(g)
+    return (torch.from_numpy(w0).cuda(), torch.from_numpy(w1).cuda(),
+            torch.from_numpy(np.ascontiguousarray(W).view(np.int16)).cuda())
+
+
+def _write_cache(csa2, torch, cache, T, seed, wts, rope, ws, chunk=1 << 17):
+    """Cache write of every sequence's T tokens of seeded N(0,1) latents."""
+    import synth
+    w0, w1, w_idx = wts
+    for b in range(cache.B):
+        view = cache.sequence(b)
+        for c0 in range(0, T, chunk):
+            n = min(chunk, T - c0)
+            x = synth.torch_latents(seed * 100_003 + b * 1_009 + c0 // chunk, (1, n), "cuda")
+            start = torch.tensor([c0 // cache.m], dtype=torch.int64, device="cuda")
+            csa2.compress_quantize(view, x.view(torch.int16), start, w0, w1, rope, w_idx, ws)
+
+
+def _events_ms(torch, fn, steps, flush=None):
+    """Device time of `steps` calls of fn.  With `flush`, every call runs after an
+    L2 flush and is timed alone (the flushes are outside the timed regions)."""
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    total = 0.0
+    for i in range(steps):
+        flush.fill_(i & 255)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / steps
+
+
+def _line(args, world, metric, unit, value, ms, dtype, config, roofline, extra):
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config, "roofline": roofline,
+            "cpu_baseline": None, "e2e": None}
+    line.update(extra)
+    return line
+
+
+def run_full131k(args, torch, csa2):
+    """Decode Full mode: index scan of every visible entry, block top-2048,
+    top-512, attention; batch 64 x 131,072 entries (2.99 GB of cache, > L2)."""
+    import synth
+    rank, world, local = dist_info()
+    B, N, dev = 64, 1 << 17, "cuda"
+    cache = csa2.Cache(B, N, 1, device=dev)
+    wts = _weights(torch, 2)
+    ones = torch.ones(D, device=dev)
+    rope = csa2.rope_table(N).to(dev)
+    ws_cw = csa2.Workspace(1 << 16, device=dev)
+    _write_cache(csa2, torch, cache, N, 2, (ones, ones, wts[2]), rope, ws_cw)
+    cache.n_entries.fill_(N)
+    assert ws_cw.sync_status()[0] == 0
+    del rope
+    q_pos = torch.full((B, 1), N - 1, dtype=torch.int64, device=dev)
+    swa_base = torch.full((B,), N - WIN, dtype=torch.int64, device=dev)
+    q_idx = synth.torch_normal(21, (B, 1, HI, DI), torch.bfloat16, dev)
+    w_head = synth.torch_normal(22, (B, 1, HI), torch.float32, dev)
+    q = synth.torch_normal(23, (B, 1, H, D), torch.bfloat16, dev)
+    swa = synth.torch_swa_rows(24, (B, WIN), dev)
+    pool = torch.empty((B, 1, M_BLK), dtype=torch.int32, device=dev)
+    sel = torch.empty((B, 1, K_SEL), dtype=torch.int32, device=dev)
+    out = torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev)
+    ws = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_FULL, B, 1, N, M_BLK, K_SEL), device=dev)
+
+    def step():
+        csa2.decode(csa2.MODE_FULL, cache, q_pos=q_pos, q=q.view(torch.int16), swa=swa.view(torch.int16),
+                    swa_base_pos=swa_base, scale=1 / math.sqrt(D), sel=sel, out=out.view(torch.int16), ws=ws,
+                    M=M_BLK, max_n=N, q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool)
+    graph = _capture(torch, step)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms = _events_ms(torch, graph.replay, args.steps)
+    ms = max_over_ranks(ms, world)
+    assert ws.sync_status()[0] == 0
+    # the dominant kernel alone: the index scan (public call, same inputs)
+    scores = torch.empty((B, 1, N), dtype=torch.float32, device=dev)
+    ws_s = csa2.Workspace(1 << 16, device=dev)
+    g_s = _capture(torch, lambda: csa2.index_score(cache, q_idx.view(torch.int16), w_head, q_pos, scores, N, ws_s))
+    g_s.replay()
+    scan_ms = _events_ms(torch, g_s.replay, max(args.steps, 20))
+    hbm, _, which = peaks()
+    scan_bytes = B * N * (IDX_ENTRY + 4) + B * (HI * DI * 2 + HI * 4)       # index K read + scores written
+    per_query = N * IDX_ENTRY + HI * DI * 2 + HI * 4 + ATTN_BYTES + M_BLK * 4 + K_SEL * 4
+    achieved = scan_bytes / (scan_ms / 1e3) / 1e9
+    return _line(args, world, "CSA2 Full decode query-tokens/s/layer at 131K ctx, batch 64", "query-tokens/s",
+                 B * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 {"workload": "decode Full mode, m=1, 64 sequences x 131,072 entries, one query each",
+                  "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
+                  "l2": "inputs larger than L2 (2.99 GB of cache; the scan reads 570 MB per step)",
+                  "launch": "one CUDA graph per step (index scan, block and entry selection, attention)"},
+                 {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                  "traffic": ncu_traffic("index_score_tc_kernel<1>"), "kernel": "index_score_tc_kernel<1>",
+                  "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
+                 {"step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
+                               "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
+                  "clocks": clk.summary(), "gpu_launches": args.steps * 5})
+
+
+def run_prefill8k(args, torch, csa2):
+    """Prefill chunk: 8192 causal queries, one Full-mode call (index scan of
+    4 queries per CTA, per-query block top-2048 and top-512, attention)."""
+    import synth
+    rank, world, local = dist_info()
+    m, P, C, dev = 2, 131072, 8192, "cuda"
+    T = P + C
+    N = T // m
+    cache = csa2.Cache(1, N, m, device=dev)
+    wts = _weights(torch, 4)
+    rope = csa2.rope_table(N).to(dev)
+    ws_cw = csa2.Workspace(1 << 16, device=dev)
+    _write_cache(csa2, torch, cache, T, 4, wts, rope, ws_cw)
+    cache.n_entries.fill_(N)
+    assert ws_cw.sync_status()[0] == 0
+    Q = C
+    q_pos = torch.arange(P, T, dtype=torch.int64, device=dev)[None]
+    swa_base = torch.full((1,), P - (WIN - 1), dtype=torch.int64, device=dev)
+    q_idx = synth.torch_normal(41, (1, Q, HI, DI), torch.bfloat16, dev)
+    w_head = synth.torch_normal(42, (1, Q, HI), torch.float32, dev)
+    q = synth.torch_normal(43, (1, Q, H, D), torch.bfloat16, dev)
+    swa = synth.torch_swa_rows(44, (1, Q + WIN - 1), dev)
+    pool = torch.empty((1, Q, M_BLK), dtype=torch.int32, device=dev)
+    sel = torch.empty((1, Q, K_SEL), dtype=torch.int32, device=dev)
+    out = torch.empty((1, Q, H, D), dtype=torch.bfloat16, device=dev)
+    ws = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_FULL, 1, Q, N, M_BLK, K_SEL), device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        csa2.decode(csa2.MODE_FULL, cache, q_pos=q_pos, q=q.view(torch.int16), swa=swa.view(torch.int16),
+                    swa_base_pos=swa_base, scale=1 / math.sqrt(D), sel=sel, out=out.view(torch.int16), ws=ws,
+                    M=M_BLK, max_n=N, q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool)
+    graph = _capture(torch, step)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms = _events_ms(torch, graph.replay, args.steps, flush=flush)
+    ms = max_over_ranks(ms, world)
+    assert ws.sync_status()[0] == 0
+    # the tensor-core kernel alone: the grouped index scan (public call, same inputs)
+    scores = torch.empty((1, Q, N), dtype=torch.float32, device=dev)
+    ws_s = csa2.Workspace(1 << 16, device=dev)
+    g_s = _capture(torch, lambda: csa2.index_score(cache, q_idx.view(torch.int16), w_head, q_pos, scores, N, ws_s))
+    g_s.replay()
+    scan_ms = _events_ms(torch, g_s.replay, max(args.steps, 10), flush=flush)
+    _, bf16, which = peaks()
+    pairs = sum(min((t + 1) // m, N) for t in range(P, T))                  # (query, visible entry) pairs
+    flops = pairs * HI * DI * 2
+    fp4_peak = bf16 * FP4_PER_BF16
+    achieved = flops / (scan_ms / 1e3) / 1e12
+    return _line(args, world, "CSA2 prefill-chunk query-tokens/s, 8192 new tokens on a 131K prefix",
+                 "query-tokens/s", Q * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 {"workload": "prefill chunk, m=2, 131,072-token prefix + 8192 new tokens (69,632 entries), "
+                              "8192 causal queries, batch 1",
+                  "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
+                  "l2": "L2 flushed (256 MB write) before every timed step; the caches (24 MB) fit in L2",
+                  "launch": "one CUDA graph per step"},
+                 {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+                  "frac": achieved / fp4_peak, "traffic": None, "kernel": "index_score_tc_kernel<4>",
+                  "algorithmic_flops_per_launch": flops, "avg_launch_ms": scan_ms,
+                  "peak_source": f"{which} bf16 x {FP4_PER_BF16:g} (nominal fp4:bf16 dense ratio)"},
+                 {"clocks": clk.summary(), "gpu_launches": args.steps * 5})
+
+
+def run_cachewrite(args, torch, csa2):
+    """Cache write of 4 source layers (3 at m=2, 1 at m=1) over 1,048,576 tokens:
+    compressor, RMSNorm, RoPE, E2M1 + E4M3 main KV, index-K projection + MXFP4."""
+    import synth
+    rank, world, local = dist_info()
+    T, dev = 1 << 20, "cuda"
+    wts = _weights(torch, 1)
+    rope = csa2.rope_table(T).to(dev)
+    ws = csa2.Workspace(1 << 16, device=dev)
+    layers = []
+    for layer, m in enumerate((2, 2, 2, 1)):
+        x = synth.torch_latents(10 + layer, (1, T), dev)                      # 1 GiB of bf16 latents each
+        layers.append((csa2.Cache(1, T // m, m, device=dev), x))
+    start = torch.zeros((1,), dtype=torch.int64, device=dev)
+
+    def step():
+        for cache, x in layers:
+            csa2.compress_quantize(cache, x.view(torch.int16), start, wts[0], wts[1], rope, wts[2], ws)
+    graph = _capture(torch, step)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms = _events_ms(torch, graph.replay, args.steps)
+    ms = max_over_ranks(ms, world)
+    assert ws.sync_status()[0] == 0
+    entries = sum(T // m for m in (2, 2, 2, 1))
+    out_bytes = sum(c.main_kv.numel() + c.idx_codes.numel() + c.idx_scales.numel() for c, _ in layers)
+    assert out_bytes == 890 * T
+    fma = entries * DI * D                                                 # the index-K projection
+    clocks = clk.summary()
+    props = torch.cuda.get_device_properties(0)
+    sm_mhz = clocks.get("sm_max_mhz") or 2070.0
+    fma_peak = props.multi_processor_count * FP32_FMA_PER_SM_CLK * sm_mhz * 1e6
+    achieved = fma / (ms / 1e3)
+    hbm, _, which = peaks()
+    bytes_step = 4 * T * D * 2 + out_bytes
+    return _line(args, world, "CSA2 cache-write tokens/s (4 source layers x 1M tokens)", "tokens/s",
+                 4 * T * world / (ms / 1e3), ms, "bf16 in, fp32 math, fp4/fp8 codes out",
+                 {"workload": "cache write, 4 source layers (3 at m=2, 1 at m=1) x 1,048,576 tokens, 890 B/token out",
+                  "l2": "inputs larger than L2 (4 GiB of latents per step)", "launch": "one CUDA graph per step"},
+                 {"bound": "alu", "achieved": achieved / 1e12, "peak": fma_peak / 1e12, "unit": "TFMA/s",
+                  "frac": achieved / fma_peak, "traffic": None, "kernel": "cache_write_kernel",
+                  "algorithmic_fma_per_step": fma, "avg_launch_ms": ms / 4,
+                  "peak_source": f"{props.multi_processor_count} SMs x {FP32_FMA_PER_SM_CLK} fp32 FMA/clk x "
+                                 f"{sm_mhz:.0f} MHz"},
+                 {"step_hbm": {"algorithmic_bytes": bytes_step, "GB_s": bytes_step / (ms / 1e3) / 1e9,
+                               "frac": bytes_step / (ms / 1e3) / 1e9 / hbm},
+                  "clocks": clocks, "gpu_launches": args.steps * 4})
+
+
 # ------------------------------------------------------------------ CPU oracle sample
 class OracleChain:
     """Oracle (binary64 numpy + C cache write) on the per-query work of the
@@ -518,7 +766,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode1m", choices=["decode1m"])
+    ap.add_argument("--workload", default="decode1m", choices=["decode1m", "full131k", "prefill8k", "cachewrite"])
     ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
@@ -539,6 +787,12 @@ def main():
         dist.init_process_group("nccl")
     import fp4_kv_cache_csa2_gb300 as csa2
     csa2.load()
+    if args.workload != "decode1m":
+        fn = {"full131k": run_full131k, "prefill8k": run_prefill8k, "cachewrite": run_cachewrite}[args.workload]
+        line = fn(args, torch, csa2)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     res = run_decode1m(args, torch, csa2)
     if rank == 0:
         line = {"metric": METRIC, "value": res.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
