@@ -24,13 +24,16 @@
 //
 // Structure (persistent kernel, one CTA per SM, 256 threads):
 //   smem  W^T as bf16 [512 ch][128 o] (128 KB, loaded once per CTA)
-//         y tile   fp32 [512 ch][32 entries] (64 KB)
-//   phase 1  warp per entry: coalesced 128-bit loads of the token rows,
-//            compress/normalise/rotate in registers, write the 288-byte main
-//            entry, stage y' in smem.
+//         y tile   fp32 [32 entries][512 ch] (64 KB)
+//   phase 1  warp per entry, 4 entries per warp: the 128-bit loads of all
+//            four entries' token rows are issued first, then each entry is
+//            compressed/normalised/rotated in registers, its 288-byte main
+//            entry written and y' staged in smem (16-byte stores, no bank
+//            conflicts); the next tile's token rows are prefetched into L2.
 //   phase 2  each thread owns 4 outputs x 4 entries (16 independent fma
-//            chains); W^T row reads are contiguous across the warp, y reads
-//            are broadcasts.  This phase is FP32-ALU bound (65,536 fma per entry).
+//            chains), four channels at a time; W^T row reads are contiguous
+//            across the warp, y reads are broadcasts.  This phase is
+//            FP32-ALU bound (65,536 fma per entry).
 //   phase 3  MXFP4 of k: 8 lanes form one 32-wide block.
 #include "params.cuh"
 
@@ -38,7 +41,7 @@ namespace csa2 {
 
 constexpr int CW_THREADS = 256;
 constexpr int CW_TILE = 32;                       // entries per tile
-constexpr int CW_SMEM = D * DI * 2 + D * CW_TILE * 4;  // 131072 + 65536
+constexpr int CW_SMEM = D * DI * 2 + CW_TILE * D * 4;  // 131072 + 65536
 
 
 __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) {
@@ -67,8 +70,13 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
     const int64_t e0 = p.entry_start[b];
     __syncthreads();   // previous tile's readers of ytile are done (and W^T is ready)
 
-    // ---------------- phase 1: warp per entry
-    for (int t = warp; t < CW_TILE; t += CW_THREADS / 32) {
+    // ---------------- phase 1: warp per entry, loads of all four entries first
+    constexpr int EPW = CW_TILE / (CW_THREADS / 32);             // entries per warp
+    uint4 xr[EPW][4];                                             // rows x_{2j}, x_{2j+1} (m = 2) or x_j
+    bool ok[EPW];
+#pragma unroll
+    for (int u = 0; u < EPW; u++) {
+      const int t = warp + u * (CW_THREADS / 32);
       const int64_t j = j0 + t;
       const int64_t e = e0 + j;
       bool valid = j < n_local;
@@ -76,26 +84,36 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
         if (lane == 0) report(p.hdr, CSA2_ERR_BOUNDS, e);
         valid = false;
       }
+      ok[u] = valid;
       if (lane == 0) tile_valid[t] = valid;
-      float y[16];
       if (valid) {
-        const uint16_t* x0 = p.x + ((int64_t)b * p.T + j * p.m) * D + lane * 16;
-        uint4 a0 = __ldg(reinterpret_cast<const uint4*>(x0));
-        uint4 a1 = __ldg(reinterpret_cast<const uint4*>(x0) + 1);
-        uint32_t xa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint4* x0 = reinterpret_cast<const uint4*>(p.x + ((int64_t)b * p.T + j * p.m) * D + lane * 16);
+        xr[u][0] = __ldg(x0);
+        xr[u][1] = __ldg(x0 + 1);
+        if (p.m == 2) {
+          xr[u][2] = __ldg(x0 + D / 8);
+          xr[u][3] = __ldg(x0 + D / 8 + 1);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < EPW; u++) {
+      const int t = warp + u * (CW_THREADS / 32);
+      const int64_t e = e0 + j0 + t;
+      float y[16];
+      if (ok[u]) {
+        uint32_t xa[8] = {xr[u][0].x, xr[u][0].y, xr[u][0].z, xr[u][0].w, xr[u][1].x, xr[u][1].y, xr[u][1].z, xr[u][1].w};
         float c[16];
         if (p.m == 2) {
-          const uint16_t* x1 = x0 + D;
-          uint4 b0 = __ldg(reinterpret_cast<const uint4*>(x1));
-          uint4 b1 = __ldg(reinterpret_cast<const uint4*>(x1) + 1);
-          uint32_t xb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          uint32_t xb[8] = {xr[u][2].x, xr[u][2].y, xr[u][2].z, xr[u][2].w,
+                            xr[u][3].x, xr[u][3].y, xr[u][3].z, xr[u][3].w};
           const float4* w0v = reinterpret_cast<const float4*>(p.w0 + lane * 16);
           const float4* w1v = reinterpret_cast<const float4*>(p.w1 + lane * 16);
           float w0r[16], w1r[16];
 #pragma unroll
           for (int q = 0; q < 4; q++) {
-            float4 u = __ldg(w0v + q), v = __ldg(w1v + q);
-            w0r[4 * q] = u.x; w0r[4 * q + 1] = u.y; w0r[4 * q + 2] = u.z; w0r[4 * q + 3] = u.w;
+            float4 uu = __ldg(w0v + q), v = __ldg(w1v + q);
+            w0r[4 * q] = uu.x; w0r[4 * q + 1] = uu.y; w0r[4 * q + 2] = uu.z; w0r[4 * q + 3] = uu.w;
             w1r[4 * q] = v.x; w1r[4 * q + 1] = v.y; w1r[4 * q + 2] = v.z; w1r[4 * q + 3] = v.w;
           }
 #pragma unroll
@@ -153,8 +171,21 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
 #pragma unroll
         for (int k = 0; k < 16; k++) y[k] = 0.0f;
       }
+      float4* yrow = reinterpret_cast<float4*>(ytile + t * D + lane * 16);
 #pragma unroll
-      for (int k = 0; k < 16; k++) ytile[(lane * 16 + k) * CW_TILE + t] = y[k];
+      for (int q = 0; q < 4; q++) yrow[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+    }
+    // next tile's token rows into L2 while this tile's projection runs
+    {
+      const int64_t nt = tile + gridDim.x;
+      if (nt < n_tiles) {
+        const int nb = (int)(nt / tiles_per_seq);
+        const int64_t nj0 = (nt % tiles_per_seq) * CW_TILE;
+        const int64_t rows = (nj0 + CW_TILE <= n_local ? CW_TILE : n_local - nj0) * p.m;
+        const char* base = reinterpret_cast<const char*>(p.x + ((int64_t)nb * p.T + nj0 * p.m) * D);
+        for (int64_t off = (int64_t)tid * 128; off < rows * D * 2; off += (int64_t)CW_THREADS * 128)
+          asm volatile("prefetch.global.L2 [%0];" :: "l"(base + off));
+      }
     }
     __syncthreads();
 
@@ -166,17 +197,24 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
     for (int a = 0; a < 4; a++)
 #pragma unroll
       for (int bq = 0; bq < 4; bq++) acc[a][bq] = 0.0f;
-#pragma unroll 4
-    for (int ch = 0; ch < D; ch++) {
-      uint2 wv = *reinterpret_cast<const uint2*>(wt + ch * DI + og * 4);
-      float4 yv = *reinterpret_cast<const float4*>(ytile + ch * CW_TILE + eg * 4);
-      float wf[4] = {__uint_as_float(wv.x << 16), __uint_as_float(wv.x & 0xFFFF0000u),
-                     __uint_as_float(wv.y << 16), __uint_as_float(wv.y & 0xFFFF0000u)};
-      float yf[4] = {yv.x, yv.y, yv.z, yv.w};
+    const float* yb = ytile + eg * 4 * D;                         // this thread's 4 entries
+#pragma unroll 2
+    for (int c4 = 0; c4 < D; c4 += 4) {
+      float4 yv[4];
 #pragma unroll
-      for (int a = 0; a < 4; a++)
+      for (int bq = 0; bq < 4; bq++) yv[bq] = *reinterpret_cast<const float4*>(yb + bq * D + c4);
 #pragma unroll
-        for (int bq = 0; bq < 4; bq++) acc[a][bq] = __fmaf_rn(yf[bq], wf[a], acc[a][bq]);
+      for (int cc = 0; cc < 4; cc++) {                              // channels in order
+        const uint2 wv = *reinterpret_cast<const uint2*>(wt + (c4 + cc) * DI + og * 4);
+        const float wf[4] = {__uint_as_float(wv.x << 16), __uint_as_float(wv.x & 0xFFFF0000u),
+                             __uint_as_float(wv.y << 16), __uint_as_float(wv.y & 0xFFFF0000u)};
+#pragma unroll
+        for (int bq = 0; bq < 4; bq++) {
+          const float yc = cc == 0 ? yv[bq].x : cc == 1 ? yv[bq].y : cc == 2 ? yv[bq].z : yv[bq].w;
+#pragma unroll
+          for (int a = 0; a < 4; a++) acc[a][bq] = __fmaf_rn(yc, wf[a], acc[a][bq]);
+        }
+      }
     }
 
     // ---------------- phase 3: MXFP4 (8 lanes = one 32-wide block of outputs)
