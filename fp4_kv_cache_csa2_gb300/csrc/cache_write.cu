@@ -96,84 +96,102 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
         }
       }
     }
+    // The four entries go through every step together (independent chains
+    // side by side); invalid entries are computed on zeros and not stored.
+    float y[EPW][16];
+    if (p.m == 2) {
+      float w0r[16], w1r[16];
+      const float4* w0v = reinterpret_cast<const float4*>(p.w0 + lane * 16);
+      const float4* w1v = reinterpret_cast<const float4*>(p.w1 + lane * 16);
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const float4 uu = __ldg(w0v + q), v = __ldg(w1v + q);
+        w0r[4 * q] = uu.x; w0r[4 * q + 1] = uu.y; w0r[4 * q + 2] = uu.z; w0r[4 * q + 3] = uu.w;
+        w1r[4 * q] = v.x; w1r[4 * q + 1] = v.y; w1r[4 * q + 2] = v.z; w1r[4 * q + 3] = v.w;
+      }
+#pragma unroll
+      for (int k = 0; k < 16; k++) {
+        const float den = __fadd_rn(w0r[k], w1r[k]);
+#pragma unroll
+        for (int u = 0; u < EPW; u++) {
+          const uint32_t wa = k < 8 ? (&xr[u][0].x)[k / 2] : (&xr[u][1].x)[(k - 8) / 2];
+          const uint32_t wb = k < 8 ? (&xr[u][2].x)[k / 2] : (&xr[u][3].x)[(k - 8) / 2];
+          const float a = ok[u] ? bf16_bits_to_f32((wa >> (16 * (k & 1))) & 0xFFFFu) : 0.0f;
+          const float bb = ok[u] ? bf16_bits_to_f32((wb >> (16 * (k & 1))) & 0xFFFFu) : 0.0f;
+          y[u][k] = __fdiv_rn(__fmaf_rn(w0r[k], a, __fmul_rn(w1r[k], bb)), den);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < EPW; u++)
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+          const uint32_t wa = k < 8 ? (&xr[u][0].x)[k / 2] : (&xr[u][1].x)[(k - 8) / 2];
+          y[u][k] = ok[u] ? bf16_bits_to_f32((wa >> (16 * (k & 1))) & 0xFFFFu) : 0.0f;
+        }
+    }
+    // RMSNorm
+    float ps[EPW];
 #pragma unroll
     for (int u = 0; u < EPW; u++) {
+      ps[u] = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 16; k++) ps[u] = __fmaf_rn(y[u][k], y[u][k], ps[u]);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+      for (int u = 0; u < EPW; u++) ps[u] = __fadd_rn(ps[u], __shfl_xor_sync(0xFFFFFFFFu, ps[u], off));
+#pragma unroll
+    for (int u = 0; u < EPW; u++) {
+      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ps[u], 512.0f), 1e-6f)));
+#pragma unroll
+      for (int k = 0; k < 16; k++) y[u][k] = __fmul_rn(y[u][k], r);
+    }
+    // RoPE on channels 448..511 = lanes 28..31, pairs i = 8*(lane-28) + k/2
+    if (lane >= 28) {
+#pragma unroll
+      for (int u = 0; u < EPW; u++) {
+        const int64_t e = ok[u] ? e0 + j0 + warp + u * (CW_THREADS / 32) : 0;
+        const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + (e * 32 + (lane - 28) * 8) * 2);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const float4 v = __ldg(cs + q);          // two pairs: (cos, sin, cos, sin)
+          const float y0 = y[u][4 * q], y1 = y[u][4 * q + 1], y2 = y[u][4 * q + 2], y3 = y[u][4 * q + 3];
+          y[u][4 * q + 0] = __fmaf_rn(y0, v.x, -__fmul_rn(y1, v.y));
+          y[u][4 * q + 1] = __fmaf_rn(y0, v.y, __fmul_rn(y1, v.x));
+          y[u][4 * q + 2] = __fmaf_rn(y2, v.z, -__fmul_rn(y3, v.w));
+          y[u][4 * q + 3] = __fmaf_rn(y2, v.w, __fmul_rn(y3, v.z));
+        }
+      }
+    }
+    // main FP4: this lane's 16 channels are exactly one scale group
+#pragma unroll
+    for (int u = 0; u < EPW; u++) {
+      float amax = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 16; k++) amax = fmaxf(amax, fabsf(y[u][k]));
+      const uint32_t sb = e4m3_byte(__fdiv_rn(amax, 6.0f));
+      const float s = e4m3_value(sb);
+      uint32_t packed[2] = {0u, 0u};
+      if (s != 0.0f) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const uint32_t byte = e2m1x2(__fdiv_rn(y[u][2 * k], s), __fdiv_rn(y[u][2 * k + 1], s));
+          packed[k / 4] |= byte << (8 * (k % 4));
+        }
+      }
       const int t = warp + u * (CW_THREADS / 32);
-      const int64_t e = e0 + j0 + t;
-      float y[16];
       if (ok[u]) {
-        uint32_t xa[8] = {xr[u][0].x, xr[u][0].y, xr[u][0].z, xr[u][0].w, xr[u][1].x, xr[u][1].y, xr[u][1].z, xr[u][1].w};
-        float c[16];
-        if (p.m == 2) {
-          uint32_t xb[8] = {xr[u][2].x, xr[u][2].y, xr[u][2].z, xr[u][2].w,
-                            xr[u][3].x, xr[u][3].y, xr[u][3].z, xr[u][3].w};
-          const float4* w0v = reinterpret_cast<const float4*>(p.w0 + lane * 16);
-          const float4* w1v = reinterpret_cast<const float4*>(p.w1 + lane * 16);
-          float w0r[16], w1r[16];
-#pragma unroll
-          for (int q = 0; q < 4; q++) {
-            float4 uu = __ldg(w0v + q), v = __ldg(w1v + q);
-            w0r[4 * q] = uu.x; w0r[4 * q + 1] = uu.y; w0r[4 * q + 2] = uu.z; w0r[4 * q + 3] = uu.w;
-            w1r[4 * q] = v.x; w1r[4 * q + 1] = v.y; w1r[4 * q + 2] = v.z; w1r[4 * q + 3] = v.w;
-          }
-#pragma unroll
-          for (int k = 0; k < 16; k++) {
-            float a = bf16_bits_to_f32((xa[k / 2] >> (16 * (k & 1))) & 0xFFFFu);
-            float bb = bf16_bits_to_f32((xb[k / 2] >> (16 * (k & 1))) & 0xFFFFu);
-            float num = __fmaf_rn(w0r[k], a, __fmul_rn(w1r[k], bb));
-            float den = __fadd_rn(w0r[k], w1r[k]);
-            c[k] = __fdiv_rn(num, den);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; k++) c[k] = bf16_bits_to_f32((xa[k / 2] >> (16 * (k & 1))) & 0xFFFFu);
-        }
-        // RMSNorm
-        float ps = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 16; k++) ps = __fmaf_rn(c[k], c[k], ps);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) ps = __fadd_rn(ps, __shfl_xor_sync(0xFFFFFFFFu, ps, off));
-        float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ps, 512.0f), 1e-6f)));
-#pragma unroll
-        for (int k = 0; k < 16; k++) y[k] = __fmul_rn(c[k], r);
-        // RoPE on channels 448..511 = lanes 28..31, pairs i = 8*(lane-28) + k/2
-        if (lane >= 28) {
-          const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + (e * 32 + (lane - 28) * 8) * 2);
-#pragma unroll
-          for (int q = 0; q < 4; q++) {
-            float4 v = __ldg(cs + q);          // two pairs: (cos, sin, cos, sin)
-            float y0 = y[4 * q], y1 = y[4 * q + 1], y2 = y[4 * q + 2], y3 = y[4 * q + 3];
-            y[4 * q + 0] = __fmaf_rn(y0, v.x, -__fmul_rn(y1, v.y));
-            y[4 * q + 1] = __fmaf_rn(y0, v.y, __fmul_rn(y1, v.x));
-            y[4 * q + 2] = __fmaf_rn(y2, v.z, -__fmul_rn(y3, v.w));
-            y[4 * q + 3] = __fmaf_rn(y2, v.w, __fmul_rn(y3, v.z));
-          }
-        }
-        // main FP4: this lane's 16 channels are exactly one scale group
-        float amax = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 16; k++) amax = fmaxf(amax, fabsf(y[k]));
-        uint32_t sb = e4m3_byte(__fdiv_rn(amax, 6.0f));
-        float s = e4m3_value(sb);
-        uint32_t packed[2] = {0u, 0u};
-        if (s != 0.0f) {
-#pragma unroll
-          for (int k = 0; k < 8; k++) {
-            uint32_t byte = e2m1x2(__fdiv_rn(y[2 * k], s), __fdiv_rn(y[2 * k + 1], s));
-            packed[k / 4] |= byte << (8 * (k % 4));
-          }
-        }
-        uint8_t* ent = p.main_kv + ((int64_t)b * p.cap + e) * MAIN_BYTES;
+        uint8_t* ent = p.main_kv + ((int64_t)b * p.cap + e0 + j0 + t) * MAIN_BYTES;
         *reinterpret_cast<uint2*>(ent + lane * 8) = make_uint2(packed[0], packed[1]);
         ent[256 + lane] = (uint8_t)sb;
-      } else {
-#pragma unroll
-        for (int k = 0; k < 16; k++) y[k] = 0.0f;
       }
       float4* yrow = reinterpret_cast<float4*>(ytile + t * D + lane * 16);
 #pragma unroll
-      for (int q = 0; q < 4; q++) yrow[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+      for (int q = 0; q < 4; q++)
+        yrow[q] = ok[u] ? make_float4(y[u][4 * q], y[u][4 * q + 1], y[u][4 * q + 2], y[u][4 * q + 3])
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     // next tile's token rows into L2 while this tile's projection runs
     {
@@ -189,14 +207,16 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
     }
     __syncthreads();
 
-    // ---------------- phase 2: k = W y', 4 outputs x 4 entries per thread
+    // ---------------- phase 2: k = W y', 4 outputs x 4 entries per thread,
+    // as packed pairs of outputs (fma.rn.f32x2: two round-to-nearest fmas, the
+    // same results as scalar ones), four channels at a time in channel order
     const int og = tid & 31;        // outputs 4*og .. 4*og+3
     const int eg = tid >> 5;        // entries 4*eg .. 4*eg+3
-    float acc[4][4];
+    unsigned long long acc2[2][4];  // [output pair][entry] = (out 2i, out 2i+1)
 #pragma unroll
-    for (int a = 0; a < 4; a++)
+    for (int a = 0; a < 2; a++)
 #pragma unroll
-      for (int bq = 0; bq < 4; bq++) acc[a][bq] = 0.0f;
+      for (int bq = 0; bq < 4; bq++) acc2[a][bq] = 0ull;          // (+0, +0)
     const float* yb = ytile + eg * 4 * D;                         // this thread's 4 entries
 #pragma unroll 2
     for (int c4 = 0; c4 < D; c4 += 4) {
@@ -206,15 +226,24 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
 #pragma unroll
       for (int cc = 0; cc < 4; cc++) {                              // channels in order
         const uint2 wv = *reinterpret_cast<const uint2*>(wt + (c4 + cc) * DI + og * 4);
-        const float wf[4] = {__uint_as_float(wv.x << 16), __uint_as_float(wv.x & 0xFFFF0000u),
-                             __uint_as_float(wv.y << 16), __uint_as_float(wv.y & 0xFFFF0000u)};
+        unsigned long long w01, w23;                                // bf16 -> fp32 pairs
+        asm("mov.b64 %0, {%1, %2};" : "=l"(w01) : "r"(wv.x << 16), "r"(wv.x & 0xFFFF0000u));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(w23) : "r"(wv.y << 16), "r"(wv.y & 0xFFFF0000u));
 #pragma unroll
         for (int bq = 0; bq < 4; bq++) {
           const float yc = cc == 0 ? yv[bq].x : cc == 1 ? yv[bq].y : cc == 2 ? yv[bq].z : yv[bq].w;
-#pragma unroll
-          for (int a = 0; a < 4; a++) acc[a][bq] = __fmaf_rn(yc, wf[a], acc[a][bq]);
+          unsigned long long yy;
+          asm("mov.b64 %0, {%1, %1};" : "=l"(yy) : "f"(yc));
+          asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[0][bq]) : "l"(yy), "l"(w01));
+          asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[1][bq]) : "l"(yy), "l"(w23));
         }
       }
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int bq = 0; bq < 4; bq++) {
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[0][bq]), "=f"(acc[1][bq]) : "l"(acc2[0][bq]));
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2][bq]), "=f"(acc[3][bq]) : "l"(acc2[1][bq]));
     }
 
     // ---------------- phase 3: MXFP4 (8 lanes = one 32-wide block of outputs)
