@@ -22,15 +22,18 @@
 //   MXFP4      per 32: X = floor(log2 amax) - 2 clamped to [-127,127];
 //              code = E2M1(k * 2^-X); amax == 0 -> scale byte 0, codes +0
 //
-// Structure (persistent kernel, one CTA per SM, 256 threads):
+// Structure (persistent kernel, one CTA per SM, 512 threads in two roles that
+// hand each 32-entry tile over through named barriers; setmaxnreg gives the
+// entry pipeline 168 registers a thread and the projection 88):
 //   smem  W^T as bf16 [512 ch][128 o] (128 KB, loaded once per CTA)
 //         y tile   fp32 [32 entries][512 ch] (64 KB)
-//   phase 1  warp per entry, 4 entries per warp: the 128-bit loads of all
+//   phase 1  (warps 8..15, one tile ahead) warp per entry, 4 entries per
+//            warp: the 128-bit loads of all
 //            four entries' token rows are issued first, then each entry is
 //            compressed/normalised/rotated in registers, its 288-byte main
 //            entry written and y' staged in smem (16-byte stores, no bank
 //            conflicts); the next tile's token rows are prefetched into L2.
-//   phase 2  each thread owns 4 outputs x 4 entries (16 independent fma
+//   phase 2  (warps 0..7) each thread owns 4 outputs x 4 entries (16 independent fma
 //            chains), four channels at a time; W^T row reads are contiguous
 //            across the warp, y reads are broadcasts.  This phase is
 //            FP32-ALU bound (65,536 fma per entry).
@@ -39,8 +42,14 @@
 
 namespace csa2 {
 
-constexpr int CW_THREADS = 256;
+constexpr int CW_THREADS = 512;                   // warps 0..7 projection, 8..15 entry pipeline
+constexpr int CW_MATH_THREADS = 256;
+constexpr int CW_LOAD_WARPS = 8;
 constexpr int CW_TILE = 32;                       // entries per tile
+constexpr int CW_MATH_REGS = 88;                  // setmaxnreg split of the 128 x 512 registers:
+constexpr int CW_LOAD_REGS = 168;                 // 256 x 88 + 256 x 168 = 65,536
+static_assert(CW_MATH_THREADS * CW_MATH_REGS + (CW_THREADS - CW_MATH_THREADS) * CW_LOAD_REGS <= 65536,
+              "register split");
 constexpr int CW_SMEM = D * DI * 2 + CW_TILE * D * 4;  // 131072 + 65536
 
 
@@ -48,7 +57,7 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* wt = reinterpret_cast<uint16_t*>(smem);                  // [512][128]
   float* ytile = reinterpret_cast<float*>(smem + D * DI * 2);        // [512][32]
-  __shared__ int tile_valid[CW_TILE];
+  __shared__ int tile_valid[2][CW_TILE];           // by tile parity
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -63,20 +72,27 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
   const int64_t n_local = p.T / p.m;                   // entries per sequence
   const int64_t tiles_per_seq = ceil_div(n_local, CW_TILE);
   const int64_t n_tiles = tiles_per_seq * p.B;
+  __syncthreads();                                     // W^T ready
 
-  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+  // Two roles over the same tile sequence, handing the y tile over with named
+  // barriers: FULL (1) when the entry pipeline has stored a tile's y', EMPTY (2)
+  // when the projection has finished reading it.  The entry pipeline computes
+  // tile i+1 in registers while the projection runs on tile i.
+  if (warp >= CW_MATH_THREADS / 32) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(CW_LOAD_REGS));
+    const int lwarp = warp - CW_MATH_THREADS / 32;
+  for (int64_t tile = blockIdx.x, it = 0; tile < n_tiles; tile += gridDim.x, it++) {
     const int b = (int)(tile / tiles_per_seq);
     const int64_t j0 = (tile % tiles_per_seq) * CW_TILE;
     const int64_t e0 = p.entry_start[b];
-    __syncthreads();   // previous tile's readers of ytile are done (and W^T is ready)
 
     // ---------------- phase 1: warp per entry, loads of all four entries first
-    constexpr int EPW = CW_TILE / (CW_THREADS / 32);             // entries per warp
+    constexpr int EPW = CW_TILE / CW_LOAD_WARPS;                  // entries per warp
     uint4 xr[EPW][4];                                             // rows x_{2j}, x_{2j+1} (m = 2) or x_j
     bool ok[EPW];
 #pragma unroll
     for (int u = 0; u < EPW; u++) {
-      const int t = warp + u * (CW_THREADS / 32);
+      const int t = lwarp + u * CW_LOAD_WARPS;
       const int64_t j = j0 + t;
       const int64_t e = e0 + j;
       bool valid = j < n_local;
@@ -85,7 +101,6 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
         valid = false;
       }
       ok[u] = valid;
-      if (lane == 0) tile_valid[t] = valid;
       if (valid) {
         const uint4* x0 = reinterpret_cast<const uint4*>(p.x + ((int64_t)b * p.T + j * p.m) * D + lane * 16);
         xr[u][0] = __ldg(x0);
@@ -152,7 +167,7 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
     if (lane >= 28) {
 #pragma unroll
       for (int u = 0; u < EPW; u++) {
-        const int64_t e = ok[u] ? e0 + j0 + warp + u * (CW_THREADS / 32) : 0;
+        const int64_t e = ok[u] ? e0 + j0 + lwarp + u * CW_LOAD_WARPS : 0;
         const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + (e * 32 + (lane - 28) * 8) * 2);
 #pragma unroll
         for (int q = 0; q < 4; q++) {
@@ -181,17 +196,23 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
           packed[k / 4] |= byte << (8 * (k % 4));
         }
       }
-      const int t = warp + u * (CW_THREADS / 32);
+      const int t = lwarp + u * CW_LOAD_WARPS;
       if (ok[u]) {
         uint8_t* ent = p.main_kv + ((int64_t)b * p.cap + e0 + j0 + t) * MAIN_BYTES;
         *reinterpret_cast<uint2*>(ent + lane * 8) = make_uint2(packed[0], packed[1]);
         ent[256 + lane] = (uint8_t)sb;
       }
+    }
+    if (it > 0) asm volatile("bar.sync 2, %0;" :: "n"(CW_THREADS) : "memory");   // EMPTY
+#pragma unroll
+    for (int u = 0; u < EPW; u++) {
+      const int t = lwarp + u * CW_LOAD_WARPS;
       float4* yrow = reinterpret_cast<float4*>(ytile + t * D + lane * 16);
 #pragma unroll
       for (int q = 0; q < 4; q++)
         yrow[q] = ok[u] ? make_float4(y[u][4 * q], y[u][4 * q + 1], y[u][4 * q + 2], y[u][4 * q + 3])
                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane == 0) tile_valid[it & 1][t] = ok[u];
     }
     // next tile's token rows into L2 while this tile's projection runs
     {
@@ -201,11 +222,20 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
         const int64_t nj0 = (nt % tiles_per_seq) * CW_TILE;
         const int64_t rows = (nj0 + CW_TILE <= n_local ? CW_TILE : n_local - nj0) * p.m;
         const char* base = reinterpret_cast<const char*>(p.x + ((int64_t)nb * p.T + nj0 * p.m) * D);
-        for (int64_t off = (int64_t)tid * 128; off < rows * D * 2; off += (int64_t)CW_THREADS * 128)
+        const int ltid = tid - CW_MATH_THREADS;
+        for (int64_t off = (int64_t)ltid * 128; off < rows * D * 2; off += (int64_t)(CW_THREADS - CW_MATH_THREADS) * 128)
           asm volatile("prefetch.global.L2 [%0];" :: "l"(base + off));
       }
     }
-    __syncthreads();
+    asm volatile("bar.arrive 1, %0;" :: "n"(CW_THREADS) : "memory");            // FULL
+  }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(CW_MATH_REGS));
+  for (int64_t tile = blockIdx.x, it = 0; tile < n_tiles; tile += gridDim.x, it++) {
+    const int b = (int)(tile / tiles_per_seq);
+    const int64_t j0 = (tile % tiles_per_seq) * CW_TILE;
+    const int64_t e0 = p.entry_start[b];
+    asm volatile("bar.sync 1, %0;" :: "n"(CW_THREADS) : "memory");              // FULL
 
     // ---------------- phase 2: k = W y', 4 outputs x 4 entries per thread,
     // as packed pairs of outputs (fma.rn.f32x2: two round-to-nearest fmas, the
@@ -239,6 +269,7 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
         }
       }
     }
+    if (tile + gridDim.x < n_tiles) asm volatile("bar.arrive 2, %0;" :: "n"(CW_THREADS) : "memory");  // EMPTY
     float acc[4][4];
 #pragma unroll
     for (int bq = 0; bq < 4; bq++) {
@@ -254,7 +285,7 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
       float amax = fmaxf(fmaxf(fabsf(acc[0][bq]), fabsf(acc[1][bq])), fmaxf(fabsf(acc[2][bq]), fabsf(acc[3][bq])));
 #pragma unroll
       for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-      if (!tile_valid[t]) continue;     // uniform across the warp
+      if (!tile_valid[it & 1][t]) continue;     // uniform across the warp
       const int64_t e = e0 + j;
       uint32_t scale_byte, codes = 0;
       if (amax == 0.0f) {
@@ -274,6 +305,7 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
       *reinterpret_cast<uint16_t*>(cdst + og * 2) = (uint16_t)codes;
       if ((og & 7) == 0) p.idx_scales[((int64_t)b * p.cap + e) * IDX_SCALE_BYTES + (og >> 3)] = (uint8_t)scale_byte;
     }
+  }
   }
 }
 
