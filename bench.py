@@ -13,7 +13,10 @@ own 5.97 GB cache copy) and software-pipelines them: step s runs the Reindex
 layer of instance s, Reuse-1 of instance s-d, Reuse-2 of s-2d and Reuse-3 of
 s-3d, so roughly d steps (d * 44 MB > L2) pass between two layers touching
 the same instance.  One step = four layer calls of batch 16 = 64
-query-token-layers.
+query-token-layers.  The four calls of a step belong to four different
+instances, so they are independent and run as parallel branches of the step's
+CUDA graph (four streams); the line also reports the same steps with the calls
+in sequence on one stream (``serial_schedule``).
 
 ``--seq-len`` shrinks the cache (the same step on fewer entries; used for
 small profiler captures), ``--cpu-sample-queries 0`` skips the CPU oracle leg.
@@ -221,11 +224,17 @@ class Decode1M:
                 "sel": torch.empty((B, 1, K), dtype=torch.int32, device=dev),
             }
             self.inst.append(inst)
-        self.ws = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REINDEX, B, 1, N, M, K), device=dev)
+        # one workspace per layer slot: the four layer calls of a step may run at once
+        self.ws = [csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REINDEX if l == 0 else csa2.MODE_REUSE,
+                                                             B, 1, N, M, K), device=dev) for l in range(4)]
+        # the Reindex branch (fused score/select + attention) is the step's critical
+        # path: it runs on a high-priority stream and is enqueued first
+        self.hi = torch.cuda.Stream(priority=-1)
+        self.side = [torch.cuda.Stream() for _ in range(3)]
         for r in range(self.R):          # every instance starts with a published selection
             self.layer(0, r)
         torch.cuda.synchronize()
-        assert self.ws.sync_status()[0] == 0
+        self.check_status()
         self.setup_s = time.time() - t0
 
     def layer(self, layer: int, r: int):
@@ -233,18 +242,40 @@ class Decode1M:
         mode = csa2.MODE_REINDEX if layer == 0 else csa2.MODE_REUSE
         csa2.decode(mode, self.caches[r], q_pos=self.q_pos, q=inst["q"][layer].view(torch.int16),
                     swa=inst["swa"][layer].view(torch.int16), swa_base_pos=self.swa_base, scale=1 / math.sqrt(D),
-                    sel=inst["sel"], out=inst["out"][layer].view(torch.int16), ws=self.ws, M=M_BLK, max_n=self.N,
+                    sel=inst["sel"], out=inst["out"][layer].view(torch.int16), ws=self.ws[layer], M=M_BLK, max_n=self.N,
                     q_idx=inst["q_idx"].view(torch.int16), w_head=inst["w_head"], pool_blocks=self.pool)
 
-    def step(self, s: int, events=None):
-        """Reindex(s), Reuse1(s-d), Reuse2(s-2d), Reuse3(s-3d) over instances mod R."""
-        for layer in range(4):
-            r = (s - layer * self.d) % self.R
-            if events is not None:
-                events[layer][0].record()
-            self.layer(layer, r)
-            if events is not None:
-                events[layer][1].record()
+    def check_status(self):
+        for ws in self.ws:
+            st, detail = ws.sync_status()
+            assert st == 0, f"device status {st} ({detail})"
+
+    def step(self, s: int, concurrent: bool = True):
+        """Reindex(s), Reuse1(s-d), Reuse2(s-2d), Reuse3(s-3d) over instances mod R.
+        The four calls touch four different instances (R > 3d), so they are
+        independent: concurrently they run as parallel branches (the Reindex call
+        on the current stream, the Reuse calls on three side streams), otherwise
+        one after another on the current stream."""
+        torch = self.torch
+        if not concurrent:
+            for layer in range(4):
+                self.layer(layer, (s - layer * self.d) % self.R)
+            return
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        self.hi.wait_event(fork)
+        with torch.cuda.stream(self.hi):
+            self.layer(0, s % self.R)
+        for layer in range(1, 4):
+            st = self.side[layer - 1]
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                self.layer(layer, (s - layer * self.d) % self.R)
+        for st in (self.hi, *self.side):
+            join = torch.cuda.Event()
+            join.record(st)
+            main.wait_event(join)
 
     def prologue(self):
         for s in range(3 * self.d):
@@ -308,15 +339,26 @@ def run_decode1m(args, torch, csa2):
         torch.cuda.nvtx.range_pop()
     barrier(world)
     total_ms = max_over_ranks(start.elapsed_time(stop), world)
-    st, detail = w.ws.sync_status()
-    assert st == 0, f"device status {st} ({detail})"
+    w.check_status()
+    # the same steps with the four layer calls one after another on one stream
+    serial = [_capture(torch, lambda i=i: w.step(s_base + i, concurrent=False)) for i in range(w.R)]
+    for s in range(args.warmup):
+        serial[s % w.R].replay()
+    torch.cuda.synchronize()
+    n_serial = min(n_steps, 1000)
+    start.record()
+    for i in range(n_serial):
+        serial[(s0 + i) % w.R].replay()
+    stop.record()
+    torch.cuda.synchronize()
+    serial_ms = max_over_ranks(start.elapsed_time(stop), world) / n_serial
+    w.check_status()
     # per-layer-call durations, same pipeline (cold instances), timed by layer type
     reindex_g = _capture(torch, lambda: [w.layer(0, r) for r in range(w.R)])
     reuse_g = _capture(torch, lambda: [w.layer(1 + (r % 3), r) for r in range(w.R)])
     reindex_ms = _graph_ms(torch, reindex_g, 20) / w.R
     reuse_ms = _graph_ms(torch, reuse_g, 20) / w.R
-    st, detail = w.ws.sync_status()
-    assert st == 0, f"device status {st} ({detail})"
+    w.check_status()
 
     ms_step = total_ms / n_steps
     qtl_per_step = w.B * 4
@@ -336,7 +378,9 @@ def run_decode1m(args, torch, csa2):
                    "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                    "l2": f"inputs larger than L2: {w.R} pipelined instances x "
                          f"{w.B * w.N * (MAIN_ENTRY + IDX_ENTRY) / 1e9:.2f} GB, layer distance {w.d} steps",
-                   "launch": "one CUDA graph per pipeline phase (4 layer calls)",
+                   "launch": "one CUDA graph per pipeline phase: the 4 layer calls (4 different pipelined "
+                             "instances, so independent) as parallel branches on 4 streams, the Reindex "
+                             "branch first at high priority",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -346,6 +390,9 @@ def run_decode1m(args, torch, csa2):
         "step_hbm": {"algorithmic_bytes": bytes_step, "GB_s": bytes_step / (ms_step / 1e3) / 1e9,
                      "frac": bytes_step / (ms_step / 1e3) / 1e9 / hbm},
         "layer_ms": {"reindex": reindex_ms, "reuse": reuse_ms},
+        "serial_schedule": {"value": qtl_per_step * world / (serial_ms / 1e3), "ms_per_step": serial_ms,
+                            "steps": n_serial, "launch": "the same graphs with the 4 layer calls in sequence "
+                                                         "on one stream"},
         "full_scan_1m_ms_untimed_setup": w.full_scan_ms,
         "clocks": clk.summary(),
         # Reindex layer: fused score + select kernel and attention; Reuse: attention
@@ -394,10 +441,10 @@ def run_decode1m_e2e(args, torch, csa2, w):
                 d[off_w: off_w + wh_bytes].view(torch.float32).view(B, 1, HI),
                 [dev_out[k][l * q_bytes:(l + 1) * q_bytes].view(torch.int16).view(B, 1, H, D) for l in range(4)])
     bufs = [views(0), views(1)]
-    main = torch.cuda.current_stream()
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
     def step(s):
+        main = torch.cuda.current_stream()          # the capturing stream when captured
         k = s % 2
         q_view, row_view, qidx_view, w_view, out_view = bufs[k]
         fork = torch.cuda.Event()
@@ -408,15 +455,22 @@ def run_decode1m_e2e(args, torch, csa2, w):
             dev_in[1 - k].copy_(host_in, non_blocking=True)          # inputs of step s + 1
         with torch.cuda.stream(d2h):
             host_out.copy_(dev_out[1 - k], non_blocking=True)        # outputs of step s - 1
-        for layer in range(4):
+        def layer_call(layer):
             r = (s - layer * w.d) % w.R
             inst = w.inst[r]
             inst["swa"][layer][:, WIN - 1].view(torch.int16).copy_(row_view[layer])
             mode = csa2.MODE_REINDEX if layer == 0 else csa2.MODE_REUSE
             csa2.decode(mode, w.caches[r], q_pos=w.q_pos, q=q_view[layer], swa=inst["swa"][layer].view(torch.int16),
                         swa_base_pos=w.swa_base, scale=1 / math.sqrt(D), sel=inst["sel"], out=out_view[layer],
-                        ws=w.ws, M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view, pool_blocks=w.pool)
-        for st in (h2d, d2h):
+                        ws=w.ws[layer], M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view, pool_blocks=w.pool)
+        w.hi.wait_event(fork)                      # independent instances: parallel branches,
+        with torch.cuda.stream(w.hi):              # the Reindex branch first and at high priority
+            layer_call(0)
+        for layer in range(1, 4):
+            w.side[layer - 1].wait_event(fork)
+            with torch.cuda.stream(w.side[layer - 1]):
+                layer_call(layer)
+        for st in (h2d, d2h, w.hi, *w.side):
             join = torch.cuda.Event()
             join.record(st)
             main.wait_event(join)
@@ -426,6 +480,10 @@ def run_decode1m_e2e(args, torch, csa2, w):
     for i in range(args.warmup):
         graphs[i % w.R].replay()
     torch.cuda.synchronize()
+    # fresh host data and a cleared output block: the checks below prove that the
+    # graphs carry both copies
+    host_in[off_w:].view(torch.float32).normal_()
+    host_out.zero_()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for i in range(args.steps):
@@ -433,10 +491,15 @@ def run_decode1m_e2e(args, torch, csa2, w):
     stop.record()
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / args.steps
+    w.check_status()
+    k_last = (s0 + (args.warmup + args.steps - 1) % w.R) % 2
+    assert torch.equal(dev_in[1 - k_last].cpu(), host_in), "input copy missing from the step graph"
+    assert torch.equal(host_out, dev_out[1 - k_last].cpu()) and bool(host_out.any()), \
+        "output copy missing from the step graph"
     return {"value": B * 4 / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": in_bytes,
             "d2h_bytes_per_step": out_bytes, "launch": "one CUDA graph per pipeline phase: the next step's "
             "input copy and the previous step's output copy on two copy streams, overlapped with 4 window-row "
-            "placements and 4 layer calls"}
+            "placements and 4 layer calls in parallel branches"}
 
 
 # ------------------------------------------------------------------ other configurations
