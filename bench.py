@@ -301,6 +301,28 @@ def _capture(torch, fn):
     return g
 
 
+class PhaseGraphs:
+    """CUDA graphs of a pipelined step: one per pipeline phase (step s depends
+    only on s mod R) and one of a whole cycle of R consecutive phases, so that
+    long runs launch one graph per R steps."""
+
+    def __init__(self, torch, step_fn, R: int, s_base: int):
+        self.R = R
+        self.single = [_capture(torch, lambda i=i: step_fn(s_base + i)) for i in range(R)]
+        self.cycle = _capture(torch, lambda: [step_fn(s_base + i) for i in range(R)])
+
+    def run(self, first: int, n: int):
+        """Replays steps first .. first + n - 1 (exactly n steps)."""
+        i = 0
+        while i < n:
+            if (first + i) % self.R == 0 and n - i >= self.R:
+                self.cycle.replay()
+                i += self.R
+            else:
+                self.single[(first + i) % self.R].replay()
+                i += 1
+
+
 def _graph_ms(torch, graph, reps):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     graph.replay()
@@ -318,11 +340,10 @@ def run_decode1m(args, torch, csa2):
     w = Decode1M(csa2, torch, N=args.seq_len, d=args.pipeline_distance)
     w.prologue()
     torch.cuda.synchronize()
-    # one graph per pipeline phase: step s only depends on s mod R
+    # graphs per pipeline phase and per cycle of R phases: step s only depends on s mod R
     s_base = 3 * w.d
-    graphs = [_capture(torch, lambda i=i: w.step(s_base + i)) for i in range(w.R)]
-    for s in range(args.warmup):
-        graphs[s % w.R].replay()
+    graphs = PhaseGraphs(torch, w.step, w.R, s_base)
+    graphs.run(0, args.warmup)
     torch.cuda.synchronize()
     n_steps = args.steps
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -332,8 +353,7 @@ def run_decode1m(args, torch, csa2):
     with ClockSampler(local) as clk:
         torch.cuda.nvtx.range_push("timed")
         start.record()
-        for i in range(n_steps):
-            graphs[(s0 + i) % w.R].replay()
+        graphs.run(s0, n_steps)
         stop.record()
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
@@ -341,14 +361,12 @@ def run_decode1m(args, torch, csa2):
     total_ms = max_over_ranks(start.elapsed_time(stop), world)
     w.check_status()
     # the same steps with the four layer calls one after another on one stream
-    serial = [_capture(torch, lambda i=i: w.step(s_base + i, concurrent=False)) for i in range(w.R)]
-    for s in range(args.warmup):
-        serial[s % w.R].replay()
+    serial = PhaseGraphs(torch, lambda s: w.step(s, concurrent=False), w.R, s_base)
+    serial.run(0, args.warmup)
     torch.cuda.synchronize()
     n_serial = min(n_steps, 1000)
     start.record()
-    for i in range(n_serial):
-        serial[(s0 + i) % w.R].replay()
+    serial.run(s0, n_serial)
     stop.record()
     torch.cuda.synchronize()
     serial_ms = max_over_ranks(start.elapsed_time(stop), world) / n_serial
@@ -378,9 +396,9 @@ def run_decode1m(args, torch, csa2):
                    "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                    "l2": f"inputs larger than L2: {w.R} pipelined instances x "
                          f"{w.B * w.N * (MAIN_ENTRY + IDX_ENTRY) / 1e9:.2f} GB, layer distance {w.d} steps",
-                   "launch": "one CUDA graph per pipeline phase: the 4 layer calls (4 different pipelined "
-                             "instances, so independent) as parallel branches on 4 streams, the Reindex "
-                             "branch first at high priority",
+                   "launch": "CUDA graphs of 10 consecutive steps (one per phase for a remainder); in a "
+                             "step the 4 layer calls (4 different pipelined instances, so independent) are "
+                             "parallel branches on 4 streams, the Reindex branch first at high priority",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -476,9 +494,8 @@ def run_decode1m_e2e(args, torch, csa2, w):
             main.wait_event(join)
 
     s0 = 3 * w.d
-    graphs = [_capture(torch, lambda i=i: step(s0 + i)) for i in range(w.R)]
-    for i in range(args.warmup):
-        graphs[i % w.R].replay()
+    graphs = PhaseGraphs(torch, step, w.R, s0)
+    graphs.run(0, args.warmup)
     torch.cuda.synchronize()
     # fresh host data and a cleared output block: the checks below prove that the
     # graphs carry both copies
@@ -486,8 +503,7 @@ def run_decode1m_e2e(args, torch, csa2, w):
     host_out.zero_()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
-    for i in range(args.steps):
-        graphs[(args.warmup + i) % w.R].replay()
+    graphs.run(args.warmup, args.steps)
     stop.record()
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / args.steps
@@ -497,7 +513,7 @@ def run_decode1m_e2e(args, torch, csa2, w):
     assert torch.equal(host_out, dev_out[1 - k_last].cpu()) and bool(host_out.any()), \
         "output copy missing from the step graph"
     return {"value": B * 4 / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": in_bytes,
-            "d2h_bytes_per_step": out_bytes, "launch": "one CUDA graph per pipeline phase: the next step's "
+            "d2h_bytes_per_step": out_bytes, "launch": "CUDA graphs of 10 consecutive steps; per step the next step's "
             "input copy and the previous step's output copy on two copy streams, overlapped with 4 window-row "
             "placements and 4 layer calls in parallel branches"}
 
