@@ -433,7 +433,7 @@ constexpr int RS_CAP = 8192;                     // candidates kept per row and 
 constexpr int RS_THREADS = 256;
 constexpr int RS_WARPS = RS_THREADS / 32;
 constexpr int RS_TILE = 512;                     // entries per warp tile: lane l holds 128 i + 4 l + c
-constexpr int RS_TILES = 2;                      // warp tiles loaded together
+constexpr int RS_TILES = 1;                      // warp tiles loaded together
 constexpr int RS_BATCH = RS_WARPS * RS_TILE * RS_TILES;   // 8,192 entries: one batch of a scan CTA
 constexpr int RS_SCAN_CTAS_PER_SM = 4;           // resident scan CTAs per SM (launch bounds)
 constexpr int RS_MAX_OUT = CSA2_MAX_M;           // >= CSA2_MAX_K
