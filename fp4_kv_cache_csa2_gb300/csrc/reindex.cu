@@ -148,6 +148,7 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
 
   uint32_t prefix = 0, mask = 0;
   int remaining = K;
+  bool take_all = false;                                   // at most K candidates in the cluster
   for (int pass = 0; pass < 4; pass++) {
     const int shift = 24 - 8 * pass, buf = pass & 1;
 #pragma unroll
@@ -210,17 +211,21 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
       if (here >= (uint32_t)remaining && above < (uint32_t)remaining) {
         fs.bcast[0] = tid;                                 // the digit of the K-th largest key
         fs.bcast[1] = remaining - (int)above;
+        fs.bcast[2] = (int)(here - above);                 // keys of the cluster in that digit's bin
       }
     }
     __syncthreads();
     const int d = fs.bcast[0];
+    // the rest of the threshold bin is taken whole: the keys' remaining bits
+    // need not be looked at (the usual case after the third digit)
+    const bool whole = d >= 0 && fs.bcast[2] == fs.bcast[1];
     if (tid < RX_CL) {
       const uint32_t* row = fs.rows[buf][tid];
       fs.gt_all[tid] += (int)(d < 0 ? row[0] : (d < 255 ? row[d + 1] : 0u));
-      if (pass == 3) fs.eq_all[tid] = (int)(row[d] - (d < 255 ? row[d + 1] : 0u));
+      if (pass == 3 || whole) fs.eq_all[tid] = (int)(row[d] - (d < 255 ? row[d + 1] : 0u));
     }
-    if (d < 0) {                                           // threshold 0: every valid key is above it
-      prefix = 0;
+    if (d < 0) {                                           // every valid key is taken
+      take_all = true;
       remaining = 0;
       break;
     }
@@ -228,6 +233,7 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
     mask |= 255u << shift;
     remaining = fs.bcast[1];
     __syncthreads();                                       // bcast read before the next pass writes it
+    if (whole) break;
   }
   const uint32_t thr = prefix;
   const int take_eq = remaining;                           // keys equal to thr still to take, in slot order
@@ -263,8 +269,9 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
   for (int j = 0; j < KPT; j++) {
     const uint32_t k = kr[j];
     if (k == 0u) continue;
-    if (k > thr) gt++;
-    else if (k == thr) eq++;
+    const uint32_t km = k & mask;                          // digits fixed so far (all 32 bits after 4 passes)
+    if (take_all || km > thr) gt++;
+    else if (km == thr) eq++;
   }
   int gt_tot, eq_tot;
   const int gt_before = cta_exclusive_scan(gt, fs, &gt_tot);    // (its barriers also publish bcast)
@@ -277,8 +284,9 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
   for (int j = 0; j < KPT; j++) {
     const uint32_t k = kr[j];
     if (k == 0u) continue;
-    bool take = k > thr;
-    if (!take && k == thr && used < mine_eq) { take = true; used++; }
+    const uint32_t km = k & mask;
+    bool take = take_all || km > thr;
+    if (!take && km == thr && used < mine_eq) { take = true; used++; }
     if (take) out(i0 + j, r++);
   }
   return total;                    // the last push preceded the last cluster barrier
