@@ -30,15 +30,18 @@
 //     the MN-major bf16 B operand [key][head] of the second product, L_c = sum P;
 //   * O^T = V^T P^T reuses the key buffer as an MN-major A operand: 4 tiles of
 //     M=128 dims x N=64 heads x K=128 keys;
-//   * every CTA stages its normalised share O_c / L_c of each 128-dim tile in
-//     fp16 (a convex combination of key vectors, relative rounding 2^-11) and
-//     bulk-copies the tiles it does not own, each followed by its (m_c, L_c)
-//     rows, into the owner's receive slots over distributed shared memory; the
-//     owner weights the C shares by L_c exp(m_c - M) / sum_c' L_c' exp(m_c' - M),
-//     M = max_c m_c, in fp32, rounds to bf16 and stores.  A split cluster
-//     barrier (arrive once the receive slots are dead, wait before sending)
-//     orders the exchange; no CTA reads another's shared memory, and the
-//     owners' byte counts make a closing cluster barrier unnecessary.
+//   * every CTA bulk-copies its (m_c, L_c) rows to every owner as soon as its
+//     second product is done, then stages its normalised share O_c / L_c of
+//     each 128-dim tile in fp16 (a convex combination of key vectors, relative
+//     rounding 2^-11) and bulk-copies the tiles it does not own into the
+//     owners' receive slots over distributed shared memory, one mbarrier per
+//     slot; the owner weights the C shares by
+//     L_c exp(m_c - M) / sum_c' L_c' exp(m_c' - M), M = max_c m_c, in fp32,
+//     folds each share in as it lands, rounds to bf16 and stores.  Two split
+//     cluster barriers order the exchange (phase 1: every mbarrier is
+//     initialised; phase 2: every receive slot is dead); no CTA reads another's
+//     shared memory, and the owners' byte counts make a closing cluster
+//     barrier unnecessary.
 // All mbarrier waits are bounded; a timeout reports CSA2_ERR_TIMEOUT.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
@@ -70,11 +73,14 @@ struct AtSmall {
   int kvalid[AT_KEYS];
   int32_t kid[AT_KEYS];
   alignas(16) float ml[2 * H];           // this CTA's row maxima m_c, then row sums L_c (sent to the owners)
-  alignas(16) float recv_ml[4][2 * H];   // (m, L) rows received with each share
+  alignas(16) float recv_ml[4][2 * H];   // (m, L) rows received from each other CTA (index = sender rank,
+                                         // minus one above this CTA's own)
   float inv_l[H];
   float red[4][H];                       // per-warp column maxima / sums (warp w & 3, head)
   float wgt[AT_MAXC][H];                 // combination weight of each CTA's share, per head
-  uint64_t bar_kv, bar_s, bar_o, bar_red;
+  uint64_t bar_kv, bar_s, bar_o;
+  uint64_t bar_ml;                       // every other CTA's (m, L) rows received (owners only)
+  uint64_t bar_slot[4];                  // receive slot s holds a complete share
   uint64_t bar_q;                        // all of Q landed (chunks 0..3 and 4..7: two arrivals)
   uint64_t bar_keys;                     // every warp's dequantised keys are in shared memory
   uint32_t tmem_base;
@@ -158,7 +164,8 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::bar_init(&sm.bar_kv, 1);
     tc::bar_init(&sm.bar_s, 1);
     tc::bar_init(&sm.bar_o, 1);
-    tc::bar_init(&sm.bar_red, 1);
+    tc::bar_init(&sm.bar_ml, 1);
+    for (int i = 0; i < 4; i++) tc::bar_init(&sm.bar_slot[i], 1);
     tc::bar_init(&sm.bar_q, 2);
     tc::bar_init(&sm.bar_keys, AT_THREADS / 32);
     sm.err = 0;
@@ -197,6 +204,10 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   tc::fence_before_sync();
   __syncthreads();                       // local barriers and key flags visible (no remote access yet)
   tc::fence_after_sync();
+  // cluster barrier phase 1 (waited on after the second product): every CTA's
+  // mbarriers are initialised before any other CTA signals them (the init
+  // fence above releases them, so the arrival itself can be relaxed)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const uint32_t tmem = sm.tmem_base;
 
   // ---------------- copies: window rows (window CTA) and all of Q
@@ -236,6 +247,10 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     __syncthreads();
+    // Bank order: a quarter-warp (8 lanes) covers 4 entries x 2 halves.  The
+    // odd lane of a pair walks its pieces and 16-channel groups in a permuted
+    // order (pieces k ^ 1, groups g ^ 2), so that within every 128-bit access
+    // the 8 lanes touch 8 different 16-byte bank groups, loads and stores alike.
     const int s = warp * 16 + (lane >> 1), hf = lane & 1;
     uint4 code[8], scl = make_uint4(0u, 0u, 0u, 0u);     // masked keys: +0 codes, scale 0 -> zero rows
 #pragma unroll
@@ -243,7 +258,7 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     if (sm.kvalid[s] == 1) {
       const uint4* ent = reinterpret_cast<const uint4*>(stage + s * MAIN_BYTES);
 #pragma unroll
-      for (int k = 0; k < 8; k++) code[k] = ent[hf * 8 + k];
+      for (int k = 0; k < 8; k++) code[k] = ent[hf * 8 + (k ^ hf)];   // odd lane: the chunk's two pieces swapped
       scl = ent[16 + hf];
     }
     tc::fence_proxy_async_smem();
@@ -252,7 +267,13 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
       tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
       for (int c = 4; c < 8; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
     }
-    const uint32_t scw[4] = {scl.x, scl.y, scl.z, scl.w};
+    // odd lane: scale bytes rotated by two, matching its group order g ^ 2
+    const uint32_t rot = hf ? 16u : 0u;
+    const uint32_t scw[4] = {__funnelshift_r(scl.x, scl.x, rot), __funnelshift_r(scl.y, scl.y, rot),
+                             __funnelshift_r(scl.z, scl.z, rot), __funnelshift_r(scl.w, scl.w, rot)};
+    // SW128 row s: 16-byte unit u of a chunk row lands at unit u ^ (s & 7); the
+    // odd lane's group g ^ 2 is unit pair (2g, 2g + 1) ^ 4
+    const uint32_t xr = ((uint32_t)s & 7u) ^ ((uint32_t)hf << 2);
 #pragma unroll
     for (int i = 0; i < 4; i++) {
       unsigned char* rowp = kbuf + (4 * hf + i) * AT_CHUNK_BYTES;
@@ -267,8 +288,9 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
         e2m1x8_to_bf16(cw[2 * g + 1], o + 4);
 #pragma unroll
         for (int k = 0; k < 8; k++) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(o[k]), "r"(sc2));
-        *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(rowp + sw128((uint32_t)s, (uint32_t)g * 32u + 16u)) = make_uint4(o[4], o[5], o[6], o[7]);
+        unsigned char* dst = rowp + s * 128;
+        *reinterpret_cast<uint4*>(dst + (((2u * g) ^ xr) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + (((2u * g + 1u) ^ xr) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     }
     tc::fence_proxy_async_smem();
@@ -299,8 +321,12 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   __syncwarp();
 
   // ---------------- softmax straight from TMEM: warp w holds keys 32(w&3) .. +31 (one
-  // per lane) and heads 32(w>>2) .. +31 (one per register)
-  at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
+  // per lane) and heads 32(w>>2) .. +31 (one per register).  The issuing thread
+  // observes the completion late while its own MMAs are in flight, so warp 1
+  // takes it from warp 0 through a named barrier instead of the mbarrier.
+  if (warp != 1) at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
+  if (warp == 0) asm volatile("bar.arrive 1, 64;" ::: "memory");
+  else if (warp == 1) asm volatile("bar.sync 1, 64;" ::: "memory");
   tc::fence_after_sync();
   {
     const int q4 = warp & 3, half = warp >> 2;
@@ -363,6 +389,7 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
       const float sum = sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
       sm.ml[H + tid] = sum;
       sm.inv_l[tid] = sum > 0.f ? 1.0f / sum : 0.f;
+      tc::fence_proxy_async_smem();                // the (m, L) rows are read by bulk copies
     }
   }
   // ---------------- O^T = V^T P^T  (4 tiles of M = 128 dims, N = 64 heads, K = 128 keys)
@@ -381,11 +408,36 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::commit(&sm.bar_o);
   }
   __syncwarp();
-  at_wait(&sm.bar_o, 0, sm, p.hdr, 14);
-  __syncthreads();                                         // 1 / L_c visible to every thread
+  if (warp != 1) at_wait(&sm.bar_o, 0, sm, p.hdr, 14);   // (the issuing warp: by the barrier below)
+  __syncthreads();                                         // O^T complete; 1 / L_c visible to every thread
   tc::fence_after_sync();
-  // S^T and P are dead, so this CTA's receive slots (over them) are free
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // phase 1 (long complete)
+  // phase 2: S^T and P are dead, so this CTA's receive slots (over them) are
+  // free.  The tensor cores have read P (its completion was observed above),
+  // so no write of this CTA into the slots is still in flight and the arrival
+  // needs no release (a releasing arrival costs about half a microsecond).
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // Tile t of the output is owned by CTA t % C.  Every CTA sends its (m, L)
+  // rows to every other owner now, ahead of the shares, so the owners can
+  // weight the shares as soon as their own are staged.
+  int owned = 0;
+  for (int tile = rank; tile < 4; tile += C) owned++;
+  if (tid == 0) {
+    if (owned) {
+      tc::bar_arrive_expect_tx(&sm.bar_ml, (uint32_t)((C - 1) * 2 * H * 4));
+      for (int sl = 0; sl < owned * (C - 1); sl++) tc::bar_arrive_expect_tx(&sm.bar_slot[sl], (uint32_t)AT_SHARE_BYTES);
+    }
+    const int n_owners = C < 4 ? C : 4;
+    for (int owner = 0; owner < n_owners; owner++) {
+      if (owner == rank) continue;
+      uint32_t dml, rbar;
+      const int si = rank < owner ? rank : rank - 1;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dml) : "r"(tc::smem_u32(sm.recv_ml[si])), "r"(owner));
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(tc::smem_u32(&sm.bar_ml)), "r"(owner));
+      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                   :: "r"(dml), "r"(tc::smem_u32(sm.ml)), "r"(2 * H * 4), "r"(rbar) : "memory");
+    }
+  }
   // this CTA's share O_c / L_c per tile as fp16 [dim][head], 16-byte units swizzled by dim
   {
     const int q4 = warp & 3, half = warp >> 2;
@@ -428,33 +480,30 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   }
   tc::fence_proxy_async_smem();
   __syncthreads();
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every owner's slots are free
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // phase 2: every owner's slots are free
 
-  // ---------------- cluster reduction: tile t is owned by CTA t % C; the others send
-  // their fp16 share and (m, L) rows into the owner's slot (j * (C - 1) + sender index)
-  int owned = 0;
-  for (int tile = rank; tile < 4; tile += C) owned++;
+  // ---------------- cluster reduction: the CTAs send their fp16 share of tile t into
+  // its owner's slot j * (C - 1) + sender index (j = t / C), each slot with its own
+  // barrier; the owner weights them (its (m, L) rows are in) and folds each share
+  // in as it lands
   if (tid == 0) {
-    if (owned) tc::bar_arrive_expect_tx(&sm.bar_red, (uint32_t)(owned * (C - 1) * (AT_SHARE_BYTES + 2 * H * 4)));
-    for (int tile = 0; tile < 4; tile++) {
+    // senders start on different owners: tile order rank + 1, rank + 2, ... (mod 4)
+    for (int k = 1; k <= 4; k++) {
+      const int tile = (rank + k) & 3;
       const int owner = tile % C;
       if (owner == rank) continue;
-      const int j = tile / C;
-      const int slot = j * (C - 1) + (rank < owner ? rank : rank - 1);
-      uint32_t dst, dml, rbar;
+      const int slot = (tile / C) * (C - 1) + (rank < owner ? rank : rank - 1);
+      uint32_t dst, rbar;
       asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(tc::smem_u32(orecv + slot * (128 * H))), "r"(owner));
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dml) : "r"(tc::smem_u32(sm.recv_ml[slot])), "r"(owner));
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(tc::smem_u32(&sm.bar_red)), "r"(owner));
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(tc::smem_u32(&sm.bar_slot[slot])), "r"(owner));
       asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                    :: "r"(dst), "r"(tc::smem_u32(ostage + tile * (128 * H))), "r"(AT_SHARE_BYTES), "r"(rbar) : "memory");
-      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                   :: "r"(dml), "r"(tc::smem_u32(sm.ml)), "r"(2 * H * 4), "r"(rbar) : "memory");
     }
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   }
   if (owned) {
-    at_wait(&sm.bar_red, 0, sm, p.hdr, 15);
     if (tid < H) {                             // weight of each CTA's share for head tid
+      at_wait(&sm.bar_ml, 0, sm, p.hdr, 15);
       float mc[AT_MAXC], lc[AT_MAXC];
       float M = -INFINITY;
 #pragma unroll
@@ -496,41 +545,47 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
     int j = 0;
     for (int tile = rank; tile < 4; tile += C, j++) {
-#pragma unroll 2
+      float acc[4][8];
+#pragma unroll
       for (int k = 0; k < 4; k++) {
         const int d = lane + 32 * k;
-        const int off = d * H + ((u ^ (d & 7)) << 3);
-        float acc[8];
-        {
-          const uint4 v = *reinterpret_cast<const uint4*>(ostage + tile * (128 * H) + off);
+        const uint4 v = *reinterpret_cast<const uint4*>(ostage + tile * (128 * H) + d * H + ((u ^ (d & 7)) << 3));
+        const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const float2 f = __half22float2(h2[e]);
+          acc[k][2 * e] = f.x * wself[2 * e];
+          acc[k][2 * e + 1] = f.y * wself[2 * e + 1];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < AT_MAXC - 1; r++) {  // the other CTAs' shares, each as soon as it is in
+        if (r >= C - 1) break;
+        const int slot = j * (C - 1) + r;
+        at_wait(&sm.bar_slot[slot], 0, sm, p.hdr, 15);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const int d = lane + 32 * k;
+          const uint4 v = *reinterpret_cast<const uint4*>(orecv + slot * (128 * H) + d * H + ((u ^ (d & 7)) << 3));
           const __half2* h2 = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const float2 f = __half22float2(h2[e]);
-            acc[2 * e] = f.x * wself[2 * e];
-            acc[2 * e + 1] = f.y * wself[2 * e + 1];
+            acc[k][2 * e] = fmaf(f.x, wr[r][2 * e], acc[k][2 * e]);
+            acc[k][2 * e + 1] = fmaf(f.y, wr[r][2 * e + 1], acc[k][2 * e + 1]);
           }
         }
+      }
 #pragma unroll
-        for (int r = 0; r < AT_MAXC - 1; r++) {
-          if (r >= C - 1) break;
-          const uint4 v = *reinterpret_cast<const uint4*>(orecv + (j * (C - 1) + r) * (128 * H) + off);
-          const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+      for (int k = 0; k < 4; k++) {
+        uint16_t* o = out + (u * 8) * D + tile * 128 + lane + 32 * k;
 #pragma unroll
-          for (int e = 0; e < 4; e++) {
-            const float2 f = __half22float2(h2[e]);
-            acc[2 * e] = fmaf(f.x, wr[r][2 * e], acc[2 * e]);
-            acc[2 * e + 1] = fmaf(f.y, wr[r][2 * e + 1], acc[2 * e + 1]);
-          }
-        }
-        uint16_t* o = out + (u * 8) * D + tile * 128 + d;
-#pragma unroll
-        for (int e = 0; e < 8; e++) o[e * D] = (uint16_t)(pack_bf16x2(acc[e], 0.f) & 0xFFFFu);
+        for (int e = 0; e < 8; e++) o[e * D] = (uint16_t)(pack_bf16x2(acc[k][e], 0.f) & 0xFFFFu);
       }
     }
   }
   // A sender's shares stay in place until its copies have read them; an owner
-  // has received every byte sent to it (bar_red) before it gets here, so no
+  // has received every byte sent to it (bar_ml, bar_slot) before it gets here, so no
   // cross-CTA access remains and no final cluster barrier is needed.
   if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   tc::fence_before_sync();
