@@ -62,7 +62,7 @@ struct RxSmem {
   float w[HI];
   uint32_t sfb[HI];
   uint32_t keys[RX_MAX_TILES * RX_TILE];        // slot keys; 0 = outside the search domain
-  uint32_t hist[256];                           // this CTA's digit histogram of the current pass
+  alignas(16) uint32_t hist[256];               // this CTA's digit histogram of the current pass
   alignas(16) uint32_t rows[2][RX_CL][256];     // every CTA's histogram, pushed by its owner (double buffered)
   int32_t gt_all[RX_CL];                       // every CTA's keys above the threshold (same in all CTAs)
   int32_t eq_all[RX_CL];                       // every CTA's keys equal to it
@@ -70,6 +70,7 @@ struct RxSmem {
   int32_t bcast[4];
   uint32_t suf[257];                            // cluster-wide suffix sums of the current histogram
   uint64_t mma_done[RX_ROUNDS];
+  uint64_t bar_rows[2];                         // rows[buf] holds every CTA's histogram of the pass
   uint32_t tmem_base;
 };
 constexpr size_t RX_SMEM = sizeof(RxSmem) + 1024;
@@ -110,7 +111,6 @@ __device__ __forceinline__ void tmem_ld_x32_nowait(uint32_t taddr, uint32_t* r) 
                : "r"(taddr) : "memory");
 }
 
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Top-K over the keys of every CTA of the cluster (key 0 = not a candidate) by
@@ -118,9 +118,11 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 // CTAs 0..r-1.  Exact radix select over four 8-bit digits.  In every pass each
 // CTA builds the histogram of the digit over its keys that match the prefix
 // chosen so far (warp-aggregated with match_any in the first pass, where most
-// keys share a digit) and stores it into row crank of every CTA's row array;
-// after one cluster barrier every CTA holds all histograms, turns each row
-// into suffix sums (keys with a digit >= b), and finds the same threshold
+// keys share a digit) and bulk-copies it into row crank of every CTA's row
+// array, where an mbarrier per row buffer counts the bytes of all RX_CL rows
+// (no cluster barrier, no releasing fence); then every CTA holds all
+// histograms, turns each row into suffix sums (keys with a digit >= b), and
+// finds the same threshold
 // digit and the same number of ties still to take.  The suffix sums also give,
 // for every CTA, its keys above the threshold digit, and after the last digit
 // its keys equal to the threshold, so the output offsets need no further
@@ -128,7 +130,7 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 // ranks after those of CTAs 0..r-1) and the function returns the cluster
 // total.  Each thread keeps its contiguous chunk of keys in registers.
 template <class Out>
-__device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxSmem& fs, Out out) {
+__device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxSmem& fs, WsHeader* hdr, Out out) {
   constexpr int KPT = (RX_MAX_TILES * RX_TILE + RX_THREADS - 1) / RX_THREADS;   // keys per thread
   static_assert(RX_THREADS == 256, "one histogram bin per thread");
   static_assert(RX_CL <= RX_WARPS, "one warp per CTA row");
@@ -144,7 +146,7 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
   }
   fs.hist[tid] = 0;
   __syncthreads();
-  cluster_wait();                                          // (arrived at set-up) every CTA runs: rows may be pushed
+  cluster_wait();        // (arrived at set-up) every CTA runs and its row barriers are initialised
 
   uint32_t prefix = 0, mask = 0;
   int remaining = K;
@@ -163,23 +165,28 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
         atomicAdd(&fs.hist[digit], 1u);
       }
     }
+    tc::fence_proxy_async_smem();                          // the histogram is read by bulk copies
     __syncthreads();
-    if (tid < 64) {                                        // push this CTA's histogram to every CTA
-      const uint4 v = *reinterpret_cast<const uint4*>(&fs.hist[4 * tid]);
-      const uint32_t local = tc::smem_u32(&fs.rows[buf][crank][4 * tid]);
+    if (tid == 0) {                                        // push this CTA's histogram to every CTA
+      tc::bar_arrive_expect_tx(&fs.bar_rows[buf], (uint32_t)(RX_CL * 256 * 4));
+      const uint32_t local = tc::smem_u32(&fs.rows[buf][crank][0]), lbar = tc::smem_u32(&fs.bar_rows[buf]);
 #pragma unroll
       for (int r = 0; r < RX_CL; r++) {
-        uint32_t a;
+        uint32_t a, rb;
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(r));
-        asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(lbar), "r"(r));
+        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     :: "r"(a), "r"(tc::smem_u32(fs.hist)), "r"(256 * 4), "r"(rb) : "memory");
       }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
-    // every CTA's histogram of this pass has landed everywhere; the other row
-    // buffer was read by all CTAs before they arrived here
-    cluster_arrive();
-    cluster_wait();
-    fs.hist[tid] = 0;                                      // for the next pass (pushed already)
+    // Every CTA's histogram of this pass has landed here.  A CTA pushes into
+    // rows[buf] again two passes later, after it has seen this CTA's push of
+    // the pass in between, which this CTA makes only after it has finished
+    // reading rows[buf]; so the two buffers never overlap in use.
+    if (!tc::bar_wait(&fs.bar_rows[buf], (uint32_t)((pass >> 1) & 1)) && tid == 0)
+      report(hdr, CSA2_ERR_TIMEOUT, 20 + pass);
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the pushes read the histogram
     if (warp < RX_CL) {                                    // row `warp` -> suffix sums, in place
       uint32_t* row = fs.rows[buf][warp];
       uint32_t c[8], sum = 0;
@@ -196,6 +203,7 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
       for (int q = 0; q < 8; q++) { run += c[q]; row[255 - 8 * lane - q] = run; }
     }
     __syncthreads();
+    fs.hist[tid] = 0;                                      // for the next pass (its pushes have read it)
     {
       uint32_t t = 0;
 #pragma unroll
@@ -289,7 +297,7 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
     if (!take && km == thr && used < mine_eq) { take = true; used++; }
     if (take) out(i0 + j, r++);
   }
-  return total;                    // the last push preceded the last cluster barrier
+  return total;                    // every push into this CTA has landed, and its own have been read
 }
 
 __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams p) {
@@ -303,6 +311,8 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   if (warp == 0) tc::tmem_alloc(&sm.tmem_base, RX_TMEM_COLS);
   if (tid == 0) {
     for (int r = 0; r < RX_ROUNDS; r++) tc::bar_init(&sm.mma_done[r], 1);
+    tc::bar_init(&sm.bar_rows[0], 1);
+    tc::bar_init(&sm.bar_rows[1], 1);
     tc::bar_init_fence();
   }
   // everything above reads no input: with programmatic dependent launch it
@@ -336,7 +346,9 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  cluster_arrive();                                             // waited for before the first histogram push
+  // waited for before the first histogram push; the init fence above releases
+  // the row barriers, so the arrival itself is relaxed
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // ---- 1. copies: warp w takes tiles w, w + 8, w + 16; one warp instruction per block
   for (int i = warp; i < n; i += RX_WARPS) {
@@ -445,7 +457,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
 
   // ---- 4. exact top-K over the whole pool, across the cluster
   int32_t* sel = p.sel + (int64_t)bq * p.K;
-  const int ns = cluster_select(sm.keys, n * RX_TILE, p.K, crank, sm, [&](int i, int r) {
+  const int ns = cluster_select(sm.keys, n * RX_TILE, p.K, crank, sm, p.hdr, [&](int i, int r) {
     sel[r] = sm.pool[i / BLK] * BLK + (i % BLK);
   });
   if (crank == RX_CL - 1)
