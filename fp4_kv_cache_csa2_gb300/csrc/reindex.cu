@@ -118,9 +118,9 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 // CTAs 0..r-1.  Exact radix select over four 8-bit digits.  In every pass each
 // CTA builds the histogram of the digit over its keys that match the prefix
 // chosen so far (warp-aggregated with match_any in the first pass, where most
-// keys share a digit) and bulk-copies it into row crank of every CTA's row
-// array, where an mbarrier per row buffer counts the bytes of all RX_CL rows
-// (no cluster barrier, no releasing fence); then every CTA holds all
+// keys share a digit) and stores it into row crank of every CTA's row array
+// by asynchronous remote stores, which an mbarrier per row buffer counts in
+// bytes (no cluster barrier, no releasing fence); then every CTA holds all
 // histograms, turns each row into suffix sums (keys with a digit >= b), and
 // finds the same threshold
 // digit and the same number of ties still to take.  The suffix sums also give,
@@ -165,20 +165,19 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
         atomicAdd(&fs.hist[digit], 1u);
       }
     }
-    tc::fence_proxy_async_smem();                          // the histogram is read by bulk copies
     __syncthreads();
-    if (tid == 0) {                                        // push this CTA's histogram to every CTA
-      tc::bar_arrive_expect_tx(&fs.bar_rows[buf], (uint32_t)(RX_CL * 256 * 4));
-      const uint32_t local = tc::smem_u32(&fs.rows[buf][crank][0]), lbar = tc::smem_u32(&fs.bar_rows[buf]);
+    if (tid == 0) tc::bar_arrive_expect_tx(&fs.bar_rows[buf], (uint32_t)(RX_CL * 256 * 4));
+    if (tid < 64) {                                        // push this CTA's histogram to every CTA
+      const uint4 v = *reinterpret_cast<const uint4*>(&fs.hist[4 * tid]);
+      const uint32_t local = tc::smem_u32(&fs.rows[buf][crank][4 * tid]), lbar = tc::smem_u32(&fs.bar_rows[buf]);
 #pragma unroll
       for (int r = 0; r < RX_CL; r++) {
         uint32_t a, rb;
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(r));
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(lbar), "r"(r));
-        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     :: "r"(a), "r"(tc::smem_u32(fs.hist)), "r"(256 * 4), "r"(rb) : "memory");
+        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                     :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rb) : "memory");
       }
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
     // Every CTA's histogram of this pass has landed here.  A CTA pushes into
     // rows[buf] again two passes later, after it has seen this CTA's push of
@@ -186,7 +185,6 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
     // reading rows[buf]; so the two buffers never overlap in use.
     if (!tc::bar_wait(&fs.bar_rows[buf], (uint32_t)((pass >> 1) & 1)) && tid == 0)
       report(hdr, CSA2_ERR_TIMEOUT, 20 + pass);
-    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the pushes read the histogram
     if (warp < RX_CL) {                                    // row `warp` -> suffix sums, in place
       uint32_t* row = fs.rows[buf][warp];
       uint32_t c[8], sum = 0;
@@ -203,7 +201,7 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
       for (int q = 0; q < 8; q++) { run += c[q]; row[255 - 8 * lane - q] = run; }
     }
     __syncthreads();
-    fs.hist[tid] = 0;                                      // for the next pass (its pushes have read it)
+    fs.hist[tid] = 0;                                      // for the next pass (pushed from registers)
     {
       uint32_t t = 0;
 #pragma unroll
@@ -297,7 +295,7 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
     if (!take && km == thr && used < mine_eq) { take = true; used++; }
     if (take) out(i0 + j, r++);
   }
-  return total;                    // every push into this CTA has landed, and its own have been read
+  return total;                    // every push into this CTA has landed
 }
 
 __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams p) {
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   // ---- set-up: TMEM, barriers, head weights, this CTA's pool blocks
   if (warp == 0) tc::tmem_alloc(&sm.tmem_base, RX_TMEM_COLS);
   if (tid == 0) {
-    for (int r = 0; r < RX_ROUNDS; r++) tc::bar_init(&sm.mma_done[r], 1);
+    for (int r = 0; r < RX_ROUNDS; r++) tc::bar_init(&sm.mma_done[r], 2);   // one commit per issuing thread
     tc::bar_init(&sm.bar_rows[0], 1);
     tc::bar_init(&sm.bar_rows[1], 1);
     tc::bar_init_fence();
@@ -364,12 +362,18 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
                    :: "r"(tc::smem_u32(codes + trow * 64 + ((c ^ ((trow >> 1) & 3)) * 16))),
                       "l"(p.idx_codes + (row_base + (int64_t)blk * BLK) * IDX_CODE_BYTES + lane * 16) : "memory");
     }
-    const int sb = lane >> 1, half = lane & 1;                  // scale words: 32 bytes per block
-    const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, sb);
-    if (blk >= 0)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                   :: "r"(tc::smem_u32(codes + RX_CODES + sb * 32 + half * 16)),
-                      "l"(p.idx_scales + (row_base + (int64_t)blk * BLK) * IDX_SCALE_BYTES + half * 16) : "memory");
+    // scale words, 4 blocks per instruction: the word of slot s lands in row
+    // s % 32, word s / 32 of the tile's 512-byte scale area, the order in which
+    // a 32x128b.warpx4 copy hands row m's word to TMEM lane m, column base + m / 32
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const int sb = 4 * q + (lane >> 3), r = lane & 7, slot = sb * BLK + r;
+      const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, sb);
+      if (blk >= 0)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                     :: "r"(tc::smem_u32(codes + RX_CODES + (slot & 31) * 16 + (slot >> 5) * 4)),
+                        "l"(p.idx_scales + (row_base + (int64_t)blk * BLK + r) * IDX_SCALE_BYTES) : "memory");
+    }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   if (warp == RX_WARPS - 1) quantize_index_query_warp(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
@@ -377,14 +381,10 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   tc::fence_proxy_async_smem();                                 // copies and query codes feed the tensor cores
   __syncthreads();
 
-  // ---- 2. scale words to TMEM: tile row m -> lane m, column base + m / 32;
-  // the query's words to lane 32 q + head of every quarter q
+  // ---- 2. the query's scale words to TMEM lane 32 q + head of every quarter q
+  // (the tiles' words follow by tcgen05.cp, each just before its MMAs)
   if (warp < 4) {
-    const int m = warp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    for (int i = 0; i < n; i++)
-      tc::tmem_st_x1(tmem + lane_off + RX_SFA_COL + i * 4 + warp,
-                     *reinterpret_cast<const uint32_t*>(sm.tile[i] + RX_CODES + m * 4));
     tc::tmem_st_x1(tmem + lane_off + RX_SFB_COL, sm.sfb[lane]);
     tc::tmem_wait_st();
   }
@@ -399,14 +399,15 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   bool ok_all = true;
   for (int r0 = 0, round = 0; r0 < n; r0 += RX_ROUND, round++) {
     const int rn = min(RX_ROUND, n - r0);
-    if (tid == 0) {
+    if (lane == 0 && warp < 2) {             // two issuing threads: even and odd tiles of the round
       const uint64_t bdesc = tc::smem_desc(tc::smem_u32(sm.qcodes), 16, 512, tc::SW_64B);
       constexpr uint32_t id0 = tc::idesc_mxf4(RX_TILE, HI, 0, 0);
       constexpr uint32_t id1 = tc::idesc_mxf4(RX_TILE, HI, 2, 2);
-      for (int j = 0; j < rn; j++) {
+      for (int j = warp; j < rn; j += 2) {
         const int i = r0 + j;
         const uint64_t adesc = tc::smem_desc(tc::smem_u32(sm.tile[i]), 16, 512, tc::SW_64B);
         const uint32_t d = tmem + RX_ACC_COL + j * HI, sfa = tmem + RX_SFA_COL + i * 4;
+        tc::tmem_cp_32x128b_warpx4(sfa, tc::smem_desc(tc::smem_u32(sm.tile[i] + RX_CODES), 128, 128, tc::SW_NONE));
         tc::mma_mxf4(d, adesc, bdesc, id0, sfa, tmem + RX_SFB_COL, 0);
         tc::mma_mxf4(d, adesc + 2, bdesc + 2, id1, sfa, tmem + RX_SFB_COL, 1);   // next 32 bytes of K
       }
