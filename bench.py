@@ -279,8 +279,8 @@ class Decode1M:
             join.record(st)
             main.wait_event(join)
 
-    def cycle(self, s_base: int):
-        """Steps s_base .. s_base + R - 1 with only the dependencies the data
+    def cycle(self, s_base: int, n_steps: int = 0):
+        """Steps s_base .. s_base + n_steps - 1 (default R) with only the dependencies the data
         imposes, so that consecutive steps overlap: every layer slot keeps its
         own stream (and workspace) across the steps, a Reuse-k call waits for
         the Reindex call that produced its instance's selection (step s - 3k
@@ -294,7 +294,7 @@ class Decode1M:
         for st in streams:
             st.wait_event(fork)
         done = {}
-        for i in range(self.R):
+        for i in range(n_steps or self.R):
             s = s_base + i
             for layer in range(4):
                 st = streams[layer]
@@ -341,22 +341,31 @@ def _capture(torch, fn):
 
 class PhaseGraphs:
     """CUDA graphs of a pipelined step: one per pipeline phase (step s depends
-    only on s mod R) and one of a whole cycle of R consecutive phases, so that
-    long runs launch one graph per R steps."""
+    only on s mod R), one of a whole cycle of R consecutive phases and one of
+    `cycles` whole cycles, so that long runs launch one graph per cycles * R
+    steps (consecutive graph launches serialise, so a longer graph leaves fewer
+    drain-and-fill gaps between steps)."""
 
-    def __init__(self, torch, step_fn, R: int, s_base: int, cycle_fn=None):
+    def __init__(self, torch, step_fn, R: int, s_base: int, cycle_fn=None, cycles: int = 1):
         self.R = R
+        self.cycles = max(1, cycles)
         self.single = [_capture(torch, lambda i=i: step_fn(s_base + i)) for i in range(R)]
         if cycle_fn is None:
             self.cycle = _capture(torch, lambda: [step_fn(s_base + i) for i in range(R)])
+            self.multi = None
         else:
-            self.cycle = _capture(torch, lambda: cycle_fn(s_base))
+            self.cycle = _capture(torch, lambda: cycle_fn(s_base, R))
+            self.multi = _capture(torch, lambda: cycle_fn(s_base, R * self.cycles)) if self.cycles > 1 else None
 
     def run(self, first: int, n: int):
         """Replays steps first .. first + n - 1 (exactly n steps)."""
         i = 0
+        long = self.R * self.cycles
         while i < n:
-            if (first + i) % self.R == 0 and n - i >= self.R:
+            if self.multi is not None and (first + i) % self.R == 0 and n - i >= long:
+                self.multi.replay()
+                i += long
+            elif (first + i) % self.R == 0 and n - i >= self.R:
                 self.cycle.replay()
                 i += self.R
             else:
@@ -383,7 +392,7 @@ def run_decode1m(args, torch, csa2):
     torch.cuda.synchronize()
     # graphs per pipeline phase and per cycle of R phases: step s only depends on s mod R
     s_base = 3 * w.d
-    graphs = PhaseGraphs(torch, w.step, w.R, s_base, cycle_fn=w.cycle)
+    graphs = PhaseGraphs(torch, w.step, w.R, s_base, cycle_fn=w.cycle, cycles=args.graph_cycles)
     graphs.run(0, args.warmup)
     torch.cuda.synchronize()
     n_steps = args.steps
@@ -437,9 +446,11 @@ def run_decode1m(args, torch, csa2):
                    "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                    "l2": f"inputs larger than L2: {w.R} pipelined instances x "
                          f"{w.B * w.N * (MAIN_ENTRY + IDX_ENTRY) / 1e9:.2f} GB, layer distance {w.d} steps",
-                   "launch": "CUDA graphs of 10 consecutive steps (one per phase for a remainder); in a "
-                             "step the 4 layer calls (4 different pipelined instances, so independent) are "
-                             "parallel branches on 4 streams, the Reindex branch first at high priority",
+                   "launch": f"CUDA graphs of {w.R * max(1, args.graph_cycles)} consecutive steps "
+                             f"(whole cycles of {w.R}; one graph per step for a remainder) with only the data's "
+                             "dependencies between steps; in a step the 4 layer calls (4 different pipelined "
+                             "instances, so independent) are parallel branches on 4 streams, the Reindex branch "
+                             "first at high priority",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -534,8 +545,8 @@ def run_decode1m_e2e(args, torch, csa2, w):
             join.record(st)
             main.wait_event(join)
 
-    def cycle(s_base):
-        """R steps with only the data's dependencies (see Decode1M.cycle), plus
+    def cycle(s_base, n_steps=0):
+        """Steps s_base .. s_base + n_steps - 1 (default R) with only the data's dependencies (see Decode1M.cycle), plus
         the staging buffers': the layer calls of step s wait for the copy that
         brought their inputs (issued during step s - 1) and for the copy-out of
         step s - 2 (which read the output block they overwrite); the input copy
@@ -548,7 +559,7 @@ def run_decode1m_e2e(args, torch, csa2, w):
         for st in (*streams, h2d, d2h):
             st.wait_event(fork)
         done, h2d_done, d2h_done = {}, {}, {}
-        for i in range(w.R):
+        for i in range(n_steps or w.R):
             s = s_base + i
             k = s % 2
             q_view, row_view, qidx_view, w_view, out_view = bufs[k]
@@ -594,7 +605,7 @@ def run_decode1m_e2e(args, torch, csa2, w):
             main.wait_event(join)
 
     s0 = 3 * w.d
-    graphs = PhaseGraphs(torch, step, w.R, s0, cycle_fn=cycle)
+    graphs = PhaseGraphs(torch, step, w.R, s0, cycle_fn=cycle, cycles=args.graph_cycles)
     graphs.run(0, args.warmup)
     torch.cuda.synchronize()
     # fresh host data and a cleared output block: the checks below prove that the
@@ -613,7 +624,8 @@ def run_decode1m_e2e(args, torch, csa2, w):
     assert torch.equal(host_out, dev_out[1 - k_last].cpu()) and bool(host_out.any()), \
         "output copy missing from the step graph"
     return {"value": B * 4 / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": in_bytes,
-            "d2h_bytes_per_step": out_bytes, "launch": "CUDA graphs of 10 consecutive steps with only the data's "
+            "d2h_bytes_per_step": out_bytes,
+            "launch": f"CUDA graphs of {w.R * max(1, args.graph_cycles)} consecutive steps with only the data's "
             "dependencies between them; per step the next step's "
             "input copy and the previous step's output copy on two copy streams, overlapped with 4 window-row "
             "placements and 4 layer calls in parallel branches"}
@@ -950,6 +962,8 @@ def main():
     ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
+    ap.add_argument("--graph-cycles", type=int, default=1,
+                    help="decode: pipeline cycles (of 3 d + 1 steps) per replayed CUDA graph")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
