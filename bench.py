@@ -162,7 +162,7 @@ def max_over_ranks(x: float, world: int) -> float:
 class Decode1M:
     """Reindex + 3 Reuse at 1,048,576 entries, batch 16, R pipelined instances."""
 
-    def __init__(self, csa2, torch, B=16, N=1 << 20, d=3, seed=3):
+    def __init__(self, csa2, torch, B=16, N=1 << 20, d=3, seed=3, lanes=2):
         import synth
         self.csa2, self.torch = csa2, torch
         self.B, self.N, self.d = B, N, d
@@ -227,28 +227,40 @@ class Decode1M:
             }
             self.inst.append(inst)
         # one workspace per layer slot: the four layer calls of a step may run at once
-        self.ws = [csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REINDEX if l == 0 else csa2.MODE_REUSE,
-                                                             B, 1, N, M, K), device=dev) for l in range(4)]
+        # lanes per layer slot (stream + workspace), taken by step number modulo the
+        # lane count, so that the same layer's calls of consecutive steps (different
+        # instances) can overlap
+        self.lanes = lanes
+        self.ws = [[csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REINDEX if l == 0 else csa2.MODE_REUSE,
+                                                              B, 1, N, M, K), device=dev) for _ in range(self.lanes)]
+                   for l in range(4)]
         # the Reindex branch (fused score/select + attention) is the step's critical
         # path: it runs on a high-priority stream and is enqueued first
-        self.hi = torch.cuda.Stream(priority=-1)
-        self.side = [torch.cuda.Stream() for _ in range(3)]
+        self.hi = [torch.cuda.Stream(priority=-1) for _ in range(self.lanes)]
+        self.side = [[torch.cuda.Stream() for _ in range(self.lanes)] for _ in range(3)]
         for r in range(self.R):          # every instance starts with a published selection
             self.layer(0, r)
         torch.cuda.synchronize()
         self.check_status()
         self.setup_s = time.time() - t0
 
-    def layer(self, layer: int, r: int):
+    def stream_of(self, layer: int, s: int):
+        return (self.hi if layer == 0 else self.side[layer - 1])[s % self.lanes]
+
+    def all_streams(self):
+        return [*self.hi, *(st for lane in self.side for st in lane)]
+
+    def layer(self, layer: int, r: int, lane: int = 0):
         csa2, inst, torch = self.csa2, self.inst[r], self.torch
         mode = csa2.MODE_REINDEX if layer == 0 else csa2.MODE_REUSE
         csa2.decode(mode, self.caches[r], q_pos=self.q_pos, q=inst["q"][layer].view(torch.int16),
                     swa=inst["swa"][layer].view(torch.int16), swa_base_pos=self.swa_base, scale=1 / math.sqrt(D),
-                    sel=inst["sel"], out=inst["out"][layer].view(torch.int16), ws=self.ws[layer], M=M_BLK, max_n=self.N,
+                    sel=inst["sel"], out=inst["out"][layer].view(torch.int16), ws=self.ws[layer][lane], M=M_BLK,
+                    max_n=self.N,
                     q_idx=inst["q_idx"].view(torch.int16), w_head=inst["w_head"], pool_blocks=self.pool)
 
     def check_status(self):
-        for ws in self.ws:
+        for ws in (w for lane in self.ws for w in lane):
             st, detail = ws.sync_status()
             assert st == 0, f"device status {st} ({detail})"
 
@@ -266,17 +278,15 @@ class Decode1M:
         main = torch.cuda.current_stream()
         fork = torch.cuda.Event()
         fork.record(main)
-        self.hi.wait_event(fork)
-        with torch.cuda.stream(self.hi):
-            self.layer(0, s % self.R)
-        for layer in range(1, 4):
-            st = self.side[layer - 1]
+        lane = s % self.lanes
+        for layer in range(4):
+            st = self.stream_of(layer, s)
             st.wait_event(fork)
             with torch.cuda.stream(st):
-                self.layer(layer, (s - layer * self.d) % self.R)
-        for st in (self.hi, *self.side):
+                self.layer(layer, (s - layer * self.d) % self.R, lane)
+        for layer in range(4):
             join = torch.cuda.Event()
-            join.record(st)
+            join.record(self.stream_of(layer, s))
             main.wait_event(join)
 
     def cycle(self, s_base: int, n_steps: int = 0):
@@ -288,7 +298,7 @@ class Decode1M:
         its instance's previous selection (steps s - R + 3k)."""
         torch = self.torch
         main = torch.cuda.current_stream()
-        streams = [self.hi] + self.side
+        streams = self.all_streams()
         fork = torch.cuda.Event()
         fork.record(main)
         for st in streams:
@@ -297,7 +307,7 @@ class Decode1M:
         for i in range(n_steps or self.R):
             s = s_base + i
             for layer in range(4):
-                st = streams[layer]
+                st = self.stream_of(layer, s)
                 if layer > 0:
                     dep = [(0, s - layer * self.d)]
                 else:
@@ -306,7 +316,7 @@ class Decode1M:
                     if key in done:
                         st.wait_event(done[key])
                 with torch.cuda.stream(st):
-                    self.layer(layer, (s - layer * self.d) % self.R)
+                    self.layer(layer, (s - layer * self.d) % self.R, s % self.lanes)
                 ev = torch.cuda.Event()
                 ev.record(st)
                 done[(layer, s)] = ev
@@ -387,7 +397,7 @@ def _graph_ms(torch, graph, reps):
 
 def run_decode1m(args, torch, csa2):
     rank, world, local = dist_info()
-    w = Decode1M(csa2, torch, N=args.seq_len, d=args.pipeline_distance)
+    w = Decode1M(csa2, torch, N=args.seq_len, d=args.pipeline_distance, lanes=args.lanes)
     w.prologue()
     torch.cuda.synchronize()
     # graphs per pipeline phase and per cycle of R phases: step s only depends on s mod R
@@ -449,8 +459,9 @@ def run_decode1m(args, torch, csa2):
                    "launch": f"CUDA graphs of {w.R * max(1, args.graph_cycles)} consecutive steps "
                              f"(whole cycles of {w.R}; one graph per step for a remainder) with only the data's "
                              "dependencies between steps; in a step the 4 layer calls (4 different pipelined "
-                             "instances, so independent) are parallel branches on 4 streams, the Reindex branch "
-                             "first at high priority",
+                             "instances, so independent) are parallel branches, the Reindex branch first at high "
+                             f"priority; every layer slot has {w.lanes} stream + workspace lanes taken by step "
+                             f"number mod {w.lanes}",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -477,13 +488,14 @@ def run_decode1m_e2e(args, torch, csa2, w):
     the Reindex layer's index queries and head weights) travel in one pinned
     host block and one copy; the four layers' outputs come back in one copy into
     one pinned block.  Serving-style overlap: while step s computes from staging
-    buffer s % 2, a copy stream brings step s+1's inputs into the other buffer
+    buffer s % NB, a copy stream brings step s+1's inputs into the next buffer
     and a second copy stream returns step s-1's outputs, so every timed step
-    carries one full input copy and one full output copy.  One CUDA graph per
-    pipeline phase (R is even, so the buffer parity is the same on every
-    replay)."""
+    carries one full input copy and one full output copy.  NB (the lane count,
+    else 2) divides R, so a graph of whole phases uses the same buffers on every
+    replay."""
     B = w.B
-    assert w.R % 2 == 0
+    NB = w.lanes if w.lanes >= 2 and w.R % w.lanes == 0 else 2
+    assert w.R % NB == 0
     q_bytes = B * H * D * 2
     row_bytes = B * D * 2
     qidx_bytes = B * HI * DI * 2
@@ -497,8 +509,8 @@ def run_decode1m_e2e(args, torch, csa2, w):
     host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
     host_in.view(torch.int16).random_(-16000, 16000)       # bf16 bit patterns of moderate magnitude
     host_in[off_w:].view(torch.float32).normal_()
-    dev_in = [torch.empty(in_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    dev_out = [torch.zeros(out_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    dev_in = [torch.empty(in_bytes, dtype=torch.uint8, device="cuda") for _ in range(NB)]
+    dev_out = [torch.zeros(out_bytes, dtype=torch.uint8, device="cuda") for _ in range(NB)]
     for t in dev_in:
         t.copy_(host_in)
 
@@ -510,21 +522,21 @@ def run_decode1m_e2e(args, torch, csa2, w):
                 d[off_qidx: off_qidx + qidx_bytes].view(torch.int16).view(B, 1, HI, DI),
                 d[off_w: off_w + wh_bytes].view(torch.float32).view(B, 1, HI),
                 [dev_out[k][l * q_bytes:(l + 1) * q_bytes].view(torch.int16).view(B, 1, H, D) for l in range(4)])
-    bufs = [views(0), views(1)]
+    bufs = [views(k) for k in range(NB)]
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
     def step(s):
         main = torch.cuda.current_stream()          # the capturing stream when captured
-        k = s % 2
+        k = s % NB
         q_view, row_view, qidx_view, w_view, out_view = bufs[k]
         fork = torch.cuda.Event()
         fork.record(main)
         h2d.wait_event(fork)
         d2h.wait_event(fork)
         with torch.cuda.stream(h2d):
-            dev_in[1 - k].copy_(host_in, non_blocking=True)          # inputs of step s + 1
+            dev_in[(s + 1) % NB].copy_(host_in, non_blocking=True)   # inputs of step s + 1
         with torch.cuda.stream(d2h):
-            host_out.copy_(dev_out[1 - k], non_blocking=True)        # outputs of step s - 1
+            host_out.copy_(dev_out[(s - 1) % NB], non_blocking=True) # outputs of step s - 1
         def layer_call(layer):
             r = (s - layer * w.d) % w.R
             inst = w.inst[r]
@@ -532,15 +544,14 @@ def run_decode1m_e2e(args, torch, csa2, w):
             mode = csa2.MODE_REINDEX if layer == 0 else csa2.MODE_REUSE
             csa2.decode(mode, w.caches[r], q_pos=w.q_pos, q=q_view[layer], swa=inst["swa"][layer].view(torch.int16),
                         swa_base_pos=w.swa_base, scale=1 / math.sqrt(D), sel=inst["sel"], out=out_view[layer],
-                        ws=w.ws[layer], M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view, pool_blocks=w.pool)
-        w.hi.wait_event(fork)                      # independent instances: parallel branches,
-        with torch.cuda.stream(w.hi):              # the Reindex branch first and at high priority
-            layer_call(0)
-        for layer in range(1, 4):
-            w.side[layer - 1].wait_event(fork)
-            with torch.cuda.stream(w.side[layer - 1]):
+                        ws=w.ws[layer][s % w.lanes], M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view,
+                        pool_blocks=w.pool)
+        for layer in range(4):                     # independent instances: parallel branches,
+            st = w.stream_of(layer, s)             # the Reindex branch first and at high priority
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
                 layer_call(layer)
-        for st in (h2d, d2h, w.hi, *w.side):
+        for st in (h2d, d2h, *(w.stream_of(layer, s) for layer in range(4))):
             join = torch.cuda.Event()
             join.record(st)
             main.wait_event(join)
@@ -549,11 +560,11 @@ def run_decode1m_e2e(args, torch, csa2, w):
         """Steps s_base .. s_base + n_steps - 1 (default R) with only the data's dependencies (see Decode1M.cycle), plus
         the staging buffers': the layer calls of step s wait for the copy that
         brought their inputs (issued during step s - 1) and for the copy-out of
-        step s - 2 (which read the output block they overwrite); the input copy
-        issued during step s waits for step s - 1's calls (which read that
+        step s - NB (which read the output block they overwrite); the input copy
+        issued during step s waits for step s + 1 - NB's calls (which read that
         buffer) and the output copy for step s - 1's calls."""
         main = torch.cuda.current_stream()
-        streams = [w.hi] + w.side
+        streams = w.all_streams()
         fork = torch.cuda.Event()
         fork.record(main)
         for st in (*streams, h2d, d2h):
@@ -561,32 +572,33 @@ def run_decode1m_e2e(args, torch, csa2, w):
         done, h2d_done, d2h_done = {}, {}, {}
         for i in range(n_steps or w.R):
             s = s_base + i
-            k = s % 2
+            k = s % NB
             q_view, row_view, qidx_view, w_view, out_view = bufs[k]
-            prev = [done[(l, s - 1)] for l in range(4) if (l, s - 1) in done]
-            for ev in prev:
-                h2d.wait_event(ev)
-                d2h.wait_event(ev)
+            for l in range(4):
+                if (l, s + 1 - NB) in done:
+                    h2d.wait_event(done[(l, s + 1 - NB)])
+                if (l, s - 1) in done:
+                    d2h.wait_event(done[(l, s - 1)])
             with torch.cuda.stream(h2d):
-                dev_in[1 - k].copy_(host_in, non_blocking=True)          # inputs of step s + 1
+                dev_in[(s + 1) % NB].copy_(host_in, non_blocking=True)   # inputs of step s + 1
             e = torch.cuda.Event()
             e.record(h2d)
             h2d_done[s + 1] = e
             with torch.cuda.stream(d2h):
-                host_out.copy_(dev_out[1 - k], non_blocking=True)        # outputs of step s - 1
+                host_out.copy_(dev_out[(s - 1) % NB], non_blocking=True) # outputs of step s - 1
             e = torch.cuda.Event()
             e.record(d2h)
             d2h_done[s - 1] = e
             for layer in range(4):
-                st = streams[layer]
+                st = w.stream_of(layer, s)
                 dep = [(0, s - layer * w.d)] if layer > 0 else [(kk, s - w.R + kk * w.d) for kk in range(1, 4)]
                 for key in dep:
                     if key in done:
                         st.wait_event(done[key])
                 if s in h2d_done:
                     st.wait_event(h2d_done[s])
-                if s - 2 in d2h_done:
-                    st.wait_event(d2h_done[s - 2])
+                if s - NB in d2h_done:
+                    st.wait_event(d2h_done[s - NB])
                 r = (s - layer * w.d) % w.R
                 inst = w.inst[r]
                 with torch.cuda.stream(st):
@@ -594,7 +606,8 @@ def run_decode1m_e2e(args, torch, csa2, w):
                     mode = csa2.MODE_REINDEX if layer == 0 else csa2.MODE_REUSE
                     csa2.decode(mode, w.caches[r], q_pos=w.q_pos, q=q_view[layer],
                                 swa=inst["swa"][layer].view(torch.int16), swa_base_pos=w.swa_base,
-                                scale=1 / math.sqrt(D), sel=inst["sel"], out=out_view[layer], ws=w.ws[layer],
+                                scale=1 / math.sqrt(D), sel=inst["sel"], out=out_view[layer],
+                                ws=w.ws[layer][s % w.lanes],
                                 M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view, pool_blocks=w.pool)
                 ev = torch.cuda.Event()
                 ev.record(st)
@@ -619,14 +632,14 @@ def run_decode1m_e2e(args, torch, csa2, w):
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / args.steps
     w.check_status()
-    k_last = (s0 + (args.warmup + args.steps - 1) % w.R) % 2
-    assert torch.equal(dev_in[1 - k_last].cpu(), host_in), "input copy missing from the step graph"
-    assert torch.equal(host_out, dev_out[1 - k_last].cpu()) and bool(host_out.any()), \
+    s_last = s0 + (args.warmup + args.steps - 1) % w.R
+    assert torch.equal(dev_in[(s_last + 1) % NB].cpu(), host_in), "input copy missing from the step graph"
+    assert torch.equal(host_out, dev_out[(s_last - 1) % NB].cpu()) and bool(host_out.any()), \
         "output copy missing from the step graph"
     return {"value": B * 4 / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": in_bytes,
             "d2h_bytes_per_step": out_bytes,
             "launch": f"CUDA graphs of {w.R * max(1, args.graph_cycles)} consecutive steps with only the data's "
-            "dependencies between them; per step the next step's "
+            f"dependencies between them; {NB} staging buffers; per step the next step's "
             "input copy and the previous step's output copy on two copy streams, overlapped with 4 window-row "
             "placements and 4 layer calls in parallel branches"}
 
@@ -962,6 +975,8 @@ def main():
     ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
+    ap.add_argument("--lanes", type=int, default=5,
+                    help="decode: stream + workspace lanes per layer slot")
     ap.add_argument("--graph-cycles", type=int, default=1,
                     help="decode: pipeline cycles (of 3 d + 1 steps) per replayed CUDA graph")
     args = ap.parse_args()
