@@ -99,18 +99,6 @@ __device__ int cta_exclusive_scan(int v, RxSmem& fs, int* total) {
   return base + x - v;
 }
 
-// 32 consecutive 32-bit TMEM columns of this thread's lane, without waiting.
-__device__ __forceinline__ void tmem_ld_x32_nowait(uint32_t taddr, uint32_t* r) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-                 "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-                 "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-                 "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-               : "r"(taddr) : "memory");
-}
-
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Top-K over the keys of every CTA of the cluster (key 0 = not a candidate) by
@@ -429,7 +417,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
 #pragma unroll
         for (int jj = 0; jj < 4; jj++) {
           const int j = jb + 2 * jj;
-          if (j < rn) tmem_ld_x32_nowait(tmem + lane_off + RX_ACC_COL + j * HI, acc[jj]);
+          if (j < rn) tc::tmem_ld_x32_nowait(tmem + lane_off + RX_ACC_COL + j * HI, acc[jj]);
         }
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
