@@ -103,6 +103,7 @@ __device__ __forceinline__ bool poll_at_least(const uint32_t* word, uint32_t tar
     asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(tc::smem_u32(word)) : "memory");
     if ((int32_t)(v - target) >= 0) return true;
     if (sm.abort_flag) return false;
+    __nanosleep(32);          // leave the issue slots to the epilogue warps of this SM sub-partition
   }
   sm.abort_flag = 1;
   report(hdr, CSA2_ERR_TIMEOUT, 1);
