@@ -20,16 +20,16 @@
 //     loaded over the staging buffer; every warp then dequantises its 16 keys
 //     exactly (E2M1 -> bf16 by byte permutes, times the E4M3 scale; the
 //     product has at most 6 significant bits);
-//   * S^T = K Q^T is one M=128 (keys) x N=64 (heads) x K=512 tcgen05 bf16 MMA
-//     chain into TMEM, issued back to back once keys and Q are in place (an
-//     mbarrier wait between MMAs of the issuing thread costs more than the
-//     overlap with the dequantisation would gain);
+//   * S^T = K Q^T is an M=128 (keys) x N=64 (heads) x K=512 tcgen05 bf16 MMA
+//     product, issued as two chains of 16 back-to-back MMAs (dims 0..255 and
+//     256..511) into two TMEM accumulators by two threads at once (a chain is
+//     bound by its thread's issue rate); the softmax adds the two halves;
 //   * softmax over this CTA's keys with its own row maxima m_c, straight from
 //     TMEM (thread = key, 32 heads in registers; per-warp column maxima and
 //     sums by transpose-reductions over the lanes): P = exp(S - m_c) becomes
 //     the MN-major bf16 B operand [key][head] of the second product, L_c = sum P;
 //   * O^T = V^T P^T reuses the key buffer as an MN-major A operand: 4 tiles of
-//     M=128 dims x N=64 heads x K=128 keys;
+//     M=128 dims x N=64 heads x K=128 keys, one issuing thread per tile;
 //   * every CTA bulk-copies its (m_c, L_c) rows to every owner as soon as its
 //     second product is done, then stages its normalised share O_c / L_c of
 //     each 128-dim tile in fp16 (a convex combination of key vectors, relative
@@ -67,7 +67,8 @@ constexpr int AT_OFF_P = AT_OFF_Q;                       // after S: P^T [128 ke
 constexpr int AT_OFF_SMALL = AT_OFF_STAGE + AT_STAGE_BYTES;
 constexpr int AT_SHARE_BYTES = 128 * H * 2;             // one O^T tile share in fp16: 16 KB
 constexpr int AT_OFF_RECV = AT_OFF_Q;                    // after O: 4 receive slots over the Q region
-constexpr int AT_TMEM_COLS = 512;                        // S^T: 64 cols, O^T: 4 x 64 cols
+constexpr int AT_TMEM_COLS = 512;                        // S^T halves at 0 and 320, O^T: 4 x 64 cols from 64
+constexpr int AT_S2_COL = 320;                            // S^T over dims 256..511
 
 struct AtSmall {
   int kvalid[AT_KEYS];
@@ -162,8 +163,9 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   if (warp == 1) tc::tmem_alloc(&sm.tmem_base, AT_TMEM_COLS);
   if (tid == 0) {
     tc::bar_init(&sm.bar_kv, 1);
-    tc::bar_init(&sm.bar_s, 1);
-    tc::bar_init(&sm.bar_o, 1);
+    tc::bar_init(&sm.bar_s, 2);                          // two S^T chains
+
+    tc::bar_init(&sm.bar_o, 4);                          // four O^T tiles
     tc::bar_init(&sm.bar_ml, 1);
     for (int i = 0; i < 4; i++) tc::bar_init(&sm.bar_slot[i], 1);
     tc::bar_init(&sm.bar_q, 2);
@@ -232,10 +234,10 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   }
 
   // ---------------- keys: FP4 entries by 16-byte asynchronous copies into the
-  // staging buffer; lanes 2k and 2k+1 of warp w then take the halves of entry
-  // 16w + k (128 code bytes = dims 256h .. 256h+255, and their 16 scale bytes)
-  // into registers, the staging buffer receives Q chunks 4..7, and every warp
-  // dequantises its 16 keys and arrives on bar_keys (8 arrivals complete it)
+  // staging buffer; lanes 2k and 2k+1 of warp w then take entry 16w + k into
+  // registers (lane h: dims 128h .. 128h+127 and 256+128h .. 256+128h+127, with
+  // their scale bytes), the staging buffer receives Q chunks 4..7, and every
+  // warp dequantises its 16 keys and arrives on bar_keys (8 arrivals complete it)
   if (!window_cta) {
     for (int i = tid; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS) {
       const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
@@ -247,19 +249,25 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    // Bank order: a quarter-warp (8 lanes) covers 4 entries x 2 halves.  The
-    // odd lane of a pair walks its pieces and 16-channel groups in a permuted
-    // order (pieces k ^ 1, groups g ^ 2), so that within every 128-bit access
-    // the 8 lanes touch 8 different 16-byte bank groups, loads and stores alike.
+    // Bank order: a quarter-warp (8 lanes) covers 4 entries x 2 lanes.  The
+    // odd lane of a pair walks the two 16-byte pieces of each 64-dim chunk
+    // swapped (and so its 16-channel groups as g ^ 2), so that within every
+    // 128-bit access the 8 lanes touch 8 different 16-byte bank groups, loads
+    // and stores alike.
     const int s = warp * 16 + (lane >> 1), hf = lane & 1;
-    uint4 code[8], scl = make_uint4(0u, 0u, 0u, 0u);     // masked keys: +0 codes, scale 0 -> zero rows
+    uint4 code[8];                                         // masked keys: +0 codes, scale 0 -> zero rows
+    uint2 sca = make_uint2(0u, 0u), scb = make_uint2(0u, 0u);
 #pragma unroll
     for (int k = 0; k < 8; k++) code[k] = make_uint4(0u, 0u, 0u, 0u);
     if (sm.kvalid[s] == 1) {
       const uint4* ent = reinterpret_cast<const uint4*>(stage + s * MAIN_BYTES);
 #pragma unroll
-      for (int k = 0; k < 8; k++) code[k] = ent[hf * 8 + (k ^ hf)];   // odd lane: the chunk's two pieces swapped
-      scl = ent[16 + hf];
+      for (int k = 0; k < 4; k++) {
+        code[k] = ent[4 * hf + (k ^ hf)];                  // chunks 2hf, 2hf + 1
+        code[4 + k] = ent[8 + 4 * hf + (k ^ hf)];          // chunks 4 + 2hf, 5 + 2hf
+      }
+      sca = *reinterpret_cast<const uint2*>(stage + s * MAIN_BYTES + 256 + 8 * hf);   // their scale bytes
+      scb = *reinterpret_cast<const uint2*>(stage + s * MAIN_BYTES + 272 + 8 * hf);
     }
     tc::fence_proxy_async_smem();
     __syncthreads();                                       // the staging buffer is free
@@ -269,29 +277,31 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     }
     // odd lane: scale bytes rotated by two, matching its group order g ^ 2
     const uint32_t rot = hf ? 16u : 0u;
-    const uint32_t scw[4] = {__funnelshift_r(scl.x, scl.x, rot), __funnelshift_r(scl.y, scl.y, rot),
-                             __funnelshift_r(scl.z, scl.z, rot), __funnelshift_r(scl.w, scl.w, rot)};
+    const uint32_t scw[4] = {__funnelshift_r(sca.x, sca.x, rot), __funnelshift_r(sca.y, sca.y, rot),
+                             __funnelshift_r(scb.x, scb.x, rot), __funnelshift_r(scb.y, scb.y, rot)};
     // SW128 row s: 16-byte unit u of a chunk row lands at unit u ^ (s & 7); the
     // odd lane's group g ^ 2 is unit pair (2g, 2g + 1) ^ 4
     const uint32_t xr = ((uint32_t)s & 7u) ^ ((uint32_t)hf << 2);
+    auto dequant_chunk = [&](int chunk, const uint4& c0, const uint4& c1, uint32_t sw) {
+      unsigned char* dst = kbuf + chunk * AT_CHUNK_BYTES + s * 128;
+      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-      unsigned char* rowp = kbuf + (4 * hf + i) * AT_CHUNK_BYTES;
-      const uint32_t cw[8] = {code[2 * i].x, code[2 * i].y, code[2 * i].z, code[2 * i].w,
-                              code[2 * i + 1].x, code[2 * i + 1].y, code[2 * i + 1].z, code[2 * i + 1].w};
-#pragma unroll
-      for (int g = 0; g < 4; g++) {                      // 16 channels per E4M3 scale
-        const float sc = e4m3_value((scw[i] >> (8 * g)) & 255u);
+      for (int g = 0; g < 4; g++) {                        // 16 channels per E4M3 scale
+        const float sc = e4m3_value((sw >> (8 * g)) & 255u);
         const uint32_t sc2 = pack_bf16x2(sc, sc);
         uint32_t o[8];
         e2m1x8_to_bf16(cw[2 * g], o);
         e2m1x8_to_bf16(cw[2 * g + 1], o + 4);
 #pragma unroll
         for (int k = 0; k < 8; k++) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(o[k]), "r"(sc2));
-        unsigned char* dst = rowp + s * 128;
         *reinterpret_cast<uint4*>(dst + (((2u * g) ^ xr) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(dst + (((2u * g + 1u) ^ xr) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
+    };
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+      dequant_chunk(2 * hf + i, code[2 * i], code[2 * i + 1], scw[i]);
+      dequant_chunk(4 + 2 * hf + i, code[4 + 2 * i], code[5 + 2 * i], scw[2 + i]);
     }
     tc::fence_proxy_async_smem();
     __syncwarp();
@@ -303,30 +313,35 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     __syncthreads();
   }
 
-  // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims)
-  if (warp == 1 && lane == 0) {
+  // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims) as two
+  // chains of 16 MMAs into two accumulators (dims 0..255 at column 0, 256..511 at
+  // AT_S2_COL), issued by two threads at once: one thread's chain is bound by its
+  // own issue rate, not by the tensor core; the softmax adds the halves
+  if ((warp == 1 || warp == 2) && lane == 0) {
     constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
+    const int c0 = warp == 1 ? 0 : 4;
+    const uint32_t acc = tmem + (warp == 1 ? 0u : (uint32_t)AT_S2_COL);
     bool ok = at_wait(window_cta ? &sm.bar_kv : &sm.bar_keys, 0, sm, p.hdr, window_cta ? 11 : 16);
     if (ok) ok = at_wait(&sm.bar_q, 0, sm, p.hdr, 12);
     tc::fence_after_sync();
-    for (int c = 0; c < 8 && ok; c++) {
+    for (int c = c0; c < c0 + 4 && ok; c++) {
       const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + c * AT_QCHUNK_BYTES);
 #pragma unroll
       for (int ks = 0; ks < 4; ks++)
-        tc::mma_bf16(tmem, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
-                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c | ks) ? 1u : 0u);
+        tc::mma_bf16(acc, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
+                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c > c0 || ks) ? 1u : 0u);
     }
     tc::commit(&sm.bar_s);
   }
   __syncwarp();
 
   // ---------------- softmax straight from TMEM: warp w holds keys 32(w&3) .. +31 (one
-  // per lane) and heads 32(w>>2) .. +31 (one per register).  The issuing thread
-  // observes the completion late while its own MMAs are in flight, so warp 1
-  // takes it from warp 0 through a named barrier instead of the mbarrier.
-  if (warp != 1) at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
-  if (warp == 0) asm volatile("bar.arrive 1, 64;" ::: "memory");
-  else if (warp == 1) asm volatile("bar.sync 1, 64;" ::: "memory");
+  // per lane) and heads 32(w>>2) .. +31 (one per register).  An issuing thread
+  // observes the completion late while its own MMAs are in flight, so warps 1
+  // and 2 take it from warp 0 through a named barrier instead of the mbarrier.
+  if (warp == 0 || warp > 2) at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
+  if (warp == 0) asm volatile("bar.arrive 1, 96;" ::: "memory");
+  else if (warp <= 2) asm volatile("bar.sync 1, 96;" ::: "memory");
   tc::fence_after_sync();
   {
     const int q4 = warp & 3, half = warp >> 2;
@@ -334,7 +349,15 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + half * 32;
     const bool valid = sm.kvalid[m] != 0;
     float v[32], r[32];
-    tc::tmem_ld_x32(taddr, v);
+    {
+      uint32_t s1[32], s2[32];
+      tc::tmem_ld_x32_nowait(taddr, s1);
+      tc::tmem_ld_x32_nowait(taddr + AT_S2_COL, s2);
+      tc::tmem_wait_ld_regs(s1);
+      tc::tmem_wait_ld_regs(s2);
+#pragma unroll
+      for (int j = 0; j < 32; j++) v[j] = __uint_as_float(s1[j]) + __uint_as_float(s2[j]);
+    }
 #pragma unroll
     for (int j = 0; j < 32; j++) r[j] = v[j] = valid ? v[j] * p.scale : -INFINITY;
     // transpose-reduction: afterwards lane l holds the maximum of column l over the warp's keys
@@ -392,23 +415,23 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
       tc::fence_proxy_async_smem();                // the (m, L) rows are read by bulk copies
     }
   }
-  // ---------------- O^T = V^T P^T  (4 tiles of M = 128 dims, N = 64 heads, K = 128 keys)
-  if (warp == 1 && lane == 0) {
+  // ---------------- O^T = V^T P^T  (4 tiles of M = 128 dims, N = 64 heads, K = 128 keys),
+  // tile t issued by warp t's lane 0 (four chains at once)
+  if (warp < 4 && lane == 0) {
     constexpr uint32_t idesc_o = tc::idesc_bf16(128, H, 1, 1);
     const uint32_t kb = tc::smem_u32(kbuf), pb = tc::smem_u32(pbuf);
-    for (int tile = 0; tile < 4; tile++) {
+    const int tile = warp;
 #pragma unroll
-      for (int ks = 0; ks < AT_KEYS / 16; ks++) {
-        const uint64_t ad = tc::smem_desc(kb + (2 * tile) * AT_CHUNK_BYTES + ks * 2048, AT_CHUNK_BYTES, 1024,
-                                          tc::SW_128B);
-        const uint64_t bd = tc::smem_desc(pb + ks * 2048, 8192, 1024, tc::SW_128B);
-        tc::mma_bf16(tmem + 64 + tile * 64, ad, bd, idesc_o, ks ? 1u : 0u);
-      }
+    for (int ks = 0; ks < AT_KEYS / 16; ks++) {
+      const uint64_t ad = tc::smem_desc(kb + (2 * tile) * AT_CHUNK_BYTES + ks * 2048, AT_CHUNK_BYTES, 1024,
+                                        tc::SW_128B);
+      const uint64_t bd = tc::smem_desc(pb + ks * 2048, 8192, 1024, tc::SW_128B);
+      tc::mma_bf16(tmem + 64 + tile * 64, ad, bd, idesc_o, ks ? 1u : 0u);
     }
     tc::commit(&sm.bar_o);
   }
   __syncwarp();
-  if (warp != 1) at_wait(&sm.bar_o, 0, sm, p.hdr, 14);   // (the issuing warp: by the barrier below)
+  if (warp >= 4) at_wait(&sm.bar_o, 0, sm, p.hdr, 14);    // (the issuing warps: by the barrier below)
   __syncthreads();                                         // O^T complete; 1 / L_c visible to every thread
   tc::fence_after_sync();
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // phase 1 (long complete)
