@@ -719,40 +719,57 @@ __global__ void __launch_bounds__(RS_THREADS, RS_SCAN_CTAS_PER_SM) rs_filter_ker
       const int t0 = e_lo + ((bt * RS_TILES + k) * RS_WARPS + warp) * RS_TILE;
       if (t0 >= ri.nv) break;                    // warp-uniform
       if (ri.do_e) {
-        // keys in or above the threshold bin are rare: one vote per value slot,
-        // the appends only where some lane holds one
+        // keys in or above the threshold bin are rare: each lane marks its value
+        // slots that hold one (no votes), then the warp walks the marks, one
+        // slot per lane per round, with warp-aggregated appends (a rolled loop:
+        // small code, usually one or two rounds)
+        uint32_t mask = 0;
 #pragma unroll
         for (int j = 0; j < 16; j++) {
-          const uint32_t key = float_key(v[k][j]);
+          const int e = t0 + 128 * (j >> 2) + 4 * lane + (j & 3);
+          mask |= (uint32_t)((float_key(v[k][j]) >> RS_SHIFT) >= b1e && e < ri.nv) << j;
+        }
+        while (__any_sync(0xFFFFFFFFu, mask != 0u)) {
+          const bool have = mask != 0u;
+          const int j = have ? __ffs(mask) - 1 : 0;
+          mask &= mask - 1u;
+          float x = v[k][0];
+#pragma unroll
+          for (int jj = 1; jj < 16; jj++) x = jj == j ? v[k][jj] : x;
+          const uint32_t key = float_key(x);
           const uint32_t d = key >> RS_SHIFT;
           const int e = t0 + 128 * (j >> 2) + 4 * lane + (j & 3);
-          const bool ok = e < ri.nv;
-          if (__any_sync(0xFFFFFFFFu, ok && d >= b1e)) {
-            stage_append<int32_t>(ok && d > b1e, &s_n[0], s_gt_e, CSA2_MAX_K, &row_e.n_gt, gt_e, (uint32_t)p.K,
-                                  (int32_t)e);
-            if (keep_e)
-              stage_append<unsigned long long>(ok && d == b1e, &s_n[1], s_eq_e, SE, &row_e.n_eq, cd_e,
-                                               (uint32_t)RS_CAP,
-                                               ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)e);
-          }
+          stage_append<int32_t>(have && d > b1e, &s_n[0], s_gt_e, CSA2_MAX_K, &row_e.n_gt, gt_e, (uint32_t)p.K,
+                                (int32_t)e);
+          if (keep_e)
+            stage_append<unsigned long long>(have && d == b1e, &s_n[1], s_eq_e, SE, &row_e.n_eq, cd_e,
+                                             (uint32_t)RS_CAP,
+                                             ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)e);
         }
       }
       if (ri.do_b) {
         uint32_t bk[4];
         bool bok[4];
         rs_block_keys(v[k], t0, ri.nb, bk, bok);
+        // the same walk over the (even) lanes' four block keys
+        uint32_t mask = 0;
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-          const uint32_t d = bk[i] >> RS_SHIFT;
-          if (__any_sync(0xFFFFFFFFu, bok[i] && d >= b1b)) {
-            const int r = t0 / BLK + 16 * i + (lane >> 1);
-            stage_append<int32_t>(bok[i] && d > b1b, &s_n[2], s_gt_b, CSA2_MAX_M, &row_b.n_gt, gt_b, (uint32_t)p.M,
-                                  (int32_t)r);
-            if (keep_b)
-              stage_append<unsigned long long>(bok[i] && d == b1b, &s_n[3], s_eq_b, SE, &row_b.n_eq, cd_b,
-                                               (uint32_t)RS_CAP,
-                                               ((unsigned long long)bk[i] << 32) | (uint32_t)~(uint32_t)r);
-          }
+        for (int i = 0; i < 4; i++) mask |= (uint32_t)(bok[i] && (bk[i] >> RS_SHIFT) >= b1b) << i;
+        while (__any_sync(0xFFFFFFFFu, mask != 0u)) {
+          const bool have = mask != 0u;
+          const int i = have ? __ffs(mask) - 1 : 0;
+          mask &= mask - 1u;
+          uint32_t key = bk[0];
+#pragma unroll
+          for (int ii = 1; ii < 4; ii++) key = ii == i ? bk[ii] : key;
+          const uint32_t d = key >> RS_SHIFT;
+          const int r = t0 / BLK + 16 * i + (lane >> 1);
+          stage_append<int32_t>(have && d > b1b, &s_n[2], s_gt_b, CSA2_MAX_M, &row_b.n_gt, gt_b, (uint32_t)p.M,
+                                (int32_t)r);
+          if (keep_b)
+            stage_append<unsigned long long>(have && d == b1b, &s_n[3], s_eq_b, SE, &row_b.n_eq, cd_b,
+                                             (uint32_t)RS_CAP,
+                                             ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)r);
         }
       }
     }
