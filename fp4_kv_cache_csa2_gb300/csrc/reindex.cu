@@ -136,9 +136,11 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
   __syncthreads();
   cluster_wait();        // (arrived at set-up) every CTA runs and its row barriers are initialised
 
+  const uint32_t hist_base = tc::smem_u32(fs.hist);
   uint32_t prefix = 0, mask = 0;
   int remaining = K;
   bool take_all = false;                                   // at most K candidates in the cluster
+#pragma unroll 1
   for (int pass = 0; pass < 4; pass++) {
     const int shift = 24 - 8 * pass, buf = pass & 1;
 #pragma unroll
@@ -148,9 +150,10 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
       const uint32_t digit = (k >> shift) & 255u;
       if (pass == 0) {                                     // few distinct digits: aggregate per warp
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, ok ? digit : 256u);
-        if (ok && lane == __ffs(peers) - 1) atomicAdd(&fs.hist[digit], (uint32_t)__popc(peers));
+        if (ok && lane == __ffs(peers) - 1)
+          asm volatile("red.shared.add.u32 [%0], %1;" :: "r"(hist_base + 4u * digit), "r"((uint32_t)__popc(peers)) : "memory");
       } else if (ok) {
-        atomicAdd(&fs.hist[digit], 1u);
+        asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * digit) : "memory");
       }
     }
     __syncthreads();
