@@ -51,9 +51,12 @@ UNIT = "query-token-layers/s"
 IDX_ENTRY, MAIN_ENTRY = 68, 288
 K_SEL, M_BLK, WIN, D, H, HI, DI = 512, 2048, 128, 512, 64, 32, 128
 ATTN_BYTES = K_SEL * MAIN_ENTRY + WIN * D * 2 + H * D * 2 + H * D * 2          # 409,600
-REINDEX_BYTES = M_BLK * 8 * IDX_ENTRY + M_BLK * 4 + HI * DI * 2 + HI * 4 + K_SEL * 4 + ATTN_BYTES
+# the Reindex layer also writes the packed copy of its selection (K x 288 B),
+# which the Reuse layers read in place of the gather (the same byte count)
+REINDEX_BYTES = (M_BLK * 8 * IDX_ENTRY + M_BLK * 4 + HI * DI * 2 + HI * 4 + K_SEL * 4 + ATTN_BYTES
+                 + K_SEL * MAIN_ENTRY)                                           # 1,689,728
 REUSE_BYTES = K_SEL * 4 + ATTN_BYTES                                             # 411,648
-CHAIN_BYTES = REINDEX_BYTES + 3 * REUSE_BYTES                                    # 2,777,216
+CHAIN_BYTES = REINDEX_BYTES + 3 * REUSE_BYTES                                    # 2,924,672
 
 
 def peaks():
@@ -162,7 +165,7 @@ def max_over_ranks(x: float, world: int) -> float:
 class Decode1M:
     """Reindex + 3 Reuse at 1,048,576 entries, batch 16, R pipelined instances."""
 
-    def __init__(self, csa2, torch, B=16, N=1 << 20, d=3, seed=3, lanes=2):
+    def __init__(self, csa2, torch, B=16, N=1 << 20, d=3, seed=3, lanes=2, packed=True):
         import synth
         self.csa2, self.torch = csa2, torch
         self.B, self.N, self.d = B, N, d
@@ -224,6 +227,8 @@ class Decode1M:
                 "swa": [synth.torch_swa_rows(s + 20 + l, (B, WIN), dev) for l in range(4)],
                 "out": [torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev) for l in range(4)],
                 "sel": torch.empty((B, 1, K), dtype=torch.int32, device=dev),
+                # the selected entries packed by the Reindex call, read by the Reuse calls
+                "packed": torch.empty((B, 1, K, MAIN_ENTRY), dtype=torch.uint8, device=dev) if packed else None,
             }
             self.inst.append(inst)
         # one workspace per layer slot: the four layer calls of a step may run at once
@@ -256,7 +261,7 @@ class Decode1M:
         csa2.decode(mode, self.caches[r], q_pos=self.q_pos, q=inst["q"][layer].view(torch.int16),
                     swa=inst["swa"][layer].view(torch.int16), swa_base_pos=self.swa_base, scale=1 / math.sqrt(D),
                     sel=inst["sel"], out=inst["out"][layer].view(torch.int16), ws=self.ws[layer][lane], M=M_BLK,
-                    max_n=self.N,
+                    max_n=self.N, packed_sel=inst["packed"],
                     q_idx=inst["q_idx"].view(torch.int16), w_head=inst["w_head"], pool_blocks=self.pool)
 
     def check_status(self):
@@ -397,7 +402,8 @@ def _graph_ms(torch, graph, reps):
 
 def run_decode1m(args, torch, csa2):
     rank, world, local = dist_info()
-    w = Decode1M(csa2, torch, N=args.seq_len, d=args.pipeline_distance, lanes=args.lanes)
+    w = Decode1M(csa2, torch, N=args.seq_len, d=args.pipeline_distance, lanes=args.lanes,
+                 packed=bool(args.packed_selection))
     w.prologue()
     torch.cuda.synchronize()
     # graphs per pipeline phase and per cycle of R phases: step s only depends on s mod R
@@ -462,6 +468,9 @@ def run_decode1m(args, torch, csa2):
                              "instances, so independent) are parallel branches, the Reindex branch first at high "
                              f"priority; every layer slot has {w.lanes} stream + workspace lanes taken by step "
                              f"number mod {w.lanes}",
+                   "selection": ("the Reindex call writes a packed copy of its selected entries (K x 288 B per "
+                                 "query), which the three Reuse calls read contiguously instead of gathering"
+                                 if args.packed_selection else "every layer gathers the selected entries"),
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -545,7 +554,7 @@ def run_decode1m_e2e(args, torch, csa2, w):
             csa2.decode(mode, w.caches[r], q_pos=w.q_pos, q=q_view[layer], swa=inst["swa"][layer].view(torch.int16),
                         swa_base_pos=w.swa_base, scale=1 / math.sqrt(D), sel=inst["sel"], out=out_view[layer],
                         ws=w.ws[layer][s % w.lanes], M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view,
-                        pool_blocks=w.pool)
+                        pool_blocks=w.pool, packed_sel=inst["packed"])
         for layer in range(4):                     # independent instances: parallel branches,
             st = w.stream_of(layer, s)             # the Reindex branch first and at high priority
             st.wait_event(fork)
@@ -608,7 +617,8 @@ def run_decode1m_e2e(args, torch, csa2, w):
                                 swa=inst["swa"][layer].view(torch.int16), swa_base_pos=w.swa_base,
                                 scale=1 / math.sqrt(D), sel=inst["sel"], out=out_view[layer],
                                 ws=w.ws[layer][s % w.lanes],
-                                M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view, pool_blocks=w.pool)
+                                M=M_BLK, max_n=w.N, q_idx=qidx_view, w_head=w_view, pool_blocks=w.pool,
+                                packed_sel=inst["packed"])
                 ev = torch.cuda.Event()
                 ev.record(st)
                 done[(layer, s)] = ev
@@ -975,6 +985,8 @@ def main():
     ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
+    ap.add_argument("--packed-selection", type=int, default=1,
+                    help="decode: the Reindex call packs its selected entries for the Reuse calls (1) or not (0)")
     ap.add_argument("--lanes", type=int, default=5,
                     help="decode: stream + workspace lanes per layer slot")
     ap.add_argument("--graph-cycles", type=int, default=1,

@@ -45,7 +45,7 @@ class DecodeArgs(ctypes.Structure):
                 ("q_pos", ctypes.c_void_p), ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
                 ("w_head", ctypes.c_void_p), ("swa", ctypes.c_void_p),
                 ("swa_base_pos", ctypes.c_void_p), ("pool_blocks", ctypes.c_void_p),
-                ("sel", ctypes.c_void_p), ("out", ctypes.c_void_p)]
+                ("sel", ctypes.c_void_p), ("out", ctypes.c_void_p), ("packed_sel", ctypes.c_void_p)]
 
 
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -241,11 +241,11 @@ def decode_workspace_size(mode: int, B: int, Q: int, max_n: int, M: int, K: int)
 
 def decode(mode: int, cache: Cache, *, q_pos, q, swa, swa_base_pos, scale: float, sel, out,
            ws: Workspace, M: int = 0, max_n: int = 0, q_idx=None, w_head=None, pool_blocks=None,
-           stream=None):
+           packed_sel=None, stream=None):
     B, Q = q_pos.shape
     a = DecodeArgs(mode, B, Q, M, sel.shape[-1], swa.shape[1], max_n, float(scale), _ptr(q_pos),
                    _ptr(q), _ptr(q_idx), _ptr(w_head), _ptr(swa), _ptr(swa_base_pos),
-                   _ptr(pool_blocks), _ptr(sel), _ptr(out))
+                   _ptr(pool_blocks), _ptr(sel), _ptr(out), _ptr(packed_sel))
     c = cache.struct()
     _check("csa2_decode", load().csa2_decode(ctypes.byref(c), ctypes.byref(a), ws.ptr, ws.nbytes,
                                              _stream(stream)))

@@ -84,6 +84,7 @@ struct AtSmall {
   uint64_t bar_slot[4];                  // receive slot s holds a complete share
   uint64_t bar_q;                        // all of Q landed (chunks 0..3 and 4..7: two arrivals)
   uint64_t bar_keys;                     // every warp's dequantised keys are in shared memory
+  uint64_t bar_pk;                       // the packed selected entries landed in the staging buffer
   uint32_t tmem_base;
   int err;
 };
@@ -170,6 +171,7 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     for (int i = 0; i < 4; i++) tc::bar_init(&sm.bar_slot[i], 1);
     tc::bar_init(&sm.bar_q, 2);
     tc::bar_init(&sm.bar_keys, AT_THREADS / 32);
+    tc::bar_init(&sm.bar_pk, 1);
     sm.err = 0;
     tc::bar_init_fence();
   }
@@ -181,6 +183,14 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   // overlaps the previous kernel, which may have produced q, sel or the window
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // this CTA's run of a packed selection: one contiguous copy, in flight while
+  // the ids are read (they still say which slots exist)
+  const int n_sel = window_cta ? 0 : min(AT_KEYS, p.K - slot0);
+  if (p.packed_in && !window_cta && tid == 0) {
+    tc::bar_arrive_expect_tx(&sm.bar_pk, (uint32_t)(n_sel * MAIN_BYTES));
+    tc::bulk_load(stage, p.packed_in + ((int64_t)bq * p.K + slot0) * MAIN_BYTES, (uint32_t)(n_sel * MAIN_BYTES),
+                  &sm.bar_pk);
+  }
   const int64_t t = p.q_pos[bq];
   if (tid < AT_KEYS) {                       // which keys of this CTA exist
     int kind = 0;
@@ -234,21 +244,34 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   }
 
   // ---------------- keys: FP4 entries by 16-byte asynchronous copies into the
-  // staging buffer; lanes 2k and 2k+1 of warp w then take entry 16w + k into
-  // registers (lane h: dims 128h .. 128h+127 and 256+128h .. 256+128h+127, with
-  // their scale bytes), the staging buffer receives Q chunks 4..7, and every
-  // warp dequantises its 16 keys and arrives on bar_keys (8 arrivals complete it)
+  // staging buffer (or the packed selection by one copy); with packed_out the
+  // staged entries are also copied out, contiguously; lanes 2k and 2k+1 of
+  // warp w then take entry 16w + k into registers (lane h: dims 128h .. 128h+127
+  // and 256+128h .. 256+128h+127, with their scale bytes), the staging buffer
+  // receives Q chunks 4..7, and every warp dequantises its 16 keys and arrives
+  // on bar_keys (8 arrivals complete it)
   if (!window_cta) {
-    for (int i = tid; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS) {
-      const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
-      if (sm.kvalid[s] == 1) {
-        const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + sm.kid[s]) * MAIN_BYTES + part * 16;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                     :: "r"(tc::smem_u32(stage + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
+    if (p.packed_in) {
+      at_wait(&sm.bar_pk, 0, sm, p.hdr, 19);
+    } else {
+      for (int i = tid; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS) {
+        const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
+        if (sm.kvalid[s] == 1) {
+          const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + sm.kid[s]) * MAIN_BYTES + part * 16;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                       :: "r"(tc::smem_u32(stage + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
+        }
+      }
+      asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+      if (p.packed_out) tc::fence_proxy_async_smem();      // the staged bytes are read by a bulk copy
+      __syncthreads();
+      if (p.packed_out && tid == 0) {
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                     :: "l"(p.packed_out + ((int64_t)bq * p.K + slot0) * MAIN_BYTES), "r"(tc::smem_u32(stage)),
+                        "r"((uint32_t)(n_sel * MAIN_BYTES)) : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
     // Bank order: a quarter-warp (8 lanes) covers 4 entries x 2 lanes.  The
     // odd lane of a pair walks the two 16-byte pieces of each 64-dim chunk
     // swapped (and so its 16-channel groups as g ^ 2), so that within every
@@ -272,6 +295,7 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
     tc::fence_proxy_async_smem();
     __syncthreads();                                       // the staging buffer is free
     if (tid == 0) {
+      if (p.packed_out) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // (copied out)
       tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
       for (int c = 4; c < 8; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
     }

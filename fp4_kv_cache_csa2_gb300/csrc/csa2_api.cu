@@ -94,7 +94,8 @@ csa2_status do_index_score(const csa2_cache* cache, const uint16_t* q_idx, const
 
 csa2_status do_attention(const csa2_cache* cache, const uint16_t* q, const int32_t* sel, int K,
                          const uint16_t* swa, const int64_t* swa_base, int S, const int64_t* q_pos, float scale,
-                         uint16_t* out, int B, int Q, void* part_ws, WsHeader* hdr, cudaStream_t stream) {
+                         uint16_t* out, int B, int Q, void* part_ws, WsHeader* hdr, cudaStream_t stream,
+                         const uint8_t* packed_in = nullptr, uint8_t* packed_out = nullptr) {
   AttnParams p{};
   p.main_kv = cache->main_kv;
   p.cap = cache->cap;
@@ -109,6 +110,8 @@ csa2_status do_attention(const csa2_cache* cache, const uint16_t* q, const int32
   p.out = out;
   p.Q = Q;
   p.hdr = hdr;
+  p.packed_in = packed_in;
+  p.packed_out = packed_out;
   return from_cuda(launch_attention(p, B, reinterpret_cast<float*>(part_ws), stream));
 }
 
@@ -324,6 +327,9 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
   if (a->mode != CSA2_MODE_REUSE && (!a->q_idx || !a->w_head || !a->pool_blocks)) return CSA2_ERR_INVALID_ARG;
   if (!aligned16(a->q) || !aligned16(a->swa) || !aligned16(a->out)) return CSA2_ERR_INVALID_ARG;
   if (a->mode != CSA2_MODE_REUSE && !aligned16(a->q_idx)) return CSA2_ERR_INVALID_ARG;
+  if (a->packed_sel && !aligned16(a->packed_sel)) return CSA2_ERR_INVALID_ARG;
+  const uint8_t* packed_in = a->mode == CSA2_MODE_REUSE ? a->packed_sel : nullptr;
+  uint8_t* packed_out = a->mode == CSA2_MODE_REUSE ? nullptr : a->packed_sel;
 
   cudaStream_t s = (cudaStream_t)stream;
   WsHeader* hdr = header(ws);
@@ -341,7 +347,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
                                        a->sel, a->M, a->pool_blocks, cur, s));
       if (st != CSA2_OK) return st;
       return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out,
-                          a->B, a->Q, part, hdr, s);
+                          a->B, a->Q, part, hdr, s, packed_in, packed_out);
     }
     st = from_cuda(launch_block_topk(scores, a->q_pos, cache->n_entries, cache->m, a->B, a->Q, a->max_n, a->M,
                                      a->pool_blocks, gkeys, s));
@@ -371,7 +377,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
     if (st != CSA2_OK) return st;
   }
   return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out, a->B,
-                      a->Q, part, hdr, s);
+                      a->Q, part, hdr, s, packed_in, packed_out);
 }
 
 }  // extern "C"

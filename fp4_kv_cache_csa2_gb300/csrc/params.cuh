@@ -55,6 +55,8 @@ struct AttnParams {
   float scale;
   uint16_t* out;              // [BQ][64][512]
   int Q, n_chunks;            // n_chunks set by the launcher
+  const uint8_t* packed_in;   // [BQ][K][288] selected entries to read instead of gathering, or null
+  uint8_t* packed_out;        // [BQ][K][288] where to write the gathered selected entries, or null
   float* opart;               // [BQ][n_chunks][64][512]
   float* mpart;               // [BQ][n_chunks][64]
   float* lpart;               // [BQ][n_chunks][64]

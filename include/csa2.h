@@ -264,6 +264,14 @@ csa2_status csa2_sparse_swa_attn(const csa2_cache *cache, const uint16_t *q, con
  *            writes sel (top-K inside the pool), attends.
  *   Reuse:   attends with the given sel; q_idx, w_head and pool_blocks unused.
  * All pointer fields are device memory; shapes as in the calls above.
+ * packed_sel (optional, NULL to skip) is a packed copy of the selected
+ * entries, uint8 [B][Q][K][288], 16-byte aligned: a Full or Reindex call
+ * writes the main-KV bytes of entry sel[b][q][k] to slot k (slots whose sel is
+ * -1 hold unspecified bytes); a Reuse call given the sel of that call reads the
+ * entries from there instead of gathering them from the cache.  The Reuse
+ * layers that share a selection then read it contiguously; the result is the
+ * same as without it as long as the cache entries named by sel are unchanged
+ * in between (the caller's contract).
  */
 typedef struct {
     csa2_mode mode;
@@ -281,6 +289,7 @@ typedef struct {
     int32_t *pool_blocks;       /* [B][Q][M]  Full: out, Reindex: in            */
     int32_t *sel;               /* [B][Q][K]  Full/Reindex: out, Reuse: in      */
     uint16_t *out;              /* [B][Q][64][512]                              */
+    uint8_t *packed_sel;        /* [B][Q][K][288] or NULL: Full/Reindex out, Reuse in */
 } csa2_decode_args;
 
 size_t csa2_decode_workspace_size(csa2_mode mode, int B, int Q, int64_t max_n, int M, int K);

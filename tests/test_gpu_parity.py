@@ -434,6 +434,57 @@ def test_decode_reindex_with_all_blocks_equals_full_selection(csa2):
     assert torch.equal(out, out2)
 
 
+@pytest.mark.parametrize("mode_out,K,Q,T", [(0, 200, 3, 1200), (1, 512, 2, 4096), (0, 20, 2, 300)])
+def test_decode_packed_selection_roundtrip(csa2, mode_out, K, Q, T):
+    """A Full or Reindex call with packed_sel copies the main-KV bytes of every
+    selected entry into slot order; a Reuse call reading them gives the same
+    output, bit for bit, as a Reuse call that gathers from the cache (K spans
+    several 128-slot runs and a partial one)."""
+    M = 150 if T >= 1200 else 40
+    case = cases.make_case(B=2, T=T, m=1, Q=Q, M=M, K=K, seed=811 + K)
+    L = GpuLayer(csa2, case)
+    B, max_n = 2, T
+    pool = torch.empty((B, Q, M), dtype=torch.int32, device=DEV)
+    sel = torch.empty((B, Q, K), dtype=torch.int32, device=DEV)
+    out = torch.empty((B, Q, 64, 512), dtype=torch.int16, device=DEV)
+    packed = torch.full((B, Q, K, 288), 0xA5, dtype=torch.uint8, device=DEV)
+    ws = csa2.Workspace(max(csa2.decode_workspace_size(m, B, Q, max_n, M, K) for m in (0, 1, 2)), device=DEV)
+    common = dict(q_pos=L.q_pos, q=L.q, swa=L.swa, swa_base_pos=L.swa_base, scale=case.scale, ws=ws, M=M,
+                  max_n=max_n, q_idx=L.q_idx, w_head=L.w_head)
+    if mode_out == 1:                       # a pool first, then the Reindex call writes the packed copy
+        csa2.decode(csa2.MODE_FULL, L.cache, sel=sel, out=out, pool_blocks=pool, **common)
+        csa2.decode(csa2.MODE_REINDEX, L.cache, sel=sel, out=out, pool_blocks=pool, packed_sel=packed, **common)
+    else:
+        csa2.decode(csa2.MODE_FULL, L.cache, sel=sel, out=out, pool_blocks=pool, packed_sel=packed, **common)
+    assert ws.sync_status()[0] == 0
+    s_h, p_h, main = host(sel), host(packed), host(L.cache.main_kv)
+    valid = s_h >= 0
+    assert valid.sum() > 0
+    for b in range(B):
+        for qi in range(Q):
+            ids = s_h[b, qi][valid[b, qi]]
+            assert np.array_equal(p_h[b, qi][valid[b, qi]], main[b, ids])
+    out_gather = torch.empty_like(out)
+    out_packed = torch.empty_like(out)
+    csa2.decode(csa2.MODE_REUSE, L.cache, sel=sel, out=out_gather, **common)
+    csa2.decode(csa2.MODE_REUSE, L.cache, sel=sel, out=out_packed, packed_sel=packed, **common)
+    assert ws.sync_status()[0] == 0
+    assert torch.equal(out_gather, out_packed)
+    assert torch.equal(out_gather, out)     # Reuse with the same selection and queries = the writing call
+
+
+def test_decode_packed_selection_must_be_aligned(csa2):
+    case = cases.make_case(B=1, T=300, m=1, Q=1, M=40, K=20, seed=815)
+    L = GpuLayer(csa2, case)
+    sel = torch.zeros((1, 1, 20), dtype=torch.int32, device=DEV)
+    out = torch.empty((1, 1, 64, 512), dtype=torch.int16, device=DEV)
+    packed = torch.zeros(20 * 288 + 16, dtype=torch.uint8, device=DEV)
+    ws = csa2.Workspace(csa2.decode_workspace_size(2, 1, 1, 300, 40, 20), device=DEV)
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):
+        csa2.decode(csa2.MODE_REUSE, L.cache, q_pos=L.q_pos, q=L.q, swa=L.swa, swa_base_pos=L.swa_base,
+                    scale=case.scale, sel=sel, out=out, ws=ws, packed_sel=packed[8:])
+
+
 def test_decode_reindex_cluster_select_ties_and_short_pool(csa2):
     """Reindex selection is one radix select across the 8 CTAs that each score an
     eighth of the pool.  Query 0: every block in the pool, and eight blocks spread
