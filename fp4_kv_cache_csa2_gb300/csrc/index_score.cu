@@ -8,9 +8,10 @@
 // 890 字节" §4.4 (index K is OCP MXFP4: E2M1 + one E8M0 scale per 32), §4.7.
 //
 // One CTA scores a run of 128-entry tiles for a group of NQ queries of one
-// sequence (NQ = 1 for decode and pool scans; NQ = 4 when a sequence brings many
+// sequence (NQ = 1 for decode and pool scans; NQ = 5 when a sequence brings many
 // queries, as a prefill chunk does, so that every tile of keys loaded feeds a
-// 128-column MMA instead of a 32-column one):
+// 160-column MMA instead of a 32-column one; three 160-column accumulators and
+// the scale-word columns fill the 512 TMEM columns):
 //   warp 0      producer: full scans load 128-entry tiles of index-K codes
 //               (SW64 K-major, 64 B per entry) with a 3-D tensor map that puts
 //               slot 4g + q of the tile in row 32q + g, and the 4-byte E8M0
@@ -18,7 +19,7 @@
 //               gather the 16 candidate blocks of a tile with cp.async, one
 //               512-byte block per warp instruction, into the same rows.
 //               6-stage ring.
-//   warp 1..I   MMA issuers (I = 2 for NQ = 1, 3 for NQ = 4; warp 1 owns
+//   warp 1..I   MMA issuers (I = 2 for NQ = 1, 3 for NQ = 5; warp 1 owns
 //               TMEM): issuer k takes every I-th tile into its own TMEM
 //               accumulator: one tcgen05.cp of the tile's 512 bytes of scale
 //               words into TMEM (with that row order, 16 contiguous bytes per
@@ -49,7 +50,7 @@ constexpr int IS_TILE = 128;
 constexpr int IS_CODES = IS_TILE * IDX_CODE_BYTES;         // 8192
 constexpr int IS_STAGE_BYTES = IS_CODES + 1024;            // codes + 512 B scales, 1 KB aligned stride
 constexpr int IS_POOL_MAX = CSA2_MAX_M;
-constexpr int IS_GROUP = 4;                                 // queries per CTA for many-query sequences
+constexpr int IS_GROUP = 5;                                 // queries per CTA for many-query sequences
 
 // Warp roles: 0 producer; 1..ISSUERS MMA issuers (issuer k takes tiles
 // i = k mod ISSUERS into accumulator k); ISSUERS+1 publisher; then 4*NQ
