@@ -77,7 +77,8 @@ struct AtSmall {
   alignas(16) float recv_ml[4][2 * H];   // (m, L) rows received from each other CTA (index = sender rank,
                                          // minus one above this CTA's own)
   float inv_l[H];
-  float red[4][H];                       // per-warp column maxima / sums (warp w & 3, head)
+  float red[4][H];                       // per-warp column maxima (warp w & 3, head)
+  float red_sum[4][H];                   // per-warp column sums
   float wgt[AT_MAXC][H];                 // combination weight of each CTA's share, per head
   uint64_t bar_kv, bar_s, bar_o;
   uint64_t bar_ml;                       // every other CTA's (m, L) rows received (owners only)
@@ -405,7 +406,6 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
 #pragma unroll
     for (int j = 0; j < 32; j++) mx[j] = __shfl_sync(0xFFFFFFFFu, mlane, j);
     if (q4 == 0) sm.ml[hl] = mlane;
-    __syncthreads();                                 // every thread has read the per-warp maxima
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 32; j++) {
@@ -428,12 +428,12 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
         r[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, k);
       }
     }
-    sm.red[q4][half * 32 + lane] = r[0];
+    sm.red_sum[q4][half * 32 + lane] = r[0];
     tc::fence_before_sync();
     __syncthreads();                                 // P^T complete, every warp's column sums visible
     tc::fence_after_sync();
     if (tid < H) {
-      const float sum = sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
+      const float sum = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
       sm.ml[H + tid] = sum;
       sm.inv_l[tid] = sum > 0.f ? 1.0f / sum : 0.f;
       tc::fence_proxy_async_smem();                // the (m, L) rows are read by bulk copies

@@ -270,9 +270,10 @@ __device__ int cluster_select(const uint32_t* keys, int n, int K, int crank, RxS
     if (take_all || km > thr) gt++;
     else if (km == thr) eq++;
   }
-  int gt_tot, eq_tot;
-  const int gt_before = cta_exclusive_scan(gt, fs, &gt_tot);    // (its barriers also publish bcast)
-  const int eq_before = cta_exclusive_scan(eq, fs, &eq_tot);
+  // one scan of (gt, eq) packed in 16-bit halves (a CTA holds < 2^16 keys)
+  int both_tot;
+  const int both_before = cta_exclusive_scan((gt << 16) | eq, fs, &both_tot);   // (its barriers publish bcast)
+  const int gt_before = both_before >> 16, eq_before = both_before & 0xFFFF;
   const int my_base = fs.bcast[0], my_budget = fs.bcast[1], total = fs.bcast[2];
   const int mine_eq = max(0, min(eq, my_budget - eq_before));
   int r = my_base + gt_before + min(eq_before, my_budget);
