@@ -183,7 +183,6 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   // everything above reads no input: with programmatic dependent launch it
   // overlaps the previous kernel, which may have produced q, sel or the window
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // this CTA's run of a packed selection: one contiguous copy, in flight while
   // the ids are read (they still say which slots exist)
   const int n_sel = window_cta ? 0 : min(AT_KEYS, p.K - slot0);
@@ -631,6 +630,9 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
       }
     }
   }
+  // the next kernel of the stream may be scheduled now (triggered at the start,
+  // its CTAs would hold SMs idle in their own wait for this whole kernel)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // A sender's shares stay in place until its copies have read them; an owner
   // has received every byte sent to it (bar_ml, bar_slot) before it gets here, so no
   // cross-CTA access remains and no final cluster barrier is needed.

@@ -308,7 +308,6 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   // everything above reads no input: with programmatic dependent launch it
   // overlaps the previous kernel, which may have produced the pool or the queries
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[b]);
   if (nv > p.cap) {
     if (tid == 0 && crank == 0) report(p.hdr, CSA2_ERR_BOUNDS, nv);
@@ -453,6 +452,9 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   const int ns = cluster_select(sm.keys, n * RX_TILE, p.K, crank, sm, p.hdr, [&](int i, int r) {
     sel[r] = sm.pool[i / BLK] * BLK + (i % BLK);
   });
+  // the attention may be scheduled now (it reads sel after its own wait, which
+  // returns once this grid has completed and its writes are visible)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (crank == RX_CL - 1)
     for (int i = ns + tid; i < p.K; i += RX_THREADS) sel[i] = -1;
 }
