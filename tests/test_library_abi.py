@@ -77,3 +77,32 @@ def test_missing_library_fails_loudly(tmp_path):
             csa2.load(str(tmp_path / "libcsa2.so"))
     finally:
         csa2._lib = saved
+
+
+def _c_layout(tmp_path, struct: str, fields: list[str]) -> list[int]:
+    """sizeof(struct) followed by offsetof(struct, f) for each field, from a
+    small C program compiled against include/csa2.h with the host compiler."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    src = tmp_path / "layout.c"
+    body = "".join(f'  printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields)
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "csa2.h"\n'
+                   f'int main(void) {{\n  printf("%zu\\n", sizeof({struct}));\n{body}  return 0;\n}}\n')
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    return [int(x) for x in out]
+
+
+def test_binding_structs_match_the_c_layout(tmp_path):
+    """The ctypes mirrors of csa2_cache and csa2_decode_args (including the
+    packed_sel field appended last) have the C structs' sizes and offsets."""
+    import fp4_kv_cache_csa2_gb300 as csa2
+    for cls, struct in ((csa2.DecodeArgs, "csa2_decode_args"), (csa2.CacheStruct, "csa2_cache")):
+        names = [f[0] for f in cls._fields_]
+        c = _c_layout(tmp_path, struct, names)
+        assert c[0] == ctypes.sizeof(cls), struct
+        assert c[1:] == [getattr(cls, n).offset for n in names], struct
