@@ -784,6 +784,88 @@ def run_full131k(args, torch, csa2):
                   "clocks": clk.summary(), "gpu_launches": args.steps * 5})
 
 
+def run_decoder1m(args, torch, csa2):
+    """One token through a whole decoder at 1M entries, batch 16: the source
+    layer in Full mode + 3 Reuse layers, then 4 x (Reindex + 3 Reuse) on the
+    same cache (1 Full scan, 4 Reindexes and 15 Reuses per token); each
+    Full/Reindex call packs its selection for its 3 Reuse layers.  One CUDA
+    graph per token, calls in order on one stream."""
+    import synth
+    rank, world, local = dist_info()
+    B, N, dev = 16, args.seq_len, "cuda"
+    cache = csa2.Cache(B, N, 1, device=dev)
+    ones = torch.ones(D, device=dev)
+    wts = _weights(torch, 3)
+    rope = csa2.rope_table(N).to(dev)
+    ws_cw = csa2.Workspace(1 << 16, device=dev)
+    _write_cache(csa2, torch, cache, N, 3, (ones, ones, wts[2]), rope, ws_cw)
+    cache.n_entries.fill_(N)
+    assert ws_cw.sync_status()[0] == 0
+    del rope
+    q_pos = torch.full((B, 1), N - 1, dtype=torch.int64, device=dev)
+    swa_base = torch.full((B,), N - WIN, dtype=torch.int64, device=dev)
+    n_layers, groups = 20, 5                      # layer 4g is Full (g = 0) or Reindex, then 3 Reuse
+    qs = [synth.torch_normal(300 + l, (B, 1, H, D), torch.bfloat16, dev) for l in range(n_layers)]
+    swas = [synth.torch_swa_rows(400 + l, (B, WIN), dev) for l in range(n_layers)]
+    q_idx = [synth.torch_normal(500 + g, (B, 1, HI, DI), torch.bfloat16, dev) for g in range(groups)]
+    w_head = [synth.torch_normal(600 + g, (B, 1, HI), torch.float32, dev) for g in range(groups)]
+    pool = torch.empty((B, 1, M_BLK), dtype=torch.int32, device=dev)
+    sels = [torch.empty((B, 1, K_SEL), dtype=torch.int32, device=dev) for _ in range(groups)]
+    packs = [torch.empty((B, 1, K_SEL, MAIN_ENTRY), dtype=torch.uint8, device=dev) for _ in range(groups)]
+    outs = [torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    modes = [csa2.MODE_FULL, csa2.MODE_REINDEX, csa2.MODE_REUSE]
+    wss = {m: csa2.Workspace(csa2.decode_workspace_size(m, B, 1, N, M_BLK, K_SEL), device=dev) for m in modes}
+
+    def step():
+        for l in range(n_layers):
+            g, k = divmod(l, 4)
+            mode = csa2.MODE_REUSE if k else (csa2.MODE_FULL if g == 0 else csa2.MODE_REINDEX)
+            csa2.decode(mode, cache, q_pos=q_pos, q=qs[l].view(torch.int16), swa=swas[l].view(torch.int16),
+                        swa_base_pos=swa_base, scale=1 / math.sqrt(D), sel=sels[g], out=outs[l].view(torch.int16),
+                        ws=wss[mode], M=M_BLK, max_n=N, q_idx=q_idx[g].view(torch.int16), w_head=w_head[g],
+                        pool_blocks=pool, packed_sel=packs[g])
+    graph = _capture(torch, step)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms = _events_ms(torch, graph.replay, args.steps)
+    ms = max_over_ranks(ms, world)
+    for w in wss.values():
+        assert w.sync_status()[0] == 0
+    # the dominant kernel alone: the Full layer's index scan over 16 x N entries
+    scores = torch.empty((B, 1, N), dtype=torch.float32, device=dev)
+    ws_s = csa2.Workspace(1 << 16, device=dev)
+    g_s = _capture(torch, lambda: csa2.index_score(cache, q_idx[0].view(torch.int16), w_head[0], q_pos, scores,
+                                                   N, ws_s))
+    g_s.replay()
+    scan_ms = _events_ms(torch, g_s.replay, max(args.steps, 20))
+    hbm, _, which = peaks()
+    scan_bytes = B * N * (IDX_ENTRY + 4) + B * (HI * DI * 2 + HI * 4)
+    full_q = N * IDX_ENTRY + HI * DI * 2 + HI * 4 + ATTN_BYTES + M_BLK * 4 + K_SEL * 4 + K_SEL * MAIN_ENTRY
+    per_query = full_q + 4 * REINDEX_BYTES + 15 * REUSE_BYTES
+    achieved = scan_bytes / (scan_ms / 1e3) / 1e9
+    return _line(args, world, "CSA2 whole-decoder query-token-layers/s at 1M ctx (Full + 3 Reuse, 4 x (Reindex + "
+                 "3 Reuse)), batch 16", UNIT, B * n_layers * world / (ms / 1e3), ms,
+                 "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 {"workload": f"one token through a 20-layer decoder block chain, {N:,} entries/seq, batch 16: "
+                              "Full source layer + 3 Reuse, then 4 x (Reindex on the Full layer's pool + 3 Reuse), "
+                              "one cache", "global_batch": B, "seq_len": N, "M_blocks": M_BLK, "K": K_SEL,
+                  "window": WIN,
+                  "l2": "the Full scan reads the 1.1 GB of index K every token (larger than L2); the Reindex layers "
+                        "share the Full layer's pool",
+                  "selection": "each Full/Reindex call packs its selected entries for its 3 Reuse calls",
+                  "launch": "one CUDA graph per token, the 20 calls in order on one stream"},
+                 {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                  "traffic": None, "kernel": "index_score_tc_kernel<1> (Full layer at 1M)",
+                  "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
+                 {"step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
+                               "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
+                  "ms_per_token": ms, "clocks": clk.summary(),
+                  "gpu_launches": args.steps * (5 + 4 * 2 + 15)})   # Full 5, Reindex 2, Reuse 1
+
+
 def run_prefill8k(args, torch, csa2):
     """Prefill chunk: 8192 causal queries, one Full-mode call (index scan of
     5 queries per CTA, per-query block top-2048 and top-512, attention)."""
@@ -848,6 +930,82 @@ def run_prefill8k(args, torch, csa2):
                   "algorithmic_flops_per_launch": flops, "avg_launch_ms": scan_ms,
                   "peak_source": f"{which} bf16 x {FP4_PER_BF16:g} (nominal fp4:bf16 dense ratio)"},
                  {"clocks": clk.summary(), "gpu_launches": args.steps * 5})
+
+
+def run_prefillblock(args, torch, csa2):
+    """An encoder block over the prefill chunk: the source layer (m=2) in Full
+    mode + 5 Reuse layers with fresh queries and windows, reading the Full
+    layer's selection from the same (L2-resident) cache.  One CUDA graph per
+    chunk, L2 flushed before each."""
+    import synth
+    rank, world, local = dist_info()
+    m, P, C, dev = 2, 131072, 8192, "cuda"
+    T = P + C
+    N = T // m
+    cache = csa2.Cache(1, N, m, device=dev)
+    wts = _weights(torch, 4)
+    rope = csa2.rope_table(N).to(dev)
+    ws_cw = csa2.Workspace(1 << 16, device=dev)
+    _write_cache(csa2, torch, cache, T, 4, wts, rope, ws_cw)
+    cache.n_entries.fill_(N)
+    assert ws_cw.sync_status()[0] == 0
+    Q, n_layers = C, 6
+    q_pos = torch.arange(P, T, dtype=torch.int64, device=dev)[None]
+    swa_base = torch.full((1,), P - (WIN - 1), dtype=torch.int64, device=dev)
+    q_idx = synth.torch_normal(41, (1, Q, HI, DI), torch.bfloat16, dev)
+    w_head = synth.torch_normal(42, (1, Q, HI), torch.float32, dev)
+    qs = [synth.torch_normal(700 + l, (1, Q, H, D), torch.bfloat16, dev) for l in range(n_layers)]
+    swas = [synth.torch_swa_rows(800 + l, (1, Q + WIN - 1), dev) for l in range(n_layers)]
+    pool = torch.empty((1, Q, M_BLK), dtype=torch.int32, device=dev)
+    sel = torch.empty((1, Q, K_SEL), dtype=torch.int32, device=dev)
+    outs = [torch.empty((1, Q, H, D), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    ws_f = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_FULL, 1, Q, N, M_BLK, K_SEL), device=dev)
+    ws_r = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REUSE, 1, Q, N, M_BLK, K_SEL), device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        for l in range(n_layers):
+            csa2.decode(csa2.MODE_FULL if l == 0 else csa2.MODE_REUSE, cache, q_pos=q_pos,
+                        q=qs[l].view(torch.int16), swa=swas[l].view(torch.int16), swa_base_pos=swa_base,
+                        scale=1 / math.sqrt(D), sel=sel, out=outs[l].view(torch.int16), ws=ws_f if l == 0 else ws_r,
+                        M=M_BLK, max_n=N, q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool)
+    graph = _capture(torch, step)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms = _events_ms(torch, graph.replay, args.steps, flush=flush)
+    ms = max_over_ranks(ms, world)
+    assert ws_f.sync_status()[0] == 0 and ws_r.sync_status()[0] == 0
+    # the tensor-bound kernel alone: the grouped index scan
+    scores = torch.empty((1, Q, N), dtype=torch.float32, device=dev)
+    ws_s = csa2.Workspace(1 << 16, device=dev)
+    g_s = _capture(torch, lambda: csa2.index_score(cache, q_idx.view(torch.int16), w_head, q_pos, scores, N, ws_s))
+    g_s.replay()
+    scan_ms = _events_ms(torch, g_s.replay, max(args.steps, 10), flush=flush)
+    _, bf16, which = peaks()
+    pairs = sum(min((t + 1) // m, N) for t in range(P, T))
+    flops = pairs * HI * DI * 2
+    fp4_peak = bf16 * FP4_PER_BF16
+    achieved = flops / (scan_ms / 1e3) / 1e12
+    attn_flops = n_layers * Q * (K_SEL + WIN) * H * D * 4
+    return _line(args, world, "CSA2 encoder-block prefill query-token-layers/s (Full + 5 Reuse), 8192 new tokens "
+                 "on a 131K prefix", UNIT, Q * n_layers * world / (ms / 1e3), ms,
+                 "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 {"workload": "encoder block on a prefill chunk, m=2, 131,072-token prefix + 8192 new tokens "
+                              "(69,632 entries): the Full source layer + 5 Reuse layers (fresh queries and windows) "
+                              "on its selection, batch 1",
+                  "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
+                  "l2": "L2 flushed (256 MB write) before every timed chunk; the caches (24 MB) fit in L2",
+                  "selection": "the Reuse layers gather from the L2-resident cache (no packed copy)",
+                  "launch": "one CUDA graph per chunk, the 6 calls in order"},
+                 {"bound": "tensor", "achieved": achieved, "peak": bf16 * FP4_PER_BF16, "unit": "TFLOP/s",
+                  "frac": achieved / fp4_peak, "traffic": None, "kernel": "index_score_tc_kernel<5>",
+                  "algorithmic_flops_per_launch": flops, "avg_launch_ms": scan_ms,
+                  "peak_source": f"{which} bf16 x {FP4_PER_BF16:g} (nominal fp4:bf16 dense ratio)"},
+                 {"attention_bf16_flops_per_chunk": attn_flops, "clocks": clk.summary(),
+                  "gpu_launches": args.steps * (5 + 5)})   # Full: scan, 3 selection, attention; Reuse: attention
 
 
 def run_cachewrite(args, torch, csa2):
@@ -981,7 +1139,8 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode1m", choices=["decode1m", "full131k", "prefill8k", "cachewrite"])
+    ap.add_argument("--workload", default="decode1m",
+                    choices=["decode1m", "full131k", "prefill8k", "cachewrite", "decoder1m", "prefillblock"])
     ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
@@ -1009,7 +1168,8 @@ def main():
     import fp4_kv_cache_csa2_gb300 as csa2
     csa2.load()
     if args.workload != "decode1m":
-        fn = {"full131k": run_full131k, "prefill8k": run_prefill8k, "cachewrite": run_cachewrite}[args.workload]
+        fn = {"full131k": run_full131k, "prefill8k": run_prefill8k, "cachewrite": run_cachewrite,
+              "decoder1m": run_decoder1m, "prefillblock": run_prefillblock}[args.workload]
         line = fn(args, torch, csa2)
         if rank == 0:
             print(json.dumps(line), flush=True)
