@@ -13,6 +13,8 @@ What it computes (plain, slow, in the order the pages state it):
                      q_h MXFP4-quantised like the index keys
   block top-M     -> ``block_topm``: g_r = max over blocks of 8 (last block padded
                      with -inf), newest visible block forced to +inf, top-M blocks
+  HISA variant    -> ``block_summary`` (mean index key per block of 8, MXFP4) and
+                     ``hisa_blocks`` (top-M blocks by the score of their mean key)
   top-K           -> ``select_topk``: Full over all visible entries, Reindex over
                      the candidate pool only; order (score desc, index asc)
   attention       -> ``attention``: one softmax over [selected main-KV entries ||
@@ -245,6 +247,48 @@ def block_topm(scores: np.ndarray, n_visible: int, M: int) -> np.ndarray:
     chosen = np.sort(order[:M])
     out[:len(chosen)] = chosen
     return out
+
+
+def block_summary(idx_codes: np.ndarray, idx_scales: np.ndarray, n: int):
+    """HISA block summaries of the first n index-K entries.  [zartbot §2.3.4,
+    the HISA paragraph: every block of consecutive positions keeps the mean of
+    its indexer keys, a decode step updating only the newest block]
+
+    Block r covers entries [8r, min(8r + 8, n)).  Its mean key is computed in
+    binary32: the dequantised keys (exact in binary32) are added in entry order
+    starting from +0, and the sum is divided by the number of entries in the
+    block; the mean is then stored as MXFP4 like every index key.  Returns
+    (codes [nb, 64], scales [nb, 4]) with nb = ceil(n / 8).
+    """
+    n = int(n)
+    nb = (n + BLOCK - 1) // BLOCK
+    kd = np.zeros((nb * BLOCK, D_IDX), np.float32)
+    kd[:n] = dequant_index(idx_codes[:n], idx_scales[:n]).astype(np.float32)   # exact
+    kd = kd.reshape(nb, BLOCK, D_IDX)
+    acc = np.zeros((nb, D_IDX), np.float32)
+    for p in range(BLOCK):                               # entry order; absent entries add +0
+        acc = acc + kd[:, p]
+    count = np.minimum(BLOCK, n - BLOCK * np.arange(nb)).astype(np.float32)
+    mean = acc / count[:, None]
+    return mxfp4_quantize(mean)
+
+
+def hisa_blocks(q_idx: np.ndarray, w_head: np.ndarray, sum_codes: np.ndarray,
+                sum_scales: np.ndarray, n_visible: int, M: int) -> np.ndarray:
+    """HISA first stage for one query: the indexer score of every block that
+    holds a visible entry, computed on the block's mean key (the same
+    s = sum_h w_h ReLU(q_h . k)), and the M best blocks by (score desc, block
+    asc), returned ascending and -1 padded.  No block is forced in (the forced
+    newest block is HSI's boundary rule).  The second stage scores the chosen
+    blocks' visible entries, as a Reindex layer does over its pool.  [zartbot
+    §2.3.4, the HISA paragraph]
+    """
+    nv = int(n_visible)
+    nb = (nv + BLOCK - 1) // BLOCK
+    if nb == 0:
+        return np.full(M, -1, np.int32)
+    g = index_scores(q_idx, w_head, sum_codes[:nb], sum_scales[:nb])
+    return select_topk(g, np.arange(nb), M)
 
 
 def pool_entries(blocks: np.ndarray, n_visible: int) -> np.ndarray:

@@ -432,6 +432,77 @@ def test_full_topk_inside_pool_when_M_exceeds_K():
         assert set(top[top >= 0]) <= set(pool)
 
 
+def test_hisa_summary_of_identical_keys_is_the_key():
+    """The mean of copies of one key is that key (exactly, in binary32), and an
+    MXFP4 key quantises back to its own values: the summary of such a block
+    has the entry's values and scales (a negative-zero code comes back as +0,
+    the sum starting from +0), for a partial block of 3 copies as well."""
+    g, (main, codes, scales) = _tiny_cache(21, 40)
+    rep_c = np.repeat(codes[[5, 17, 30]], 8, axis=0)[:19]      # blocks of 8, 8 and 3 copies
+    rep_s = np.repeat(scales[[5, 17, 30]], 8, axis=0)[:19]
+    sc, ss = oracle.block_summary(rep_c, rep_s, 19)
+    np.testing.assert_array_equal(ss, scales[[5, 17, 30]])
+    np.testing.assert_array_equal(oracle.dequant_index(sc, ss), oracle.dequant_index(codes[[5, 17, 30]],
+                                                                                     scales[[5, 17, 30]]))
+
+
+def test_hisa_summary_is_the_mean_within_mxfp4_rounding():
+    """Dequantised summary = the block's mean key up to MXFP4 rounding: per
+    32-wide group with scale 2^X, X = floor(log2 amax) - 2, the E2M1 grid's
+    largest spacing is 2 * 2^X and values in [6, 8) * 2^X saturate to 6, so the
+    error is at most 2 * 2^X; opposite keys give a zero block (zero codes, zero
+    scale byte)."""
+    g, (main, codes, scales) = _tiny_cache(22, 61)
+    sc, ss = oracle.block_summary(codes, scales, 61)
+    assert sc.shape == (8, 64)
+    kd = oracle.dequant_index(codes, scales)
+    got = oracle.dequant_index(sc, ss)
+    for r in range(8):
+        rows = kd[8 * r:min(8 * r + 8, 61)]
+        mean = rows.sum(axis=0) / len(rows)
+        for grp in range(4):
+            m = mean[32 * grp:32 * grp + 32]
+            amax = np.abs(m).max()
+            bound = 2.0 ** (math.floor(math.log2(amax)) - 1) if amax > 0 else 0.0
+            assert np.all(np.abs(got[r, 32 * grp:32 * grp + 32] - m) <= bound)
+    neg_c, neg_s = oracle.mxfp4_quantize(-kd[3].astype(np.float32))
+    pc = np.stack([codes[3], neg_c])
+    ps = np.stack([scales[3], neg_s])
+    zc, zs = oracle.block_summary(pc, ps, 2)
+    assert not zc.any() and not zs.any()
+
+
+def test_hisa_with_every_block_equals_exhaustive_topk():
+    """With M at least the number of visible blocks HISA keeps every block, and
+    its second stage (top-K over the pool) is the exhaustive top-K."""
+    g, (main, codes, scales) = _tiny_cache(23, 203)
+    q = synth.index_queries(g)
+    w = synth.head_weights(g)
+    sc, ss = oracle.block_summary(codes, scales, 203)
+    nv = 199
+    blocks = oracle.hisa_blocks(q, w, sc, ss, nv, 30)
+    np.testing.assert_array_equal(blocks[:25], np.arange(25))
+    assert np.all(blocks[25:] == -1)
+    s = oracle.index_scores(q, w, codes, scales)
+    pool = oracle.pool_entries(blocks, nv)
+    np.testing.assert_array_equal(oracle.select_topk(s, pool, 16), oracle.select_topk(s, np.arange(nv), 16))
+
+
+def test_hisa_blocks_rank_by_the_mean_key_score():
+    """Brute force on a small cache: the chosen blocks are the M highest scores
+    of the block mean keys (ties to the lower block), none forced."""
+    g, (main, codes, scales) = _tiny_cache(24, 120)
+    q = synth.index_queries(g)
+    w = synth.head_weights(g)
+    sc, ss = oracle.block_summary(codes, scales, 120)
+    qd = oracle.quantize_index_query(q)
+    kd = oracle.dequant_index(sc, ss)
+    score = [sum(float(w[h]) * max(0.0, float(qd[h] @ kd[r])) for h in range(32)) for r in range(15)]
+    want = sorted(sorted(range(15), key=lambda r: (-score[r], r))[:4])
+    got = oracle.hisa_blocks(q, w, sc, ss, 120, 4)
+    assert list(got) == want
+
+
 # ---------------------------------------------------------------- attention
 def _attn_inputs(seed, n_entries=40, S=160):
     g, (main, codes, scales) = _tiny_cache(seed, n_entries)
