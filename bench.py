@@ -662,6 +662,9 @@ def run_decode1m_e2e(args, torch, csa2, w):
 #              t = 131,072..139,263 over 69,632 entries, causal
 #   cachewrite cache write of 4 source layers (3 at m=2, 1 at m=1) over
 #              1,048,576 tokens each
+#   hisa131k   HISA decode (block-mean first stage, Reindex second stage) on
+#              the full131k cache, the HSI Full call timed beside it
+#   hisa1m     the same at batch 16 x 1,048,576 entries
 FP4_PER_BF16 = 13.5 / 2.25          # nominal dense fp4 : bf16 tensor ratio
 FP32_FMA_PER_SM_CLK = 128           # fp32 FMA lanes per SM and clock
 
@@ -782,6 +785,115 @@ def run_full131k(args, torch, csa2):
                  {"step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
                                "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
                   "clocks": clk.summary(), "gpu_launches": args.steps * 5})
+
+
+def _hisa_workload(args, torch, csa2, B, N, seed):
+    """HISA decode on a decoder source layer (m = 1), one query per sequence at
+    t = N - 1: the newest block's summary update, the first stage (summary
+    scan and top-2048 blocks) and the Reindex second stage with attention.
+    The HSI Full call on the same cache and queries is timed beside it."""
+    import synth
+    rank, world, local = dist_info()
+    dev = "cuda"
+    cache = csa2.Cache(B, N, 1, device=dev)
+    wts = _weights(torch, seed)
+    ones = torch.ones(D, device=dev)
+    rope = csa2.rope_table(N).to(dev)
+    ws_cw = csa2.Workspace(1 << 16, device=dev)
+    _write_cache(csa2, torch, cache, N, seed, (ones, ones, wts[2]), rope, ws_cw)
+    cache.n_entries.fill_(N)
+    assert ws_cw.sync_status()[0] == 0
+    del rope
+    nb = -(-N // 8)
+    store = csa2.BlockSummaries(cache, device=dev)
+    first0 = torch.zeros(B, dtype=torch.int64, device=dev)
+    build_ms = _events_ms(torch, lambda: csa2.block_summary(cache, store, first0, nb, ws_cw), 3)
+    q_pos = torch.full((B, 1), N - 1, dtype=torch.int64, device=dev)
+    newest = torch.full((B,), (N - 1) // 8, dtype=torch.int64, device=dev)
+    swa_base = torch.full((B,), N - WIN, dtype=torch.int64, device=dev)
+    q_idx = synth.torch_normal(seed * 10 + 1, (B, 1, HI, DI), torch.bfloat16, dev)
+    w_head = synth.torch_normal(seed * 10 + 2, (B, 1, HI), torch.float32, dev)
+    q = synth.torch_normal(seed * 10 + 3, (B, 1, H, D), torch.bfloat16, dev)
+    swa = synth.torch_swa_rows(seed * 10 + 4, (B, WIN), dev)
+    pool = torch.empty((B, 1, M_BLK), dtype=torch.int32, device=dev)
+    sel = torch.empty((B, 1, K_SEL), dtype=torch.int32, device=dev)
+    out = torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev)
+    ws_s = csa2.Workspace(1 << 16, device=dev)
+    ws_h = csa2.Workspace(csa2.hisa_blocks_workspace_size(B, 1, N), device=dev)
+    ws_r = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REINDEX, B, 1, N, M_BLK, K_SEL), device=dev)
+    common = dict(q_pos=q_pos, q=q.view(torch.int16), swa=swa.view(torch.int16), swa_base_pos=swa_base,
+                  scale=1 / math.sqrt(D), sel=sel, out=out.view(torch.int16), M=M_BLK, max_n=N,
+                  q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool)
+
+    def summary():
+        csa2.block_summary(cache, store, newest, 1, ws_s)
+
+    def stage1():
+        csa2.hisa_blocks(cache, store, q_idx.view(torch.int16), w_head, q_pos, N, M_BLK, pool, ws_h)
+
+    def stage2():
+        csa2.decode(csa2.MODE_REINDEX, cache, ws=ws_r, **common)
+
+    graph = _capture(torch, lambda: (summary(), stage1(), stage2()))
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms = _events_ms(torch, graph.replay, args.steps)
+    ms = max_over_ranks(ms, world)
+    for w in (ws_s, ws_h, ws_r):
+        assert w.sync_status()[0] == 0
+    reps = max(args.steps, 20)
+    parts = {}
+    for name, fn in (("summary_update", summary), ("stage1_blocks", stage1), ("stage2_reindex", stage2)):
+        g = _capture(torch, fn)
+        parts[name] = _graph_ms(torch, g, reps)
+    # the HSI Full call on the same cache and query, for comparison
+    ws_f = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_FULL, B, 1, N, M_BLK, K_SEL), device=dev)
+    g_full = _capture(torch, lambda: csa2.decode(csa2.MODE_FULL, cache, ws=ws_f, **common))
+    full_ms = _graph_ms(torch, g_full, reps)
+    # the summary scan alone: the index scan over the summary store read as a
+    # cache of nb rows (the view hisa_blocks builds on the device)
+    view = csa2.Cache.__new__(csa2.Cache)
+    view.B, view.cap, view.m = B, store.sum_cap, 1
+    view.main_kv, view.idx_codes, view.idx_scales = cache.main_kv, store.codes, store.scales
+    view.n_entries = torch.full((B,), nb, dtype=torch.int32, device=dev)
+    view_pos = torch.full((B, 1), nb - 1, dtype=torch.int64, device=dev)
+    scores = torch.empty((B, 1, nb), dtype=torch.float32, device=dev)
+    g_scan = _capture(torch, lambda: csa2.index_score(view, q_idx.view(torch.int16), w_head, view_pos, scores, nb,
+                                                      ws_s))
+    scan_ms = _graph_ms(torch, g_scan, reps)
+    assert ws_s.sync_status()[0] == 0
+    hbm, _, which = peaks()
+    scan_bytes = B * nb * (IDX_ENTRY + 4) + B * (HI * DI * 2 + HI * 4)
+    achieved = scan_bytes / (scan_ms / 1e3) / 1e9
+    per_query = (8 * IDX_ENTRY + IDX_ENTRY) + nb * (IDX_ENTRY + 4 + 4) + M_BLK * 4 + REINDEX_BYTES
+    kname = "index_score_tc_kernel<1>"
+    return _line(args, world, f"CSA2 HISA decode query-tokens/s/layer at {N // 1024}K ctx, batch {B}",
+                 "query-tokens/s", B * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 {"workload": f"HISA decode, m=1, {B} sequences x {N:,} entries, one query each: newest block "
+                              f"summary, top-{M_BLK} blocks by mean-key score, Reindex top-{K_SEL} over them, "
+                              f"attention",
+                  "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
+                  "l2": "inputs larger than L2 (the summary store and cache exceed 129 MB)",
+                  "launch": "one CUDA graph per step (summary update, view, summary scan, block selection, "
+                            "Reindex scan+select, attention)"},
+                 {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                  "traffic": None, "kernel": kname + " over the summary store",
+                  "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
+                 {"parts_ms": parts, "hsi_full_call_ms": full_ms, "summary_build_ms": build_ms,
+                  "step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
+                               "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
+                  "clocks": clk.summary(), "gpu_launches": args.steps * 6})
+
+
+def run_hisa131k(args, torch, csa2):
+    return _hisa_workload(args, torch, csa2, 64, 1 << 17, 2)
+
+
+def run_hisa1m(args, torch, csa2):
+    return _hisa_workload(args, torch, csa2, 16, 1 << 20, 3)
 
 
 def run_decoder1m(args, torch, csa2):
@@ -1140,7 +1252,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode1m",
-                    choices=["decode1m", "full131k", "prefill8k", "cachewrite", "decoder1m", "prefillblock"])
+                    choices=["decode1m", "full131k", "prefill8k", "cachewrite", "decoder1m", "prefillblock",
+                             "hisa131k", "hisa1m"])
     ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
@@ -1169,7 +1282,8 @@ def main():
     csa2.load()
     if args.workload != "decode1m":
         fn = {"full131k": run_full131k, "prefill8k": run_prefill8k, "cachewrite": run_cachewrite,
-              "decoder1m": run_decoder1m, "prefillblock": run_prefillblock}[args.workload]
+              "decoder1m": run_decoder1m, "prefillblock": run_prefillblock, "hisa131k": run_hisa131k,
+              "hisa1m": run_hisa1m}[args.workload]
         line = fn(args, torch, csa2)
         if rank == 0:
             print(json.dumps(line), flush=True)

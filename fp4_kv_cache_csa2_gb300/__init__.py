@@ -68,6 +68,10 @@ _SIGNATURES = {
     "csa2_attn_workspace_size": (_SZ, [_I, _I, _I]),
     "csa2_sparse_swa_attn": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I, _P, _P, _I, _P, _F, _P,
                                   _I, _I, _P, _SZ, _P]),
+    "csa2_block_summary": (_I, [ctypes.POINTER(CacheStruct), _P, _I64, _I, _P, _P, _I64, _P, _SZ, _P]),
+    "csa2_hisa_blocks_workspace_size": (_SZ, [_I, _I, _I64]),
+    "csa2_hisa_blocks": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I64, _P, _P, _P, _I, _I, _I64, _I, _P,
+                              _P, _SZ, _P]),
     "csa2_decode_workspace_size": (_SZ, [_I, _I, _I, _I64, _I, _I]),
     "csa2_decode": (_I, [ctypes.POINTER(CacheStruct), ctypes.POINTER(DecodeArgs), _P, _SZ, _P]),
 }
@@ -233,6 +237,41 @@ def sparse_swa_attn(cache: Cache, q, sel, swa, swa_base_pos, q_pos, scale: float
     _check("csa2_sparse_swa_attn", load().csa2_sparse_swa_attn(
         ctypes.byref(c), _ptr(q), _ptr(sel), K, _ptr(swa), _ptr(swa_base_pos), swa.shape[1], _ptr(q_pos),
         float(scale), _ptr(out), B, Q, ws.ptr, ws.nbytes, _stream(stream)))
+
+
+class BlockSummaries:
+    """HISA summary store of a cache: one MXFP4 key per block of 8 entries
+    (caller-owned tensors, [B][sum_cap][64] codes and [B][sum_cap][4] scales)."""
+
+    def __init__(self, cache: Cache, device="cuda"):
+        import torch
+        self.B = cache.B
+        rows = -(-cache.cap // BLOCK)                 # one row per block
+        self.sum_cap = -(-rows // BLOCK) * BLOCK      # the library needs sum_cap % 8 == 0
+        self.codes = torch.zeros((cache.B, self.sum_cap, INDEX_CODE_BYTES), dtype=torch.uint8, device=device)
+        self.scales = torch.zeros((cache.B, self.sum_cap, INDEX_SCALE_BYTES), dtype=torch.uint8, device=device)
+
+
+def block_summary(cache: Cache, summaries: BlockSummaries, first_block, n_blocks: int, ws: Workspace,
+                  stream=None):
+    """Recompute blocks first_block[b] .. first_block[b] + n_blocks - 1 of every sequence."""
+    c = cache.struct()
+    _check("csa2_block_summary", load().csa2_block_summary(
+        ctypes.byref(c), _ptr(first_block), n_blocks, cache.B, _ptr(summaries.codes), _ptr(summaries.scales),
+        summaries.sum_cap, ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def hisa_blocks_workspace_size(B: int, Q: int, max_n: int) -> int:
+    return load().csa2_hisa_blocks_workspace_size(B, Q, max_n)
+
+
+def hisa_blocks(cache: Cache, summaries: BlockSummaries, q_idx, w_head, q_pos, max_n: int, M: int, pool_blocks,
+                ws: Workspace, stream=None):
+    B, Q = q_pos.shape
+    c = cache.struct()
+    _check("csa2_hisa_blocks", load().csa2_hisa_blocks(
+        ctypes.byref(c), _ptr(summaries.codes), _ptr(summaries.scales), summaries.sum_cap, _ptr(q_idx),
+        _ptr(w_head), _ptr(q_pos), B, Q, max_n, M, _ptr(pool_blocks), ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def decode_workspace_size(mode: int, B: int, Q: int, max_n: int, M: int, K: int) -> int:

@@ -18,10 +18,10 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libcsa2.so")
 
-SOURCES = ["csa2_api.cu", "cache_write.cu", "index_score.cu", "reindex.cu", "topk.cu", "attention.cu"]
-# cache_write.cu keeps the binary32 order written in the source: no implicit
-# multiply-add contraction anywhere in that unit.
-EXTRA = {"cache_write.cu": ["-fmad=false"]}
+SOURCES = ["csa2_api.cu", "cache_write.cu", "index_score.cu", "reindex.cu", "topk.cu", "attention.cu", "hisa.cu"]
+# cache_write.cu and hisa.cu keep the binary32 order written in the source: no
+# implicit multiply-add contraction anywhere in those units.
+EXTRA = {"cache_write.cu": ["-fmad=false"], "hisa.cu": ["-fmad=false"]}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

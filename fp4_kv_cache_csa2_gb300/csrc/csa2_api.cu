@@ -298,6 +298,90 @@ csa2_status csa2_sparse_swa_attn(const csa2_cache* cache, const uint16_t* q, con
                       (cudaStream_t)stream);
 }
 
+csa2_status csa2_block_summary(const csa2_cache* cache, const int64_t* first_block, int64_t n_blocks, int B,
+                               uint8_t* sum_codes, uint8_t* sum_scales, int64_t sum_cap, void* ws, size_t ws_bytes,
+                               void* stream) {
+  csa2_status st = check_cache(cache);
+  if (st != CSA2_OK) return st;
+  if (B < 0 || n_blocks < 0 || sum_cap < 0) return CSA2_ERR_INVALID_ARG;
+  if ((sum_cap % BLK) != 0) return CSA2_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, HDR)) != CSA2_OK) return st;
+  if (B == 0 || n_blocks == 0) return CSA2_OK;
+  if (!first_block || !sum_codes || !sum_scales) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(sum_codes) || !aligned16(sum_scales)) return CSA2_ERR_INVALID_ARG;
+  HsParams p{};
+  p.idx_codes = cache->idx_codes;
+  p.idx_scales = cache->idx_scales;
+  p.cap = cache->cap;
+  p.n_entries = cache->n_entries;
+  p.first_block = first_block;
+  p.B = B;
+  p.n_blocks = n_blocks;
+  p.sum_codes = sum_codes;
+  p.sum_scales = sum_scales;
+  p.sum_cap = sum_cap;
+  p.hdr = header(ws);
+  return from_cuda(launch_block_summary(p, (cudaStream_t)stream));
+}
+
+size_t csa2_hisa_blocks_workspace_size(int B, int Q, int64_t max_n) {
+  if (B < 0 || Q < 0 || max_n < 0) return 0;
+  const int64_t nb = ceil_div(max_n, BLK);
+  return HDR + align256((size_t)B * Q * sizeof(int64_t)) + align256((size_t)B * sizeof(int32_t)) +
+         align256((size_t)B * Q * nb * sizeof(float)) + (long_rows(nb) ? align256(row_select_bytes((int64_t)B * Q)) : 0);
+}
+
+csa2_status csa2_hisa_blocks(const csa2_cache* cache, const uint8_t* sum_codes, const uint8_t* sum_scales,
+                             int64_t sum_cap, const uint16_t* q_idx, const float* w_head, const int64_t* q_pos,
+                             int B, int Q, int64_t max_n, int M, int32_t* pool_blocks, void* ws, size_t ws_bytes,
+                             void* stream) {
+  csa2_status st = check_cache(cache);
+  if (st != CSA2_OK) return st;
+  if ((st = check_q(B, Q)) != CSA2_OK) return st;
+  if (max_n < 0 || sum_cap < 0 || (sum_cap % BLK) != 0) return CSA2_ERR_INVALID_ARG;
+  if (M < 1 || M > CSA2_MAX_M) return CSA2_ERR_UNSUPPORTED;
+  if ((st = check_ws(ws, ws_bytes, csa2_hisa_blocks_workspace_size(B, Q, max_n))) != CSA2_OK) return st;
+  if (B == 0 || Q == 0) return CSA2_OK;
+  if (!sum_codes || !sum_scales || !q_idx || !w_head || !q_pos || !pool_blocks) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(sum_codes) || !aligned16(sum_scales) || !aligned16(q_idx)) return CSA2_ERR_INVALID_ARG;
+  // rows past the summary store cannot be scored
+  if (ceil_div(cache->cap, BLK) > sum_cap) return CSA2_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  WsHeader* hdr = header(ws);
+  unsigned char* cur = scratch(ws);
+  const int64_t nb = ceil_div(max_n, BLK);
+  HvParams vp{};
+  vp.q_pos = q_pos;
+  vp.n_entries = cache->n_entries;
+  vp.m = cache->m;
+  vp.B = B;
+  vp.Q = Q;
+  vp.cap = cache->cap;
+  vp.max_n = max_n;
+  vp.view_pos = reinterpret_cast<int64_t*>(cur);
+  cur += align256((size_t)B * Q * sizeof(int64_t));
+  vp.view_n = reinterpret_cast<int32_t*>(cur);
+  cur += align256((size_t)B * sizeof(int32_t));
+  float* scores = reinterpret_cast<float*>(cur);
+  cur += align256((size_t)B * Q * nb * sizeof(float));
+  st = from_cuda(launch_hisa_view(vp, s));
+  if (st != CSA2_OK) return st;
+  // the summary store read as an m = 1 cache of ceil(n / 8) rows per sequence
+  csa2_cache view{};
+  view.main_kv = cache->main_kv;
+  view.idx_codes = const_cast<uint8_t*>(sum_codes);
+  view.idx_scales = const_cast<uint8_t*>(sum_scales);
+  view.cap = sum_cap;
+  view.n_entries = vp.view_n;
+  view.m = 1;
+  st = do_index_score(&view, q_idx, w_head, vp.view_pos, nullptr, M, scores, B, Q, nb, hdr, s);
+  if (st != CSA2_OK) return st;
+  if (long_rows(nb))
+    return from_cuda(launch_row_select(scores, vp.view_pos, vp.view_n, 1, B, Q, nb, M, pool_blocks, 0, nullptr,
+                                       cur, s));
+  return from_cuda(launch_select_topk(scores, vp.view_pos, vp.view_n, 1, nullptr, M, M, pool_blocks, B, Q, nb, s));
+}
+
 size_t csa2_decode_workspace_size(csa2_mode mode, int B, int Q, int64_t max_n, int M, int K) {
   if (B < 0 || Q < 0 || max_n < 0 || M < 0 || K < 0) return 0;
   size_t need = HDR + align256(attn_partials_bytes((int64_t)B * Q, K));

@@ -63,6 +63,29 @@ struct AttnParams {
   WsHeader* hdr;
 };
 
+struct HsParams {             // HISA block summaries
+  const uint8_t* idx_codes;
+  const uint8_t* idx_scales;
+  int64_t cap;
+  const int32_t* n_entries;
+  const int64_t* first_block; // [B]
+  int B;
+  int64_t n_blocks;           // blocks per sequence from first_block
+  uint8_t* sum_codes;         // [B][sum_cap][64]
+  uint8_t* sum_scales;        // [B][sum_cap][4]
+  int64_t sum_cap;
+  WsHeader* hdr;
+};
+
+struct HvParams {             // HISA view of the summary store as an m = 1 cache
+  const int64_t* q_pos;       // [B][Q]
+  const int32_t* n_entries;   // [B]
+  int m, B, Q;
+  int64_t cap, max_n;
+  int64_t* view_pos;          // [B][Q] out
+  int32_t* view_n;            // [B] out
+};
+
 cudaError_t launch_cache_write(const CwParams& p, cudaStream_t stream, int num_sms);
 cudaError_t launch_index_score(IsParams p, cudaStream_t stream);
 cudaError_t launch_reindex_select(IsParams p, cudaStream_t stream);
@@ -81,5 +104,7 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
                               cudaStream_t stream);
 cudaError_t launch_attention(AttnParams p, int B, float* partials, cudaStream_t stream);
 size_t attn_partials_bytes(int64_t BQ, int K);
+cudaError_t launch_block_summary(const HsParams& p, cudaStream_t stream);
+cudaError_t launch_hisa_view(const HvParams& p, cudaStream_t stream);
 
 }  // namespace csa2

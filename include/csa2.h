@@ -256,6 +256,50 @@ csa2_status csa2_sparse_swa_attn(const csa2_cache *cache, const uint16_t *q, con
                                  int B, int Q, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * HISA block summaries.  [zartbot §2.3.4, the HISA paragraph: each block of
+ * consecutive positions keeps the mean of its indexer keys, and a decode step
+ * updates only the newest block]
+ * Block r of sequence b covers entries [8r, min(8r + 8, n)), n =
+ * min(n_entries[b], cap).  Its summary key is the mean of the entries'
+ * dequantised index keys, computed in binary32 (the keys, exact in binary32,
+ * added in entry order starting from +0, then one correctly rounded division
+ * by the number of entries), stored as MXFP4 by the index-K rule.
+ *   first_block  device int64 [B]: first block to compute per sequence.
+ *   n_blocks     blocks computed per sequence: first_block[b] .. + n_blocks - 1.
+ *   sum_codes    out [B][sum_cap][64], sum_scales out [B][sum_cap][4]: the
+ *                summary of block r in row r (same format as idx_codes and
+ *                idx_scales); both 16-byte aligned.
+ *   sum_cap      rows per sequence, a multiple of 8, >= ceil(cap / 8).
+ * Blocks with no entry (8r >= n, or r < 0) are skipped and not written; a
+ * block r >= sum_cap, or n_entries[b] > cap, raises CSA2_ERR_BOUNDS in the
+ * status word.  Needs only the workspace header.
+ */
+csa2_status csa2_block_summary(const csa2_cache *cache, const int64_t *first_block, int64_t n_blocks, int B,
+                               uint8_t *sum_codes, uint8_t *sum_scales, int64_t sum_cap, void *ws,
+                               size_t ws_bytes, void *stream);
+
+/*
+ * HISA candidate blocks (first stage).  Every block holding a visible entry
+ * (r < ceil(nv / 8), nv = the query's visible entries, at most max_n) is
+ * scored on its summary key with the indexer score of csa2_index_score, and
+ * the M best blocks by (score desc, block id asc) are kept; no block is forced
+ * in.  The second stage is a Reindex call (csa2_decode, mode REINDEX) given
+ * these blocks as its pool.  [zartbot §2.3.4, the HISA paragraph]
+ *   sum_codes, sum_scales, sum_cap  the summary store of csa2_block_summary,
+ *                up to date for every visible block.
+ *   q_idx, w_head, q_pos  as in csa2_index_score.
+ *   pool_blocks  out int32 [B][Q][M]: chosen block ids ascending, -1 padded.
+ * Workspace: csa2_hisa_blocks_workspace_size (per-query summary scores and,
+ * when ceil(max_n / 8) > 16384, the long-row selection lists).
+ * Errors: INVALID_ARG when sum_cap < ceil(cap / 8).
+ */
+size_t csa2_hisa_blocks_workspace_size(int B, int Q, int64_t max_n);
+csa2_status csa2_hisa_blocks(const csa2_cache *cache, const uint8_t *sum_codes, const uint8_t *sum_scales,
+                             int64_t sum_cap, const uint16_t *q_idx, const float *w_head, const int64_t *q_pos,
+                             int B, int Q, int64_t max_n, int M, int32_t *pool_blocks, void *ws,
+                             size_t ws_bytes, void *stream);
+
+/*
  * One decode (or prefill-chunk) call of a CSA2 layer in a given mode.
  * [zartbot §3.2 access table; dilfish §4.3]
  *   Full:    scores every visible entry with q_idx/w_head, writes pool_blocks

@@ -14,6 +14,9 @@ Distributions (one seed per workload):
   * head weights       N(0,1) float32, [.., 32]
   * main queries       N(0,1) bf16, [.., 64 heads, 512]
   * SWA rows           N(0,1) rows scaled to unit root-mean-square, then bf16
+  * index-key bytes    for tests that need a long index cache without the
+                       cache write: uniform code bytes (every E2M1 nibble
+                       equally likely) and E8M0 scale bytes uniform in 121..127
 
 All bf16 tensors are returned as ``uint16`` bit patterns so that both sides
 consume byte-identical inputs.
@@ -90,6 +93,14 @@ def swa_rows(g: np.random.Generator, *shape: int) -> np.ndarray:
     z = g.standard_normal((*shape, D_LATENT))
     z = z / np.sqrt(np.mean(z * z, axis=-1, keepdims=True))
     return f32_to_bf16_bits(z.astype(np.float32))
+
+
+def index_key_bytes(g: np.random.Generator, *shape: int) -> tuple[np.ndarray, np.ndarray]:
+    """Random MXFP4 index keys as stored bytes: codes uint8 [..., 64] and
+    scales uint8 [..., 4]."""
+    codes = g.integers(0, 256, size=(*shape, D_INDEX // 2), dtype=np.uint8)
+    scales = g.integers(121, 128, size=(*shape, D_INDEX // 32), dtype=np.uint8)
+    return codes, scales
 
 
 # ---------------------------------------------------------------- device side
