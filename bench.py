@@ -853,6 +853,20 @@ def _hisa_workload(args, torch, csa2, B, N, seed):
     ws_f = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_FULL, B, 1, N, M_BLK, K_SEL), device=dev)
     g_full = _capture(torch, lambda: csa2.decode(csa2.MODE_FULL, cache, ws=ws_f, **common))
     full_ms = _graph_ms(torch, g_full, reps)
+    # pool recall: the share of the Full call's top-512 (the exact top-K over
+    # every visible entry) whose block is in the HISA pool, and in the HSI pool
+    sel_f, pool_f = torch.empty_like(sel), torch.empty_like(pool)
+    csa2.decode(csa2.MODE_FULL, cache, ws=ws_f, **dict(common, sel=sel_f, pool_blocks=pool_f))
+    stage1()
+    torch.cuda.synchronize()
+    recall = {}
+    for name, pb in (("hisa", pool), ("hsi", pool_f)):
+        hit = tot = 0
+        for b in range(B):
+            ids = sel_f[b, 0][sel_f[b, 0] >= 0]
+            hit += int(torch.isin(torch.div(ids, 8, rounding_mode="floor"), pb[b, 0]).sum())
+            tot += int(ids.numel())
+        recall[name] = hit / max(tot, 1)
     # the summary scan alone: the index scan over the summary store read as a
     # cache of nb rows (the view hisa_blocks builds on the device)
     view = csa2.Cache.__new__(csa2.Cache)
@@ -880,12 +894,15 @@ def _hisa_workload(args, torch, csa2, B, N, seed):
                   "launch": "one CUDA graph per step (summary update, view, summary scan, block selection, "
                             "Reindex scan+select, attention)"},
                  {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                  "traffic": None, "kernel": kname + " over the summary store",
+                  "traffic": ncu_traffic(f"{kname}:summaries_{B}x{nb}"), "kernel": kname + " over the summary store",
                   "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
                  {"parts_ms": parts, "hsi_full_call_ms": full_ms, "summary_build_ms": build_ms,
+                  "pool_recall_of_exact_top512": recall,
                   "step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
                                "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
-                  "clocks": clk.summary(), "gpu_launches": args.steps * 6})
+                  "clocks": clk.summary(),
+                  # summary, view, scan, 3 selection kernels (rows over 4,096 blocks), Reindex, attention
+                  "gpu_launches": args.steps * 8})
 
 
 def run_hisa131k(args, torch, csa2):

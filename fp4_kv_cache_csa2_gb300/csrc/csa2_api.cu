@@ -324,11 +324,18 @@ csa2_status csa2_block_summary(const csa2_cache* cache, const int64_t* first_blo
   return from_cuda(launch_block_summary(p, (cudaStream_t)stream));
 }
 
+// HISA keeps up to 2048 of its summary rows: past 4096 blocks a row goes to
+// the multi-CTA selection (a single CTA spends most of its time on the
+// output once M is a large part of the row)
+constexpr int64_t HISA_ROW_SELECT_MIN = 4096;
+bool hisa_long_rows(int64_t nb) { return nb > HISA_ROW_SELECT_MIN; }
+
 size_t csa2_hisa_blocks_workspace_size(int B, int Q, int64_t max_n) {
   if (B < 0 || Q < 0 || max_n < 0) return 0;
   const int64_t nb = ceil_div(max_n, BLK);
   return HDR + align256((size_t)B * Q * sizeof(int64_t)) + align256((size_t)B * sizeof(int32_t)) +
-         align256((size_t)B * Q * nb * sizeof(float)) + (long_rows(nb) ? align256(row_select_bytes((int64_t)B * Q)) : 0);
+         align256((size_t)B * Q * nb * sizeof(float)) +
+         (hisa_long_rows(nb) ? align256(row_select_bytes((int64_t)B * Q)) : 0);
 }
 
 csa2_status csa2_hisa_blocks(const csa2_cache* cache, const uint8_t* sum_codes, const uint8_t* sum_scales,
@@ -376,7 +383,7 @@ csa2_status csa2_hisa_blocks(const csa2_cache* cache, const uint8_t* sum_codes, 
   view.m = 1;
   st = do_index_score(&view, q_idx, w_head, vp.view_pos, nullptr, M, scores, B, Q, nb, hdr, s);
   if (st != CSA2_OK) return st;
-  if (long_rows(nb))
+  if (hisa_long_rows(nb))
     return from_cuda(launch_row_select(scores, vp.view_pos, vp.view_n, 1, B, Q, nb, M, pool_blocks, 0, nullptr,
                                        cur, s));
   return from_cuda(launch_select_topk(scores, vp.view_pos, vp.view_n, 1, nullptr, M, M, pool_blocks, B, Q, nb, s));

@@ -290,7 +290,7 @@ csa2_status csa2_block_summary(const csa2_cache *cache, const int64_t *first_blo
  *   q_idx, w_head, q_pos  as in csa2_index_score.
  *   pool_blocks  out int32 [B][Q][M]: chosen block ids ascending, -1 padded.
  * Workspace: csa2_hisa_blocks_workspace_size (per-query summary scores and,
- * when ceil(max_n / 8) > 16384, the long-row selection lists).
+ * when ceil(max_n / 8) > 4096, the long-row selection lists).
  * Errors: INVALID_ARG when sum_cap < ceil(cap / 8).
  */
 size_t csa2_hisa_blocks_workspace_size(int B, int Q, int64_t max_n);

@@ -170,8 +170,9 @@ def test_hisa_blocks_match_oracle(csa2, M):
 
 
 def test_hisa_blocks_long_rows_match_oracle(csa2):
-    """Summary rows longer than 16,384 blocks (over 131,072 entries) take the
-    multi-CTA row selection; m = 2 visibility."""
+    """Summary rows longer than 4,096 blocks (over 32,768 entries) take the
+    multi-CTA row selection; m = 2 visibility, rows of 20,001 and 17,501
+    blocks."""
     B, Q, n, M = 1, 3, 8 * 20000 + 3, 2048
     cache, codes, scales, g = _random_cache(csa2, B, n, seed=760, m=2)
     q_pos = np.array([[2 * n - 1, 2 * n - 6, 2 * 140000 + 1]], np.int64)
