@@ -19,6 +19,8 @@ What it computes (plain, slow, in the order the pages state it):
                      the candidate pool only; order (score desc, index asc)
   attention       -> ``attention``: one softmax over [selected main-KV entries ||
                      SWA window], K = V = the shared 512-d latent, binary64
+  FP8 window      -> ``swa_fp8_quantize`` (every window value to E4M3 on its own);
+                     ``attention`` takes such rows (uint8) in place of bf16 rows
   modes           -> ``decode``: Full / Reindex / Reuse composition
 
 Sources (web pages about DeepSeek-V4.1-Flash):
@@ -314,6 +316,20 @@ def select_topk(scores: np.ndarray, domain: np.ndarray, K: int) -> np.ndarray:
 
 
 # ------------------------------------------------------------ attention
+def swa_fp8_quantize(swa_bits: np.ndarray) -> np.ndarray:
+    """FP8 SWA rows: every bf16 window value rounded to E4M3 on its own (nearest,
+    ties to the even code, saturating at +-448, no scale factor).  The pages say
+    only that the quantisation-sensitive SWA KV keeps FP8 precision while the
+    main KV drops to FP4; E4M3 covers the latent's range (RMS 1 after the norm,
+    largest values near 10) without a scale.  [zartbot §2.4.4; sarnas, the FP4
+    cache paragraph]  bf16 bits [..., 512] -> uint8 [..., 512]."""
+    v = bf16_to_f64(np.asarray(swa_bits)).astype(np.float32)         # exact
+    out = np.zeros(v.shape, np.uint8)
+    v = np.ascontiguousarray(v)
+    native.lib().oracle_e4m3_encode_rows(ptr(v), v.size, ptr(out))
+    return out
+
+
 def window_positions(t: int) -> np.ndarray:
     """Raw positions of the SWA window of a query at raw position t (self included)."""
     return np.arange(max(0, int(t) - WINDOW + 1), int(t) + 1)
@@ -325,7 +341,8 @@ def attention(q: np.ndarray, sel: np.ndarray, main_kv: np.ndarray, swa: np.ndarr
 
     Keys and values are the same vectors (K = V = the shared latent): the
     dequantised main-KV entries listed in ``sel`` (ids >= 0) followed by the SWA
-    rows of the window [max(0, t-127), t] (row = position - swa_base).  One
+    rows of the window [max(0, t-127), t] (row = position - swa_base): bf16 bits
+    (uint16) or FP8 rows from ``swa_fp8_quantize`` (uint8, E4M3 values).  One
     softmax of scale * q_h . v_i over all of them; o_h = sum_i p_hi v_i.
     q bf16 bits [64, 512]; returns binary64 [64, 512].  [zartbot §3.3.2 readout
     of SWA and selected main KV in one sparse attention; §3.3.2.1 key = value]
@@ -334,7 +351,7 @@ def attention(q: np.ndarray, sel: np.ndarray, main_kv: np.ndarray, swa: np.ndarr
     ids = ids[ids >= 0].astype(np.int64)
     keys = [dequant_main(main_kv[ids])] if len(ids) else []
     rows = window_positions(t) - int(swa_base)
-    keys.append(bf16_to_f64(swa[rows]))
+    keys.append(_E4M3[swa[rows]] if swa.dtype == np.uint8 else bf16_to_f64(swa[rows]))
     V = np.concatenate(keys, axis=0)                    # [n_keys, 512]
     qd = bf16_to_f64(q)                                 # [64, 512]
     logits = (qd @ V.T) * scale                         # [64, n_keys]

@@ -113,6 +113,11 @@ uint8_t oracle_e4m3_encode(float v) {
     return (uint8_t)(sign | best);
 }
 
+/* FP8 SWA rows: n binary32 values -> n E4M3 bytes, each on its own (no scale). */
+void oracle_e4m3_encode_rows(const float *v, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_encode(v[i]);
+}
+
 /* ------------------------------------------------------- group quantisers */
 
 /* Main KV group (R4): 16 binary32 values -> 8 code bytes + 1 E4M3 scale. */

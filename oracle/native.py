@@ -58,6 +58,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
     L.oracle_fp4_group_quantize.restype = None
     L.oracle_fp4_group_quantize.argtypes = [_P, _P, _P]
+    L.oracle_e4m3_encode_rows.restype = None
+    L.oracle_e4m3_encode_rows.argtypes = [_P, _I64, _P]
     L.oracle_mxfp4_block_quantize.restype = None
     L.oracle_mxfp4_block_quantize.argtypes = [_P, _P, _P]
     L.oracle_mxfp4_rows.restype = None

@@ -556,6 +556,57 @@ def test_attention_single_and_identical_keys():
     np.testing.assert_allclose(out, np.broadcast_to(v, out.shape), rtol=1e-12)
 
 
+# ---------------------------------------------------------------- FP8 window
+def test_swa_fp8_keeps_every_e4m3_value():
+    """Every finite E4M3 value is a bf16 value; quantising it returns its own
+    code (both zeros included)."""
+    vals = oracle.e4m3_values()
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    bits = synth.f32_to_bf16_bits(vals[codes].astype(np.float32))
+    assert np.array_equal(synth.bf16_bits_to_f32(bits).astype(np.float64), vals[codes])
+    np.testing.assert_array_equal(oracle.swa_fp8_quantize(bits), codes)
+
+
+def test_swa_fp8_rounds_to_nearest_and_saturates():
+    """Brute force over bf16 values spanning the E4M3 range: the chosen code is
+    a nearest finite value (ties to the even code), signs kept, |x| >= 448 ->
+    448; the row shape is kept."""
+    g = np.random.default_rng(31)
+    x = np.concatenate([g.standard_normal(3000) * 4.0, g.uniform(-600, 600, 500),
+                        2.0 ** g.uniform(-12, -6, 500) * g.choice([-1, 1], 500)]).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(x)[:4000].reshape(8, 500)
+    got = oracle.swa_fp8_quantize(bits)
+    assert got.shape == (8, 500)
+    vals = oracle.e4m3_values()
+    finite = np.array([c for c in range(128) if c != 0x7F])
+    for b, c in zip(bits.ravel(), got.ravel()):
+        v = float(synth.bf16_bits_to_f32(np.array([b], np.uint16))[0])
+        a = abs(v)
+        if a >= 448:
+            assert vals[c] == math.copysign(448.0, v)
+            continue
+        d = np.abs(vals[finite] - a)
+        best = finite[d == d.min()]
+        want = best[0] if len(best) == 1 else [k for k in best if k % 2 == 0][0]
+        assert (c & 0x7F) == want and (vals[c] == 0 or math.copysign(1, vals[c]) == math.copysign(1, v))
+
+
+def test_attention_fp8_window_is_attention_over_its_values():
+    """FP8 rows enter the softmax as their E4M3 values: the same attention as
+    bf16 rows holding those values (E4M3 is a subset of bf16), and not the
+    attention over the unrounded rows."""
+    g, main, q, swa = _attn_inputs(18, 30, 300)
+    sel = np.arange(1, 30, 4).astype(np.int32)
+    t, base = 250, 50
+    fp8 = oracle.swa_fp8_quantize(swa)
+    as_bf16 = synth.f32_to_bf16_bits(oracle.e4m3_values()[fp8].astype(np.float32))
+    a = oracle.attention(q, sel, main, fp8, base, t, 1 / math.sqrt(512))
+    b = oracle.attention(q, sel, main, as_bf16, base, t, 1 / math.sqrt(512))
+    c = oracle.attention(q, sel, main, swa, base, t, 1 / math.sqrt(512))
+    np.testing.assert_array_equal(a, b)
+    assert np.abs(a - c).max() > 1e-6
+
+
 # ---------------------------------------------------------------- modes
 def test_modes_reuse_equals_full_attention_and_reindex_all_blocks():
     g = synth.rng(18)
