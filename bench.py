@@ -165,9 +165,10 @@ def max_over_ranks(x: float, world: int) -> float:
 class Decode1M:
     """Reindex + 3 Reuse at 1,048,576 entries, batch 16, R pipelined instances."""
 
-    def __init__(self, csa2, torch, B=16, N=1 << 20, d=3, seed=3, lanes=2, packed=True):
+    def __init__(self, csa2, torch, B=16, N=1 << 20, d=3, seed=3, lanes=2, packed=True, swa_fp8=False):
         import synth
         self.csa2, self.torch = csa2, torch
+        self.swa_fp8 = swa_fp8
         self.B, self.N, self.d = B, N, d
         self.R = 3 * d + 1
         dev = "cuda"
@@ -230,6 +231,10 @@ class Decode1M:
                 # the selected entries packed by the Reindex call, read by the Reuse calls
                 "packed": torch.empty((B, 1, K, MAIN_ENTRY), dtype=torch.uint8, device=dev) if packed else None,
             }
+            if swa_fp8:          # the window rows stored as E4M3, quantised once
+                inst["swa8"] = [torch.empty((B, WIN, D), dtype=torch.uint8, device=dev) for _ in range(4)]
+                for l in range(4):
+                    csa2.swa_quantize_fp8(inst["swa"][l].view(torch.int16), inst["swa8"][l])
             self.inst.append(inst)
         # one workspace per layer slot: the four layer calls of a step may run at once
         # lanes per layer slot (stream + workspace), taken by step number modulo the
@@ -258,10 +263,11 @@ class Decode1M:
     def layer(self, layer: int, r: int, lane: int = 0):
         csa2, inst, torch = self.csa2, self.inst[r], self.torch
         mode = csa2.MODE_REINDEX if layer == 0 else csa2.MODE_REUSE
+        swa = inst["swa8"][layer] if self.swa_fp8 else inst["swa"][layer].view(torch.int16)
         csa2.decode(mode, self.caches[r], q_pos=self.q_pos, q=inst["q"][layer].view(torch.int16),
-                    swa=inst["swa"][layer].view(torch.int16), swa_base_pos=self.swa_base, scale=1 / math.sqrt(D),
+                    swa=swa, swa_base_pos=self.swa_base, scale=1 / math.sqrt(D),
                     sel=inst["sel"], out=inst["out"][layer].view(torch.int16), ws=self.ws[layer][lane], M=M_BLK,
-                    max_n=self.N, packed_sel=inst["packed"],
+                    max_n=self.N, packed_sel=inst["packed"], swa_fp8=self.swa_fp8,
                     q_idx=inst["q_idx"].view(torch.int16), w_head=inst["w_head"], pool_blocks=self.pool)
 
     def check_status(self):
@@ -402,8 +408,9 @@ def _graph_ms(torch, graph, reps):
 
 def run_decode1m(args, torch, csa2):
     rank, world, local = dist_info()
+    fp8 = args.swa_format == "fp8"
     w = Decode1M(csa2, torch, N=args.seq_len, d=args.pipeline_distance, lanes=args.lanes,
-                 packed=bool(args.packed_selection))
+                 packed=bool(args.packed_selection), swa_fp8=fp8)
     w.prologue()
     torch.cuda.synchronize()
     # graphs per pipeline phase and per cycle of R phases: step s only depends on s mod R
@@ -448,18 +455,20 @@ def run_decode1m(args, torch, csa2):
     qtl_per_step = w.B * 4
     value = qtl_per_step * world / (ms_step / 1e3)
     hbm, bf16, which = peaks()
-    bytes_step = w.B * CHAIN_BYTES
+    win_saved = WIN * D if fp8 else 0                  # an E4M3 window row is 512 B, a bf16 one 1 KB
+    bytes_step = w.B * (CHAIN_BYTES - 4 * win_saved)
     dom_is_reuse = 3 * reuse_ms >= reindex_ms          # Reuse calls are 3 of the 4 layers
     dom_ms = reuse_ms if dom_is_reuse else reindex_ms
-    dom_bytes = w.B * (REUSE_BYTES if dom_is_reuse else REINDEX_BYTES)
+    dom_bytes = w.B * ((REUSE_BYTES if dom_is_reuse else REINDEX_BYTES) - win_saved)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     dom_kernel = "attn_tc_kernel" if dom_is_reuse else "reindex_select_kernel"
-    traffic = ncu_traffic(dom_kernel) if w.N == 1 << 20 else None
-    e2e = run_decode1m_e2e(args, torch, csa2, w)
+    traffic = ncu_traffic(dom_kernel) if w.N == 1 << 20 and not fp8 else None
+    e2e = None if fp8 else run_decode1m_e2e(args, torch, csa2, w)
     return {
         "value": value, "ms_per_step": ms_step, "dtype": "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
         "config": {"workload": f"decode Reindex + 3 Reuse, {w.N:,} entries/seq, batch 16 per layer call",
                    "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
+                   "window_rows": "E4M3, 512 B per row" if fp8 else "bf16, 1 KB per row",
                    "l2": f"inputs larger than L2: {w.R} pipelined instances x "
                          f"{w.B * w.N * (MAIN_ENTRY + IDX_ENTRY) / 1e9:.2f} GB, layer distance {w.d} steps",
                    "launch": f"CUDA graphs of {w.R * max(1, args.graph_cycles)} consecutive steps "
@@ -1278,6 +1287,9 @@ def main():
                     help="decode: the Reindex call packs its selected entries for the Reuse calls (1) or not (0)")
     ap.add_argument("--lanes", type=int, default=5,
                     help="decode: stream + workspace lanes per layer slot")
+    ap.add_argument("--swa-format", default="bf16", choices=["bf16", "fp8"],
+                    help="decode: window rows as bf16 (the configuration) or E4M3 (the pages' FP8 window); "
+                         "fp8 reports no end-to-end figure")
     ap.add_argument("--graph-cycles", type=int, default=1,
                     help="decode: pipeline cycles (of 3 d + 1 steps) per replayed CUDA graph")
     args = ap.parse_args()

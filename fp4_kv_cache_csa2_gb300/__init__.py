@@ -45,7 +45,8 @@ class DecodeArgs(ctypes.Structure):
                 ("q_pos", ctypes.c_void_p), ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
                 ("w_head", ctypes.c_void_p), ("swa", ctypes.c_void_p),
                 ("swa_base_pos", ctypes.c_void_p), ("pool_blocks", ctypes.c_void_p),
-                ("sel", ctypes.c_void_p), ("out", ctypes.c_void_p), ("packed_sel", ctypes.c_void_p)]
+                ("sel", ctypes.c_void_p), ("out", ctypes.c_void_p), ("packed_sel", ctypes.c_void_p),
+                ("swa_fp8", ctypes.c_int32)]
 
 
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -68,6 +69,7 @@ _SIGNATURES = {
     "csa2_attn_workspace_size": (_SZ, [_I, _I, _I]),
     "csa2_sparse_swa_attn": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I, _P, _P, _I, _P, _F, _P,
                                   _I, _I, _P, _SZ, _P]),
+    "csa2_swa_quantize_fp8": (_I, [_P, _I64, _P, _P]),
     "csa2_block_summary": (_I, [ctypes.POINTER(CacheStruct), _P, _I64, _I, _P, _P, _I64, _P, _SZ, _P]),
     "csa2_hisa_blocks_workspace_size": (_SZ, [_I, _I, _I64]),
     "csa2_hisa_blocks": (_I, [ctypes.POINTER(CacheStruct), _P, _P, _I64, _P, _P, _P, _I, _I, _I64, _I, _P,
@@ -261,6 +263,13 @@ def block_summary(cache: Cache, summaries: BlockSummaries, first_block, n_blocks
         summaries.sum_cap, ws.ptr, ws.nbytes, _stream(stream)))
 
 
+def swa_quantize_fp8(x, out, stream=None):
+    """FP8 window rows: out (uint8 [..., 512]) = E4M3 of x (bf16 as int16, same shape)."""
+    n_rows = x.numel() // D_LATENT
+    assert out.numel() == x.numel()
+    _check("csa2_swa_quantize_fp8", load().csa2_swa_quantize_fp8(_ptr(x), n_rows, _ptr(out), _stream(stream)))
+
+
 def hisa_blocks_workspace_size(B: int, Q: int, max_n: int) -> int:
     return load().csa2_hisa_blocks_workspace_size(B, Q, max_n)
 
@@ -280,11 +289,13 @@ def decode_workspace_size(mode: int, B: int, Q: int, max_n: int, M: int, K: int)
 
 def decode(mode: int, cache: Cache, *, q_pos, q, swa, swa_base_pos, scale: float, sel, out,
            ws: Workspace, M: int = 0, max_n: int = 0, q_idx=None, w_head=None, pool_blocks=None,
-           packed_sel=None, stream=None):
+           packed_sel=None, swa_fp8: bool = False, stream=None):
+    """swa: bf16 rows [B][S][512] (as int16), or with swa_fp8 the uint8 rows of
+    swa_quantize_fp8."""
     B, Q = q_pos.shape
     a = DecodeArgs(mode, B, Q, M, sel.shape[-1], swa.shape[1], max_n, float(scale), _ptr(q_pos),
                    _ptr(q), _ptr(q_idx), _ptr(w_head), _ptr(swa), _ptr(swa_base_pos),
-                   _ptr(pool_blocks), _ptr(sel), _ptr(out), _ptr(packed_sel))
+                   _ptr(pool_blocks), _ptr(sel), _ptr(out), _ptr(packed_sel), 1 if swa_fp8 else 0)
     c = cache.struct()
     _check("csa2_decode", load().csa2_decode(ctypes.byref(c), ctypes.byref(a), ws.ptr, ws.nbytes,
                                              _stream(stream)))

@@ -13,7 +13,10 @@
 // positions.  In every CTA:
 //   * Q (64 heads x 512, bf16) lands by TMA in 8 SW128 column chunks;
 //   * keys land in shared memory as bf16 [128 keys][512] in 8 SW128 column
-//     chunks of 64 dims: window rows by 2-D TMA straight from the bf16 window;
+//     chunks of 64 dims: window rows by 2-D TMA straight from the bf16 window
+//     (FP8 window: 64-byte column slices of the E4M3 rows land in the upper
+//     half of each chunk and every thread widens its row half to bf16 in place,
+//     exactly, two chunks per CTA barrier);
 //     selected FP4 entries by 16-byte asynchronous copies into a staging
 //     buffer (consecutive threads take consecutive pieces of an entry), from
 //     there into registers, two lanes per entry, after which Q chunks 4..7 are
@@ -128,6 +131,17 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t out[4]) {
   out[3] = prmt(l1, h1, 0x7362u);
 }
 
+// Two E4M3 bytes (element 0 in bits 0..7) -> one bf16x2 word (element 0 in the
+// low half).  Exact: every E4M3 value is an f16 and a bf16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  uint32_t h2;
+  asm("{ .reg .b16 lo16, hi16; mov.b32 {lo16, hi16}, %1; cvt.rn.f16x2.e4m3x2 %0, lo16; }" : "=r"(h2) : "r"(two));
+  float lo, hi;
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
+      : "=f"(lo), "=f"(hi) : "r"(h2));
+  return pack_bf16x2(lo, hi);
+}
+
 // byte offset of (row, byte) in a 1 KB-aligned SW128 region of 128-byte rows
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte) {
   return row * 128u + ((((byte >> 4) ^ (row & 7u)) << 4) | (byte & 15u));
@@ -226,9 +240,15 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   if (tid == 0) {
     if (window_cta) {
       if (p.S > 0) {         // rows outside this sequence's window are masked (kvalid == 0) but finite
-        tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * AT_CHUNK_BYTES);
         const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
-        for (int c = 0; c < 8; c++) tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.bar_kv);
+        if (p.swa_fp8) {     // [128 rows][64 B] E4M3 slices into the upper half of each chunk
+          tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * (AT_CHUNK_BYTES / 2));
+          for (int c = 0; c < 8; c++)
+            tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES + AT_CHUNK_BYTES / 2, &map_swa, c * 64, row0, &sm.bar_kv);
+        } else {
+          tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * AT_CHUNK_BYTES);
+          for (int c = 0; c < 8; c++) tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.bar_kv);
+        }
       } else {
         tc::bar_arrive_expect_tx(&sm.bar_kv, 0u);
       }
@@ -333,6 +353,40 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
   } else if (p.S == 0) {                                   // no window rows supplied: zero keys
     for (int i = tid; i < 8 * AT_CHUNK_BYTES / 16; i += AT_THREADS)
       reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0, 0, 0, 0);
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+  } else if (p.swa_fp8) {
+    // FP8 window: thread (r, h) takes row r = tid / 2, dims 32h .. 32h+31 of
+    // each chunk (32 E4M3 bytes at 8 KB + 64 r + 32 h), widens them to four
+    // 16-byte bf16 units (unit 4h + j = dims 8(4h + j) ..) and stores them at
+    // their SW128 places in the same chunk; every thread reads a pair of chunks
+    // before any thread overwrites it
+    at_wait(&sm.bar_kv, 0, sm, p.hdr, 20);
+    const int r = tid >> 1, h = tid & 1;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 8; c0 += 2) {
+      uint4 raw[2][2];
+#pragma unroll
+      for (int i = 0; i < 2; i++) {
+        const uint4* src = reinterpret_cast<const uint4*>(kbuf + (c0 + i) * AT_CHUNK_BYTES + AT_CHUNK_BYTES / 2 +
+                                                          r * 64 + h * 32);
+        raw[i][0] = src[0];
+        raw[i][1] = src[1];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 2; i++) {
+        unsigned char* dst = kbuf + (c0 + i) * AT_CHUNK_BYTES;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          const uint4& w = raw[i][j >> 1];
+          const uint32_t lo = (j & 1) ? w.z : w.x, hi = (j & 1) ? w.w : w.y;   // bytes 8j .. 8j+7
+          const uint4 o = make_uint4(e4m3x2_to_bf16x2(lo & 0xFFFFu), e4m3x2_to_bf16x2(lo >> 16),
+                                     e4m3x2_to_bf16x2(hi & 0xFFFFu), e4m3x2_to_bf16x2(hi >> 16));
+          *reinterpret_cast<uint4*>(dst + sw128((uint32_t)r, (uint32_t)(64 * h + 16 * j))) = o;
+        }
+      }
+    }
     tc::fence_proxy_async_smem();
     __syncthreads();
   }
@@ -658,6 +712,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
   return fn;
 }
 
+// E4M3 matrix [rows][512] with unswizzled boxes of 64 bytes x box_rows rows.
+static bool encode_u8_rows512(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = at_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 matrix [rows][512] with SW128 boxes of 64 columns x box_rows rows.
 static bool encode_bf16_rows512(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
   auto fn = at_encode_fn();
@@ -687,7 +754,9 @@ cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
   CUtensorMap map_q, map_swa;
   if (!encode_bf16_rows512(&map_q, p.q, (uint64_t)BQ * H, 64)) return cudaErrorInvalidValue;
   const uint64_t swa_rows = (uint64_t)B * (uint64_t)(p.S > 0 ? p.S : 1);
-  if (!encode_bf16_rows512(&map_swa, p.swa, swa_rows, AT_KEYS)) return cudaErrorInvalidValue;
+  const bool swa_ok = p.swa_fp8 ? encode_u8_rows512(&map_swa, p.swa, swa_rows, AT_KEYS)
+                                : encode_bf16_rows512(&map_swa, p.swa, swa_rows, AT_KEYS);
+  if (!swa_ok) return cudaErrorInvalidValue;
   const int C = (p.K + AT_KEYS - 1) / AT_KEYS + 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(BQ * C));

@@ -309,6 +309,34 @@ __global__ void __launch_bounds__(CW_THREADS, 1) cache_write_kernel(CwParams p) 
   }
 }
 
+// FP8 sliding-window rows: every bf16 value to E4M3 (nearest even,
+// saturating at +-448, no scale).  One thread per 8 values: a 16-byte load,
+// four paired conversions, an 8-byte store.
+__global__ void swa_fp8_kernel(const uint16_t* __restrict__ x, int64_t n8, uint8_t* __restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t pk[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      uint16_t r;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+          : "=h"(r) : "f"(bf16_bits_to_f32(w[k] >> 16)), "f"(bf16_bits_to_f32(w[k] & 0xFFFFu)));
+      pk[k] = r;
+    }
+    reinterpret_cast<uint2*>(out)[i] = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
+  }
+}
+
+cudaError_t launch_swa_fp8(const uint16_t* x, int64_t n_rows, uint8_t* out, cudaStream_t stream) {
+  const int64_t n8 = n_rows * (D / 8);
+  if (n8 == 0) return cudaSuccess;
+  int64_t grid = ceil_div(n8, 256);
+  if (grid > 152 * 16) grid = 152 * 16;
+  swa_fp8_kernel<<<(unsigned)grid, 256, 0, stream>>>(x, n8, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_cache_write(const CwParams& p, cudaStream_t stream, int num_sms) {
   static bool attr_set = false;
   if (!attr_set) {

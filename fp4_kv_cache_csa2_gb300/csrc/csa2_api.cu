@@ -95,7 +95,7 @@ csa2_status do_index_score(const csa2_cache* cache, const uint16_t* q_idx, const
 csa2_status do_attention(const csa2_cache* cache, const uint16_t* q, const int32_t* sel, int K,
                          const uint16_t* swa, const int64_t* swa_base, int S, const int64_t* q_pos, float scale,
                          uint16_t* out, int B, int Q, void* part_ws, WsHeader* hdr, cudaStream_t stream,
-                         const uint8_t* packed_in = nullptr, uint8_t* packed_out = nullptr) {
+                         const uint8_t* packed_in = nullptr, uint8_t* packed_out = nullptr, bool swa_fp8 = false) {
   AttnParams p{};
   p.main_kv = cache->main_kv;
   p.cap = cache->cap;
@@ -105,6 +105,7 @@ csa2_status do_attention(const csa2_cache* cache, const uint16_t* q, const int32
   p.swa = swa;
   p.swa_base = swa_base;
   p.S = S;
+  p.swa_fp8 = swa_fp8 ? 1 : 0;
   p.q_pos = q_pos;
   p.scale = scale;
   p.out = out;
@@ -276,6 +277,13 @@ csa2_status csa2_select_topk(const csa2_cache* cache, const float* scores, const
                                       max_n, (cudaStream_t)stream));
 }
 
+csa2_status csa2_swa_quantize_fp8(const uint16_t* x, int64_t n_rows, uint8_t* out, void* stream) {
+  if (n_rows < 0) return CSA2_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out)) return CSA2_ERR_INVALID_ARG;
+  return from_cuda(launch_swa_fp8(x, n_rows, out, (cudaStream_t)stream));
+}
+
 size_t csa2_attn_workspace_size(int B, int Q, int K) {
   if (B < 0 || Q < 0 || K < 0) return 0;
   return HDR + align256(attn_partials_bytes((int64_t)B * Q, K));
@@ -419,6 +427,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
   if (!aligned16(a->q) || !aligned16(a->swa) || !aligned16(a->out)) return CSA2_ERR_INVALID_ARG;
   if (a->mode != CSA2_MODE_REUSE && !aligned16(a->q_idx)) return CSA2_ERR_INVALID_ARG;
   if (a->packed_sel && !aligned16(a->packed_sel)) return CSA2_ERR_INVALID_ARG;
+  if (a->swa_fp8 != 0 && a->swa_fp8 != 1) return CSA2_ERR_INVALID_ARG;
   const uint8_t* packed_in = a->mode == CSA2_MODE_REUSE ? a->packed_sel : nullptr;
   uint8_t* packed_out = a->mode == CSA2_MODE_REUSE ? nullptr : a->packed_sel;
 
@@ -438,7 +447,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
                                        a->sel, a->M, a->pool_blocks, cur, s));
       if (st != CSA2_OK) return st;
       return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out,
-                          a->B, a->Q, part, hdr, s, packed_in, packed_out);
+                          a->B, a->Q, part, hdr, s, packed_in, packed_out, a->swa_fp8 != 0);
     }
     st = from_cuda(launch_block_topk(scores, a->q_pos, cache->n_entries, cache->m, a->B, a->Q, a->max_n, a->M,
                                      a->pool_blocks, gkeys, s));
@@ -468,7 +477,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
     if (st != CSA2_OK) return st;
   }
   return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out, a->B,
-                      a->Q, part, hdr, s, packed_in, packed_out);
+                      a->Q, part, hdr, s, packed_in, packed_out, a->swa_fp8 != 0);
 }
 
 }  // extern "C"

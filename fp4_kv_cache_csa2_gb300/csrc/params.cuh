@@ -48,9 +48,10 @@ struct AttnParams {
   const uint16_t* q;          // [BQ][64][512]
   const int32_t* sel;         // [BQ][K]
   int K;
-  const uint16_t* swa;        // [B][S][512]
+  const uint16_t* swa;        // [B][S][512] bf16, or E4M3 bytes when swa_fp8
   const int64_t* swa_base;    // [B]
   int S;
+  int swa_fp8;
   const int64_t* q_pos;       // [BQ]
   float scale;
   uint16_t* out;              // [BQ][64][512]
@@ -87,6 +88,7 @@ struct HvParams {             // HISA view of the summary store as an m = 1 cach
 };
 
 cudaError_t launch_cache_write(const CwParams& p, cudaStream_t stream, int num_sms);
+cudaError_t launch_swa_fp8(const uint16_t* x, int64_t n_rows, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_index_score(IsParams p, cudaStream_t stream);
 cudaError_t launch_reindex_select(IsParams p, cudaStream_t stream);
 cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m,

@@ -256,6 +256,17 @@ csa2_status csa2_sparse_swa_attn(const csa2_cache *cache, const uint16_t *q, con
                                  int B, int Q, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * FP8 sliding-window rows.  [zartbot §2.4.4: the quantisation-sensitive SWA
+ * KV keeps FP8 precision while the main KV is FP4]
+ *   x      bf16 [n_rows][512] window rows.
+ *   out    uint8 [n_rows][512]: out[r][c] = E4M3 of x[r][c], round to nearest
+ *          even, saturating at +-448, no scale factor.
+ * Both 16-byte aligned.  Errors: INVALID_ARG for null or misaligned pointers
+ * or n_rows < 0.  Needs no workspace.
+ */
+csa2_status csa2_swa_quantize_fp8(const uint16_t *x, int64_t n_rows, uint8_t *out, void *stream);
+
+/*
  * HISA block summaries.  [zartbot §2.3.4, the HISA paragraph: each block of
  * consecutive positions keeps the mean of its indexer keys, and a decode step
  * updates only the newest block]
@@ -316,6 +327,9 @@ csa2_status csa2_hisa_blocks(const csa2_cache *cache, const uint8_t *sum_codes, 
  * layers that share a selection then read it contiguously; the result is the
  * same as without it as long as the cache entries named by sel are unchanged
  * in between (the caller's contract).
+ * swa_fp8 = 1 reads the window rows as E4M3 bytes, uint8 [B][S][512] from
+ * csa2_swa_quantize_fp8 (16-byte aligned); the attention takes their E4M3
+ * values exactly.  Other values of swa_fp8 return CSA2_ERR_INVALID_ARG.
  */
 typedef struct {
     csa2_mode mode;
@@ -334,6 +348,7 @@ typedef struct {
     int32_t *sel;               /* [B][Q][K]  Full/Reindex: out, Reuse: in      */
     uint16_t *out;              /* [B][Q][64][512]                              */
     uint8_t *packed_sel;        /* [B][Q][K][288] or NULL: Full/Reindex out, Reuse in */
+    int32_t swa_fp8;            /* 0: swa is bf16; 1: swa is E4M3 [B][S][512]   */
 } csa2_decode_args;
 
 size_t csa2_decode_workspace_size(csa2_mode mode, int B, int Q, int64_t max_n, int M, int K);
