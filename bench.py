@@ -462,7 +462,7 @@ def run_decode1m(args, torch, csa2):
     dom_bytes = w.B * ((REUSE_BYTES if dom_is_reuse else REINDEX_BYTES) - win_saved)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     dom_kernel = "attn_tc_kernel" if dom_is_reuse else "reindex_select_kernel"
-    traffic = ncu_traffic(dom_kernel) if w.N == 1 << 20 and not fp8 else None
+    traffic = ncu_traffic(dom_kernel + (":fp8_window" if fp8 else "")) if w.N == 1 << 20 else None
     e2e = None if fp8 else run_decode1m_e2e(args, torch, csa2, w)
     return {
         "value": value, "ms_per_step": ms_step, "dtype": "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
