@@ -888,6 +888,14 @@ def _hisa_workload(args, torch, csa2, B, N, seed):
                                                       ws_s))
     scan_ms = _graph_ms(torch, g_scan, reps)
     assert ws_s.sync_status()[0] == 0
+    cpu = None
+    if args.cpu_sample_queries > 0:
+        # about 10 s of oracle work at 131,072 entries (the first stage grows with N)
+        n_q = max(1, min(args.cpu_sample_queries, 400 * (1 << 17) // N))
+        cpu_v, cpu_dt = OracleHisa(N).run(n_q)
+        cpu = {"value": cpu_v, "unit": "query-tokens/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{n_q} queries over {N:,} entries (newest-block summary, first stage over "
+                         f"{nb:,} summary rows, Reindex over {M_BLK} blocks, attention), {cpu_dt:.1f} s"}
     hbm, _, which = peaks()
     scan_bytes = B * nb * (IDX_ENTRY + 4) + B * (HI * DI * 2 + HI * 4)
     achieved = scan_bytes / (scan_ms / 1e3) / 1e9
@@ -906,7 +914,7 @@ def _hisa_workload(args, torch, csa2, B, N, seed):
                   "traffic": ncu_traffic(f"{kname}:summaries_{B}x{nb}"), "kernel": kname + " over the summary store",
                   "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
                  {"parts_ms": parts, "hsi_full_call_ms": full_ms, "summary_build_ms": build_ms,
-                  "pool_recall_of_exact_top512": recall,
+                  "pool_recall_of_exact_top512": recall, "cpu_baseline": cpu,
                   "step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
                                "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
                   "clocks": clk.summary(),
@@ -1206,7 +1214,7 @@ class OracleChain:
     cache write during set-up (untimed); entry ids are compacted so the pool is
     blocks 0..2047, which leaves the per-query work unchanged."""
 
-    def __init__(self, seed: int = 9, n_query_sets: int = 8):
+    def __init__(self, seed: int = 9, n_query_sets: int = 8, swa_fp8: bool = False):
         import numpy as np
         import oracle
         import synth
@@ -1218,6 +1226,8 @@ class OracleChain:
         W = synth.index_projection(g)
         self.main, self.codes, self.scales = oracle.compress_quantize(x, 1, w0, w1, W)
         self.swa = synth.swa_rows(g, WIN)
+        if swa_fp8:                  # E4M3 window rows (quantised untimed, as the GPU leg does)
+            self.swa = oracle.swa_fp8_quantize(self.swa)
         self.pool = np.arange(M_BLK, dtype=np.int32)
         self.qs = [(synth.index_queries(g), synth.head_weights(g), [synth.main_queries(g) for _ in range(4)])
                    for _ in range(n_query_sets)]
@@ -1235,6 +1245,44 @@ class OracleChain:
                 o.decode_query(o.REUSE, q=q4[layer], sel=sel, **common)
         dt = time.perf_counter() - t0
         return n_queries * 4 / dt, dt
+
+
+class OracleHisa:
+    """Oracle on the per-query work of a HISA decode step over n entries: the
+    newest block's summary, the first stage over all ceil(n/8) summary rows,
+    the Reindex second stage over the chosen blocks and the attention.  The
+    cache is stored bytes drawn at random (index keys: synth.index_key_bytes;
+    main entries: uniform codes with E4M3 scales in [0.5, 1]), the summary
+    store is built once untimed."""
+
+    def __init__(self, n: int, seed: int = 11, n_query_sets: int = 4):
+        import numpy as np
+        import oracle
+        import synth
+        self.oracle, self.n = oracle, n
+        g = synth.rng(seed)
+        self.codes, self.scales = synth.index_key_bytes(g, n)
+        self.main = np.concatenate([g.integers(0, 256, size=(n, 256), dtype=np.uint8),
+                                    g.integers(0x30, 0x39, size=(n, 32), dtype=np.uint8)], axis=1)
+        self.sum_codes, self.sum_scales = oracle.block_summary(self.codes, self.scales, n)
+        self.swa = synth.swa_rows(g, WIN)
+        self.qs = [(synth.index_queries(g), synth.head_weights(g), synth.main_queries(g))
+                   for _ in range(n_query_sets)]
+
+    def run(self, n_queries: int) -> tuple[float, float]:
+        o, n = self.oracle, self.n
+        e0 = (n - 1) // 8 * 8
+        t0 = time.perf_counter()
+        for i in range(n_queries):
+            q_idx, wh, q = self.qs[i % len(self.qs)]
+            sc, ss = o.block_summary(self.codes[e0:n], self.scales[e0:n], n - e0)
+            self.sum_codes[e0 // 8], self.sum_scales[e0 // 8] = sc[0], ss[0]
+            pool = o.hisa_blocks(q_idx, wh, self.sum_codes, self.sum_scales, n, M_BLK)
+            o.decode_query(o.REINDEX, t=n - 1, m=1, n_entries=n, main_kv=self.main, idx_codes=self.codes,
+                           idx_scales=self.scales, q=q, swa=self.swa, swa_base=n - WIN, scale=1 / math.sqrt(D),
+                           M=M_BLK, K=K_SEL, q_idx=q_idx, w_head=wh, pool_blocks=pool)
+        dt = time.perf_counter() - t0
+        return n_queries / dt, dt
 
 
 def oracle_threads() -> int:
@@ -1325,7 +1373,7 @@ def main():
         line.update(res)
         line["cpu_baseline"] = None
         if args.cpu_sample_queries > 0:
-            cpu_v, cpu_dt = OracleChain().run(args.cpu_sample_queries)
+            cpu_v, cpu_dt = OracleChain(swa_fp8=args.swa_format == "fp8").run(args.cpu_sample_queries)
             line["cpu_baseline"] = {"value": cpu_v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
                                     "sample": f"{args.cpu_sample_queries} query tokens x (Reindex over a 16,384-"
                                               f"entry pool + 3 Reuse attentions), {cpu_dt:.1f} s"}
