@@ -778,6 +778,12 @@ def run_full131k(args, torch, csa2):
     g_s = _capture(torch, lambda: csa2.index_score(cache, q_idx.view(torch.int16), w_head, q_pos, scores, N, ws_s))
     g_s.replay()
     scan_ms = _events_ms(torch, g_s.replay, max(args.steps, 20))
+    cpu = None
+    if args.cpu_sample_queries > 0:
+        n_q = max(1, args.cpu_sample_queries // 24)
+        dt = OracleLayer(N, 1).run([N - 1] * n_q)
+        cpu = _oracle_line(n_q / dt, "query-tokens/s", f"{n_q} Full-mode queries over {N:,} entries (m=1) on a "
+                                                       f"cache of random stored bytes, {dt:.1f} s")
     hbm, _, which = peaks()
     scan_bytes = B * N * (IDX_ENTRY + 4) + B * (HI * DI * 2 + HI * 4)       # index K read + scores written
     per_query = N * IDX_ENTRY + HI * DI * 2 + HI * 4 + ATTN_BYTES + M_BLK * 4 + K_SEL * 4
@@ -793,7 +799,7 @@ def run_full131k(args, torch, csa2):
                   "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
                  {"step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
                                "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
-                  "clocks": clk.summary(), "gpu_launches": args.steps * 5})
+                  "clocks": clk.summary(), "gpu_launches": args.steps * 5, "cpu_baseline": cpu})
 
 
 def _hisa_workload(args, torch, csa2, B, N, seed):
@@ -1008,7 +1014,7 @@ def run_decoder1m(args, torch, csa2):
                   "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
                  {"step_hbm": {"algorithmic_bytes": B * per_query, "GB_s": B * per_query / (ms / 1e3) / 1e9,
                                "frac": B * per_query / (ms / 1e3) / 1e9 / hbm},
-                  "ms_per_token": ms, "clocks": clk.summary(),
+                  "ms_per_token": ms, "clocks": clk.summary(), "cpu_baseline": _decoder_oracle(args, N),
                   "gpu_launches": args.steps * (5 + 4 * 2 + 15)})   # Full 5, Reindex 2, Reuse 1
 
 
@@ -1075,7 +1081,8 @@ def run_prefill8k(args, torch, csa2):
                   "frac": achieved / fp4_peak, "traffic": None, "kernel": "index_score_tc_kernel<5>",
                   "algorithmic_flops_per_launch": flops, "avg_launch_ms": scan_ms,
                   "peak_source": f"{which} bf16 x {FP4_PER_BF16:g} (nominal fp4:bf16 dense ratio)"},
-                 {"clocks": clk.summary(), "gpu_launches": args.steps * 5})
+                 {"clocks": clk.summary(), "gpu_launches": args.steps * 5,
+                  "cpu_baseline": _prefill_oracle(args, P, T, N, m, 0)})
 
 
 def run_prefillblock(args, torch, csa2):
@@ -1151,6 +1158,7 @@ def run_prefillblock(args, torch, csa2):
                   "algorithmic_flops_per_launch": flops, "avg_launch_ms": scan_ms,
                   "peak_source": f"{which} bf16 x {FP4_PER_BF16:g} (nominal fp4:bf16 dense ratio)"},
                  {"attention_bf16_flops_per_chunk": attn_flops, "clocks": clk.summary(),
+                  "cpu_baseline": _prefill_oracle(args, P, T, N, m, 5),
                   "gpu_launches": args.steps * (5 + 5)})   # Full: scan, 3 selection, attention; Reuse: attention
 
 
@@ -1203,7 +1211,7 @@ def run_cachewrite(args, torch, csa2):
                                  f"{sm_mhz:.0f} MHz"},
                  {"step_hbm": {"algorithmic_bytes": bytes_step, "GB_s": bytes_step / (ms / 1e3) / 1e9,
                                "frac": bytes_step / (ms / 1e3) / 1e9 / hbm},
-                  "clocks": clocks, "gpu_launches": args.steps * 4})
+                  "clocks": clocks, "gpu_launches": args.steps * 4, "cpu_baseline": _cachewrite_oracle(args)})
 
 
 # ------------------------------------------------------------------ CPU oracle sample
@@ -1283,6 +1291,95 @@ class OracleHisa:
                            M=M_BLK, K=K_SEL, q_idx=q_idx, w_head=wh, pool_blocks=pool)
         dt = time.perf_counter() - t0
         return n_queries / dt, dt
+
+
+class OracleLayer:
+    """Oracle on the per-query work of a Full-mode layer over n entries of ratio
+    m (index scan of every visible entry, top-2048 blocks, top-512, attention),
+    optionally followed by Reuse layers on its selection and by Reindex groups
+    (Reindex over its blocks + 3 Reuse).  Stored bytes drawn at random as in
+    OracleHisa; each query's 128 window rows are one fixed set of rows."""
+
+    def __init__(self, n: int, m: int, seed: int = 13, n_query_sets: int = 4):
+        import numpy as np
+        import oracle
+        import synth
+        self.oracle, self.n, self.m = oracle, n, m
+        g = synth.rng(seed)
+        self.codes, self.scales = synth.index_key_bytes(g, n)
+        self.main = np.concatenate([g.integers(0, 256, size=(n, 256), dtype=np.uint8),
+                                    g.integers(0x30, 0x39, size=(n, 32), dtype=np.uint8)], axis=1)
+        self.swa = synth.swa_rows(g, WIN)
+        self.qs = [(synth.index_queries(g), synth.head_weights(g), synth.main_queries(g))
+                   for _ in range(n_query_sets)]
+
+    def run(self, positions, reuse: int = 0, reindex_groups: int = 0) -> float:
+        """Seconds for one query at each raw position in `positions`."""
+        o = self.oracle
+        common = dict(m=self.m, n_entries=self.n, main_kv=self.main, idx_codes=self.codes, idx_scales=self.scales,
+                      swa=self.swa, scale=1 / math.sqrt(D), M=M_BLK, K=K_SEL)
+        t0 = time.perf_counter()
+        for i, t in enumerate(positions):
+            q_idx, wh, q = self.qs[i % len(self.qs)]
+            c = dict(common, t=int(t), swa_base=int(t) - (WIN - 1), q=q)
+            pool, sel, _ = o.decode_query(o.FULL, q_idx=q_idx, w_head=wh, **c)
+            for _ in range(reuse):
+                o.decode_query(o.REUSE, sel=sel, **c)
+            for _ in range(reindex_groups):
+                _, sel2, _ = o.decode_query(o.REINDEX, q_idx=q_idx, w_head=wh, pool_blocks=pool, **c)
+                for _ in range(3):
+                    o.decode_query(o.REUSE, sel=sel2, **c)
+        return time.perf_counter() - t0
+
+
+def _oracle_line(value: float, unit: str, sample: str) -> dict:
+    return {"value": value, "unit": unit, "cores": oracle_threads(), "kind": "oracle", "sample": sample}
+
+
+def _decoder_oracle(args, N: int):
+    """One token through the whole decoder chain: Full + 3 Reuse, 4 x (Reindex + 3 Reuse)."""
+    if args.cpu_sample_queries <= 0:
+        return None
+    n_tok = max(1, args.cpu_sample_queries // 192)
+    dt = OracleLayer(N, 1).run([N - 1] * n_tok, reuse=3, reindex_groups=4)
+    return _oracle_line(20 * n_tok / dt, "query-token-layers/s",
+                        f"{n_tok} query tokens x 20 layer calls over {N:,} entries (m=1) on a cache of random "
+                        f"stored bytes, {dt:.1f} s")
+
+
+def _prefill_oracle(args, P: int, T: int, N: int, m: int, reuse: int):
+    """Evenly spaced queries of the chunk, each a Full query (+ `reuse` Reuse layers)."""
+    if args.cpu_sample_queries <= 0:
+        return None
+    import numpy as np
+    n_q = max(2, args.cpu_sample_queries // 24)
+    pos = np.linspace(P, T - 1, n_q).round().astype(np.int64)
+    dt = OracleLayer(N, m).run(pos, reuse=reuse)
+    unit = "query-token-layers/s" if reuse else "query-tokens/s"
+    return _oracle_line((1 + reuse) * n_q / dt, unit,
+                        f"{n_q} evenly spaced queries of t = {P:,}..{T - 1:,} over {N:,} entries (m={m}), "
+                        f"{1 + reuse} layer call(s) each, cache of random stored bytes, {dt:.1f} s")
+
+
+def _cachewrite_oracle(args):
+    """The oracle's cache write (C, the pinned binary32 order) on a sample of
+    tokens of each of the 4 source layers."""
+    if args.cpu_sample_queries <= 0:
+        return None
+    import oracle
+    import synth
+    n_tok = max(2, args.cpu_sample_queries * 64)
+    g = synth.rng(17)
+    w0, w1 = synth.compressor_weights(g)
+    W = synth.index_projection(g)
+    xs = [(synth.latents(g, n_tok), m) for m in (2, 2, 2, 1)]
+    cs = oracle.rope_table(n_tok)
+    t0 = time.perf_counter()
+    for x, m in xs:
+        oracle.compress_quantize(x, m, w0, w1, W, 0, cs=cs)
+    dt = time.perf_counter() - t0
+    return _oracle_line(4 * n_tok / dt, "tokens/s",
+                        f"{n_tok:,} tokens of each of the 4 source layers (3 at m=2, 1 at m=1), {dt:.1f} s")
 
 
 def oracle_threads() -> int:
