@@ -57,6 +57,46 @@ def test_host_only_calls_without_gpu(lib_path):
     assert lib.csa2_index_score(None, None, None, None, None, 0, None, 1, 1, 10, None, 0, None) == 1
 
 
+def test_variant_calls_host_logic_without_gpu(lib_path):
+    """Workspace arithmetic and argument checks of the HISA and FP8-window calls
+    (all return before any CUDA call)."""
+    import fp4_kv_cache_csa2_gb300 as csa2
+    lib = csa2.load(lib_path)
+    # HISA: header + view positions (int64 per query) + summary rows (int32 per
+    # sequence) + one score per summary row, each rounded to 256 bytes
+    assert lib.csa2_hisa_blocks_workspace_size(2, 3, 1000) == 256 + 256 + 256 + 3072   # 6 x 125 x 4 = 3000
+    per_rows = lib.csa2_select_topk_workspace_size(2, 3, 1 << 20) - 256               # long-row lists
+    scores = -(-6 * 4097 * 4 // 256) * 256                                               # 98,328 -> 98,560
+    assert lib.csa2_hisa_blocks_workspace_size(2, 3, 8 * 4097) == 256 + 256 + 256 + scores + per_rows
+    assert lib.csa2_hisa_blocks_workspace_size(-1, 3, 10) == 0
+    fake = ctypes.c_void_p(1 << 20)                     # never dereferenced: the calls fail on arguments
+    n = ctypes.c_int32(0)
+    cache = csa2.CacheStruct(fake.value, fake.value, fake.value, 64, ctypes.addressof(n), 1)
+    ws = ctypes.c_void_p(1 << 24)
+    # block summary: sum_cap must be a multiple of 8; negative counts
+    assert lib.csa2_block_summary(ctypes.byref(cache), fake, 1, 1, fake, fake, 12, ws, 1 << 16, None) == 1
+    assert lib.csa2_block_summary(ctypes.byref(cache), fake, -1, 1, fake, fake, 8, ws, 1 << 16, None) == 1
+    assert lib.csa2_block_summary(ctypes.byref(cache), fake, 1, 1, fake, fake, 8, None, 0, None) == 3
+    # HISA blocks: M outside 1..2048; store shorter than ceil(cap / 8) rows
+    ws_need = lib.csa2_hisa_blocks_workspace_size(1, 1, 64)
+    args = (fake, fake, fake, 1, 1, 64)                 # q_idx, w_head, q_pos, B, Q, max_n
+    assert lib.csa2_hisa_blocks(ctypes.byref(cache), fake, fake, 8, *args, 0, fake, ws, ws_need, None) == 2
+    assert lib.csa2_hisa_blocks(ctypes.byref(cache), fake, fake, 0, *args, 4, fake, ws, ws_need, None) == 1
+    assert lib.csa2_hisa_blocks(ctypes.byref(cache), fake, fake, 8, *args, 4, fake, ws, ws_need - 1, None) == 3
+    # FP8 window: alignment and counts
+    assert lib.csa2_swa_quantize_fp8(fake, 4, ctypes.c_void_p((1 << 20) + 8), None) == 1
+    assert lib.csa2_swa_quantize_fp8(fake, -4, fake, None) == 1
+    assert lib.csa2_swa_quantize_fp8(None, 0, None, None) == 0   # nothing to do
+    # decode: swa_fp8 must be 0 or 1
+    a = csa2.DecodeArgs()
+    a.mode, a.B, a.Q, a.M, a.K, a.S, a.max_n, a.scale = 2, 1, 1, 8, 8, 128, 64, 0.04
+    for f in ("q_pos", "q", "swa", "swa_base_pos", "sel", "out"):
+        setattr(a, f, fake.value)
+    a.swa_fp8 = 2
+    need = lib.csa2_decode_workspace_size(2, 1, 1, 64, 8, 8)
+    assert lib.csa2_decode(ctypes.byref(cache), ctypes.byref(a), ws, need, None) == 1
+
+
 def test_rope_table_matches_oracle_bit_for_bit(lib_path):
     """The library's table builder and the oracle's are separate restatements of
     cos/sin(p * theta^(-2i/64)); their binary32 tables agree."""
