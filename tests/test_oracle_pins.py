@@ -488,6 +488,26 @@ def test_hisa_with_every_block_equals_exhaustive_topk():
     np.testing.assert_array_equal(oracle.select_topk(s, pool, 16), oracle.select_topk(s, np.arange(nv), 16))
 
 
+def test_hisa_summary_of_a_block_depends_only_on_its_entries():
+    """Appending entries changes only the newest block's summary (so a decode
+    step recomputes one block), and a block's summary is unchanged when the
+    entries of other blocks change."""
+    g, (main, codes, scales) = _tiny_cache(25, 70)
+    sc_a, ss_a = oracle.block_summary(codes, scales, 66)      # blocks 0..8, block 8 holds 2 entries
+    sc_b, ss_b = oracle.block_summary(codes, scales, 70)      # block 8 now holds 6
+    np.testing.assert_array_equal(sc_a[:8], sc_b[:8])
+    np.testing.assert_array_equal(ss_a[:8], ss_b[:8])
+    assert not (np.array_equal(sc_a[8], sc_b[8]) and np.array_equal(ss_a[8], ss_b[8]))
+    c2 = codes.copy()
+    c2[8:16] = codes[40:48]                                    # block 1 replaced by block 5's entries
+    s2 = scales.copy()
+    s2[8:16] = scales[40:48]
+    sc_c, ss_c = oracle.block_summary(c2, s2, 70)
+    np.testing.assert_array_equal(sc_c[[0, 2, 3, 4, 5, 6, 7, 8]], sc_b[[0, 2, 3, 4, 5, 6, 7, 8]])
+    np.testing.assert_array_equal(oracle.dequant_index(sc_c[1:2], ss_c[1:2]),
+                                  oracle.dequant_index(sc_b[5:6], ss_b[5:6]))
+
+
 def test_hisa_blocks_rank_by_the_mean_key_score():
     """Brute force on a small cache: the chosen blocks are the M highest scores
     of the block mean keys (ties to the lower block), none forced."""
