@@ -47,16 +47,23 @@ sys.path.insert(0, ROOT)
 METRIC = "CSA2 decode query-tokens/s/layer at 1M ctx; % of HBM roofline"
 UNIT = "query-token-layers/s"
 
-# algorithmic bytes (per query token) of the 1M Reindex + 3 Reuse chain
+# algorithmic bytes (per query token) of the 1M Reindex + 3 Reuse chain: what the
+# layer must read and write (pool entries, ids, queries, weights, selection,
+# the selected entries, the window, q and out), nothing of this implementation's own
 IDX_ENTRY, MAIN_ENTRY = 68, 288
 K_SEL, M_BLK, WIN, D, H, HI, DI = 512, 2048, 128, 512, 64, 32, 128
 ATTN_BYTES = K_SEL * MAIN_ENTRY + WIN * D * 2 + H * D * 2 + H * D * 2          # 409,600
-# the Reindex layer also writes the packed copy of its selection (K x 288 B),
-# which the Reuse layers read in place of the gather (the same byte count)
-REINDEX_BYTES = (M_BLK * 8 * IDX_ENTRY + M_BLK * 4 + HI * DI * 2 + HI * 4 + K_SEL * 4 + ATTN_BYTES
-                 + K_SEL * MAIN_ENTRY)                                           # 1,689,728
+REINDEX_BYTES = M_BLK * 8 * IDX_ENTRY + M_BLK * 4 + HI * DI * 2 + HI * 4 + K_SEL * 4 + ATTN_BYTES   # 1,542,272
 REUSE_BYTES = K_SEL * 4 + ATTN_BYTES                                             # 411,648
-CHAIN_BYTES = REINDEX_BYTES + 3 * REUSE_BYTES                                    # 2,924,672
+CHAIN_BYTES = REINDEX_BYTES + 3 * REUSE_BYTES                                    # 2,777,216
+# traffic this implementation adds: the Reindex call writes a packed copy of its
+# selected entries (K x 288 B per query), which the Reuse calls read in place of
+# the gather (so their byte count is unchanged)
+PACKED_WRITE_BYTES = K_SEL * MAIN_ENTRY                                          # 147,456
+
+# the K-step window is replayed back to back until at least this long, and the
+# median window is reported (steady state, not a single fill and drain)
+MIN_TIMED_S = 0.5
 
 
 def peaks():
@@ -362,36 +369,61 @@ def _capture(torch, fn):
 
 class PhaseGraphs:
     """CUDA graphs of a pipelined step: one per pipeline phase (step s depends
-    only on s mod R), one of a whole cycle of R consecutive phases and one of
-    `cycles` whole cycles, so that long runs launch one graph per cycles * R
-    steps (consecutive graph launches serialise, so a longer graph leaves fewer
-    drain-and-fill gaps between steps)."""
+    only on s mod R), one of a whole cycle of R consecutive steps starting at
+    each phase, and optionally one of `cycles` whole cycles from phase 0, so
+    that a run of steps launches one graph per cycle whatever phase it starts
+    at (consecutive graph launches serialise, so every graph boundary is a
+    drain and fill of the pipeline)."""
 
     def __init__(self, torch, step_fn, R: int, s_base: int, cycle_fn=None, cycles: int = 1):
         self.R = R
         self.cycles = max(1, cycles)
         self.single = [_capture(torch, lambda i=i: step_fn(s_base + i)) for i in range(R)]
         if cycle_fn is None:
-            self.cycle = _capture(torch, lambda: [step_fn(s_base + i) for i in range(R)])
-            self.multi = None
-        else:
-            self.cycle = _capture(torch, lambda: cycle_fn(s_base, R))
-            self.multi = _capture(torch, lambda: cycle_fn(s_base, R * self.cycles)) if self.cycles > 1 else None
+            cycle_fn = lambda first, n: [step_fn(first + i) for i in range(n)]
+        self.cycle_at = [_capture(torch, lambda p=p: cycle_fn(s_base + p, R)) for p in range(R)]
+        self.multi = _capture(torch, lambda: cycle_fn(s_base, R * self.cycles)) if self.cycles > 1 else None
 
     def run(self, first: int, n: int):
         """Replays steps first .. first + n - 1 (exactly n steps)."""
         i = 0
         long = self.R * self.cycles
         while i < n:
-            if self.multi is not None and (first + i) % self.R == 0 and n - i >= long:
+            p = (first + i) % self.R
+            if self.multi is not None and p == 0 and n - i >= long:
                 self.multi.replay()
                 i += long
-            elif (first + i) % self.R == 0 and n - i >= self.R:
-                self.cycle.replay()
+            elif n - i >= self.R:
+                self.cycle_at[p].replay()
                 i += self.R
             else:
-                self.single[(first + i) % self.R].replay()
+                self.single[p].replay()
                 i += 1
+
+
+def steady_windows(torch, run_window, n_steps, first, min_s=MIN_TIMED_S, max_windows=20000):
+    """Times the same K-step window (run_window(first_step, K) enqueues exactly K
+    steps) replayed back to back: a CUDA event before the first window and after
+    each one, all on the current stream, one synchronize at the end.  The number
+    of windows is chosen from one calibration window so the whole set lasts at
+    least `min_s`.  Returns (median ms per window, windows, total seconds)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    run_window(first, n_steps)
+    e1.record()
+    torch.cuda.synchronize()
+    cal = max(e0.elapsed_time(e1), 1e-3)
+    n_win = int(min(max_windows, max(5, math.ceil(min_s * 1e3 / cal))))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_win + 1)]
+    s = first + n_steps
+    torch.cuda.synchronize()
+    ev[0].record()
+    for w in range(n_win):
+        run_window(s + w * n_steps, n_steps)
+        ev[w + 1].record()
+    torch.cuda.synchronize()
+    times = [ev[w].elapsed_time(ev[w + 1]) for w in range(n_win)]
+    return statistics.median(times), n_win, ev[0].elapsed_time(ev[-1]) / 1e3
 
 
 def _graph_ms(torch, graph, reps):
@@ -416,33 +448,26 @@ def run_decode1m(args, torch, csa2):
     # graphs per pipeline phase and per cycle of R phases: step s only depends on s mod R
     s_base = 3 * w.d
     graphs = PhaseGraphs(torch, w.step, w.R, s_base, cycle_fn=w.cycle, cycles=args.graph_cycles)
-    graphs.run(0, args.warmup)
-    torch.cuda.synchronize()
     n_steps = args.steps
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0 = args.warmup
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        torch.cuda.nvtx.range_push("timed")
-        start.record()
-        graphs.run(s0, n_steps)
-        stop.record()
+    with ClockSampler(local) as clk:             # sampling from the warm-up on
+        graphs.run(0, args.warmup)
         torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed")
+        win_ms, n_win, timed_s = steady_windows(torch, graphs.run, n_steps, s0)
         torch.cuda.nvtx.range_pop()
-    barrier(world)
-    total_ms = max_over_ranks(start.elapsed_time(stop), world)
+        barrier(world)
+    total_ms = max_over_ranks(win_ms, world)
     w.check_status()
     # the same steps with the four layer calls one after another on one stream
     serial = PhaseGraphs(torch, lambda s: w.step(s, concurrent=False), w.R, s_base)
     serial.run(0, args.warmup)
     torch.cuda.synchronize()
     n_serial = min(n_steps, 1000)
-    start.record()
-    serial.run(s0, n_serial)
-    stop.record()
-    torch.cuda.synchronize()
-    serial_ms = max_over_ranks(start.elapsed_time(stop), world) / n_serial
+    serial_win, _, _ = steady_windows(torch, serial.run, n_serial, s0, min_s=0.2)
+    serial_ms = max_over_ranks(serial_win, world) / n_serial
     w.check_status()
     # per-layer-call durations, same pipeline (cold instances), timed by layer type
     reindex_g = _capture(torch, lambda: [w.layer(0, r) for r in range(w.R)])
@@ -457,6 +482,7 @@ def run_decode1m(args, torch, csa2):
     hbm, bf16, which = peaks()
     win_saved = WIN * D if fp8 else 0                  # an E4M3 window row is 512 B, a bf16 one 1 KB
     bytes_step = w.B * (CHAIN_BYTES - 4 * win_saved)
+    extra_step = w.B * PACKED_WRITE_BYTES if args.packed_selection else 0
     dom_is_reuse = 3 * reuse_ms >= reindex_ms          # Reuse calls are 3 of the 4 layers
     dom_ms = reuse_ms if dom_is_reuse else reindex_ms
     dom_bytes = w.B * ((REUSE_BYTES if dom_is_reuse else REINDEX_BYTES) - win_saved)
@@ -472,7 +498,8 @@ def run_decode1m(args, torch, csa2):
                    "l2": f"inputs larger than L2: {w.R} pipelined instances x "
                          f"{w.B * w.N * (MAIN_ENTRY + IDX_ENTRY) / 1e9:.2f} GB, layer distance {w.d} steps",
                    "launch": f"CUDA graphs of {w.R * max(1, args.graph_cycles)} consecutive steps "
-                             f"(whole cycles of {w.R}; one graph per step for a remainder) with only the data's "
+                             f"(whole cycles of {w.R} from any phase; one graph per step for a remainder) with "
+                             "only the data's "
                              "dependencies between steps; in a step the 4 layer calls (4 different pipelined "
                              "instances, so independent) are parallel branches, the Reindex branch first at high "
                              f"priority; every layer slot has {w.lanes} stream + workspace lanes taken by step "
@@ -487,7 +514,15 @@ def run_decode1m(args, torch, csa2):
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
                      "peak_source": which},
         "step_hbm": {"algorithmic_bytes": bytes_step, "GB_s": bytes_step / (ms_step / 1e3) / 1e9,
-                     "frac": bytes_step / (ms_step / 1e3) / 1e9 / hbm},
+                     "frac": bytes_step / (ms_step / 1e3) / 1e9 / hbm,
+                     "packed_selection_write_bytes": extra_step,
+                     "note": "algorithmic bytes of the chain (pool, ids, queries, weights, selection, selected "
+                             "entries, window, q, out); the packed-selection write is this implementation's "
+                             "own extra traffic, shown apart and not counted"},
+        "timing": {"windows": n_win, "steps_per_window": n_steps, "timed_s": timed_s,
+                   "how": "the K-step window replayed back to back (CUDA events between windows on the "
+                          "launching stream, one synchronize after the set, barrier on both sides); the "
+                          "median window / K is ms_per_step"},
         "layer_ms": {"reindex": reindex_ms, "reuse": reuse_ms},
         "serial_schedule": {"value": qtl_per_step * world / (serial_ms / 1e3), "ms_per_step": serial_ms,
                             "steps": n_serial, "launch": "the same graphs with the 4 layer calls in sequence "
@@ -644,14 +679,11 @@ def run_decode1m_e2e(args, torch, csa2, w):
     # graphs carry both copies
     host_in[off_w:].view(torch.float32).normal_()
     host_out.zero_()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    graphs.run(args.warmup, args.steps)
-    stop.record()
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(stop) / args.steps
+    win_ms, n_win, _ = steady_windows(torch, graphs.run, args.steps, args.warmup)
+    ms = win_ms / args.steps
     w.check_status()
-    s_last = s0 + (args.warmup + args.steps - 1) % w.R
+    last = args.warmup + args.steps * (n_win + 1) - 1          # the last step replayed
+    s_last = s0 + last % w.R
     assert torch.equal(dev_in[(s_last + 1) % NB].cpu(), host_in), "input copy missing from the step graph"
     assert torch.equal(host_out, dev_out[(s_last - 1) % NB].cpu()) and bool(host_out.any()), \
         "output copy missing from the step graph"
@@ -1419,7 +1451,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode1m",

@@ -76,6 +76,7 @@ _SIGNATURES = {
                               _P, _SZ, _P]),
     "csa2_decode_workspace_size": (_SZ, [_I, _I, _I, _I64, _I, _I]),
     "csa2_decode": (_I, [ctypes.POINTER(CacheStruct), ctypes.POINTER(DecodeArgs), _P, _SZ, _P]),
+    "csa2_test_withhold_arrival": (_I, [_I]),
 }
 
 _lib = None

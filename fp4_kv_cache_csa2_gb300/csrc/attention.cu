@@ -50,6 +50,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include "host_once.cuh"
 #include "params.cuh"
 #include "tc.cuh"
 
@@ -700,21 +701,9 @@ attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __
 }
 
 // ------------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
 // E4M3 matrix [rows][512] with unswizzled boxes of 64 bytes x box_rows rows.
 static bool encode_u8_rows512(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
-  auto fn = at_encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, rows};
   cuuint64_t strides[1] = {(cuuint64_t)D};
@@ -727,7 +716,7 @@ static bool encode_u8_rows512(CUtensorMap* map, const void* base, uint64_t rows,
 
 // bf16 matrix [rows][512] with SW128 boxes of 64 columns x box_rows rows.
 static bool encode_bf16_rows512(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
-  auto fn = at_encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
@@ -743,14 +732,11 @@ size_t attn_partials_bytes(int64_t, int) { return 0; }
 cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
   const int64_t BQ = (int64_t)B * p.Q;
   if (BQ == 0) return cudaSuccess;
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+  static PerDeviceOnce attrs;
+  cudaError_t e = attrs.ensure([](int) {
+    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+  });
+  if (e != cudaSuccess) return e;
   CUtensorMap map_q, map_swa;
   if (!encode_bf16_rows512(&map_q, p.q, (uint64_t)BQ * H, 64)) return cudaErrorInvalidValue;
   const uint64_t swa_rows = (uint64_t)B * (uint64_t)(p.S > 0 ? p.S : 1);

@@ -38,6 +38,7 @@
 //            across the warp, y reads are broadcasts.  This phase is
 //            FP32-ALU bound (65,536 fma per entry).
 //   phase 3  MXFP4 of k: 8 lanes form one 32-wide block.
+#include "host_once.cuh"
 #include "params.cuh"
 
 namespace csa2 {
@@ -331,19 +332,21 @@ __global__ void swa_fp8_kernel(const uint16_t* __restrict__ x, int64_t n8, uint8
 cudaError_t launch_swa_fp8(const uint16_t* x, int64_t n_rows, uint8_t* out, cudaStream_t stream) {
   const int64_t n8 = n_rows * (D / 8);
   if (n8 == 0) return cudaSuccess;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) return e;
   int64_t grid = ceil_div(n8, 256);
-  if (grid > 152 * 16) grid = 152 * 16;
+  if (grid > (int64_t)sms * 16) grid = (int64_t)sms * 16;      // grid-stride, at most 16 CTAs per SM
   swa_fp8_kernel<<<(unsigned)grid, 256, 0, stream>>>(x, n8, out);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cache_write(const CwParams& p, cudaStream_t stream, int num_sms) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(cache_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CW_SMEM);
-    if (err != cudaSuccess) return err;
-    attr_set = true;
-  }
+  static PerDeviceOnce attrs;
+  cudaError_t err = attrs.ensure([](int) {
+    return cudaFuncSetAttribute(cache_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CW_SMEM);
+  });
+  if (err != cudaSuccess) return err;
   int64_t n_local = p.T / p.m;
   int64_t n_tiles = ceil_div(n_local, CW_TILE) * p.B;
   if (n_tiles == 0) return cudaSuccess;

@@ -6,7 +6,7 @@
 #include <vector>
 
 #include "common.cuh"
-
+#include "host_once.cuh"
 #include "params.cuh"
 
 using namespace csa2;
@@ -19,17 +19,6 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-int num_sms() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
 
 csa2_status check_cache(const csa2_cache* c) {
   if (!c || !c->main_kv || !c->idx_codes || !c->idx_scales || !c->n_entries) return CSA2_ERR_INVALID_ARG;
@@ -64,8 +53,12 @@ size_t select_scratch_bytes(int B, int Q, int64_t max_n, bool blocks) {
   return blocks ? gkeys_bytes(B, Q, max_n) : 0;
 }
 
+// B * Q queries per call at most: every grid stays a 1-D grid below 2^31 CTAs
+constexpr int64_t MAX_QUERIES = (int64_t)1 << 26;
+
 csa2_status check_q(int B, int Q) {
   if (B < 0 || Q < 0) return CSA2_ERR_INVALID_ARG;
+  if ((int64_t)B * Q > MAX_QUERIES) return CSA2_ERR_UNSUPPORTED;
   return CSA2_OK;
 }
 
@@ -211,7 +204,9 @@ csa2_status csa2_compress_quantize(const csa2_cache* cache, const uint16_t* x, i
   p.rope_P = rope_P;
   p.w_idx = w_idx;
   p.hdr = header(ws);
-  return from_cuda(launch_cache_write(p, (cudaStream_t)stream, num_sms()));
+  int sms = 0;
+  if (device_sms(&sms) != cudaSuccess) return CSA2_ERR_CUDA;
+  return from_cuda(launch_cache_write(p, (cudaStream_t)stream, sms));
 }
 
 csa2_status csa2_index_score(const csa2_cache* cache, const uint16_t* q_idx, const float* w_head,

@@ -38,6 +38,7 @@
 #include <cstddef>
 #include <cudaTypedefs.h>
 
+#include "host_once.cuh"
 #include "index_query.cuh"
 #include "params.cuh"
 #include "tc.cuh"
@@ -80,6 +81,7 @@ struct IsSmem {
   uint32_t sfb[NQ * HI];                     // query scale words
   uint64_t full[IS_STAGES], empty[IS_STAGES];
   uint64_t acc_full[4];
+  uint64_t test_bar;                         // test hook only: nothing ever arrives on it
   uint32_t ready[IS_STAGES];                 // tile i + 1 once tile i sits in stage i % IS_STAGES
   uint32_t acc_free[4];                      // epilogue warps done reading accumulator k, cumulative
   uint32_t tmem_base;
@@ -136,11 +138,12 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
       *reinterpret_cast<IsSmem<NQ>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int groups = (p.Q + NQ - 1) / NQ;    // query groups per sequence
-  const int b = (int)blockIdx.y / groups;
-  const int qf = ((int)blockIdx.y % groups) * NQ;
+  const int64_t group = (int64_t)blockIdx.x / p.split;   // (sequence, query group)
+  const int crank = (int)((int64_t)blockIdx.x % p.split); // slice of the group's tiles
+  const int b = (int)(group / groups);
+  const int qf = (int)(group % groups) * NQ;
   const int nq = p.Q - qf < NQ ? p.Q - qf : NQ;   // queries in this group
   const int64_t bq0 = (int64_t)b * p.Q + qf;
-  const int crank = (int)blockIdx.x;         // slice of the group's tiles
   const bool pool_mode = p.pool != nullptr;  // (NQ == 1 only)
 
   // ---- visible entries of each query; this CTA's tile range
@@ -152,11 +155,11 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
     if (j < nq) {
       v = visible_entries(p.q_pos[bq0 + j], p.m, p.n_entries[b]);
       if (v > p.cap) {
-        if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, v);
+        if (tid == 0 && crank == 0) report(p.hdr, CSA2_ERR_BOUNDS, v);
         v = p.cap;
       }
       if (!pool_mode && v > p.max_n) {
-        if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA2_ERR_BOUNDS, v);
+        if (tid == 0 && crank == 0) report(p.hdr, CSA2_ERR_BOUNDS, v);
         v = p.max_n;
       }
     }
@@ -184,6 +187,7 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
       sm.acc_free[k] = 0;
     }
     for (int s = 0; s < IS_STAGES; s++) sm.ready[s] = 0;
+    tc::bar_init(&sm.test_bar, 1);
     sm.abort_flag = 0;
     tc::bar_init_fence();
   }
@@ -231,10 +235,21 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
   if (warp == 0) {
     // ================= producer
     int issued = 0;
+    if (p.test_withhold) {
+      // test hook: a bounded wait on a barrier that no thread, copy or MMA
+      // arrives on, before anything is issued; it gives up, and the abort
+      // stops every role with nothing in flight
+      if (lane == 0 && !tc::bar_wait(&sm.test_bar, 0, 1024u)) {
+        sm.abort_flag = 1;
+        report(p.hdr, CSA2_ERR_TIMEOUT, 2);
+      }
+      __syncwarp();
+    }
     if (!pool_mode) {
       if (lane == 0) {
         for (int i = 0; i < n; i++) {
           const int s = i % IS_STAGES;
+          if (sm.abort_flag) break;
           if (i >= IS_STAGES && !wait_or_abort(&sm.empty[s], ((i / IS_STAGES) - 1) & 1, sm, p.hdr)) break;
           const int64_t row0 = row_base + (t0 + i) * IS_TILE;
           int64_t rows = rows_total - row0;
@@ -265,6 +280,7 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
       };
       for (int i = 0; i < n; i++) {
         const int s = i % IS_STAGES;
+        if (sm.abort_flag) break;
         if (i >= IS_STAGES && !wait_or_abort(&sm.empty[s], ((i / IS_STAGES) - 1) & 1, sm, p.hdr)) break;
         uint8_t* codes = sm.stage[s];
         uint8_t* scl = sm.stage[s] + IS_CODES;
@@ -308,7 +324,8 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
       constexpr uint32_t id0 = tc::idesc_mxf4(IS_TILE, C::N, 0, 0);
       constexpr uint32_t id1 = tc::idesc_mxf4(IS_TILE, C::N, 2, 2);
       const uint32_t d = tmem + C::ACC_COL + k * C::N;
-      for (int i = k, use = 0; i < n; i += C::ISSUERS, use++) {
+      int use = 0;
+      for (int i = k; i < n; i += C::ISSUERS, use++) {
         const int s = i % IS_STAGES;
         if (!poll_at_least(&sm.ready[s], (uint32_t)(i + 1), sm, p.hdr)) break;
         if (use > 0 && !poll_at_least(&sm.acc_free[k], (uint32_t)(C::EPI_WARPS * use), sm, p.hdr)) break;
@@ -322,6 +339,9 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
         tc::commit(&sm.empty[s]);
         tc::commit(&sm.acc_full[k]);
       }
+      // after an abort the epilogue may stop reading: the MMAs already issued
+      // must finish before the accumulators' TMEM is released
+      if (sm.abort_flag && use > 0) tc::bar_wait(&sm.acc_full[k], (uint32_t)(use - 1) & 1u, 1u << 20);
     }
     __syncwarp();
   } else if (warp == C::PUB_WARP) {
@@ -388,24 +408,12 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
 }
 
 // ------------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
 // Index-code rows [rows][64 B] seen as [rows/4 groups g][4 members q][64 B], so
 // that one box of 32 groups x 4 members lands member-major: shared row 32q + g
 // holds entry 4g + q of the tile (the row order the scale-word copy needs), in
 // the SW64 layout.
 static bool encode_tile_rows(CUtensorMap* map, const void* base, uint64_t rows) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {64, rows / 4, 4};
   cuuint64_t strides[2] = {4 * 64, 64};
@@ -418,31 +426,32 @@ static bool encode_tile_rows(CUtensorMap* map, const void* base, uint64_t rows) 
 }
 
 static cudaError_t set_is_attrs() {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev == dev) return cudaSuccess;
   static_assert(IsCfg<1>::MIN_CTAS * (is_smem_bytes<1>() + 1024) <= 228 * 1024, "resident CTAs");
-  cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)is_smem_bytes<1>());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(index_score_tc_kernel<IS_GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)is_smem_bytes<IS_GROUP>());
-  if (e == cudaSuccess) attr_dev = dev;
-  return e;
+  static PerDeviceOnce attrs;
+  return attrs.ensure([](int) {
+    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)is_smem_bytes<1>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(index_score_tc_kernel<IS_GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)is_smem_bytes<IS_GROUP>());
+    return e;
+  });
 }
+
+// test hook of the calling host thread (csa2_test_withhold_arrival)
+static thread_local bool g_test_withhold = false;
+static void set_test_withhold(bool on) { g_test_withhold = on; }
 
 cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   if (p.B == 0 || p.Q == 0) return cudaSuccess;
+  p.test_withhold = g_test_withhold ? 1 : 0;
   cudaError_t ae = set_is_attrs();
   if (ae != cudaSuccess) return ae;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int num_sms = 148;
-  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  int num_sms = 0;
+  if ((ae = device_sms(&num_sms)) != cudaSuccess) return ae;
   const uint64_t rows = (uint64_t)p.B * (uint64_t)p.cap;
   if (rows == 0) return cudaSuccess;
   CUtensorMap map_tile;
@@ -454,7 +463,6 @@ cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   const bool grouped = p.pool == nullptr && p.Q >= IS_GROUP;
   const int nq = grouped ? IS_GROUP : 1;
   const int64_t groups = (int64_t)p.B * ceil_div(p.Q, nq);
-  if (groups > 65535) return cudaErrorInvalidValue;
   // one wave: as many CTAs as are resident at once (the launch bounds and the
   // shared-memory carveout guarantee MIN_CTAS per SM), at least 2 tiles per CTA
   const int64_t resident = (int64_t)(grouped ? IsCfg<IS_GROUP>::MIN_CTAS : IsCfg<1>::MIN_CTAS) * num_sms;
@@ -463,7 +471,9 @@ cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   if (split < 1) split = 1;
   const int64_t per = ceil_div(tiles, split);
   p.entries_per_cta = per;     // tiles per CTA
-  dim3 grid((unsigned)ceil_div(tiles, per), (unsigned)groups);
+  p.split = ceil_div(tiles, per);
+  if (groups * p.split > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)(groups * p.split));
   if (grouped)
     index_score_tc_kernel<IS_GROUP><<<grid, IsCfg<IS_GROUP>::THREADS, is_smem_bytes<IS_GROUP>(), stream>>>(
         p, map_tile);
@@ -472,5 +482,10 @@ cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Reindex: score the pool of every query and publish its top-K in one launch.
 }  // namespace csa2
+
+extern "C" csa2_status csa2_test_withhold_arrival(int enable) {
+  if (enable != 0 && enable != 1) return CSA2_ERR_INVALID_ARG;
+  csa2::set_test_withhold(enable != 0);
+  return CSA2_OK;
+}

@@ -35,6 +35,7 @@
 #include <cstddef>
 
 #include "index_query.cuh"
+#include "host_once.cuh"
 #include "params.cuh"
 #include "tc.cuh"
 
@@ -461,15 +462,11 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
 
 cudaError_t launch_reindex_select(IsParams p, cudaStream_t stream) {
   if (p.B == 0 || p.Q == 0) return cudaSuccess;
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(reindex_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)RX_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+  static PerDeviceOnce attrs;
+  cudaError_t e = attrs.ensure([](int) {
+    return cudaFuncSetAttribute(reindex_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RX_SMEM);
+  });
+  if (e != cudaSuccess) return e;
   const int64_t tiles = ceil_div((int64_t)p.M * BLK, RX_TILE);
   p.entries_per_cta = ceil_div(tiles, RX_CL);     // tiles per CTA (<= 22)
   if (p.entries_per_cta > RX_MAX_TILES) return cudaErrorInvalidValue;

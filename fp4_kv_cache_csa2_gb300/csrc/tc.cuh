@@ -63,15 +63,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// 1-D bulk copy global -> the same shared offset of every CTA in `cta_mask`;
-// each destination CTA's mbarrier at `bar`'s offset receives the byte count.
-__device__ __forceinline__ void bulk_load_multicast(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                                    uint16_t cta_mask) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-               " [%0], [%1], %2, [%3], %4;"
-               :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }

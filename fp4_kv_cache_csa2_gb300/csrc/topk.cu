@@ -14,6 +14,7 @@
 // keys equal to it.  Output ids are ascending and padded with -1.
 #include <mutex>
 
+#include "host_once.cuh"
 #include "params.cuh"
 
 namespace csa2 {
@@ -28,11 +29,12 @@ struct BlockMaxParams {
   int m, Q;
   int64_t max_n, nb_max;
   uint32_t* gkeys;       // [B*Q][nb_max]
+  int64_t per_row;       // CTAs per row
 };
 
 __global__ void block_max_kernel(BlockMaxParams p) {
-  const int bq = blockIdx.y;
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t bq = (int64_t)blockIdx.x / p.per_row;
+  const int64_t r = ((int64_t)blockIdx.x % p.per_row) * blockDim.x + threadIdx.x;
   int64_t nv = visible_entries(p.q_pos[bq], p.m, p.n_entries[bq / p.Q]);
   if (nv > p.max_n) nv = p.max_n;
   const int64_t nb = ceil_div(nv, BLK);
@@ -367,15 +369,14 @@ __global__ void __launch_bounds__(SEL_THREADS) select_topk_kernel(SelectParams p
 }
 
 static cudaError_t set_select_smem() {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev == dev) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_DYN_SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(block_topm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_DYN_SMEM);
-  if (e == cudaSuccess) attr_dev = dev;
-  return e;
+  static PerDeviceOnce attrs;
+  return attrs.ensure([](int) {
+    cudaError_t e =
+        cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_DYN_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(block_topm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_DYN_SMEM);
+    return e;
+  });
 }
 
 cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const int32_t* n_entries, int m,
@@ -384,9 +385,10 @@ cudaError_t launch_block_topk(const float* scores, const int64_t* q_pos, const i
   if (B == 0 || Q == 0) return cudaSuccess;
   const int64_t nb_max = ceil_div(max_n, BLK);
   if (nb_max > 0) {
-    BlockMaxParams bp{scores, q_pos, n_entries, m, Q, max_n, nb_max, gkeys};
-    dim3 grid((unsigned)ceil_div(nb_max, 256), B * Q);
-    block_max_kernel<<<grid, 256, 0, stream>>>(bp);
+    const int64_t per_row = ceil_div(nb_max, 256);
+    if ((int64_t)B * Q * per_row > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    BlockMaxParams bp{scores, q_pos, n_entries, m, Q, max_n, nb_max, gkeys, per_row};
+    block_max_kernel<<<(unsigned)((int64_t)B * Q * per_row), 256, 0, stream>>>(bp);
   }
   cudaError_t e = set_select_smem();
   if (e != cudaSuccess) return e;
@@ -944,10 +946,8 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
   const int64_t BQ = (int64_t)B * Q;
   if (BQ == 0) return cudaSuccess;
   if (max_n > 0x7FFFFFFF - 2 * (int64_t)RS_BATCH) return cudaErrorInvalidValue;   // entry ids are int32
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
+  static PerDeviceOnce attrs;
+  cudaError_t ae = attrs.ensure([](int) {
     cudaError_t e = cudaFuncSetAttribute(rs_resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          RS_RESOLVE_SMEM);
     if (e == cudaSuccess)
@@ -956,9 +956,9 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(rs_hist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                2 * RS_BINS * (int)sizeof(uint32_t));
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+    return e;
+  });
+  if (ae != cudaSuccess) return ae;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   unsigned char* cur = static_cast<unsigned char*>(scratch);
   RsParams p{};
@@ -971,8 +971,8 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
   p.M = pool ? M : 0;
   p.max_n = max_n;
   // one wave of scan CTAs where the rows allow it: batches per CTA from the total
-  int dev_sms = 148;
-  cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, dev);
+  int dev_sms = 0;
+  if ((ae = device_sms(&dev_sms)) != cudaSuccess) return ae;
   const int64_t row_batches = max_n > 0 ? ceil_div(max_n, RS_BATCH) : 1;
   int64_t per = ceil_div(BQ * row_batches, (int64_t)RS_SCAN_CTAS_PER_SM * dev_sms);
   if (per < 1) per = 1;
@@ -1048,6 +1048,7 @@ extern "C" csa2_status csa2_block_topk_static(const csa2_cache* cache, const flo
   if (cache->m != 1 && cache->m != 2) return CSA2_ERR_UNSUPPORTED;
   if (B < 0 || Q < 0 || max_n < 0) return CSA2_ERR_INVALID_ARG;
   if (M < 1 || M > CSA2_MAX_M) return CSA2_ERR_UNSUPPORTED;
+  if ((int64_t)B * Q > ((int64_t)1 << 26)) return CSA2_ERR_UNSUPPORTED;     // as every other call
   if ((uint64_t)B * (uint64_t)Q * (uint64_t)ceil_div(max_n, BLK) > STATIC_BLOCK_KEYS) return CSA2_ERR_WORKSPACE;
   if (B == 0 || Q == 0) return CSA2_OK;
   if (!scores || !q_pos || !pool_blocks) return CSA2_ERR_INVALID_ARG;

@@ -31,10 +31,12 @@
  *     aligned, initialised once with csa2_workspace_init.  Its first
  *     CSA2_WS_HEADER_BYTES hold the status word.  Calls that overlap on the GPU
  *     must not share a workspace.
- *   - The library keeps no state between calls and is thread safe.  No C++
+ *   - The library keeps no state between calls other than per-device launch
+ *     attributes, set once per device under a lock, so any number of host
+ *     threads may call it at once (each with its own workspace).  No C++
  *     exception crosses this boundary.
- *   - Sizes: K <= 512, M <= 2048, m in {1, 2}.  Other values return
- *     CSA2_ERR_UNSUPPORTED.
+ *   - Sizes: K <= 512, M <= 2048, m in {1, 2}, B * Q <= 67,108,864 (2^26).
+ *     Other values return CSA2_ERR_UNSUPPORTED.
  *   - Visibility: a query at raw token position t sees the entries
  *     j < min(n_entries[b], floor((t+1)/m)) and the window positions
  *     max(0, t-127) .. t ([dilfish] §4.2: an m=2 entry exists once both of its
@@ -208,6 +210,9 @@ csa2_status csa2_block_topk(const csa2_cache *cache, const float *scores, const 
  *     until the process exits.
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: do not use this call
+ *     on a device after cudaDeviceReset (or any teardown of its primary
+ *     context) in the same process.
  *   - All calls share the one array and it keeps the previous call's contents
  *     (nothing in it needs to start at zero).  Calls that may overlap on the
  *     GPU (different streams without ordering, other threads, other processes
@@ -354,6 +359,20 @@ typedef struct {
 size_t csa2_decode_workspace_size(csa2_mode mode, int B, int Q, int64_t max_n, int M, int K);
 csa2_status csa2_decode(const csa2_cache *cache, const csa2_decode_args *args, void *ws,
                         size_t ws_bytes, void *stream);
+
+/*
+ * Test hook for the device-side timeout path; off unless a caller turns it on,
+ * and never needed in production.  The pages have no counterpart.
+ * While enabled (enable = 1) on the calling host thread, every index-scan
+ * launch that thread makes (csa2_index_score, the scan of a Full decode)
+ * first waits, with a short bound (1024 polls), on an mbarrier that no thread,
+ * copy or MMA ever arrives on.  The wait gives up before the kernel has issued
+ * any copy or MMA; the kernel then records CSA2_ERR_TIMEOUT (detail 2) in the
+ * workspace status word, stops every warp role, frees its TMEM and returns,
+ * leaving the context usable.  Its scores are not written.  enable = 0 turns
+ * it off.  Errors: INVALID_ARG for any other value.
+ */
+csa2_status csa2_test_withhold_arrival(int enable);
 
 #ifdef __cplusplus
 }

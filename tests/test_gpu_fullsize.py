@@ -224,6 +224,12 @@ def test_config4_reindex_and_reuse_at_1m_entries(csa2):
     # source layer: the pool
     s0 = oracle.index_scores(h[0]["q_idx"][b, 0], h[0]["w_head"][b, 0], codes, scales)
     check_pool(got_pool, oracle.block_topm(s0, N, M_BLK), s0, N, "source-layer pool")
+    # source layer: its own top-512 over all 1M visible entries (a row this long
+    # has its chosen ids put in order by the bitonic sort of the resolve step)
+    got0 = h[0]["sel"][b, 0]
+    want0 = oracle.select_topk(s0, np.arange(N), K_SEL)
+    cases.assert_set_within_tie_window(got0, want0, lambda j: s0[j], what="Full sel at 1M")
+    assert np.all(np.diff(got0) > 0) and got0.min() >= 0 and got0.max() < N, "Full sel ascending, in range"
     # Reindex: the layer's own scores over the pool, top-512
     dom = oracle.pool_entries(got_pool, N)
     s1 = np.full(N, -np.inf)

@@ -81,6 +81,18 @@ def test_long_rows_match_oracle_exactly(csa2, kind):
     _run(csa2, kind, 7100 + len(kind), 1, max_n, [max_n, 150_000], q_pos)
 
 
+@pytest.mark.parametrize("kind", ["normal", "grid"])
+def test_rows_past_the_bitmap_limit_match_oracle_exactly(csa2, kind):
+    """Rows of more than 524,288 visible entries, where the resolve step puts
+    the chosen ids in order with a bitonic sort instead of the row bitmap:
+    600,011-entry rows, with causal queries of 555,556 and 580,000 visible
+    entries beside one of exactly 524,288 (the last row length that takes the
+    bitmap) in the same call."""
+    max_n = 600_011
+    q_pos = np.array([[600_010, 524_287], [555_555, 2_000_000]])
+    _run(csa2, kind, 7500 + len(kind), 1, max_n, [max_n, 580_000], q_pos)
+
+
 def test_long_rows_with_short_and_empty_queries(csa2):
     """m = 2 rows where some queries see fewer than K entries or fewer than M
     blocks (all of them are chosen), and one sees nothing."""

@@ -97,6 +97,52 @@ def test_variant_calls_host_logic_without_gpu(lib_path):
     assert lib.csa2_decode(ctypes.byref(cache), ctypes.byref(a), ws, need, None) == 1
 
 
+def test_query_count_limit_and_concurrent_argument_checks(lib_path):
+    """More than 2^26 queries in one call is refused before anything is
+    enqueued (every grid is one-dimensional), by the regular and the
+    allocation-free candidate-block calls alike.  Host threads calling the
+    argument checks at once all get the same answers (ctypes releases the GIL
+    for the foreign calls, so the calls do overlap)."""
+    import threading
+    import fp4_kv_cache_csa2_gb300 as csa2
+    lib = csa2.load(lib_path)
+    fake = ctypes.c_void_p(1 << 20)                     # never dereferenced: the calls fail on arguments
+    n = ctypes.c_int32(0)
+    cache = csa2.CacheStruct(fake.value, fake.value, fake.value, 64, ctypes.addressof(n), 1)
+    ws = ctypes.c_void_p(1 << 24)
+    big_b, big_q = 1 << 13, (1 << 13) + 1               # 67,117,056 queries > 2^26
+    cases = [
+        (lambda: lib.csa2_block_topk_static(ctypes.byref(cache), fake, fake, big_b, big_q, 0, 4, fake, None), 2),
+        (lambda: lib.csa2_block_topk(ctypes.byref(cache), fake, fake, big_b, big_q, 0, 4, fake, ws, 1 << 30,
+                                     None), 2),
+        (lambda: lib.csa2_select_topk(ctypes.byref(cache), fake, fake, None, 0, 8, fake, big_b, big_q, 0, ws,
+                                      1 << 30, None), 2),
+        (lambda: lib.csa2_block_topk_static(ctypes.byref(cache), fake, fake, 1, 1, 8, 0, fake, None), 2),
+        (lambda: lib.csa2_block_topk_static(None, fake, fake, 1, 1, 8, 4, fake, None), 1),
+        (lambda: lib.csa2_select_topk(ctypes.byref(cache), fake, fake, None, 0, 8, fake, 1, 1, 64, None, 0, None),
+         3),
+    ]
+    for call, want in cases:
+        assert call() == want
+    errors = []
+
+    def worker():
+        try:
+            for _ in range(300):
+                for call, want in cases:
+                    got = call()
+                    if got != want:
+                        errors.append((want, got))
+        except Exception as e:                          # pragma: no cover - reported below
+            errors.append(e)
+    threads = [threading.Thread(target=worker) for _ in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:5]
+
+
 def test_rope_table_matches_oracle_bit_for_bit(lib_path):
     """The library's table builder and the oracle's are separate restatements of
     cos/sin(p * theta^(-2i/64)); their binary32 tables agree."""

@@ -535,7 +535,6 @@ def test_attention_brute_force():
     g, main, q, swa = _attn_inputs(15, 12, 20)
     sel = np.array([3, -1, 0, 11, 7], np.int32)
     t, base = 9, 0
-    got = oracle.attention(q[:2], sel, main, swa, base, t, 1 / math.sqrt(512)) if False else None
     qq = q.copy()
     out = oracle.attention(qq, sel, main, swa, base, t, 1 / math.sqrt(512))
     V = [oracle.dequant_main(main[j]) for j in (3, 0, 11, 7)]
@@ -648,6 +647,60 @@ def test_modes_reuse_equals_full_attention_and_reindex_all_blocks():
                                       pool_blocks=np.arange(15, dtype=np.int32), **common)
     np.testing.assert_array_equal(sel_x, sel)                   # pool = all blocks -> same as Full
     assert len(oracle.pool_entries(pool, n)) <= 15 * 8
+
+
+def _reindex_brute_force(scores_all, pool_blocks, nv, K):
+    """Reindex selection written out from the page's statement (a Reindex layer
+    scores only the candidate pool and takes its own top-K there; zartbot
+    §2.3.4): walk the pool's blocks, keep their entries that the query sees,
+    rank them by (score desc, id asc), keep K, list them ascending, pad -1."""
+    cand = []
+    for blk in pool_blocks:
+        if blk < 0:
+            continue
+        for r in range(8):
+            j = 8 * int(blk) + r
+            if j < nv:
+                cand.append(j)
+    ranked = sorted(cand, key=lambda j: (-scores_all[j], j))[:K]
+    return sorted(ranked) + [-1] * (K - len(ranked))
+
+
+@pytest.mark.parametrize("K,pool", [(16, [4, 1, -1]), (5, [4, 1, -1]), (6, [2, -1, 0, -1])])
+def test_reindex_partial_pool_brute_force(K, pool):
+    """Reindex with a pool that covers only some blocks: the newest chosen block
+    (entries 32..39) is seen only up to entry 36, and with K = 16 the pool holds
+    fewer visible entries (13) than K.  Entries outside the pool or past the
+    visible width must never be chosen, and the output is the attention over
+    exactly that selection."""
+    g = synth.rng(19)
+    n, t = 40, 36                                # 40 entries cached, 37 visible at t = 36 (m = 1)
+    x = synth.latents(g, n)
+    w0, w1 = synth.compressor_weights(g)
+    W = synth.index_projection(g)
+    main, codes, scales = oracle.compress_quantize(x, 1, w0, w1, W)
+    q = synth.main_queries(g)
+    q_idx = synth.index_queries(g)
+    wh = synth.head_weights(g)
+    swa = synth.swa_rows(g, 64)
+    nv = oracle.visible_entries(t, 1, n)
+    assert nv == 37
+    pool_blocks = np.array(pool, np.int32)
+    scores_all = oracle.index_scores(q_idx, wh, codes, scales)        # every entry, no domain argument
+    want_sel = _reindex_brute_force(scores_all, pool, nv, K)
+    common = dict(t=t, m=1, n_entries=n, main_kv=main, idx_codes=codes, idx_scales=scales, q=q, swa=swa,
+                  swa_base=0, scale=1 / math.sqrt(512), K=K, M=len(pool))
+    got_pool, sel, out = oracle.decode_query(oracle.REINDEX, q_idx=q_idx, w_head=wh, pool_blocks=pool_blocks,
+                                             **common)
+    assert list(sel) == want_sel
+    np.testing.assert_array_equal(got_pool, pool_blocks)             # the pool is an input, passed through
+    if K == 16:
+        assert want_sel[13:] == [-1, -1, -1] and max(want_sel) <= 36
+    # the best entries overall lie outside the pool: ignoring the pool would change the selection
+    top_all = sorted(range(nv), key=lambda j: (-scores_all[j], j))[:K]
+    assert set(top_all) != set(j for j in want_sel if j >= 0)
+    np.testing.assert_array_equal(out, oracle.attention(q, np.array(want_sel, np.int32), main, swa, 0, t,
+                                                        1 / math.sqrt(512)))
 
 
 def test_visibility_rule():

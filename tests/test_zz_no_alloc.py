@@ -8,6 +8,8 @@ failure here never hides the other tests; it also passes on its own."""
 import numpy as np
 import pytest
 
+import oracle
+import synth
 from tests import cases
 
 torch = pytest.importorskip("torch")
@@ -70,3 +72,41 @@ def test_static_block_topk_rejects_requests_beyond_the_scratch(csa2):
                                 8_388_616, 4, out)
     assert st == 3                                        # CSA2_ERR_WORKSPACE, nothing enqueued
     assert csa2.block_topk_static(cache, scores, q_pos, 8, 4, out) == 0
+
+
+@pytest.mark.parametrize("max_n,n_entries,q_pos", [
+    (131_072, [131_072], [[131_071, 131_064, 70_000, 5]]),
+    (200_003, [200_003], [[200_002, 150_000, 131_073, 9]]),
+])
+def test_static_block_topk_long_rows_match_regular_call_and_oracle(csa2, max_n, n_entries, q_pos):
+    """Rows long enough that the two calls take different routes: the regular
+    call hands rows over 16,384 entries to the multi-CTA row selection, the
+    allocation-free call keeps its block maxima in the fixed array and selects
+    past 131,072 entries with the single-CTA radix select.  Both must give the
+    oracle's blocks exactly, the forced newest block and the order of equal
+    maxima included; q_pos makes the queries see different prefixes."""
+    q_pos = np.array(q_pos, np.int64)
+    B, Q = q_pos.shape
+    M = 2048
+    cache = csa2.Cache(B, max_n + (-max_n) % 8, 1, device="cuda")
+    cache.n_entries.copy_(torch.tensor(n_entries, dtype=torch.int32))
+    g = synth.rng(990 + max_n % 97)
+    s = (np.round(g.standard_normal((B, Q, max_n)) * 16) / 16).astype(np.float32)   # many equal maxima
+    scores = torch.from_numpy(s).to("cuda")
+    d_pos = torch.from_numpy(q_pos).to("cuda")
+    ws = csa2.Workspace(csa2.block_topk_workspace_size(B, Q, max_n), device="cuda")
+    want = torch.full((B, Q, M), -7, dtype=torch.int32, device="cuda")
+    csa2.block_topk(cache, scores, d_pos, max_n, M, want, ws)
+    assert ws.sync_status()[0] == 0
+    for _ in range(2):
+        got = torch.full_like(want, -7)
+        assert csa2.block_topk_static(cache, scores, d_pos, max_n, M, got) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+    got_h = got.cpu().numpy()
+    for b in range(B):
+        for qi in range(Q):
+            nv = min(oracle.visible_entries(int(q_pos[b, qi]), 1, n_entries[b]), max_n)
+            np.testing.assert_array_equal(got_h[b, qi], oracle.block_topm(s[b, qi].astype(np.float64), nv, M),
+                                          err_msg=f"b={b} q={qi} nv={nv}")
+
