@@ -8,45 +8,39 @@
 // more precise format before attention: FP4 saves storage, it does not feed
 // the matrix multiply); "4. 层维度(下):CSA2 与每 token 890 字节" §4.5.
 //
-// One thread-block cluster of C CTAs per query token, 128 keys per CTA: CTAs
-// 0..C-2 take the K selected slots in runs of 128, CTA C-1 the 128 window
-// positions.  In every CTA:
-//   * Q (64 heads x 512, bf16) lands by TMA in 8 SW128 column chunks;
-//   * keys land in shared memory as bf16 [128 keys][512] in 8 SW128 column
-//     chunks of 64 dims: window rows by 2-D TMA straight from the bf16 window
-//     (FP8 window: 64-byte column slices of the E4M3 rows land in the upper
-//     half of each chunk and every thread widens its row half to bf16 in place,
-//     exactly, two chunks per CTA barrier);
-//     selected FP4 entries by 16-byte asynchronous copies into a staging
-//     buffer (consecutive threads take consecutive pieces of an entry), from
-//     there into registers, two lanes per entry, after which Q chunks 4..7 are
-//     loaded over the staging buffer; every warp then dequantises its 16 keys
-//     exactly (E2M1 -> bf16 by byte permutes, times the E4M3 scale; the
-//     product has at most 6 significant bits);
+// One CTA per query token streams its keys in chunks of 128: chunk 0 is the
+// window (positions t-127 .. t), chunks 1.. are the selected slots in runs of
+// 128.  One softmax over all of them is kept online (running maxima per head,
+// rescaling the accumulated output only when a chunk's maximum exceeds the
+// one in use by more than A_TAU, so that exp() never exceeds e^A_TAU).
+//   * Q (64 heads x 512, bf16) lands once by TMA in 8 SW128 column chunks.
+//   * The key buffer holds one chunk as bf16 [128 keys][512] in 8 SW128 column
+//     chunks of 64 dims (16 KB each).  The window chunk lands by 2-D TMA (an
+//     FP8 window as 64-byte E4M3 column slices in the upper half of each column
+//     chunk, widened to bf16 in place, exactly).  A selected chunk is
+//     dequantised by the 8 math warps from registers: every thread loads its
+//     key's FP4 bytes for the next chunk while the current one is processed
+//     (2 threads per key, 64 dims of each 128-dim tile per thread), so the
+//     gather's latency hides behind a whole chunk.  E2M1 -> bf16 by byte
+//     permutes times the E4M3 scale: the product has at most 6 significant
+//     bits, so the bf16 key is exact.
 //   * S^T = K Q^T is an M=128 (keys) x N=64 (heads) x K=512 tcgen05 bf16 MMA
-//     product, issued as two chains of 16 back-to-back MMAs (dims 0..255 and
-//     256..511) into two TMEM accumulators by two threads at once (a chain is
-//     bound by its thread's issue rate); the softmax adds the two halves;
-//   * softmax over this CTA's keys with its own row maxima m_c, straight from
-//     TMEM (thread = key, 32 heads in registers; per-warp column maxima and
-//     sums by transpose-reductions over the lanes): P = exp(S - m_c) becomes
-//     the MN-major bf16 B operand [key][head] of the second product, L_c = sum P;
-//   * O^T = V^T P^T reuses the key buffer as an MN-major A operand: 4 tiles of
-//     M=128 dims x N=64 heads x K=128 keys, one issuing thread per tile;
-//   * every CTA bulk-copies its (m_c, L_c) rows to every owner as soon as its
-//     second product is done, then stages its normalised share O_c / L_c of
-//     each 128-dim tile in fp16 (a convex combination of key vectors, relative
-//     rounding 2^-11) and bulk-copies the tiles it does not own into the
-//     owners' receive slots over distributed shared memory, one mbarrier per
-//     slot; the owner weights the C shares by
-//     L_c exp(m_c - M) / sum_c' L_c' exp(m_c' - M), M = max_c m_c, in fp32,
-//     folds each share in as it lands, rounds to bf16 and stores.  Two split
-//     cluster barriers order the exchange (phase 1: every mbarrier is
-//     initialised; phase 2: every receive slot is dead); no CTA reads another's
-//     shared memory, and the owners' byte counts make a closing cluster
-//     barrier unnecessary.
-// All mbarrier waits are bounded; a timeout reports CSA2_ERR_TIMEOUT.
-#include <cooperative_groups.h>
+//     product issued as four chains of 8 MMAs (dims 128t .. 128t + 127, one
+//     TMEM accumulator each) by four threads; chain t starts as soon as tile t
+//     of the key buffer is written (for the window: as soon as its TMA lands).
+//   * Softmax straight from TMEM (thread = key, 32 heads in registers, the four
+//     partial products added; column maxima and sums by transpose-reductions
+//     over the lanes, the four warps of a head half meet on a named barrier),
+//     in base-2 units (the scale carries log2 e): P = 2^(S - m) becomes the
+//     MN-major bf16 B operand [key][head] of the second product.
+//   * O^T += V^T P^T reuses the key buffer as an MN-major A operand: 4 tiles of
+//     M=128 dims x N=64 heads x K=128 keys, accumulated over the chunks in TMEM,
+//     one issuing thread per tile.  Once tile t of a chunk is done, its two
+//     column chunks are free and the next chunk's dequantisation writes them.
+//   * At the end every thread divides its dim row of O^T by the head sums and
+//     stores bf16 rows of the output.
+// All mbarrier waits are bounded; a timeout reports CSA2_ERR_TIMEOUT and the
+// kernel still runs to its end (every thread takes every barrier).
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -54,51 +48,39 @@
 #include "params.cuh"
 #include "tc.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace csa2 {
 
-constexpr int AT_THREADS = 256;
-constexpr int AT_KEYS = 128;                  // keys per CTA (one M = 128 tile)
-constexpr int AT_MAXC = CSA2_MAX_K / AT_KEYS + 1;
-constexpr int AT_CHUNK_BYTES = AT_KEYS * 128;            // [128 keys][64 dims] bf16 = 16 KB
-constexpr int AT_QCHUNK_BYTES = H * 128;                 // [64 heads][64 dims] bf16 = 8 KB
-constexpr int AT_OFF_K = 0;                              // 8 key chunks, 128 KB
-constexpr int AT_OFF_Q = 8 * AT_CHUNK_BYTES;             // Q chunks 0..3, 32 KB; 4..7 follow over the staging
-constexpr int AT_OFF_STAGE = AT_OFF_Q + 4 * AT_QCHUNK_BYTES;   // FP4 staging [128][288], then Q chunks 4..7
-constexpr int AT_STAGE_BYTES = AT_KEYS * MAIN_BYTES;     // 36,864
-constexpr int AT_OFF_P = AT_OFF_Q;                       // after S: P^T [128 keys][64 heads] bf16 SW128, 16 KB
-constexpr int AT_OFF_SMALL = AT_OFF_STAGE + AT_STAGE_BYTES;
-constexpr int AT_SHARE_BYTES = 128 * H * 2;             // one O^T tile share in fp16: 16 KB
-constexpr int AT_OFF_RECV = AT_OFF_Q;                    // after O: 4 receive slots over the Q region
-constexpr int AT_TMEM_COLS = 512;                        // S^T halves at 0 and 320, O^T: 4 x 64 cols from 64
-constexpr int AT_S2_COL = 320;                            // S^T over dims 256..511
+constexpr int A_MATH_WARPS = 8;                         // dequantisation, softmax, output
+constexpr int A_MATH = 32 * A_MATH_WARPS;
+constexpr int A_THREADS = A_MATH + 4 * 32;              // + 4 MMA-issuing warps (one also loads, one owns TMEM)
+constexpr int A_KEYS = 128;                             // keys per chunk (one M = 128 tile)
+constexpr int A_CHUNK_BYTES = A_KEYS * 128;             // [128 keys][64 dims] bf16 = 16 KB
+constexpr int A_QCHUNK_BYTES = H * 128;                 // [64 heads][64 dims] bf16 = 8 KB
+constexpr int A_OFF_K = 0;                              // 8 key column chunks, 128 KB
+constexpr int A_OFF_Q = 8 * A_CHUNK_BYTES;              // 8 Q column chunks, 64 KB
+constexpr int A_OFF_P = A_OFF_Q + 8 * A_QCHUNK_BYTES;   // P^T [128 keys][64 heads] bf16 SW128, 16 KB
+constexpr int A_OFF_SMALL = A_OFF_P + A_KEYS * H * 2;
+constexpr int A_TMEM_COLS = 512;
+constexpr int A_S_COL = 0;                              // S^T partial of tile t at 64 t
+constexpr int A_O_COL = 256;                            // O^T tile t at 256 + 64 t
+constexpr float A_LOG2E = 1.4426950408889634f;
+constexpr float A_TAU = 8.0f * A_LOG2E;                 // lazy rescale threshold: 2^A_TAU = e^8
 
-struct AtSmall {
-  int kvalid[AT_KEYS];
-  int32_t kid[AT_KEYS];
-  alignas(16) float ml[2 * H];           // this CTA's row maxima m_c, then row sums L_c (sent to the owners)
-  alignas(16) float recv_ml[4][2 * H];   // (m, L) rows received from each other CTA (index = sender rank,
-                                         // minus one above this CTA's own)
-  float inv_l[H];
-  float red[4][H];                       // per-warp column maxima (warp w & 3, head)
-  float red_sum[4][H];                   // per-warp column sums
-  float wgt[AT_MAXC][H];                 // combination weight of each CTA's share, per head
-  uint64_t bar_kv, bar_s, bar_o;
-  uint64_t bar_ml;                       // every other CTA's (m, L) rows received (owners only)
-  uint64_t bar_slot[4];                  // receive slot s holds a complete share
-  uint64_t bar_q;                        // all of Q landed (chunks 0..3 and 4..7: two arrivals)
-  uint64_t bar_keys;                     // every warp's dequantised keys are in shared memory
-  uint64_t bar_pk;                       // the packed selected entries landed in the staging buffer
+struct AsSmall {
+  int32_t ids[CSA2_MAX_K];            // the query's selected entry ids
+  float red[A_MATH_WARPS][32];        // per-warp column maxima / sums (warp 4 hh + q: head 32 hh + lane)
+  alignas(16) float mv[A_MATH_WARPS][32];   // each warp's maxima in use, read back by all of its lanes
+  uint64_t q_full[4], win_full[4];    // TMA: Q / window column chunks 2t, 2t + 1
+  uint64_t kready[4];                 // tile t (dims 128t ..) of a chunk is in the key buffer (8 arrivals)
+  uint64_t s_full;                    // the four S^T chains of a chunk are done (4 commits)
+  uint64_t p_ready;                   // P^T written, O^T rescaled if needed (8 arrivals)
+  uint64_t pv_done[4];                // O^T tile t of a chunk is done (1 commit)
   uint32_t tmem_base;
   int err;
 };
-constexpr int AT_SMEM = AT_OFF_SMALL + (int)sizeof(AtSmall) + 1024;
-static_assert(4 * AT_QCHUNK_BYTES <= AT_STAGE_BYTES, "Q chunks 4..7 must fit over the staging");
-static_assert(AT_THREADS / 32 * 8 == H, "the combine gives every warp one 8-head unit");
-static_assert(AT_OFF_STAGE % 1024 == 0, "SW128 destinations are 1 KB aligned");
-static_assert(4 * AT_SHARE_BYTES <= 8 * AT_CHUNK_BYTES, "O^T shares must fit over the keys");
-static_assert(4 * AT_SHARE_BYTES <= 8 * AT_QCHUNK_BYTES, "receive slots must fit over Q");
+constexpr int A_SMEM = A_OFF_SMALL + (int)sizeof(AsSmall) + 1024;
+static_assert(A_OFF_Q % 1024 == 0 && A_OFF_P % 1024 == 0, "SW128 regions are 1 KB aligned");
+static_assert(A_SMEM <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -148,555 +130,427 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte) {
   return row * 128u + ((((byte >> 4) ^ (row & 7u)) << 4) | (byte & 15u));
 }
 
-__device__ __forceinline__ bool at_wait(uint64_t* bar, uint32_t parity, AtSmall& sm, WsHeader* hdr, int where) {
+// 2^x, approximate (the MUFU unit), subnormal results flushed to zero
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ bool as_wait(uint64_t* bar, uint32_t parity, AsSmall& sm, WsHeader* hdr, int where) {
   if (tc::bar_wait(bar, parity)) return true;
   if (atomicExch(&sm.err, 1) == 0) report(hdr, CSA2_ERR_TIMEOUT, where);
   return false;
 }
 
+// The issuing threads wait with a short sleep between polls, leaving issue
+// slots to the math warps of their SM sub-partition.
+__device__ __forceinline__ bool as_wait_sleepy(uint64_t* bar, uint32_t parity, AsSmall& sm, WsHeader* hdr,
+                                               int where) {
+  for (uint32_t it = 0; it < 4000000u; it++) {
+    if (tc::bar_wait(bar, parity, 1u)) return true;
+    __nanosleep(64);
+  }
+  if (atomicExch(&sm.err, 1) == 0) report(hdr, CSA2_ERR_TIMEOUT, where);
+  return false;
+}
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
-attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_swa,
-               int C) {
+// 32 consecutive TMEM columns of this thread's lane -> r (waited)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  tc::tmem_ld_x32_nowait(taddr, r);
+  tc::tmem_wait_ld_regs(r);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                  "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+                  "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+                  "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+                  "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+
+// transpose-reduction over the 32 lanes of a warp: afterwards lane l holds the
+// reduction of column l (r[l] of every lane); r is destroyed
+template <bool MAX>
+__device__ __forceinline__ float lane_columns(float* r, int lane) {
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) {
+    const bool upper = (lane & k) != 0;
+#pragma unroll
+    for (int i = 0; i < k; i++) {
+      const float send = upper ? r[i] : r[i + k];
+      const float keep = upper ? r[i + k] : r[i];
+      const float got = __shfl_xor_sync(0xFFFFFFFFu, send, k);
+      r[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return r[0];
+}
+
+__global__ void __launch_bounds__(A_THREADS, 1)
+attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_swa) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  unsigned char* kbuf = smem + AT_OFF_K;
-  unsigned char* qbuf = smem + AT_OFF_Q;
-  unsigned char* pbuf = smem + AT_OFF_P;
-  unsigned char* stage = smem + AT_OFF_STAGE;
-  AtSmall& sm = *reinterpret_cast<AtSmall*>(smem + AT_OFF_SMALL);
-  __half* ostage = reinterpret_cast<__half*>(kbuf);          // 4 tiles x [128 dims][64 heads] fp16 shares
-  __half* orecv = reinterpret_cast<__half*>(smem + AT_OFF_RECV); // up to 4 received shares
+  unsigned char* kbuf = smem + A_OFF_K;
+  unsigned char* qbuf = smem + A_OFF_Q;
+  unsigned char* pbuf = smem + A_OFF_P;
+  AsSmall& sm = *reinterpret_cast<AsSmall*>(smem + A_OFF_SMALL);
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
-  const int bq = blockIdx.x / C;
+  const int bq = blockIdx.x;
   const int b = bq / p.Q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool window_cta = rank == C - 1;
-  const int slot0 = rank * AT_KEYS;
+  const int K = p.K;
+  const int nc = 1 + (K + A_KEYS - 1) / A_KEYS;          // window chunk + selected chunks
 
-  // ---------------- set-up
-  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, AT_TMEM_COLS);
+  // ---------------- set-up (reads no input: overlaps the previous kernel under PDL)
+  if (warp == A_MATH_WARPS + 3) tc::tmem_alloc(&sm.tmem_base, A_TMEM_COLS);
   if (tid == 0) {
-    tc::bar_init(&sm.bar_kv, 1);
-    tc::bar_init(&sm.bar_s, 2);                          // two S^T chains
-
-    tc::bar_init(&sm.bar_o, 4);                          // four O^T tiles
-    tc::bar_init(&sm.bar_ml, 1);
-    for (int i = 0; i < 4; i++) tc::bar_init(&sm.bar_slot[i], 1);
-    tc::bar_init(&sm.bar_q, 2);
-    tc::bar_init(&sm.bar_keys, AT_THREADS / 32);
-    tc::bar_init(&sm.bar_pk, 1);
+    for (int u = 0; u < 4; u++) {
+      tc::bar_init(&sm.q_full[u], 1);
+      tc::bar_init(&sm.win_full[u], 1);
+      tc::bar_init(&sm.kready[u], A_MATH_WARPS);
+    }
+    tc::bar_init(&sm.s_full, 4);
+    tc::bar_init(&sm.p_ready, A_MATH_WARPS);
+    for (int t = 0; t < 4; t++) tc::bar_init(&sm.pv_done[t], 1);
     sm.err = 0;
     tc::bar_init_fence();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp >= A_MATH_WARPS && lane == 0) {
     tc::prefetch_tensormap(&map_q);
     tc::prefetch_tensormap(&map_swa);
   }
-  // everything above reads no input: with programmatic dependent launch it
-  // overlaps the previous kernel, which may have produced q, sel or the window
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // this CTA's run of a packed selection: one contiguous copy, in flight while
-  // the ids are read (they still say which slots exist)
-  const int n_sel = window_cta ? 0 : min(AT_KEYS, p.K - slot0);
-  if (p.packed_in && !window_cta && tid == 0) {
-    tc::bar_arrive_expect_tx(&sm.bar_pk, (uint32_t)(n_sel * MAIN_BYTES));
-    tc::bulk_load(stage, p.packed_in + ((int64_t)bq * p.K + slot0) * MAIN_BYTES, (uint32_t)(n_sel * MAIN_BYTES),
-                  &sm.bar_pk);
-  }
   const int64_t t = p.q_pos[bq];
-  if (tid < AT_KEYS) {                       // which keys of this CTA exist
-    int kind = 0;
-    int32_t id = 0;
-    if (!window_cta) {
-      const int gs = slot0 + tid;
-      if (gs < p.K) {
-        id = p.sel[(int64_t)bq * p.K + gs];
-        if (id >= 0 && id < p.cap) kind = 1;
-        else if (id >= p.cap) report(p.hdr, CSA2_ERR_BOUNDS, id);
-      }
-    } else {
-      const int64_t pos = t - (WIN - 1) + tid;
-      if (pos >= 0) {
-        const int64_t row = pos - p.swa_base[b];
-        if (row >= 0 && row < p.S) kind = 2;
-        else report(p.hdr, CSA2_ERR_BOUNDS, pos);
-      }
-    }
-    sm.kvalid[tid] = kind;
-    sm.kid[tid] = kind == 1 ? id : 0;
-  }
+  for (int i = tid; i < K; i += A_THREADS) sm.ids[i] = p.sel[(int64_t)bq * K + i];
   tc::fence_before_sync();
-  __syncthreads();                       // local barriers and key flags visible (no remote access yet)
+  __syncthreads();
   tc::fence_after_sync();
-  // cluster barrier phase 1 (waited on after the second product): every CTA's
-  // mbarriers are initialised before any other CTA signals them (the init
-  // fence above releases them, so the arrival itself can be relaxed)
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const uint32_t tmem = sm.tmem_base;
 
-  // ---------------- copies: window rows (window CTA) and all of Q
-  if (tid == 0) {
-    if (window_cta) {
-      if (p.S > 0) {         // rows outside this sequence's window are masked (kvalid == 0) but finite
+  if (warp >= A_MATH_WARPS) {
+    // ================= MMA issuers: warp 8 + u issues, for every chunk, the S^T
+    // chain of tile u (dims 128u .. 128u + 127) and O^T tile u; first it loads
+    // tile u's Q and window column chunks by TMA
+    const int u = warp - A_MATH_WARPS;
+    if (lane == 0) {
+      tc::bar_arrive_expect_tx(&sm.q_full[u], 2u * A_QCHUNK_BYTES);
+      for (int c = 2 * u; c < 2 * u + 2; c++)
+        tc::tma_load_2d(qbuf + c * A_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.q_full[u]);
+      if (p.S > 0) {         // rows outside this sequence's window are masked, but finite
         const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
-        if (p.swa_fp8) {     // [128 rows][64 B] E4M3 slices into the upper half of each chunk
-          tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * (AT_CHUNK_BYTES / 2));
-          for (int c = 0; c < 8; c++)
-            tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES + AT_CHUNK_BYTES / 2, &map_swa, c * 64, row0, &sm.bar_kv);
+        if (p.swa_fp8) {     // [128 rows][64 B] E4M3 slices into the upper half of each column chunk
+          tc::bar_arrive_expect_tx(&sm.win_full[u], 2u * (A_CHUNK_BYTES / 2));
+          for (int c = 2 * u; c < 2 * u + 2; c++)
+            tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES + A_CHUNK_BYTES / 2, &map_swa, c * 64, row0, &sm.win_full[u]);
         } else {
-          tc::bar_arrive_expect_tx(&sm.bar_kv, 8u * AT_CHUNK_BYTES);
-          for (int c = 0; c < 8; c++) tc::tma_load_2d(kbuf + c * AT_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.bar_kv);
-        }
-      } else {
-        tc::bar_arrive_expect_tx(&sm.bar_kv, 0u);
-      }
-    }
-    // chunks 0..3 now; 4..7 land over the staging buffer once it is free (at
-    // once in the window CTA, which stages nothing)
-    tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
-    for (int c = 0; c < 4; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
-    if (window_cta) {
-      tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
-      for (int c = 4; c < 8; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
-    }
-  }
-
-  // ---------------- keys: FP4 entries by 16-byte asynchronous copies into the
-  // staging buffer (or the packed selection by one copy); with packed_out the
-  // staged entries are also copied out, contiguously; lanes 2k and 2k+1 of
-  // warp w then take entry 16w + k into registers (lane h: dims 128h .. 128h+127
-  // and 256+128h .. 256+128h+127, with their scale bytes), the staging buffer
-  // receives Q chunks 4..7, and every warp dequantises its 16 keys and arrives
-  // on bar_keys (8 arrivals complete it)
-  if (!window_cta) {
-    if (p.packed_in) {
-      at_wait(&sm.bar_pk, 0, sm, p.hdr, 19);
-    } else {
-      for (int i = tid; i < AT_KEYS * (MAIN_BYTES / 16); i += AT_THREADS) {
-        const int s = i / (MAIN_BYTES / 16), part = i % (MAIN_BYTES / 16);
-        if (sm.kvalid[s] == 1) {
-          const unsigned char* src = p.main_kv + ((int64_t)b * p.cap + sm.kid[s]) * MAIN_BYTES + part * 16;
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                       :: "r"(tc::smem_u32(stage + s * MAIN_BYTES + part * 16)), "l"(src) : "memory");
+          tc::bar_arrive_expect_tx(&sm.win_full[u], 2u * A_CHUNK_BYTES);
+          for (int c = 2 * u; c < 2 * u + 2; c++)
+            tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.win_full[u]);
         }
       }
-      asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-      if (p.packed_out) tc::fence_proxy_async_smem();      // the staged bytes are read by a bulk copy
-      __syncthreads();
-      if (p.packed_out && tid == 0) {
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                     :: "l"(p.packed_out + ((int64_t)bq * p.K + slot0) * MAIN_BYTES), "r"(tc::smem_u32(stage)),
-                        "r"((uint32_t)(n_sel * MAIN_BYTES)) : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      constexpr uint32_t idesc_s = tc::idesc_bf16(A_KEYS, H, 0, 0);
+      constexpr uint32_t idesc_o = tc::idesc_bf16(128, H, 1, 1);
+      // descriptors: the 14-bit start address field (address / 16) never carries
+      // (shared memory < 256 KB), so offsets are added to it directly
+      const uint64_t a_s = tc::smem_desc(tc::smem_u32(kbuf + 2 * u * A_CHUNK_BYTES), 16, 1024, tc::SW_128B);
+      const uint64_t b_s = tc::smem_desc(tc::smem_u32(qbuf + 2 * u * A_QCHUNK_BYTES), 16, 1024, tc::SW_128B);
+      const uint64_t a_o = tc::smem_desc(tc::smem_u32(kbuf + 2 * u * A_CHUNK_BYTES), A_CHUNK_BYTES, 1024,
+                                         tc::SW_128B);
+      const uint64_t b_o = tc::smem_desc(tc::smem_u32(pbuf), 8192, 1024, tc::SW_128B);
+      const uint32_t s_acc = tmem + A_S_COL + 64 * u, o_acc = tmem + A_O_COL + 64 * u;
+      bool ok = true;
+      for (int c = 0; c < nc; c++) {
+        const uint32_t ph = (uint32_t)c & 1u;
+        if (c == 0) {
+          ok = as_wait(&sm.q_full[u], 0, sm, p.hdr, 32) && ok;
+          if (p.S > 0 && !p.swa_fp8) ok = as_wait(&sm.win_full[u], 0, sm, p.hdr, 34) && ok;
+        }
+        ok = as_wait_sleepy(&sm.kready[u], ph, sm, p.hdr, 31) && ok;
+        tc::fence_after_sync();
+        if (ok) {                                     // S^T partial of tile u: column chunks 2u, 2u + 1
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const uint32_t off = (uint32_t)((i >> 2) * A_CHUNK_BYTES + (i & 3) * 32) >> 4;
+            const uint32_t offq = (uint32_t)((i >> 2) * A_QCHUNK_BYTES + (i & 3) * 32) >> 4;
+            tc::mma_bf16(s_acc, a_s + off, b_s + offq, idesc_s, i ? 1u : 0u);
+          }
+        }
+        tc::commit(&sm.s_full);
+        // O^T tile u += V^T P^T over this chunk's 128 keys
+        ok = as_wait_sleepy(&sm.p_ready, ph, sm, p.hdr, 33) && ok;
+        tc::fence_after_sync();
+        if (ok) {
+#pragma unroll
+          for (int ks = 0; ks < A_KEYS / 16; ks++)
+            tc::mma_bf16(o_acc, a_o + (uint32_t)(ks * 2048 >> 4), b_o + (uint32_t)(ks * 2048 >> 4), idesc_o,
+                         (c > 0 || ks) ? 1u : 0u);
+        }
+        tc::commit(&sm.pv_done[u]);
       }
     }
-    // Bank order: a quarter-warp (8 lanes) covers 4 entries x 2 lanes.  The
-    // odd lane of a pair walks the two 16-byte pieces of each 64-dim chunk
-    // swapped (and so its 16-channel groups as g ^ 2), so that within every
-    // 128-bit access the 8 lanes touch 8 different 16-byte bank groups, loads
-    // and stores alike.
-    const int s = warp * 16 + (lane >> 1), hf = lane & 1;
-    uint4 code[8];                                         // masked keys: +0 codes, scale 0 -> zero rows
-    uint2 sca = make_uint2(0u, 0u), scb = make_uint2(0u, 0u);
+    __syncwarp();
+  } else {
+    // ================= math warps
+    const int q4 = warp & 3, hh = warp >> 2;          // TMEM lane quarter; head half (heads 32 hh ..)
+    const int key = tid >> 1, kh = tid & 1;           // dequantisation: key row, 64-dim half of each tile
+    const int m = q4 * 32 + lane;                     // softmax / output: key row or dim row of a tile
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t xr = (uint32_t)key & 7u;
+    uint4 cd[8];                                      // FP4 codes of the next chunk: tile u in cd[2u], cd[2u+1]
+    uint4 scv[2];                                     // its 32 scale bytes
+    bool kv = false;                                  // the next chunk's key of this thread exists
+    auto prefetch = [&](int chunk) {
+      const int slot = A_KEYS * (chunk - 1) + key;
+      const int32_t id = slot < K ? sm.ids[slot] : -1;
+      kv = id >= 0 && id < p.cap;
+      if (id >= p.cap && kh == 0) report(p.hdr, CSA2_ERR_BOUNDS, id);
 #pragma unroll
-    for (int k = 0; k < 8; k++) code[k] = make_uint4(0u, 0u, 0u, 0u);
-    if (sm.kvalid[s] == 1) {
-      const uint4* ent = reinterpret_cast<const uint4*>(stage + s * MAIN_BYTES);
+      for (int i = 0; i < 8; i++) cd[i] = make_uint4(0u, 0u, 0u, 0u);
+      scv[0] = scv[1] = make_uint4(0u, 0u, 0u, 0u);
+      if (kv) {
+        const unsigned char* src = p.packed_in ? p.packed_in + ((int64_t)bq * K + slot) * MAIN_BYTES
+                                               : p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        code[k] = ent[4 * hf + (k ^ hf)];                  // chunks 2hf, 2hf + 1
-        code[4 + k] = ent[8 + 4 * hf + (k ^ hf)];          // chunks 4 + 2hf, 5 + 2hf
+        for (int u = 0; u < 4; u++) {
+          cd[2 * u] = __ldg(s4 + 4 * u + 2 * kh);
+          cd[2 * u + 1] = __ldg(s4 + 4 * u + 2 * kh + 1);
+        }
+        scv[0] = __ldg(s4 + 16);
+        scv[1] = __ldg(s4 + 17);
       }
-      sca = *reinterpret_cast<const uint2*>(stage + s * MAIN_BYTES + 256 + 8 * hf);   // their scale bytes
-      scb = *reinterpret_cast<const uint2*>(stage + s * MAIN_BYTES + 272 + 8 * hf);
-    }
-    tc::fence_proxy_async_smem();
-    __syncthreads();                                       // the staging buffer is free
-    if (tid == 0) {
-      if (p.packed_out) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // (copied out)
-      tc::bar_arrive_expect_tx(&sm.bar_q, 4u * AT_QCHUNK_BYTES);
-      for (int c = 4; c < 8; c++) tc::tma_load_2d(qbuf + c * AT_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.bar_q);
-    }
-    // odd lane: scale bytes rotated by two, matching its group order g ^ 2
-    const uint32_t rot = hf ? 16u : 0u;
-    const uint32_t scw[4] = {__funnelshift_r(sca.x, sca.x, rot), __funnelshift_r(sca.y, sca.y, rot),
-                             __funnelshift_r(scb.x, scb.x, rot), __funnelshift_r(scb.y, scb.y, rot)};
-    // SW128 row s: 16-byte unit u of a chunk row lands at unit u ^ (s & 7); the
-    // odd lane's group g ^ 2 is unit pair (2g, 2g + 1) ^ 4
-    const uint32_t xr = ((uint32_t)s & 7u) ^ ((uint32_t)hf << 2);
-    auto dequant_chunk = [&](int chunk, const uint4& c0, const uint4& c1, uint32_t sw) {
-      unsigned char* dst = kbuf + chunk * AT_CHUNK_BYTES + s * 128;
-      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    };
+    // tile u of the current chunk: 64 dims (column chunk 2u + kh) of this thread's key
+    auto dequant_tile = [&](int u) {
+      const uint4 c0 = cd[2 * u], c1 = cd[2 * u + 1];
+      const uint32_t cwd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint4& sv = scv[u >> 1];
+      const uint32_t sw = (u & 1) ? (kh ? sv.w : sv.z) : (kh ? sv.y : sv.x);   // scale bytes 8u + 4kh ..
+      unsigned char* dst = kbuf + (2 * u + kh) * A_CHUNK_BYTES + key * 128;
 #pragma unroll
-      for (int g = 0; g < 4; g++) {                        // 16 channels per E4M3 scale
-        const float sc = e4m3_value((sw >> (8 * g)) & 255u);
+      for (int i = 0; i < 4; i++) {
+        // the odd half walks its 16-channel groups as i ^ 2, so the two threads of a
+        // key never store to the same 16-byte bank group in one instruction
+        const int g = kh ? (i ^ 2) : i;
+        const uint32_t wa = kh ? cwd[2 * (i ^ 2)] : cwd[2 * i];          // static indices only
+        const uint32_t wb = kh ? cwd[2 * (i ^ 2) + 1] : cwd[2 * i + 1];
+        const uint32_t sb = (sw >> (8 * g)) & 255u;
+        const float sc = e4m3_value(sb);
         const uint32_t sc2 = pack_bf16x2(sc, sc);
         uint32_t o[8];
-        e2m1x8_to_bf16(cw[2 * g], o);
-        e2m1x8_to_bf16(cw[2 * g + 1], o + 4);
+        e2m1x8_to_bf16(wa, o);
+        e2m1x8_to_bf16(wb, o + 4);
 #pragma unroll
         for (int k = 0; k < 8; k++) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(o[k]), "r"(sc2));
         *reinterpret_cast<uint4*>(dst + (((2u * g) ^ xr) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(dst + (((2u * g + 1u) ^ xr) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     };
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-      dequant_chunk(2 * hf + i, code[2 * i], code[2 * i + 1], scw[i]);
-      dequant_chunk(4 + 2 * hf + i, code[4 + 2 * i], code[5 + 2 * i], scw[2 + i]);
-    }
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::bar_arrive(&sm.bar_keys);
-  } else if (p.S == 0) {                                   // no window rows supplied: zero keys
-    for (int i = tid; i < 8 * AT_CHUNK_BYTES / 16; i += AT_THREADS)
-      reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0, 0, 0, 0);
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-  } else if (p.swa_fp8) {
-    // FP8 window: thread (r, h) takes row r = tid / 2, dims 32h .. 32h+31 of
-    // each chunk (32 E4M3 bytes at 8 KB + 64 r + 32 h), widens them to four
-    // 16-byte bf16 units (unit 4h + j = dims 8(4h + j) ..) and stores them at
-    // their SW128 places in the same chunk; every thread reads a pair of chunks
-    // before any thread overwrites it
-    at_wait(&sm.bar_kv, 0, sm, p.hdr, 20);
-    const int r = tid >> 1, h = tid & 1;
+    if (nc > 1) prefetch(1);
+    float m_used = -INFINITY;                         // max in use for head 32 hh + lane
+    float l_part = 0.f;                               // sum of P over this warp's keys, head 32 hh + lane
+    bool ok = true;
+    for (int c = 0; c < nc; c++) {
+      const uint32_t ph = (uint32_t)c & 1u;
+      // ---------------- the chunk's keys into the key buffer
+      if (c == 0) {
+        if (p.S == 0) {                               // no window rows supplied: zero keys (all masked)
+          for (int i = tid; i < 8 * A_CHUNK_BYTES / 16; i += A_MATH)
+            reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+        } else if (p.swa_fp8) {                       // (bf16 rows: the issuers wait for the TMA themselves)
+          for (int u = 0; u < 4; u++) ok = as_wait(&sm.win_full[u], 0, sm, p.hdr, 34) && ok;
+          {
+            // thread (r, h) widens row r, dims 32h .. 32h+31 of each column chunk (32
+            // E4M3 bytes at 8 KB + 64 r + 32 h) into four 16-byte bf16 units at their
+            // SW128 places; every thread reads a pair of chunks before any writes it
+            const int r = tid >> 1, h = tid & 1;
 #pragma unroll 1
-    for (int c0 = 0; c0 < 8; c0 += 2) {
-      uint4 raw[2][2];
+            for (int c0 = 0; c0 < 8; c0 += 2) {
+              uint4 raw[2][2];
 #pragma unroll
-      for (int i = 0; i < 2; i++) {
-        const uint4* src = reinterpret_cast<const uint4*>(kbuf + (c0 + i) * AT_CHUNK_BYTES + AT_CHUNK_BYTES / 2 +
-                                                          r * 64 + h * 32);
-        raw[i][0] = src[0];
-        raw[i][1] = src[1];
-      }
-      __syncthreads();
+              for (int i = 0; i < 2; i++) {
+                const uint4* src = reinterpret_cast<const uint4*>(kbuf + (c0 + i) * A_CHUNK_BYTES +
+                                                                  A_CHUNK_BYTES / 2 + r * 64 + h * 32);
+                raw[i][0] = src[0];
+                raw[i][1] = src[1];
+              }
+              named_sync(1, A_MATH);
 #pragma unroll
-      for (int i = 0; i < 2; i++) {
-        unsigned char* dst = kbuf + (c0 + i) * AT_CHUNK_BYTES;
+              for (int i = 0; i < 2; i++) {
+                unsigned char* dst = kbuf + (c0 + i) * A_CHUNK_BYTES;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          const uint4& w = raw[i][j >> 1];
-          const uint32_t lo = (j & 1) ? w.z : w.x, hi = (j & 1) ? w.w : w.y;   // bytes 8j .. 8j+7
-          const uint4 o = make_uint4(e4m3x2_to_bf16x2(lo & 0xFFFFu), e4m3x2_to_bf16x2(lo >> 16),
-                                     e4m3x2_to_bf16x2(hi & 0xFFFFu), e4m3x2_to_bf16x2(hi >> 16));
-          *reinterpret_cast<uint4*>(dst + sw128((uint32_t)r, (uint32_t)(64 * h + 16 * j))) = o;
-        }
-      }
-    }
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-  }
-
-  // ---------------- S^T = K Q^T  (M = 128 keys, N = 64 heads, K = 512 dims) as two
-  // chains of 16 MMAs into two accumulators (dims 0..255 at column 0, 256..511 at
-  // AT_S2_COL), issued by two threads at once: one thread's chain is bound by its
-  // own issue rate, not by the tensor core; the softmax adds the halves
-  if ((warp == 1 || warp == 2) && lane == 0) {
-    constexpr uint32_t idesc_s = tc::idesc_bf16(AT_KEYS, H, 0, 0);
-    const int c0 = warp == 1 ? 0 : 4;
-    const uint32_t acc = tmem + (warp == 1 ? 0u : (uint32_t)AT_S2_COL);
-    bool ok = at_wait(window_cta ? &sm.bar_kv : &sm.bar_keys, 0, sm, p.hdr, window_cta ? 11 : 16);
-    if (ok) ok = at_wait(&sm.bar_q, 0, sm, p.hdr, 12);
-    tc::fence_after_sync();
-    for (int c = c0; c < c0 + 4 && ok; c++) {
-      const uint32_t a0 = tc::smem_u32(kbuf + c * AT_CHUNK_BYTES), b0 = tc::smem_u32(qbuf + c * AT_QCHUNK_BYTES);
-#pragma unroll
-      for (int ks = 0; ks < 4; ks++)
-        tc::mma_bf16(acc, tc::smem_desc(a0 + ks * 32, 16, 1024, tc::SW_128B),
-                     tc::smem_desc(b0 + ks * 32, 16, 1024, tc::SW_128B), idesc_s, (c > c0 || ks) ? 1u : 0u);
-    }
-    tc::commit(&sm.bar_s);
-  }
-  __syncwarp();
-
-  // ---------------- softmax straight from TMEM: warp w holds keys 32(w&3) .. +31 (one
-  // per lane) and heads 32(w>>2) .. +31 (one per register).  An issuing thread
-  // observes the completion late while its own MMAs are in flight, so warps 1
-  // and 2 take it from warp 0 through a named barrier instead of the mbarrier.
-  if (warp == 0 || warp > 2) at_wait(&sm.bar_s, 0, sm, p.hdr, 13);
-  if (warp == 0) asm volatile("bar.arrive 1, 96;" ::: "memory");
-  else if (warp <= 2) asm volatile("bar.sync 1, 96;" ::: "memory");
-  tc::fence_after_sync();
-  {
-    const int q4 = warp & 3, half = warp >> 2;
-    const int m = q4 * 32 + lane;                   // key row
-    const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + half * 32;
-    const bool valid = sm.kvalid[m] != 0;
-    float v[32], r[32];
-    {
-      uint32_t s1[32], s2[32];
-      tc::tmem_ld_x32_nowait(taddr, s1);
-      tc::tmem_ld_x32_nowait(taddr + AT_S2_COL, s2);
-      tc::tmem_wait_ld_regs(s1);
-      tc::tmem_wait_ld_regs(s2);
-#pragma unroll
-      for (int j = 0; j < 32; j++) v[j] = __uint_as_float(s1[j]) + __uint_as_float(s2[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 32; j++) r[j] = v[j] = valid ? v[j] * p.scale : -INFINITY;
-    // transpose-reduction: afterwards lane l holds the maximum of column l over the warp's keys
-#pragma unroll
-    for (int k = 16; k >= 1; k >>= 1) {
-      const bool upper = (lane & k) != 0;
-#pragma unroll
-      for (int i = 0; i < k; i++) {
-        const float send = upper ? r[i] : r[i + k];
-        const float keep = upper ? r[i + k] : r[i];
-        r[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, k));
-      }
-    }
-    sm.red[q4][half * 32 + lane] = r[0];
-    __syncthreads();
-    // lane l combines the four warps' maxima of head 32 half + l, then every
-    // lane gets all 32 by shuffles
-    const int hl = half * 32 + lane;
-    const float mlane = fmaxf(fmaxf(sm.red[0][hl], sm.red[1][hl]), fmaxf(sm.red[2][hl], sm.red[3][hl]));
-    float mx[32];
-#pragma unroll
-    for (int j = 0; j < 32; j++) mx[j] = __shfl_sync(0xFFFFFFFFu, mlane, j);
-    if (q4 == 0) sm.ml[hl] = mlane;
-    uint32_t pk[16];
-#pragma unroll
-    for (int j = 0; j < 32; j++) {
-      r[j] = (v[j] == -INFINITY) ? 0.f : __expf(v[j] - mx[j]);
-      if (j & 1) pk[j >> 1] = pack_bf16x2(r[j - 1], r[j]);
-    }
-    // P^T row m (heads 32 half .. +31 = 16-byte units 4 half .. 4 half + 3), SW128
-#pragma unroll
-    for (int u = 0; u < 4; u++)
-      *reinterpret_cast<uint4*>(pbuf + sw128((uint32_t)m, (uint32_t)(half * 64 + u * 16))) =
-          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-    tc::fence_proxy_async_smem();                    // P^T is read by the tensor cores
-#pragma unroll
-    for (int k = 16; k >= 1; k >>= 1) {
-      const bool upper = (lane & k) != 0;
-#pragma unroll
-      for (int i = 0; i < k; i++) {
-        const float send = upper ? r[i] : r[i + k];
-        const float keep = upper ? r[i + k] : r[i];
-        r[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, k);
-      }
-    }
-    sm.red_sum[q4][half * 32 + lane] = r[0];
-    tc::fence_before_sync();
-    __syncthreads();                                 // P^T complete, every warp's column sums visible
-    tc::fence_after_sync();
-    if (tid < H) {
-      const float sum = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
-      sm.ml[H + tid] = sum;
-      sm.inv_l[tid] = sum > 0.f ? 1.0f / sum : 0.f;
-      tc::fence_proxy_async_smem();                // the (m, L) rows are read by bulk copies
-    }
-  }
-  // ---------------- O^T = V^T P^T  (4 tiles of M = 128 dims, N = 64 heads, K = 128 keys),
-  // tile t issued by warp t's lane 0 (four chains at once)
-  if (warp < 4 && lane == 0) {
-    constexpr uint32_t idesc_o = tc::idesc_bf16(128, H, 1, 1);
-    const uint32_t kb = tc::smem_u32(kbuf), pb = tc::smem_u32(pbuf);
-    const int tile = warp;
-#pragma unroll
-    for (int ks = 0; ks < AT_KEYS / 16; ks++) {
-      const uint64_t ad = tc::smem_desc(kb + (2 * tile) * AT_CHUNK_BYTES + ks * 2048, AT_CHUNK_BYTES, 1024,
-                                        tc::SW_128B);
-      const uint64_t bd = tc::smem_desc(pb + ks * 2048, 8192, 1024, tc::SW_128B);
-      tc::mma_bf16(tmem + 64 + tile * 64, ad, bd, idesc_o, ks ? 1u : 0u);
-    }
-    tc::commit(&sm.bar_o);
-  }
-  __syncwarp();
-  if (warp >= 4) at_wait(&sm.bar_o, 0, sm, p.hdr, 14);    // (the issuing warps: by the barrier below)
-  __syncthreads();                                         // O^T complete; 1 / L_c visible to every thread
-  tc::fence_after_sync();
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // phase 1 (long complete)
-  // phase 2: S^T and P are dead, so this CTA's receive slots (over them) are
-  // free.  The tensor cores have read P (its completion was observed above),
-  // so no write of this CTA into the slots is still in flight and the arrival
-  // needs no release (a releasing arrival costs about half a microsecond).
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  // Tile t of the output is owned by CTA t % C.  Every CTA sends its (m, L)
-  // rows to every other owner now, ahead of the shares, so the owners can
-  // weight the shares as soon as their own are staged.
-  int owned = 0;
-  for (int tile = rank; tile < 4; tile += C) owned++;
-  if (tid == 0) {
-    if (owned) {
-      tc::bar_arrive_expect_tx(&sm.bar_ml, (uint32_t)((C - 1) * 2 * H * 4));
-      for (int sl = 0; sl < owned * (C - 1); sl++) tc::bar_arrive_expect_tx(&sm.bar_slot[sl], (uint32_t)AT_SHARE_BYTES);
-    }
-    const int n_owners = C < 4 ? C : 4;
-    for (int owner = 0; owner < n_owners; owner++) {
-      if (owner == rank) continue;
-      uint32_t dml, rbar;
-      const int si = rank < owner ? rank : rank - 1;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dml) : "r"(tc::smem_u32(sm.recv_ml[si])), "r"(owner));
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(tc::smem_u32(&sm.bar_ml)), "r"(owner));
-      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                   :: "r"(dml), "r"(tc::smem_u32(sm.ml)), "r"(2 * H * 4), "r"(rbar) : "memory");
-    }
-  }
-  // this CTA's share O_c / L_c per tile as fp16 [dim][head], 16-byte units swizzled by dim
-  {
-    const int q4 = warp & 3, half = warp >> 2;
-    float il[32];                                 // 1 / L_c of this thread's 32 heads, in registers
-#pragma unroll
-    for (int j = 0; j < 32; j++) il[j] = sm.inv_l[half * 32 + j];
-    uint32_t ta[4][32];
-#pragma unroll
-    for (int tile = 0; tile < 4; tile++) {       // issue all four TMEM loads, then wait once
-      asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                   "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                   : "=r"(ta[tile][0]), "=r"(ta[tile][1]), "=r"(ta[tile][2]), "=r"(ta[tile][3]), "=r"(ta[tile][4]),
-                     "=r"(ta[tile][5]), "=r"(ta[tile][6]), "=r"(ta[tile][7]), "=r"(ta[tile][8]), "=r"(ta[tile][9]),
-                     "=r"(ta[tile][10]), "=r"(ta[tile][11]), "=r"(ta[tile][12]), "=r"(ta[tile][13]), "=r"(ta[tile][14]),
-                     "=r"(ta[tile][15]), "=r"(ta[tile][16]), "=r"(ta[tile][17]), "=r"(ta[tile][18]), "=r"(ta[tile][19]),
-                     "=r"(ta[tile][20]), "=r"(ta[tile][21]), "=r"(ta[tile][22]), "=r"(ta[tile][23]), "=r"(ta[tile][24]),
-                     "=r"(ta[tile][25]), "=r"(ta[tile][26]), "=r"(ta[tile][27]), "=r"(ta[tile][28]), "=r"(ta[tile][29]),
-                     "=r"(ta[tile][30]), "=r"(ta[tile][31])
-                   : "r"(tmem + ((uint32_t)(q4 * 32) << 16) + 64 + tile * 64 + half * 32) : "memory");
-    }
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    const int d = q4 * 32 + lane;                 // dim row inside a tile
-#pragma unroll
-    for (int tile = 0; tile < 4; tile++) {
-      __half* row = ostage + tile * (128 * H) + d * H;
-#pragma unroll
-      for (int u = 0; u < 4; u++) {               // 16-byte units = 8 heads: half*32 + 8u .. +7
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const int j = 8 * u + 2 * e;
-          const __half2 h2 = __floats2half2_rn(__uint_as_float(ta[tile][j]) * il[j],
-                                               __uint_as_float(ta[tile][j + 1]) * il[j + 1]);
-          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        const int unit = (half * 4 + u) ^ (d & 7);
-        *reinterpret_cast<uint4*>(row + unit * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-  }
-  tc::fence_proxy_async_smem();
-  __syncthreads();
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // phase 2: every owner's slots are free
-
-  // ---------------- cluster reduction: the CTAs send their fp16 share of tile t into
-  // its owner's slot j * (C - 1) + sender index (j = t / C), each slot with its own
-  // barrier; the owner weights them (its (m, L) rows are in) and folds each share
-  // in as it lands
-  if (tid == 0) {
-    // senders start on different owners: tile order rank + 1, rank + 2, ... (mod 4)
-    for (int k = 1; k <= 4; k++) {
-      const int tile = (rank + k) & 3;
-      const int owner = tile % C;
-      if (owner == rank) continue;
-      const int slot = (tile / C) * (C - 1) + (rank < owner ? rank : rank - 1);
-      uint32_t dst, rbar;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(tc::smem_u32(orecv + slot * (128 * H))), "r"(owner));
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(tc::smem_u32(&sm.bar_slot[slot])), "r"(owner));
-      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                   :: "r"(dst), "r"(tc::smem_u32(ostage + tile * (128 * H))), "r"(AT_SHARE_BYTES), "r"(rbar) : "memory");
-    }
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  }
-  if (owned) {
-    if (tid < H) {                             // weight of each CTA's share for head tid
-      at_wait(&sm.bar_ml, 0, sm, p.hdr, 15);
-      float mc[AT_MAXC], lc[AT_MAXC];
-      float M = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < AT_MAXC; c++) {
-        if (c >= C) break;
-        const float* src = c == rank ? sm.ml : sm.recv_ml[c < rank ? c : c - 1];
-        mc[c] = src[tid];
-        lc[c] = src[H + tid];
-        if (lc[c] > 0.f) M = fmaxf(M, mc[c]);
-      }
-      float den = 0.f;
-#pragma unroll
-      for (int c = 0; c < AT_MAXC; c++) {
-        if (c >= C) break;
-        lc[c] = lc[c] > 0.f ? lc[c] * __expf(mc[c] - M) : 0.f;
-        den += lc[c];
-      }
-      const float inv = den > 0.f ? 1.0f / den : 0.f;
-#pragma unroll
-      for (int c = 0; c < AT_MAXC; c++) {
-        if (c >= C) break;
-        sm.wgt[c][tid] = lc[c] * inv;
-      }
-    }
-    __syncthreads();
-    uint16_t* out = p.out + (int64_t)bq * H * D;
-    // thread: 8-head unit u = warp (heads 8u .. 8u+7), dims lane + 32k of the tile
-    // (consecutive lanes -> coalesced bf16 stores per head row); its 8 x C
-    // weights are loaded once
-    const int u = warp;
-    float wself[8], wr[AT_MAXC - 1][8];
-#pragma unroll
-    for (int e = 0; e < 8; e++) wself[e] = sm.wgt[rank][u * 8 + e];
-#pragma unroll
-    for (int r = 0; r < AT_MAXC - 1; r++) {
-      const int sender = r < rank ? r : r + 1;
-#pragma unroll
-      for (int e = 0; e < 8; e++) wr[r][e] = (r < C - 1) ? sm.wgt[sender][u * 8 + e] : 0.f;
-    }
-    int j = 0;
-    for (int tile = rank; tile < 4; tile += C, j++) {
-      float acc[4][8];
-#pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const int d = lane + 32 * k;
-        const uint4 v = *reinterpret_cast<const uint4*>(ostage + tile * (128 * H) + d * H + ((u ^ (d & 7)) << 3));
-        const __half2* h2 = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const float2 f = __half22float2(h2[e]);
-          acc[k][2 * e] = f.x * wself[2 * e];
-          acc[k][2 * e + 1] = f.y * wself[2 * e + 1];
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < AT_MAXC - 1; r++) {  // the other CTAs' shares, each as soon as it is in
-        if (r >= C - 1) break;
-        const int slot = j * (C - 1) + r;
-        at_wait(&sm.bar_slot[slot], 0, sm, p.hdr, 15);
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const int d = lane + 32 * k;
-          const uint4 v = *reinterpret_cast<const uint4*>(orecv + slot * (128 * H) + d * H + ((u ^ (d & 7)) << 3));
-          const __half2* h2 = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; e++) {
-            const float2 f = __half22float2(h2[e]);
-            acc[k][2 * e] = fmaf(f.x, wr[r][2 * e], acc[k][2 * e]);
-            acc[k][2 * e + 1] = fmaf(f.y, wr[r][2 * e + 1], acc[k][2 * e + 1]);
+                for (int j = 0; j < 4; j++) {
+                  const uint4& w = raw[i][j >> 1];
+                  const uint32_t lo = (j & 1) ? w.z : w.x, hi = (j & 1) ? w.w : w.y;   // bytes 8j .. 8j+7
+                  const uint4 o = make_uint4(e4m3x2_to_bf16x2(lo & 0xFFFFu), e4m3x2_to_bf16x2(lo >> 16),
+                                             e4m3x2_to_bf16x2(hi & 0xFFFFu), e4m3x2_to_bf16x2(hi >> 16));
+                  *reinterpret_cast<uint4*>(dst + sw128((uint32_t)r, (uint32_t)(64 * h + 16 * j))) = o;
+                }
+              }
+            }
           }
         }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          for (int u = 0; u < 4; u++) tc::bar_arrive(&sm.kready[u]);
+      } else {
+        // selected chunk: tile u's column chunks are free once chunk c-1's O^T tile u is done
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          ok = as_wait(&sm.pv_done[u], ph ^ 1u, sm, p.hdr, 35) && ok;
+          tc::fence_after_sync();
+          dequant_tile(u);
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::bar_arrive(&sm.kready[u]);
+        }
+        if (p.packed_out && kv) {                     // the selected entry, in slot order, for Reuse layers
+          const int slot = A_KEYS * (c - 1) + key;
+          uint4* dst = reinterpret_cast<uint4*>(p.packed_out + ((int64_t)bq * K + slot) * MAIN_BYTES);
+#pragma unroll
+          for (int u = 0; u < 4; u++) {
+            dst[4 * u + 2 * kh] = cd[2 * u];
+            dst[4 * u + 2 * kh + 1] = cd[2 * u + 1];
+          }
+          dst[16 + kh] = kh ? scv[1] : scv[0];
+        }
+      }
+
+      // ---------------- softmax of the chunk, straight from TMEM
+      ok = as_wait(&sm.s_full, ph, sm, p.hdr, 36) && ok;
+      tc::fence_after_sync();
+      bool valid;
+      if (c == 0) {
+        const int64_t pos = t - (WIN - 1) + m;
+        const int64_t row = pos - p.swa_base[b];
+        valid = pos >= 0 && p.S > 0 && row >= 0 && row < p.S;
+        if (pos >= 0 && !valid && hh == 0) report(p.hdr, CSA2_ERR_BOUNDS, pos);
+      } else {
+        const int slot = A_KEYS * (c - 1) + m;
+        const int32_t id = slot < K ? sm.ids[slot] : -1;
+        valid = id >= 0 && id < p.cap;
+      }
+      float v[32], r[32];
+      {
+        const float sc2 = p.scale * A_LOG2E;          // base-2 logits
+        uint32_t s1[32], s2[32];
+        const uint32_t taddr = tmem + lane_off + A_S_COL + 32 * hh;
+        tc::tmem_ld_x32_nowait(taddr, s1);
+        tc::tmem_ld_x32_nowait(taddr + 64, s2);
+        tc::tmem_wait_ld_regs(s1);
+        tc::tmem_wait_ld_regs(s2);
+#pragma unroll
+        for (int j = 0; j < 32; j++) v[j] = __uint_as_float(s1[j]) + __uint_as_float(s2[j]);
+        tc::tmem_ld_x32_nowait(taddr + 128, s1);
+        tc::tmem_ld_x32_nowait(taddr + 192, s2);
+        tc::tmem_wait_ld_regs(s1);
+        tc::tmem_wait_ld_regs(s2);
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+          v[j] = valid ? (v[j] + (__uint_as_float(s1[j]) + __uint_as_float(s2[j]))) * sc2 : -INFINITY;
       }
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        uint16_t* o = out + (u * 8) * D + tile * 128 + lane + 32 * k;
-#pragma unroll
-        for (int e = 0; e < 8; e++) o[e * D] = (uint16_t)(pack_bf16x2(acc[k][e], 0.f) & 0xFFFFu);
+      for (int j = 0; j < 32; j++) r[j] = v[j];
+      sm.red[warp][lane] = lane_columns<true>(r, lane);
+      named_sync(2 + hh, 128);                        // the four warps of this head half
+      const float cm = fmaxf(fmaxf(sm.red[4 * hh][lane], sm.red[4 * hh + 1][lane]),
+                             fmaxf(sm.red[4 * hh + 2][lane], sm.red[4 * hh + 3][lane]));
+      // online maximum: O^T holds nothing yet (chunk 0) or only zeros (every earlier
+      // key masked) while m_used is -inf; otherwise rescale only past A_TAU
+      float alpha = 1.f;
+      if (m_used == -INFINITY) {
+        m_used = cm;
+      } else if (cm > m_used + A_TAU) {
+        alpha = ex2_ftz(m_used - cm);
+        m_used = cm;
+        l_part *= alpha;
       }
+      if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        // identical decision in the four warps of the half; every warp rescales
+        // its lane quarter of the half's 32 heads in all four O^T tiles (chunk
+        // c-1's products are complete: this chunk's S^T needed them)
+        float al[32];
+#pragma unroll
+        for (int j = 0; j < 32; j++) al[j] = __shfl_sync(0xFFFFFFFFu, alpha, j);
+#pragma unroll 1
+        for (int u = 0; u < 4; u++) {
+          uint32_t o[32];
+          const uint32_t taddr = tmem + lane_off + A_O_COL + 64 * u + 32 * hh;
+          tmem_ld32(taddr, o);
+#pragma unroll
+          for (int j = 0; j < 32; j++) o[j] = __float_as_uint(__uint_as_float(o[j]) * al[j]);
+          tmem_st32(taddr, o);
+        }
+        tc::tmem_wait_st();
+      }
+      // every lane needs the maxima in use of all 32 heads: through shared memory
+      sm.mv[warp][lane] = m_used;
+      __syncwarp();
+      uint32_t pk[16];
+#pragma unroll
+      for (int j4 = 0; j4 < 8; j4++) {
+        const float4 m4 = *reinterpret_cast<const float4*>(&sm.mv[warp][4 * j4]);
+        const float mj[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int j = 4 * j4 + e;
+          r[j] = (v[j] == -INFINITY) ? 0.f : ex2_ftz(v[j] - mj[e]);
+          if (j & 1) pk[j >> 1] = pack_bf16x2(r[j - 1], r[j]);
+        }
+      }
+      // P^T row m (heads 32 hh .. +31 = 16-byte units 4 hh .. 4 hh + 3), SW128
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+        *reinterpret_cast<uint4*>(pbuf + sw128((uint32_t)m, (uint32_t)(hh * 64 + u * 16))) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      tc::fence_proxy_async_smem();                   // P^T is read by the tensor cores
+      l_part += lane_columns<false>(r, lane);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(&sm.p_ready);
+      // the next chunk's FP4 bytes: issued after the softmax, whose shared-memory and
+      // TMEM traffic would otherwise queue behind these loads
+      if (c + 1 < nc) prefetch(c + 1);
+    }
+
+    // ---------------- output: O^T / L, bf16 rows out[head][dim]
+    for (int u = 0; u < 4; u++) ok = as_wait(&sm.pv_done[u], (uint32_t)(nc - 1) & 1u, sm, p.hdr, 37) && ok;
+    tc::fence_after_sync();
+    // the next kernel of the stream may be scheduled now (triggered at the start,
+    // its CTAs would hold SMs idle in their own wait for this whole kernel)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    sm.red[warp][lane] = l_part;
+    named_sync(2 + hh, 128);
+    const float lsum = sm.red[4 * hh][lane] + sm.red[4 * hh + 1][lane] + sm.red[4 * hh + 2][lane] +
+                       sm.red[4 * hh + 3][lane];
+    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+    float il[32];
+#pragma unroll
+    for (int j = 0; j < 32; j++) il[j] = __shfl_sync(0xFFFFFFFFu, inv, j);
+    uint16_t* out = p.out + (int64_t)bq * H * D + (int64_t)(32 * hh) * D + m;
+#pragma unroll 1
+    for (int u = 0; u < 4; u++) {
+      uint32_t o[32];
+      tmem_ld32(tmem + lane_off + A_O_COL + 64 * u + 32 * hh, o);
+#pragma unroll
+      for (int j = 0; j < 32; j++)
+        out[j * D + 128 * u] = (uint16_t)(pack_bf16x2(__uint_as_float(o[j]) * il[j], 0.f) & 0xFFFFu);
     }
   }
-  // the next kernel of the stream may be scheduled now (triggered at the start,
-  // its CTAs would hold SMs idle in their own wait for this whole kernel)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // A sender's shares stay in place until its copies have read them; an owner
-  // has received every byte sent to it (bar_ml, bar_slot) before it gets here, so no
-  // cross-CTA access remains and no final cluster barrier is needed.
-  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == A_MATH_WARPS + 3) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, AT_TMEM_COLS);
+    tc::tmem_dealloc(tmem, A_TMEM_COLS);
   }
 }
 
@@ -734,31 +588,26 @@ cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
   if (BQ == 0) return cudaSuccess;
   static PerDeviceOnce attrs;
   cudaError_t e = attrs.ensure([](int) {
-    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    return cudaFuncSetAttribute(attn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM);
   });
   if (e != cudaSuccess) return e;
   CUtensorMap map_q, map_swa;
   if (!encode_bf16_rows512(&map_q, p.q, (uint64_t)BQ * H, 64)) return cudaErrorInvalidValue;
   const uint64_t swa_rows = (uint64_t)B * (uint64_t)(p.S > 0 ? p.S : 1);
-  const bool swa_ok = p.swa_fp8 ? encode_u8_rows512(&map_swa, p.swa, swa_rows, AT_KEYS)
-                                : encode_bf16_rows512(&map_swa, p.swa, swa_rows, AT_KEYS);
+  const bool swa_ok = p.swa_fp8 ? encode_u8_rows512(&map_swa, p.swa, swa_rows, A_KEYS)
+                                : encode_bf16_rows512(&map_swa, p.swa, swa_rows, A_KEYS);
   if (!swa_ok) return cudaErrorInvalidValue;
-  const int C = (p.K + AT_KEYS - 1) / AT_KEYS + 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(BQ * C));
-  cfg.blockDim = dim3(AT_THREADS);
-  cfg.dynamicSmemBytes = AT_SMEM;
+  cfg.gridDim = dim3((unsigned)BQ);
+  cfg.blockDim = dim3(A_THREADS);
+  cfg.dynamicSmemBytes = A_SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // set-up overlaps the previous kernel
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // set-up overlaps the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, map_q, map_swa, C);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_stream_kernel, p, map_q, map_swa);
 }
 
 }  // namespace csa2

@@ -468,6 +468,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
     ip.sel = a->sel;
     ip.K = a->K;
     ip.hdr = hdr;
+    ip.scores = reinterpret_cast<float*>(cur);                   // the pool slots' keys
     st = from_cuda(launch_reindex_select(ip, s));
     if (st != CSA2_OK) return st;
   }

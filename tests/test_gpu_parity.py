@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synth
 from tests import cases
 
 torch = pytest.importorskip("torch")
@@ -338,6 +339,38 @@ def test_attention_window_clipped_at_start_and_no_selection(csa2):
     for qi in range(3):
         cases.check_attention(got[0, qi], _oracle_attention(case, main, 0, qi, sel[0, qi]))
     assert ws.sync_status()[0] == 0
+
+
+def test_attention_running_maximum_grows_past_the_rescale_threshold(csa2):
+    """Heads whose largest logit arrives in a late chunk of keys: heads 0..15
+    point at a key of the last run of 128 selected slots, heads 16..23 at
+    (twice) a key of the second run, heads 24..31 away from a key of the first
+    run; the rest are random.  The largest logits (about 22 and 45) exceed the
+    earlier chunks' maxima by far more than the kernel's rescale threshold, so
+    the accumulated output of those heads is rescaled on the way; every head
+    must still match the one-softmax oracle."""
+    case = cases.make_case(B=1, T=1500, m=1, Q=1, M=8, K=512, seed=612)
+    main, _, _ = cases.oracle_cache(case)
+    g = np.random.default_rng(612)
+    sel = g.choice(1500, 512, replace=False).astype(np.int32)
+    q = case.q.copy()
+    v_late = oracle.dequant_main(main[0, sel[400]]).astype(np.float32)
+    v_mid = oracle.dequant_main(main[0, sel[200]]).astype(np.float32)
+    v_early = oracle.dequant_main(main[0, sel[10]]).astype(np.float32)
+    q[0, 0, 0:16] = synth.f32_to_bf16_bits(np.broadcast_to(v_late, (16, 512)).copy())
+    q[0, 0, 16:24] = synth.f32_to_bf16_bits(np.broadcast_to(2 * v_mid, (8, 512)).copy())
+    q[0, 0, 24:32] = synth.f32_to_bf16_bits(np.broadcast_to(-v_early, (8, 512)).copy())
+    case.q = q
+    L = GpuLayer(csa2, case)
+    out = torch.empty((1, 1, 64, 512), dtype=torch.int16, device=DEV)
+    ws = csa2.Workspace(csa2.attn_workspace_size(1, 1, 512), device=DEV)
+    csa2.sparse_swa_attn(L.cache, L.q, dev(sel[None, None]), L.swa, L.swa_base, L.q_pos, case.scale, out, ws)
+    assert ws.sync_status()[0] == 0
+    got = bf16_to_f32(out)[0, 0]
+    want = _oracle_attention(case, main, 0, 0, sel)
+    cases.check_attention(got, want, "running maximum")
+    for h in (0, 16, 24, 40):
+        cases.check_attention(got[h:h + 1], want[h:h + 1], f"head {h}")
 
 
 def synth_bf16(bits):
