@@ -487,7 +487,7 @@ def run_decode1m(args, torch, csa2):
     dom_ms = reuse_ms if dom_is_reuse else reindex_ms
     dom_bytes = w.B * ((REUSE_BYTES if dom_is_reuse else REINDEX_BYTES) - win_saved)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    dom_kernel = "attn_tc_kernel" if dom_is_reuse else "reindex_select_kernel"
+    dom_kernel = "attn_stream_kernel" if dom_is_reuse else "reindex_select_kernel"
     traffic = ncu_traffic(dom_kernel + (":fp8_window" if fp8 else "")) if w.N == 1 << 20 else None
     e2e = None if fp8 else run_decode1m_e2e(args, torch, csa2, w)
     return {
