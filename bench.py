@@ -1476,7 +1476,7 @@ def main():
     ap.add_argument("--cpu-sample-queries", type=int, default=384)
     ap.add_argument("--packed-selection", type=int, default=1,
                     help="decode: the Reindex call packs its selected entries for the Reuse calls (1) or not (0)")
-    ap.add_argument("--lanes", type=int, default=5,
+    ap.add_argument("--lanes", type=int, default=10,
                     help="decode: stream + workspace lanes per layer slot")
     ap.add_argument("--swa-format", default="bf16", choices=["bf16", "fp8"],
                     help="decode: window rows as bf16 (the configuration) or E4M3 (the pages' FP8 window); "
