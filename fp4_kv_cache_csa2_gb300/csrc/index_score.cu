@@ -369,7 +369,8 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
     pack_head_weights(sm.w + jq * HI, w2);
     for (int j = 0; j < n; j++) {
       const int k = j % C::ISSUERS;
-      if (!wait_or_abort(&sm.acc_full[k], (j / C::ISSUERS) & 1, sm, p.hdr)) break;
+      const bool ok_tile = __all_sync(0xFFFFFFFFu, wait_or_abort(&sm.acc_full[k], (j / C::ISSUERS) & 1, sm, p.hdr));
+      if (!ok_tile) break;                                        // (the warp leaves together)
       tc::fence_after_sync();
       float v[32];
       tc::tmem_ld_x32(tmem + lane_off + C::ACC_COL + k * C::N + jq * HI, v);
