@@ -13,26 +13,33 @@
 // 128.  One softmax over all of them is kept online (running maxima per head,
 // rescaling the accumulated output only when a chunk's maximum exceeds the
 // one in use by more than A_TAU, so that exp() never exceeds e^A_TAU).
-//   * Q (64 heads x 512, bf16) lands once by TMA in 8 SW128 column chunks.
-//   * The key buffer holds one chunk as bf16 [128 keys][512] in 8 SW128 column
+// Both products run on f16 operands with fp32 accumulation:
+//   * every FP4 value times its E4M3 scale has at most 6 significant bits and
+//     lies between 2^-10 and 2688 in magnitude, so the f16 key is exact (E2M1
+//     pairs -> f16x2 by the hardware conversion, times the scale in f16x2);
+//   * E4M3 window values are f16 values; bf16 q and window rows are rounded to
+//     f16 in shared memory, exact for magnitudes in [2^-14, 65504] (smaller
+//     ones keep an absolute error below 2^-25; the layer's activations are
+//     expected inside f16's range);
+//   * P = 2^(s - m) <= 2^A_TAU is stored in f16 (11 significant bits).
+//   * Q (64 heads x 512) lands once by TMA in 8 SW128 column chunks.
+//   * The key buffer holds one chunk as f16 [128 keys][512] in 8 SW128 column
 //     chunks of 64 dims (16 KB each).  The window chunk lands by 2-D TMA (an
 //     FP8 window as 64-byte E4M3 column slices in the upper half of each column
-//     chunk, widened to bf16 in place, exactly).  A selected chunk is
-//     dequantised by the 8 math warps from registers: every thread loads its
-//     key's FP4 bytes for the next chunk while the current one is processed
-//     (2 threads per key, 64 dims of each 128-dim tile per thread), so the
-//     gather's latency hides behind a whole chunk.  E2M1 -> bf16 by byte
-//     permutes times the E4M3 scale: the product has at most 6 significant
-//     bits, so the bf16 key is exact.
-//   * S^T = K Q^T is an M=128 (keys) x N=64 (heads) x K=512 tcgen05 bf16 MMA
+//     chunk) and is converted in place tile by tile together with Q.  A
+//     selected chunk is dequantised by the 8 math warps from registers: every
+//     thread loads its key's FP4 bytes for the next chunk while the current one
+//     is processed (2 threads per key, 64 dims of each 128-dim tile per
+//     thread), so the gather's latency hides behind a whole chunk.
+//   * S^T = K Q^T is an M=128 (keys) x N=64 (heads) x K=512 tcgen05 f16 MMA
 //     product issued as four chains of 8 MMAs (dims 128t .. 128t + 127, one
 //     TMEM accumulator each) by four threads; chain t starts as soon as tile t
-//     of the key buffer is written (for the window: as soon as its TMA lands).
+//     of the key buffer is written.
 //   * Softmax straight from TMEM (thread = key, 32 heads in registers, the four
 //     partial products added; column maxima and sums by transpose-reductions
 //     over the lanes, the four warps of a head half meet on a named barrier),
 //     in base-2 units (the scale carries log2 e): P = 2^(S - m) becomes the
-//     MN-major bf16 B operand [key][head] of the second product.
+//     MN-major f16 B operand [key][head] of the second product.
 //   * O^T += V^T P^T reuses the key buffer as an MN-major A operand: 4 tiles of
 //     M=128 dims x N=64 heads x K=128 keys, accumulated over the chunks in TMEM,
 //     one issuing thread per tile.  Once tile t of a chunk is done, its two
@@ -54,11 +61,11 @@ constexpr int A_MATH_WARPS = 8;                         // dequantisation, softm
 constexpr int A_MATH = 32 * A_MATH_WARPS;
 constexpr int A_THREADS = A_MATH + 4 * 32;              // + 4 MMA-issuing warps (one also loads, one owns TMEM)
 constexpr int A_KEYS = 128;                             // keys per chunk (one M = 128 tile)
-constexpr int A_CHUNK_BYTES = A_KEYS * 128;             // [128 keys][64 dims] bf16 = 16 KB
-constexpr int A_QCHUNK_BYTES = H * 128;                 // [64 heads][64 dims] bf16 = 8 KB
+constexpr int A_CHUNK_BYTES = A_KEYS * 128;             // [128 keys][64 dims] 16-bit = 16 KB
+constexpr int A_QCHUNK_BYTES = H * 128;                 // [64 heads][64 dims] 16-bit = 8 KB
 constexpr int A_OFF_K = 0;                              // 8 key column chunks, 128 KB
 constexpr int A_OFF_Q = 8 * A_CHUNK_BYTES;              // 8 Q column chunks, 64 KB
-constexpr int A_OFF_P = A_OFF_Q + 8 * A_QCHUNK_BYTES;   // P^T [128 keys][64 heads] bf16 SW128, 16 KB
+constexpr int A_OFF_P = A_OFF_Q + 8 * A_QCHUNK_BYTES;   // P^T [128 keys][64 heads] f16 SW128, 16 KB
 constexpr int A_OFF_SMALL = A_OFF_P + A_KEYS * H * 2;
 constexpr int A_TMEM_COLS = 512;
 constexpr int A_S_COL = 0;                              // S^T partial of tile t at 64 t
@@ -94,35 +101,38 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Eight E2M1 codes (element k in bits 4k..4k+3 of w) -> four bf16x2 words
-// (element 2i in the low half of word i).  The bf16 patterns of the eight
-// magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are looked up byte-wise (high bytes
-// 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80 C0) and each code's
-// sign bit becomes bit 15 of its half.
-__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t out[4]) {
-  const uint32_t mag = w & 0x77777777u;
-  uint32_t h0 = prmt(0x3F3F3F00u, 0x40404040u, mag);
-  uint32_t h1 = prmt(0x3F3F3F00u, 0x40404040u, mag >> 16);
-  const uint32_t l0 = prmt(0xC0800000u, 0xC0804000u, mag);
-  const uint32_t l1 = prmt(0xC0800000u, 0xC0804000u, mag >> 16);
-  const uint32_t a = w << 4;                  // byte j, bit 7: sign of element 2j (w's byte j: element 2j+1)
-  h0 |= prmt(a, w, 0x5140u) & 0x80808080u;    // byte k, bit 7: sign of element k (k = 0..3)
-  h1 |= prmt(a, w, 0x7362u) & 0x80808080u;    // elements 4..7
-  out[0] = prmt(l0, h0, 0x5140u);
-  out[1] = prmt(l0, h0, 0x7362u);
-  out[2] = prmt(l1, h1, 0x5140u);
-  out[3] = prmt(l1, h1, 0x7362u);
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
 }
 
-// Two E4M3 bytes (element 0 in bits 0..7) -> one bf16x2 word (element 0 in the
-// low half).  Exact: every E4M3 value is an f16 and a bf16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-  uint32_t h2;
-  asm("{ .reg .b16 lo16, hi16; mov.b32 {lo16, hi16}, %1; cvt.rn.f16x2.e4m3x2 %0, lo16; }" : "=r"(h2) : "r"(two));
-  float lo, hi;
-  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
-      : "=f"(lo), "=f"(hi) : "r"(h2));
-  return pack_bf16x2(lo, hi);
+// two bf16 (element 0 in the low half) -> two f16, round to nearest
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Eight E2M1 codes (element k in bits 4k .. 4k+3 of w) -> four f16x2 words
+// (element 2i in the low half of word i): one hardware conversion per byte.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t o[4]) {
+  asm("{ .reg .b8 t0, t1, t2, t3;\n mov.b32 {t0, t1, t2, t3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, t0;\n cvt.rn.f16x2.e2m1x2 %1, t1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, t2;\n cvt.rn.f16x2.e2m1x2 %3, t3; }"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
+
+// Two E4M3 bytes (element 0 in bits 0..7) -> one f16x2 word (element 0 in the
+// low half).  Exact: every E4M3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t d;
+  asm("{ .reg .b16 h;\n cvt.u16.u32 h, %1;\n cvt.rn.f16x2.e4m3x2 %0, h; }" : "=r"(d) : "r"(two));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // byte offset of (row, byte) in a 1 KB-aligned SW128 region of 128-byte rows
@@ -256,8 +266,8 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
             tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.win_full[u]);
         }
       }
-      constexpr uint32_t idesc_s = tc::idesc_bf16(A_KEYS, H, 0, 0);
-      constexpr uint32_t idesc_o = tc::idesc_bf16(128, H, 1, 1);
+      constexpr uint32_t idesc_s = tc::idesc_f16(A_KEYS, H, 0, 0);
+      constexpr uint32_t idesc_o = tc::idesc_f16(128, H, 1, 1);
       // descriptors: the 14-bit start address field (address / 16) never carries
       // (shared memory < 256 KB), so offsets are added to it directly
       const uint64_t a_s = tc::smem_desc(tc::smem_u32(kbuf + 2 * u * A_CHUNK_BYTES), 16, 1024, tc::SW_128B);
@@ -269,10 +279,6 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
       bool ok = true;
       for (int c = 0; c < nc; c++) {
         const uint32_t ph = (uint32_t)c & 1u;
-        if (c == 0) {
-          ok = as_wait(&sm.q_full[u], 0, sm, p.hdr, 32) && ok;
-          if (p.S > 0 && !p.swa_fp8) ok = as_wait(&sm.win_full[u], 0, sm, p.hdr, 34) && ok;
-        }
         ok = as_wait_sleepy(&sm.kready[u], ph, sm, p.hdr, 31) && ok;
         tc::fence_after_sync();
         if (ok) {                                     // S^T partial of tile u: column chunks 2u, 2u + 1
@@ -280,7 +286,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
           for (int i = 0; i < 8; i++) {
             const uint32_t off = (uint32_t)((i >> 2) * A_CHUNK_BYTES + (i & 3) * 32) >> 4;
             const uint32_t offq = (uint32_t)((i >> 2) * A_QCHUNK_BYTES + (i & 3) * 32) >> 4;
-            tc::mma_bf16(s_acc, a_s + off, b_s + offq, idesc_s, i ? 1u : 0u);
+            tc::mma_f16(s_acc, a_s + off, b_s + offq, idesc_s, i ? 1u : 0u);
           }
         }
         tc::commit(&sm.s_full);
@@ -290,7 +296,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
         if (ok) {
 #pragma unroll
           for (int ks = 0; ks < A_KEYS / 16; ks++)
-            tc::mma_bf16(o_acc, a_o + (uint32_t)(ks * 2048 >> 4), b_o + (uint32_t)(ks * 2048 >> 4), idesc_o,
+            tc::mma_f16(o_acc, a_o + (uint32_t)(ks * 2048 >> 4), b_o + (uint32_t)(ks * 2048 >> 4), idesc_o,
                          (c > 0 || ks) ? 1u : 0u);
         }
         tc::commit(&sm.pv_done[u]);
@@ -342,14 +348,12 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
         const int g = kh ? (i ^ 2) : i;
         const uint32_t wa = kh ? cwd[2 * (i ^ 2)] : cwd[2 * i];          // static indices only
         const uint32_t wb = kh ? cwd[2 * (i ^ 2) + 1] : cwd[2 * i + 1];
-        const uint32_t sb = (sw >> (8 * g)) & 255u;
-        const float sc = e4m3_value(sb);
-        const uint32_t sc2 = pack_bf16x2(sc, sc);
+        const uint32_t sc2 = e4m3x2_to_f16x2(prmt(sw >> (8 * g), 0u, 0x0000u));   // the group's scale, twice
         uint32_t o[8];
-        e2m1x8_to_bf16(wa, o);
-        e2m1x8_to_bf16(wb, o + 4);
+        e2m1x8_to_f16(wa, o);
+        e2m1x8_to_f16(wb, o + 4);
 #pragma unroll
-        for (int k = 0; k < 8; k++) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(o[k]), "r"(sc2));
+        for (int k = 0; k < 8; k++) o[k] = hmul2(o[k], sc2);
         *reinterpret_cast<uint4*>(dst + (((2u * g) ^ xr) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(dst + (((2u * g + 1u) ^ xr) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
@@ -362,46 +366,66 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
       const uint32_t ph = (uint32_t)c & 1u;
       // ---------------- the chunk's keys into the key buffer
       if (c == 0) {
-        if (p.S == 0) {                               // no window rows supplied: zero keys (all masked)
-          for (int i = tid; i < 8 * A_CHUNK_BYTES / 16; i += A_MATH)
-            reinterpret_cast<uint4*>(kbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
-        } else if (p.swa_fp8) {                       // (bf16 rows: the issuers wait for the TMA themselves)
-          for (int u = 0; u < 4; u++) ok = as_wait(&sm.win_full[u], 0, sm, p.hdr, 34) && ok;
-          {
-            // thread (r, h) widens row r, dims 32h .. 32h+31 of each column chunk (32
-            // E4M3 bytes at 8 KB + 64 r + 32 h) into four 16-byte bf16 units at their
-            // SW128 places; every thread reads a pair of chunks before any writes it
-            const int r = tid >> 1, h = tid & 1;
+        // Q and the window rows tile by tile (column chunks 2u, 2u + 1): bf16 rounded
+        // to f16, E4M3 widened to f16, in place; then tile u is ready for its chain
 #pragma unroll 1
-            for (int c0 = 0; c0 < 8; c0 += 2) {
-              uint4 raw[2][2];
+        for (int u = 0; u < 4; u++) {
+          ok = as_wait(&sm.q_full[u], 0, sm, p.hdr, 32) && ok;
+          {
+            uint4* qv = reinterpret_cast<uint4*>(qbuf + 2 * u * A_QCHUNK_BYTES);
 #pragma unroll
-              for (int i = 0; i < 2; i++) {
-                const uint4* src = reinterpret_cast<const uint4*>(kbuf + (c0 + i) * A_CHUNK_BYTES +
-                                                                  A_CHUNK_BYTES / 2 + r * 64 + h * 32);
-                raw[i][0] = src[0];
-                raw[i][1] = src[1];
-              }
-              named_sync(1, A_MATH);
+            for (int i = tid; i < 2 * A_QCHUNK_BYTES / 16; i += A_MATH) {
+              const uint4 x = qv[i];
+              qv[i] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                                 bf16x2_to_f16x2(x.w));
+            }
+          }
+          unsigned char* kt = kbuf + 2 * u * A_CHUNK_BYTES;
+          if (p.S == 0) {                             // no window rows supplied: zero keys (all masked)
 #pragma unroll
-              for (int i = 0; i < 2; i++) {
-                unsigned char* dst = kbuf + (c0 + i) * A_CHUNK_BYTES;
+            for (int i = tid; i < 2 * A_CHUNK_BYTES / 16; i += A_MATH)
+              reinterpret_cast<uint4*>(kt)[i] = make_uint4(0u, 0u, 0u, 0u);
+          } else if (!p.swa_fp8) {
+            ok = as_wait(&sm.win_full[u], 0, sm, p.hdr, 34) && ok;
+#pragma unroll 4
+            for (int i = tid; i < 2 * A_CHUNK_BYTES / 16; i += A_MATH) {
+              uint4* kv4 = reinterpret_cast<uint4*>(kt) + i;
+              const uint4 x = *kv4;
+              *kv4 = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                                bf16x2_to_f16x2(x.w));
+            }
+          } else {
+            ok = as_wait(&sm.win_full[u], 0, sm, p.hdr, 34) && ok;
+            // thread (r, h) widens row r, dims 32h .. 32h+31 of both column chunks (32
+            // E4M3 bytes at 8 KB + 64 r + 32 h) into four 16-byte f16 units at their
+            // SW128 places; every thread reads both chunks before any writes them
+            const int r = tid >> 1, h = tid & 1;
+            uint4 raw[2][2];
 #pragma unroll
-                for (int j = 0; j < 4; j++) {
-                  const uint4& w = raw[i][j >> 1];
-                  const uint32_t lo = (j & 1) ? w.z : w.x, hi = (j & 1) ? w.w : w.y;   // bytes 8j .. 8j+7
-                  const uint4 o = make_uint4(e4m3x2_to_bf16x2(lo & 0xFFFFu), e4m3x2_to_bf16x2(lo >> 16),
-                                             e4m3x2_to_bf16x2(hi & 0xFFFFu), e4m3x2_to_bf16x2(hi >> 16));
-                  *reinterpret_cast<uint4*>(dst + sw128((uint32_t)r, (uint32_t)(64 * h + 16 * j))) = o;
-                }
+            for (int i = 0; i < 2; i++) {
+              const uint4* src = reinterpret_cast<const uint4*>(kt + i * A_CHUNK_BYTES + A_CHUNK_BYTES / 2 + r * 64 +
+                                                                h * 32);
+              raw[i][0] = src[0];
+              raw[i][1] = src[1];
+            }
+            named_sync(1, A_MATH);
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+              unsigned char* dst = kt + i * A_CHUNK_BYTES;
+#pragma unroll
+              for (int j = 0; j < 4; j++) {
+                const uint4& w = raw[i][j >> 1];
+                const uint32_t lo = (j & 1) ? w.z : w.x, hi = (j & 1) ? w.w : w.y;   // bytes 8j .. 8j+7
+                const uint4 o = make_uint4(e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi),
+                                           e4m3x2_to_f16x2(hi >> 16));
+                *reinterpret_cast<uint4*>(dst + sw128((uint32_t)r, (uint32_t)(64 * h + 16 * j))) = o;
               }
             }
           }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::bar_arrive(&sm.kready[u]);
         }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0)
-          for (int u = 0; u < 4; u++) tc::bar_arrive(&sm.kready[u]);
       } else {
         // selected chunk: tile u's column chunks are free once chunk c-1's O^T tile u is done
 #pragma unroll
@@ -504,7 +528,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
         for (int e = 0; e < 4; e++) {
           const int j = 4 * j4 + e;
           r[j] = (v[j] == -INFINITY) ? 0.f : ex2_ftz(v[j] - mj[e]);
-          if (j & 1) pk[j >> 1] = pack_bf16x2(r[j - 1], r[j]);
+          if (j & 1) pk[j >> 1] = pack_f16x2(r[j - 1], r[j]);
         }
       }
       // P^T row m (heads 32 hh .. +31 = 16-byte units 4 hh .. 4 hh + 3), SW128

@@ -253,6 +253,11 @@ csa2_status csa2_select_topk(const csa2_cache *cache, const float *scores,
  *   out          bf16 [B][Q][64][512].
  * A selected id >= cap, or a window position outside the supplied rows, is
  * skipped and raises CSA2_ERR_BOUNDS.  Workspace: csa2_attn_workspace_size.
+ * Precision: both products run on f16 operands with fp32 accumulation.  The
+ * dequantised FP4 keys and E4M3 window values are exact in f16; q and bf16
+ * window rows are rounded to f16, which is exact for magnitudes in
+ * [2^-14, 65504] (the layer's activations are expected inside f16's range;
+ * larger magnitudes are not representable).  The probabilities are f16.
  */
 size_t csa2_attn_workspace_size(int B, int Q, int K);
 csa2_status csa2_sparse_swa_attn(const csa2_cache *cache, const uint16_t *q, const int32_t *sel,
