@@ -129,7 +129,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
   return false;
 }
 
-template <int NQ>
+template <int NQ, bool OFFSET>
 __global__ void __launch_bounds__(IsCfg<NQ>::THREADS, IsCfg<NQ>::MIN_CTAS)
 index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) {
   using C = IsCfg<NQ>;
@@ -138,8 +138,14 @@ index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) 
       *reinterpret_cast<IsSmem<NQ>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int groups = (p.Q + NQ - 1) / NQ;    // query groups per sequence
-  const int64_t group = (int64_t)blockIdx.x / p.split;   // (sequence, query group)
-  const int crank = (int)((int64_t)blockIdx.x % p.split); // slice of the group's tiles
+  // grid: x = slice of the group's tiles, y = (sequence, query group), counted
+  // from p.group0 when a call has more groups than one grid holds (OFFSET: the
+  // launcher issues at most 65535 groups per launch).  Any arithmetic on the
+  // block index here (a division of a linear index, a padded z plane, even the
+  // offset) kept more values live and made the grouped scan 5-20 % slower, so
+  // calls that fit one grid use the block index as it is.
+  const int64_t group = OFFSET ? p.group0 + blockIdx.y : (int64_t)blockIdx.y;
+  const int crank = (int)blockIdx.x;
   const int b = (int)(group / groups);
   const int qf = (int)(group % groups) * NQ;
   const int nq = p.Q - qf < NQ ? p.Q - qf : NQ;   // queries in this group
@@ -430,14 +436,16 @@ static cudaError_t set_is_attrs() {
   static_assert(IsCfg<1>::MIN_CTAS * (is_smem_bytes<1>() + 1024) <= 228 * 1024, "resident CTAs");
   static PerDeviceOnce attrs;
   return attrs.ensure([](int) {
-    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)is_smem_bytes<1>());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(index_score_tc_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(index_score_tc_kernel<IS_GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)is_smem_bytes<IS_GROUP>());
+    cudaError_t e = cudaSuccess;
+    for (auto k : {index_score_tc_kernel<1, false>, index_score_tc_kernel<1, true>}) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)is_smem_bytes<1>());
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
+    for (auto k : {index_score_tc_kernel<IS_GROUP, false>, index_score_tc_kernel<IS_GROUP, true>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)is_smem_bytes<IS_GROUP>());
     return e;
   });
 }
@@ -472,15 +480,28 @@ cudaError_t launch_index_score(IsParams p, cudaStream_t stream) {
   if (split < 1) split = 1;
   const int64_t per = ceil_div(tiles, split);
   p.entries_per_cta = per;     // tiles per CTA
-  p.split = ceil_div(tiles, per);
-  if (groups * p.split > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)(groups * p.split));
-  if (grouped)
-    index_score_tc_kernel<IS_GROUP><<<grid, IsCfg<IS_GROUP>::THREADS, is_smem_bytes<IS_GROUP>(), stream>>>(
-        p, map_tile);
-  else
-    index_score_tc_kernel<1><<<grid, IsCfg<1>::THREADS, is_smem_bytes<1>(), stream>>>(p, map_tile);
-  return cudaGetLastError();
+  const int64_t split_ctas = ceil_div(tiles, per);
+  if (split_ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  // at most 65535 query groups per launch (the grid's y limit); the launches of
+  // one call are independent (disjoint queries, shared read-only inputs)
+  for (int64_t g0 = 0; g0 < groups; g0 += 65535) {
+    p.group0 = g0;
+    const dim3 grid((unsigned)split_ctas, (unsigned)(groups - g0 < 65535 ? groups - g0 : 65535));
+    const bool offset = groups > 65535;
+    if (grouped && offset)
+      index_score_tc_kernel<IS_GROUP, true><<<grid, IsCfg<IS_GROUP>::THREADS, is_smem_bytes<IS_GROUP>(), stream>>>(
+          p, map_tile);
+    else if (grouped)
+      index_score_tc_kernel<IS_GROUP, false><<<grid, IsCfg<IS_GROUP>::THREADS, is_smem_bytes<IS_GROUP>(), stream>>>(
+          p, map_tile);
+    else if (offset)
+      index_score_tc_kernel<1, true><<<grid, IsCfg<1>::THREADS, is_smem_bytes<1>(), stream>>>(p, map_tile);
+    else
+      index_score_tc_kernel<1, false><<<grid, IsCfg<1>::THREADS, is_smem_bytes<1>(), stream>>>(p, map_tile);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace csa2

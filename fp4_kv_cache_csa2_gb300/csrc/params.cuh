@@ -37,7 +37,7 @@ struct IsParams {
   int B, Q;
   int64_t max_n;
   int64_t entries_per_cta;    // set by the launcher
-  int64_t split;              // CTAs per query group (index scan; set by the launcher)
+  int64_t group0;             // first query group of this launch (index scan; set by the launcher)
   int32_t* sel;               // fused Reindex: [B][Q][K] output
   int K;
   WsHeader* hdr;
