@@ -266,6 +266,25 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
             tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.win_full[u]);
         }
       }
+    }
+    __syncwarp();
+    // the query's selected entries into L2 ahead of the math warps' per-chunk loads
+    // (by the copy engine: the load pipe stays free): a quarter of the packed
+    // selection per issuing warp, or one 288-byte entry per id
+    if (p.packed_in) {
+      if (lane == 0) {
+        const uint64_t total = (uint64_t)K * MAIN_BYTES;
+        const uint64_t a0 = (total * u / 4) & ~(uint64_t)15;
+        const uint64_t a1 = u == 3 ? total : ((total * (u + 1) / 4) & ~(uint64_t)15);
+        if (a1 > a0) tc::prefetch_l2(p.packed_in + (int64_t)bq * K * MAIN_BYTES + a0, (uint32_t)(a1 - a0));
+      }
+    } else {
+      for (int i = u * 32 + lane; i < K; i += 128) {
+        const int32_t id = sm.ids[i];
+        if (id >= 0 && id < p.cap) tc::prefetch_l2(p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES, MAIN_BYTES);
+      }
+    }
+    if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_f16(A_KEYS, H, 0, 0);
       constexpr uint32_t idesc_o = tc::idesc_f16(128, H, 1, 1);
       // descriptors: the 14-bit start address field (address / 16) never carries
