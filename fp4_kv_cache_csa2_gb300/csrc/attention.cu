@@ -222,11 +222,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
   // ---------------- set-up (reads no input: overlaps the previous kernel under PDL)
   if (warp == A_MATH_WARPS + 3) tc::tmem_alloc(&sm.tmem_base, A_TMEM_COLS);
   if (tid == 0) {
-    for (int u = 0; u < 4; u++) {
-      tc::bar_init(&sm.q_full[u], 1);
-      tc::bar_init(&sm.win_full[u], 1);
-      tc::bar_init(&sm.kready[u], A_MATH_WARPS);
-    }
+    for (int u = 0; u < 4; u++) tc::bar_init(&sm.kready[u], A_MATH_WARPS);
     tc::bar_init(&sm.s_full, 4);
     tc::bar_init(&sm.p_ready, A_MATH_WARPS);
     for (int t = 0; t < 4; t++) tc::bar_init(&sm.pv_done[t], 1);
@@ -234,11 +230,47 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
     tc::bar_init_fence();
   }
   if (warp >= A_MATH_WARPS && lane == 0) {
+    // issuer u owns the copy barriers of its tile (initialised here, used by it
+    // before the CTA barrier below, waited on by the math warps after it)
+    const int u = warp - A_MATH_WARPS;
+    tc::bar_init(&sm.q_full[u], 1);
+    tc::bar_init(&sm.win_full[u], 1);
+    tc::bar_init_fence();
     tc::prefetch_tensormap(&map_q);
     tc::prefetch_tensormap(&map_swa);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t t = p.q_pos[bq];
+  if (warp >= A_MATH_WARPS && lane == 0) {
+    // tile u's Q and window column chunks by TMA, before the selection ids are
+    // read and the CTA barrier: Q needs no other input and goes first
+    const int u = warp - A_MATH_WARPS;
+    tc::bar_arrive_expect_tx(&sm.q_full[u], 2u * A_QCHUNK_BYTES);
+    for (int c = 2 * u; c < 2 * u + 2; c++)
+      tc::tma_load_2d(qbuf + c * A_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.q_full[u]);
+    if (p.S > 0) {           // rows outside this sequence's window are masked, but finite
+      const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
+      if (p.swa_fp8) {       // [128 rows][64 B] E4M3 slices into the upper half of each column chunk
+        tc::bar_arrive_expect_tx(&sm.win_full[u], 2u * (A_CHUNK_BYTES / 2));
+        for (int c = 2 * u; c < 2 * u + 2; c++)
+          tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES + A_CHUNK_BYTES / 2, &map_swa, c * 64, row0, &sm.win_full[u]);
+      } else {
+        tc::bar_arrive_expect_tx(&sm.win_full[u], 2u * A_CHUNK_BYTES);
+        for (int c = 2 * u; c < 2 * u + 2; c++)
+          tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.win_full[u]);
+      }
+    }
+    // the query's selected entries into L2 ahead of the math warps' per-chunk loads
+    // (by the copy engine: the load pipe stays free): a quarter of the packed
+    // selection per issuing warp here, or one 288-byte entry per id once the ids
+    // are in shared memory
+    if (p.packed_in) {
+      const uint64_t total = (uint64_t)K * MAIN_BYTES;
+      const uint64_t a0 = (total * u / 4) & ~(uint64_t)15;
+      const uint64_t a1 = u == 3 ? total : ((total * (u + 1) / 4) & ~(uint64_t)15);
+      if (a1 > a0) tc::prefetch_l2(p.packed_in + (int64_t)bq * K * MAIN_BYTES + a0, (uint32_t)(a1 - a0));
+    }
+  }
   for (int i = tid; i < K; i += A_THREADS) sm.ids[i] = p.sel[(int64_t)bq * K + i];
   tc::fence_before_sync();
   __syncthreads();
@@ -247,38 +279,9 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
 
   if (warp >= A_MATH_WARPS) {
     // ================= MMA issuers: warp 8 + u issues, for every chunk, the S^T
-    // chain of tile u (dims 128u .. 128u + 127) and O^T tile u; first it loads
-    // tile u's Q and window column chunks by TMA
+    // chain of tile u (dims 128u .. 128u + 127) and O^T tile u
     const int u = warp - A_MATH_WARPS;
-    if (lane == 0) {
-      tc::bar_arrive_expect_tx(&sm.q_full[u], 2u * A_QCHUNK_BYTES);
-      for (int c = 2 * u; c < 2 * u + 2; c++)
-        tc::tma_load_2d(qbuf + c * A_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.q_full[u]);
-      if (p.S > 0) {         // rows outside this sequence's window are masked, but finite
-        const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
-        if (p.swa_fp8) {     // [128 rows][64 B] E4M3 slices into the upper half of each column chunk
-          tc::bar_arrive_expect_tx(&sm.win_full[u], 2u * (A_CHUNK_BYTES / 2));
-          for (int c = 2 * u; c < 2 * u + 2; c++)
-            tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES + A_CHUNK_BYTES / 2, &map_swa, c * 64, row0, &sm.win_full[u]);
-        } else {
-          tc::bar_arrive_expect_tx(&sm.win_full[u], 2u * A_CHUNK_BYTES);
-          for (int c = 2 * u; c < 2 * u + 2; c++)
-            tc::tma_load_2d(kbuf + c * A_CHUNK_BYTES, &map_swa, c * 64, row0, &sm.win_full[u]);
-        }
-      }
-    }
-    __syncwarp();
-    // the query's selected entries into L2 ahead of the math warps' per-chunk loads
-    // (by the copy engine: the load pipe stays free): a quarter of the packed
-    // selection per issuing warp, or one 288-byte entry per id
-    if (p.packed_in) {
-      if (lane == 0) {
-        const uint64_t total = (uint64_t)K * MAIN_BYTES;
-        const uint64_t a0 = (total * u / 4) & ~(uint64_t)15;
-        const uint64_t a1 = u == 3 ? total : ((total * (u + 1) / 4) & ~(uint64_t)15);
-        if (a1 > a0) tc::prefetch_l2(p.packed_in + (int64_t)bq * K * MAIN_BYTES + a0, (uint32_t)(a1 - a0));
-      }
-    } else {
+    if (!p.packed_in) {      // the gathered entries into L2 (the packed ones went at the start)
       for (int i = u * 32 + lane; i < K; i += 128) {
         const int32_t id = sm.ids[i];
         if (id >= 0 && id < p.cap) tc::prefetch_l2(p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES, MAIN_BYTES);
