@@ -256,9 +256,10 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   unsigned long long w2[HI / 2];
   pack_head_weights(sm.w, w2);
   bool ok_all = true;
-  for (int r0 = 0, round = 0; r0 < n_tiles; r0 += RX_ROUND, round++) {
+  // ---- 1. copies of a round's tiles: warp w takes tiles w, w + 8; one warp
+  // instruction per block
+  auto issue_copies = [&](int r0) {
     const int rn = min(RX_ROUND, n_tiles - r0);
-    // ---- 1. copies: warp w takes tiles w, w + 8 of the round; one warp instruction per block
     for (int i = warp; i < rn; i += RX_WARPS) {
       uint8_t* codes = sm.tile[i];
       const int32_t my_blk = sm.pool[(r0 + i) * 16 + (lane & 15)];
@@ -286,6 +287,10 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  issue_copies(0);
+  for (int r0 = 0, round = 0; r0 < n_tiles; r0 += RX_ROUND, round++) {
+    const int rn = min(RX_ROUND, n_tiles - r0);
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     tc::fence_proxy_async_smem();                               // the copies feed the tensor cores
     tc::fence_before_sync();
@@ -313,6 +318,8 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
       ok_all = false;
     }
     tc::fence_after_sync();
+    // the tiles are free: the next round's copies fly while this round's keys are formed
+    if (r0 + RX_ROUND < n_tiles) issue_copies(r0 + RX_ROUND);
     // ---- 3. keys: warps 0..3 take the even accumulators and warps 4..7 the odd
     // ones, four TMEM loads in flight per batch
     if (ok_all) {
@@ -342,10 +349,10 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     } else {
       for (int j = warp >> 2; j < rn; j += 2) sm.keys[key_index((r0 + j) * RX_TILE + m)] = 0u;
     }
-    tc::fence_before_sync();
-    __syncthreads();                                            // accumulators and tiles free for the next round
-    tc::fence_after_sync();
+    tc::fence_before_sync();                                    // accumulators read before the next round's MMAs
   }
+  __syncthreads();                                              // every key written, TMEM no longer read
+  tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tmem, RX_TMEM_COLS);
 
   // ---- 4. exact top-K over the pool's slot keys, written in slot order
