@@ -42,8 +42,10 @@
 //     MN-major f16 B operand [key][head] of the second product.
 //   * O^T += V^T P^T reuses the key buffer as an MN-major A operand: 4 tiles of
 //     M=128 dims x N=64 heads x K=128 keys, accumulated over the chunks in TMEM,
-//     one issuing thread per tile.  Once tile t of a chunk is done, its two
-//     column chunks are free and the next chunk's dequantisation writes them.
+//     issued tile after tile by one thread with a commit per tile, so that the
+//     tiles complete in order.  Once tile t of a chunk is done, its two column
+//     chunks are free and the next chunk's dequantisation writes them while the
+//     later tiles' products run.
 //   * At the end every thread divides its dim row of O^T by the head sums and
 //     stores bf16 rows of the output.
 // All mbarrier waits are bounded; a timeout reports CSA2_ERR_TIMEOUT and the
@@ -279,7 +281,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
 
   if (warp >= A_MATH_WARPS) {
     // ================= MMA issuers: warp 8 + u issues, for every chunk, the S^T
-    // chain of tile u (dims 128u .. 128u + 127) and O^T tile u
+    // chain of tile u (dims 128u .. 128u + 127); warp 8 also issues the four O^T tiles
     const int u = warp - A_MATH_WARPS;
     if (!p.packed_in) {      // the gathered entries into L2 (the packed ones went at the start)
       for (int i = u * 32 + lane; i < K; i += 128) {
@@ -294,10 +296,9 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
       // (shared memory < 256 KB), so offsets are added to it directly
       const uint64_t a_s = tc::smem_desc(tc::smem_u32(kbuf + 2 * u * A_CHUNK_BYTES), 16, 1024, tc::SW_128B);
       const uint64_t b_s = tc::smem_desc(tc::smem_u32(qbuf + 2 * u * A_QCHUNK_BYTES), 16, 1024, tc::SW_128B);
-      const uint64_t a_o = tc::smem_desc(tc::smem_u32(kbuf + 2 * u * A_CHUNK_BYTES), A_CHUNK_BYTES, 1024,
-                                         tc::SW_128B);
+      const uint64_t a_o = tc::smem_desc(tc::smem_u32(kbuf), A_CHUNK_BYTES, 1024, tc::SW_128B);
       const uint64_t b_o = tc::smem_desc(tc::smem_u32(pbuf), 8192, 1024, tc::SW_128B);
-      const uint32_t s_acc = tmem + A_S_COL + 64 * u, o_acc = tmem + A_O_COL + 64 * u;
+      const uint32_t s_acc = tmem + A_S_COL + 64 * u;
       bool ok = true;
       for (int c = 0; c < nc; c++) {
         const uint32_t ph = (uint32_t)c & 1u;
@@ -312,16 +313,23 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
           }
         }
         tc::commit(&sm.s_full);
-        // O^T tile u += V^T P^T over this chunk's 128 keys
+        if (u != 0) continue;
+        // O^T += V^T P^T over this chunk's 128 keys, tile by tile from one thread:
+        // the tiles complete in order, so the next chunk's dequantisation of tile
+        // 0 starts after one tile's products instead of all four
         ok = as_wait_sleepy(&sm.p_ready, ph, sm, p.hdr, 33) && ok;
         tc::fence_after_sync();
-        if (ok) {
+#pragma unroll 1
+        for (int v = 0; v < 4; v++) {
+          if (ok) {
+            const uint64_t a_v = a_o + (uint32_t)(2 * v * A_CHUNK_BYTES >> 4);
 #pragma unroll
-          for (int ks = 0; ks < A_KEYS / 16; ks++)
-            tc::mma_f16(o_acc, a_o + (uint32_t)(ks * 2048 >> 4), b_o + (uint32_t)(ks * 2048 >> 4), idesc_o,
-                         (c > 0 || ks) ? 1u : 0u);
+            for (int ks = 0; ks < A_KEYS / 16; ks++)
+              tc::mma_f16(tmem + A_O_COL + 64 * v, a_v + (uint32_t)(ks * 2048 >> 4),
+                           b_o + (uint32_t)(ks * 2048 >> 4), idesc_o, (c > 0 || ks) ? 1u : 0u);
+          }
+          tc::commit(&sm.pv_done[v]);
         }
-        tc::commit(&sm.pv_done[u]);
       }
     }
     __syncwarp();
