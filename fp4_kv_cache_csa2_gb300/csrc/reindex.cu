@@ -59,7 +59,7 @@ struct RxSmem {
   int32_t pool[CSA2_MAX_M];                     // the query's blocks (-1: none)
   float w[HI];
   uint32_t sfb[HI];
-  uint32_t keys[RX_SLOTS + RX_SLOTS / 64];      // slot keys (slot u at u + u / 64); 0 = outside the search domain
+  alignas(16) uint32_t keys[RX_SLOTS / 64 * 68];   // slot keys, rows of 64 (+ 4 pad words); 0 = outside the search domain
   alignas(16) uint32_t hist[4096];              // digit histogram of the current select pass
   int32_t wsum[RX_WARPS];
   int32_t bcast[4];
@@ -68,9 +68,11 @@ struct RxSmem {
 };
 constexpr size_t RX_SMEM = sizeof(RxSmem) + 1024;
 
-// Shared-memory index of slot u's key: one pad word per 64 keys, so that the
-// select's threads, which own 64 consecutive slots each, read distinct banks.
-__device__ __forceinline__ int key_index(int u) { return u + (u >> 6); }
+// Shared-memory index of slot u's key: rows of 64 keys padded to 68 words, so
+// that the select's threads, which own one row each and read it as 16-byte
+// vectors, hit distinct banks in every quarter-warp phase.
+constexpr int RX_KROW = 68;
+__device__ __forceinline__ int key_index(int u) { return (u >> 6) * RX_KROW + (u & 63); }
 static_assert(RX_SMEM <= 227 * 1024, "shared memory");
 
 // Exclusive prefix sum over the CTA (RX_THREADS threads); *total receives the sum.
@@ -97,28 +99,39 @@ __device__ int cta_exclusive_scan(int v, Sm& fs, int* total) {
   return base + x - v;
 }
 
-// Top-K of n keys (key 0 = not a candidate; key of index i at keys[at(i)])
-// by (key desc, index asc), within the CTA: exact radix select over digits of
-// 12, 8, 8 and 4 bits.  Each pass builds the shared histogram of the digit
-// over the keys that match the digits chosen so far; a scan of the bins from
-// the top (each thread sums a run of bins) gives the threshold digit and the
-// number of ties still to take, and a threshold bin taken whole ends the
-// passes early.  The wide first digit (sign, exponent and three mantissa bits
-// of the score) already separates the keys near the K-th, so the later passes
-// touch few keys.  out(i, r) is called for the chosen keys in index order
-// (r = 0, 1, ...); the function returns their number.  Each thread keeps a
-// contiguous chunk of KPT keys in registers.
-template <int KPT, class Sm, class At, class Out>
-__device__ int cta_select(const uint32_t* keys, At at, int n, int K, Sm& fs, Out out) {
-  static_assert(RX_THREADS == 256, "bin runs per thread");
+// Top-K of n keys (n a multiple of 64; key 0 = not a candidate; key of index i
+// at keys[key_index(i)]) by (key desc, index asc), within the CTA: exact radix
+// select over digits of 12, 8, 8 and 4 bits.
+//   * Every thread brings the second largest of the keys it formed (second):
+//     those 2 x 256 >= K distinct keys are all at least the smallest of them,
+//     so no key below it can be among the top K, and the passes skip such keys
+//     (typically most of them; nothing is skipped when a thread formed fewer
+//     than two candidates).
+//   * Each pass builds the shared histogram of the digit over the candidates
+//     that match the digits chosen so far; a scan of the bins from the top (each
+//     thread sums a run of bins) gives the threshold digit and the number of
+//     ties still to take; a threshold bin taken whole ends the passes early.
+//   * Thread t owns keys 64 t .. 64 t + 63 and walks them as 16-byte vectors in
+//     short rolled loops (the select runs once per launch, its code is fetched
+//     cold); the last walk records its keys above and at the threshold as bit
+//     masks, so the output visits the chosen keys only.
+// out(i, r) is called for the chosen keys in index order (r = 0, 1, ...); the
+// function returns their number.
+template <class Sm, class Out>
+__device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t second, Sm& fs, Out out) {
+  static_assert(RX_THREADS == 256 && 2 * RX_THREADS >= CSA2_MAX_K, "bin runs per thread; the candidate floor");
   if (K <= 0) return 0;
-  const int tid = threadIdx.x;
-  const int chunk = (n + RX_THREADS - 1) / RX_THREADS;                         // <= KPT
-  const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
-  uint32_t kr[KPT];
-#pragma unroll
-  for (int j = 0; j < KPT; j++) kr[j] = (i0 + j < i1) ? keys[at(i0 + j)] : 0u;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool mine = 64 * tid < n;
+  // row t holds 64 keys and 4 pad words: the look-ahead load of vector 16 stays in the row
+  const uint4* row = reinterpret_cast<const uint4*>(keys + tid * RX_KROW);
   const uint32_t hist_base = tc::smem_u32(fs.hist);
+  uint32_t lo = __reduce_min_sync(0xFFFFFFFFu, second);
+  if (lane == 0) fs.wsum[warp] = (int)lo;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < RX_WARPS; w++) lo = min(lo, (uint32_t)fs.wsum[w]);
+  lo = max(lo, 1u);                                        // key 0 is never a candidate
   uint32_t prefix = 0, mask = 0;
   int remaining = K;
   bool take_all = false;                                   // at most K candidates
@@ -130,11 +143,18 @@ __device__ int cta_select(const uint32_t* keys, At at, int n, int K, Sm& fs, Out
     const uint32_t dmask = (uint32_t)nbins - 1u;
     for (int b = tid; b < nbins; b += RX_THREADS) fs.hist[b] = 0;
     __syncthreads();
+    if (mine) {
+      uint4 nx = row[0];
+#pragma unroll 1
+      for (int v = 0; v < 16; v++) {
+        const uint4 q = nx;
+        nx = row[v + 1];
+        const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int j = 0; j < KPT; j++) {
-      const uint32_t k = kr[j];
-      if (k != 0u && (k & mask) == prefix)
-        asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * ((k >> shift) & dmask)) : "memory");
+        for (int e = 0; e < 4; e++)
+          if (kk[e] >= lo && (kk[e] & mask) == prefix)
+            asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * ((kk[e] >> shift) & dmask)));
+      }
     }
     __syncthreads();
     // thread t sums the run of bpt bins below nbins - bpt t (larger digits go to lower threads)
@@ -177,30 +197,42 @@ __device__ int cta_select(const uint32_t* keys, At at, int n, int K, Sm& fs, Out
   }
   const uint32_t thr = prefix;
   const int take_eq = remaining;                           // keys equal to thr still to take, in index order
-  int gt = 0, eq = 0;
+  uint64_t gtm = 0, eqm = 0;                               // this thread's keys above / at the threshold
+  if (mine) {
+    uint4 nx = row[0];
+#pragma unroll 1
+    for (int v = 0; v < 16; v++) {
+      const uint4 q = nx;
+      nx = row[v + 1];
+      const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int j = 0; j < KPT; j++) {
-    const uint32_t k = kr[j];
-    if (k == 0u) continue;
-    const uint32_t km = k & mask;                          // digits fixed so far
-    if (take_all || km > thr) gt++;
-    else if (km == thr) eq++;
+      for (int e = 0; e < 4; e++) {
+        const uint32_t km = kk[e] & mask;                  // digits fixed so far
+        const uint64_t bit = 1ull << (4 * v + e);
+        if (kk[e] >= lo) {
+          if (take_all || km > thr) gtm |= bit;
+          else if (km == thr) eqm |= bit;
+        }
+      }
+    }
   }
+  const int gt = __popcll(gtm), eq = __popcll(eqm);
   // one scan of (gt, eq) packed in 16-bit halves (fewer than 2^16 keys)
   int both_tot;
   const int both_before = cta_exclusive_scan((gt << 16) | eq, fs, &both_tot);
   const int gt_before = both_before >> 16, eq_before = both_before & 0xFFFF;
   const int mine_eq = max(0, min(eq, take_eq - eq_before));
+  uint64_t take = gtm;
+  for (int q = 0; q < mine_eq; q++) {                      // the first mine_eq ties, in index order
+    const uint64_t low = eqm & (~eqm + 1ull);
+    take |= low;
+    eqm ^= low;
+  }
   int r = gt_before + min(eq_before, take_eq);
-  int used = 0;
-#pragma unroll
-  for (int j = 0; j < KPT; j++) {
-    const uint32_t k = kr[j];
-    if (k == 0u) continue;
-    const uint32_t km = k & mask;
-    bool take = take_all || km > thr;
-    if (!take && km == thr && used < mine_eq) { take = true; used++; }
-    if (take) out(i0 + j, r++);
+  while (take != 0ull) {
+    const int bit = __ffsll((long long)take) - 1;
+    take &= take - 1ull;
+    out(64 * tid + bit, r++);
   }
   return (both_tot >> 16) + min(both_tot & 0xFFFF, take_eq);
 }
@@ -256,6 +288,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   unsigned long long w2[HI / 2];
   pack_head_weights(sm.w, w2);
   bool ok_all = true;
+  uint32_t first = 0u, second = 0u;
   // ---- 1. copies of a round's tiles: warp w takes tiles w, w + 8; one warp
   // instruction per block
   auto issue_copies = [&](int r0) {
@@ -343,7 +376,10 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
           const int32_t blk = sm.pool[u / BLK];
           const int64_t e = (int64_t)blk * BLK + (u % BLK);
           const bool ok = blk >= 0 && e < nv && u < n_slots;
-          sm.keys[key_index(u)] = ok ? float_key(sc) : 0u;
+          const uint32_t key = ok ? float_key(sc) : 0u;
+          sm.keys[key_index(u)] = key;
+          second = max(second, min(first, key));                // the two largest keys this thread formed
+          first = max(first, key);
         }
       }
     } else {
@@ -357,7 +393,8 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
 
   // ---- 4. exact top-K over the pool's slot keys, written in slot order
   int32_t* sel = p.sel + (int64_t)bq * p.K;
-  const int ns = cta_select<RX_SLOTS / RX_THREADS>(sm.keys, [](int u) { return key_index(u); }, n_tiles * RX_TILE, p.K, sm,
+  static_assert(RX_TILE % 64 == 0 && RX_SLOTS / 64 == RX_THREADS, "one key row per select thread");
+  const int ns = cta_select(sm.keys, n_tiles * RX_TILE, p.K, second, sm,
                                                   [&](int u, int r) {
     sel[r] = sm.pool[u / BLK] * BLK + (u % BLK);
   });
