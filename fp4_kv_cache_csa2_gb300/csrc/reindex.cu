@@ -9,16 +9,19 @@
 //
 // One CTA (256 threads, one per SM) takes one query and scores its whole pool
 // (up to 2048 blocks = 128 tiles of 128 slots) in bulk-synchronous rounds of
-// RX_ROUND tiles, with no per-tile hand-offs:
-//   1. every warp copies whole tiles (one 512-byte block of index codes per
-//      warp instruction, into the SW64 K-major layout, plus the blocks' scale
-//      words) with cp.async;
-//   2. two threads issue the block-scaled MMAs (M = 128 entries, N = 32 heads,
-//      K = 128 as two K = 64 halves; the tile's E8M0 words go to TMEM by
-//      tcgen05.cp just before) into one TMEM accumulator per tile;
-//   3. all warps read the accumulators back (lane = entry, column = head) and
-//      form s = sum_h w_h ReLU(q_h . k), kept as an order-preserving key per
-//      pool slot (0 for slots outside the search domain).
+// RX_ROUND tiles, with no per-tile hand-offs.  Tiles and TMEM accumulators are
+// double-buffered, so that one CTA barrier per round separates three stages of
+// three consecutive rounds:
+//   1. warps 0..6 copy the next round's tiles, one tile each (one 512-byte block
+//      of index codes per warp instruction, into the SW64 K-major layout, plus
+//      the blocks' scale words) with cp.async;
+//   2. meanwhile one thread of warp 7 issues this round's block-scaled MMAs
+//      (M = 128 entries, N = 32 heads, K = 128 as two K = 64 halves; the tile's
+//      E8M0 words go to TMEM by tcgen05.cp just before), one accumulator per tile;
+//   3. then all warps read the previous round's accumulators back (lane = entry,
+//      column = head) and form s = sum_h w_h ReLU(q_h . k), kept as an
+//      order-preserving key per pool slot (0 for slots outside the search
+//      domain).
 // The query is quantised to MXFP4 and its scale words stored in TMEM once.
 // Then one exact radix select over all slot keys in shared memory takes the
 // top K by (score desc, slot asc) and writes the entries in slot order.
@@ -44,17 +47,18 @@ constexpr int RX_THREADS = 256;
 constexpr int RX_WARPS = RX_THREADS / 32;
 constexpr int RX_TILE = 128;                                    // pool slots per tile
 constexpr int RX_SLOTS = CSA2_MAX_M * BLK;                      // 16,384
-constexpr int RX_ROUND = 13;                                    // tiles (and TMEM accumulators) per round
+constexpr int RX_ROUND = 7;                                     // tiles (and TMEM accumulators) per round
+constexpr int RX_BUFS = 2;                                      // rounds whose tiles / accumulators are live
 constexpr int RX_CODES = RX_TILE * IDX_CODE_BYTES;              // 8192
 constexpr int RX_TILE_BYTES = RX_CODES + 512;                   // codes + 512 B scale words (SW64 atoms: 512 B aligned)
 constexpr int RX_TMEM_COLS = 512;
-constexpr int RX_ACC_COL = 0;                                   // RX_ROUND accumulators of 32 columns
-constexpr int RX_SFA_COL = RX_ROUND * HI;                       // 4 columns per tile of the round
-constexpr int RX_SFB_COL = RX_SFA_COL + 4 * RX_ROUND;
+constexpr int RX_ACC_COL = 0;                                   // tile j of buffer b: 32 columns at 32 (RX_ROUND b + j)
+constexpr int RX_SFA_COL = RX_BUFS * RX_ROUND * HI;             // its scale words: 4 columns at RX_SFA_COL + 4 (RX_ROUND b + j)
+constexpr int RX_SFB_COL = RX_SFA_COL + 4 * RX_BUFS * RX_ROUND;
 static_assert(RX_SFB_COL + 4 <= RX_TMEM_COLS, "TMEM columns");
 
 struct RxSmem {
-  uint8_t tile[RX_ROUND][RX_TILE_BYTES];        // SW64 codes, then 128 scale words
+  uint8_t tile[RX_BUFS][RX_ROUND][RX_TILE_BYTES];   // SW64 codes, then 128 scale words
   uint8_t qcodes[HI * IDX_CODE_BYTES];          // 2 KB, SW64
   int32_t pool[CSA2_MAX_M];                     // the query's blocks (-1: none)
   float w[HI];
@@ -63,7 +67,7 @@ struct RxSmem {
   alignas(16) uint32_t hist[4096];              // digit histogram of the current select pass
   int32_t wsum[RX_WARPS];
   int32_t bcast[4];
-  uint64_t mma_done;
+  uint64_t mma_done[RX_BUFS];
   uint32_t tmem_base;
 };
 constexpr size_t RX_SMEM = sizeof(RxSmem) + 1024;
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   // ---- set-up: TMEM, barrier, head weights, the pool, the query
   if (warp == 0) tc::tmem_alloc(&sm.tmem_base, RX_TMEM_COLS);
   if (tid == 0) {
-    tc::bar_init(&sm.mma_done, 2);                              // one commit per issuing thread
+    for (int b = 0; b < RX_BUFS; b++) tc::bar_init(&sm.mma_done[b], 1);
     tc::bar_init_fence();
   }
   // everything above reads no input: with programmatic dependent launch it
@@ -289,13 +293,14 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   pack_head_weights(sm.w, w2);
   bool ok_all = true;
   uint32_t first = 0u, second = 0u;
-  // ---- 1. copies of a round's tiles: warp w takes tiles w, w + 8; one warp
-  // instruction per block
-  auto issue_copies = [&](int r0) {
+  // ---- 1. copies of the round of tiles r0 .. into buffer b: warp w < 7 takes
+  // tile w; one warp instruction per block
+  auto issue_copies = [&](int r0, int b) {
     const int rn = min(RX_ROUND, n_tiles - r0);
-    for (int i = warp; i < rn; i += RX_WARPS) {
-      uint8_t* codes = sm.tile[i];
-      const int32_t my_blk = sm.pool[(r0 + i) * 16 + (lane & 15)];
+    static_assert(RX_ROUND <= RX_WARPS - 1, "one tile per copying warp");
+    if (warp < rn) {
+      uint8_t* codes = sm.tile[b][warp];
+      const int32_t my_blk = sm.pool[(r0 + warp) * 16 + (lane & 15)];
       const int r = lane >> 2, c = lane & 3;                    // entry of the block, 16-byte chunk
 #pragma unroll 4
       for (int sb = 0; sb < 16; sb++) {
@@ -321,74 +326,86 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  issue_copies(0);
-  for (int r0 = 0, round = 0; r0 < n_tiles; r0 += RX_ROUND, round++) {
+  // ---- 3. keys of the round of tiles r0 .. from accumulator buffer b: warps
+  // 0..3 take the even tiles and warps 4..7 the odd ones, all TMEM loads in flight
+  auto form_keys = [&](int r0, int b) {
     const int rn = min(RX_ROUND, n_tiles - r0);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    tc::fence_proxy_async_smem();                               // the copies feed the tensor cores
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    // ---- 2. MMAs: two issuing threads, even and odd tiles of the round
-    if (lane == 0 && warp < 2) {
-      const uint64_t bdesc = tc::smem_desc(tc::smem_u32(sm.qcodes), 16, 512, tc::SW_64B);
-      constexpr uint32_t id0 = tc::idesc_mxf4(RX_TILE, HI, 0, 0);
-      constexpr uint32_t id1 = tc::idesc_mxf4(RX_TILE, HI, 2, 2);
-      if (ok_all) {
-        for (int j = warp; j < rn; j += 2) {
-          const uint64_t adesc = tc::smem_desc(tc::smem_u32(sm.tile[j]), 16, 512, tc::SW_64B);
-          const uint32_t d = tmem + RX_ACC_COL + j * HI, sfa = tmem + RX_SFA_COL + j * 4;
-          tc::tmem_cp_32x128b_warpx4(sfa, tc::smem_desc(tc::smem_u32(sm.tile[j] + RX_CODES), 128, 128, tc::SW_NONE));
-          tc::mma_mxf4(d, adesc, bdesc, id0, sfa, tmem + RX_SFB_COL, 0);
-          tc::mma_mxf4(d, adesc + 2, bdesc + 2, id1, sfa, tmem + RX_SFB_COL, 1);   // next 32 bytes of K
-        }
-      }
-      tc::commit(&sm.mma_done);
-    }
-    __syncwarp();
-    if (!tc::bar_wait(&sm.mma_done, (uint32_t)round & 1u)) {
-      if (tid == 0) report(p.hdr, CSA2_ERR_TIMEOUT, 2);
-      ok_all = false;
-    }
-    tc::fence_after_sync();
-    // the tiles are free: the next round's copies fly while this round's keys are formed
-    if (r0 + RX_ROUND < n_tiles) issue_copies(r0 + RX_ROUND);
-    // ---- 3. keys: warps 0..3 take the even accumulators and warps 4..7 the odd
-    // ones, four TMEM loads in flight per batch
     if (ok_all) {
-      for (int jb = warp >> 2; jb < rn; jb += 8) {
-        uint32_t acc[4][32];
+      static_assert(RX_ROUND <= 8, "one batch of TMEM loads per round");
+      uint32_t acc[4][32];
 #pragma unroll
-        for (int jj = 0; jj < 4; jj++) {
-          const int j = jb + 2 * jj;
-          if (j < rn) tc::tmem_ld_x32_nowait(tmem + lane_off + RX_ACC_COL + j * HI, acc[jj]);
-        }
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      for (int jj = 0; jj < 4; jj++) {
+        const int j = (warp >> 2) + 2 * jj;
+        if (j < rn) tc::tmem_ld_x32_nowait(tmem + lane_off + RX_ACC_COL + (b * RX_ROUND + j) * HI, acc[jj]);
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int jj = 0; jj < 4; jj++) {
-          const int j = jb + 2 * jj;
-          if (j >= rn) break;
-          float v[32];
+      for (int jj = 0; jj < 4; jj++) {
+        const int j = (warp >> 2) + 2 * jj;
+        if (j >= rn) break;
+        float v[32];
 #pragma unroll
-          for (int h = 0; h < HI; h++) v[h] = __uint_as_float(acc[jj][h]);
-          const float sc = index_head_sum(v, w2);
-          const int u = (r0 + j) * RX_TILE + m;                 // pool slot
-          const int32_t blk = sm.pool[u / BLK];
-          const int64_t e = (int64_t)blk * BLK + (u % BLK);
-          const bool ok = blk >= 0 && e < nv && u < n_slots;
-          const uint32_t key = ok ? float_key(sc) : 0u;
-          sm.keys[key_index(u)] = key;
-          second = max(second, min(first, key));                // the two largest keys this thread formed
-          first = max(first, key);
-        }
+        for (int h = 0; h < HI; h++) v[h] = __uint_as_float(acc[jj][h]);
+        const float sc = index_head_sum(v, w2);
+        const int u = (r0 + j) * RX_TILE + m;                   // pool slot
+        const int32_t blk = sm.pool[u / BLK];
+        const int64_t e = (int64_t)blk * BLK + (u % BLK);
+        const bool ok = blk >= 0 && e < nv && u < n_slots;
+        const uint32_t key = ok ? float_key(sc) : 0u;
+        sm.keys[key_index(u)] = key;
+        second = max(second, min(first, key));                  // the two largest keys this thread formed
+        first = max(first, key);
       }
     } else {
       for (int j = warp >> 2; j < rn; j += 2) sm.keys[key_index((r0 + j) * RX_TILE + m)] = 0u;
     }
-    tc::fence_before_sync();                                    // accumulators read before the next round's MMAs
-  }
-  __syncthreads();                                              // every key written, TMEM no longer read
+  };
+  const int n_rounds = (n_tiles + RX_ROUND - 1) / RX_ROUND;
+  issue_copies(0, 0);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  tc::fence_proxy_async_smem();                                 // the copies feed the tensor cores
+  tc::fence_before_sync();
+  __syncthreads();
   tc::fence_after_sync();
+  for (int round = 0; round <= n_rounds; round++) {
+    const int b = round & 1;
+    // ---- 2. this round's MMAs: its tiles landed before the barrier above, and
+    // its accumulators were last read by the keys of round - 2, also before it
+    if (round < n_rounds && warp == RX_WARPS - 1 && lane == 0) {
+      const int r0 = round * RX_ROUND, rn = min(RX_ROUND, n_tiles - r0);
+      const uint64_t bdesc = tc::smem_desc(tc::smem_u32(sm.qcodes), 16, 512, tc::SW_64B);
+      constexpr uint32_t id0 = tc::idesc_mxf4(RX_TILE, HI, 0, 0);
+      constexpr uint32_t id1 = tc::idesc_mxf4(RX_TILE, HI, 2, 2);
+      if (ok_all) {
+        for (int j = 0; j < rn; j++) {
+          const uint64_t adesc = tc::smem_desc(tc::smem_u32(sm.tile[b][j]), 16, 512, tc::SW_64B);
+          const uint32_t d = tmem + RX_ACC_COL + (b * RX_ROUND + j) * HI;
+          const uint32_t sfa = tmem + RX_SFA_COL + (b * RX_ROUND + j) * 4;
+          tc::tmem_cp_32x128b_warpx4(sfa, tc::smem_desc(tc::smem_u32(sm.tile[b][j] + RX_CODES), 128, 128, tc::SW_NONE));
+          tc::mma_mxf4(d, adesc, bdesc, id0, sfa, tmem + RX_SFB_COL, 0);
+          tc::mma_mxf4(d, adesc + 2, bdesc + 2, id1, sfa, tmem + RX_SFB_COL, 1);   // next 32 bytes of K
+        }
+      }
+      tc::commit(&sm.mma_done[b]);
+    }
+    __syncwarp();
+    // ---- the previous round's products are complete: its tiles may be
+    // overwritten by the next round's copies, its accumulators hold its scores
+    if (round >= 1) {
+      if (!tc::bar_wait(&sm.mma_done[b ^ 1], (uint32_t)((round - 1) >> 1) & 1u)) {
+        if (tid == 0) report(p.hdr, CSA2_ERR_TIMEOUT, 2);
+        ok_all = false;
+      }
+      tc::fence_after_sync();
+    }
+    if (round + 1 < n_rounds) issue_copies((round + 1) * RX_ROUND, b ^ 1);
+    if (round >= 1) form_keys((round - 1) * RX_ROUND, b ^ 1);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();                                    // accumulators read before they are written again
+    __syncthreads();
+    tc::fence_after_sync();
+  }
   if (warp == 0) tc::tmem_dealloc(tmem, RX_TMEM_COLS);
 
   // ---- 4. exact top-K over the pool's slot keys, written in slot order
