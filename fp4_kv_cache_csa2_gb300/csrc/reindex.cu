@@ -66,6 +66,7 @@ struct RxSmem {
   alignas(16) uint32_t keys[RX_SLOTS / 64 * 68];   // slot keys, rows of 64 (+ 4 pad words); 0 = outside the search domain
   alignas(16) uint32_t hist[4096];              // digit histogram of the current select pass
   int32_t wsum[RX_WARPS];
+  uint32_t wmax[RX_WARPS];
   int32_t bcast[4];
   uint64_t mma_done[RX_BUFS];
   uint32_t tmem_base;
@@ -105,12 +106,17 @@ __device__ int cta_exclusive_scan(int v, Sm& fs, int* total) {
 
 // Top-K of n keys (n a multiple of 64; key 0 = not a candidate; key of index i
 // at keys[key_index(i)]) by (key desc, index asc), within the CTA: exact radix
-// select over digits of 12, 8, 8 and 4 bits.
-//   * Every thread brings the second largest of the keys it formed (second):
-//     those 2 x 256 >= K distinct keys are all at least the smallest of them,
-//     so no key below it can be among the top K, and the passes skip such keys
-//     (typically most of them; nothing is skipped when a thread formed fewer
-//     than two candidates).
+// select.
+//   * Every thread brings the largest and the second largest of the keys it
+//     formed (first, second).  Those 2 x 256 >= K distinct keys are all at
+//     least the smallest second, lo, so no key below lo can be among the top K:
+//     the candidates are the keys >= lo (all nonzero keys when a thread formed
+//     fewer than two), typically a small fraction.
+//   * The select runs on kp = key - lo, which orders the candidates as the keys
+//     do, over digits of kp: the first 12 bits just below the span of the
+//     candidates (max key - lo), so that they spread over all 4096 bins (few
+//     share one, few shared-memory atomics collide, and the threshold bin
+//     usually holds just the keys still to take), then 8 bits at a time.
 //   * Each pass builds the shared histogram of the digit over the candidates
 //     that match the digits chosen so far; a scan of the bins from the top (each
 //     thread sums a run of bins) gives the threshold digit and the number of
@@ -122,7 +128,7 @@ __device__ int cta_exclusive_scan(int v, Sm& fs, int* total) {
 // out(i, r) is called for the chosen keys in index order (r = 0, 1, ...); the
 // function returns their number.
 template <class Sm, class Out>
-__device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t second, Sm& fs, Out out) {
+__device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, uint32_t second, Sm& fs, Out out) {
   static_assert(RX_THREADS == 256 && 2 * RX_THREADS >= CSA2_MAX_K, "bin runs per thread; the candidate floor");
   if (K <= 0) return 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -130,19 +136,29 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t second, S
   // row t holds 64 keys and 4 pad words: the look-ahead load of vector 16 stays in the row
   const uint4* row = reinterpret_cast<const uint4*>(keys + tid * RX_KROW);
   const uint32_t hist_base = tc::smem_u32(fs.hist);
-  uint32_t lo = __reduce_min_sync(0xFFFFFFFFu, second);
-  if (lane == 0) fs.wsum[warp] = (int)lo;
+  {
+    const uint32_t wlo = __reduce_min_sync(0xFFFFFFFFu, second), whi = __reduce_max_sync(0xFFFFFFFFu, first);
+    if (lane == 0) {
+      fs.wsum[warp] = (int)wlo;
+      fs.wmax[warp] = whi;
+    }
+  }
   __syncthreads();
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
-  for (int w = 0; w < RX_WARPS; w++) lo = min(lo, (uint32_t)fs.wsum[w]);
+  for (int w = 0; w < RX_WARPS; w++) {
+    lo = min(lo, (uint32_t)fs.wsum[w]);
+    hi = max(hi, fs.wmax[w]);
+  }
   lo = max(lo, 1u);                                        // key 0 is never a candidate
-  uint32_t prefix = 0, mask = 0;
+  const uint32_t span = hi >= lo ? hi - lo : 0u;           // every candidate's kp is at most span
+  const int span_bits = span ? 32 - __clz(span) : 0;
+  uint32_t prefix = 0, mask = 0;                           // digits of kp fixed so far
   int remaining = K;
   bool take_all = false;                                   // at most K candidates
+  int shift = max(0, span_bits - 12), width = 12;
 #pragma unroll 1
-  for (int pass = 0; pass < 4; pass++) {
-    const int width = pass == 0 ? 12 : (pass == 3 ? 4 : 8);
-    const int shift = pass == 0 ? 20 : (pass == 1 ? 12 : (pass == 2 ? 4 : 0));
+  for (int pass = 0;; pass++) {
     const int nbins = 1 << width;
     const uint32_t dmask = (uint32_t)nbins - 1u;
     for (int b = tid; b < nbins; b += RX_THREADS) fs.hist[b] = 0;
@@ -155,17 +171,22 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t second, S
         nx = row[v + 1];
         const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int e = 0; e < 4; e++)
-          if (kk[e] >= lo && (kk[e] & mask) == prefix)
-            asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * ((kk[e] >> shift) & dmask)));
+        for (int e = 0; e < 4; e++) {
+          const uint32_t kp = kk[e] - lo;
+          if (kk[e] >= lo && (kp & mask) == prefix)
+            asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * ((kp >> shift) & dmask)));
+        }
       }
     }
     __syncthreads();
-    // thread t sums the run of bpt bins below nbins - bpt t (larger digits go to lower threads)
+    // thread t sums the run of bpt bins below nbins - bpt t (larger digits go to
+    // lower threads), each lane starting at its own bin of the run (no two lanes
+    // of a warp on one bank)
     const int bpt = nbins >= RX_THREADS ? nbins / RX_THREADS : 1;
     const int top = nbins - bpt * tid;                     // bins [top - bpt, top) when top > 0
     int c = 0;
-    for (int q = 0; q < bpt && top - 1 - q >= 0; q++) c += (int)fs.hist[top - 1 - q];
+    if (top > 0)
+      for (int q = 0; q < bpt; q++) c += (int)fs.hist[top - 1 - ((q + lane) & (bpt - 1))];
     int tot;
     const int above = cta_exclusive_scan(c, fs, &tot);     // keys with a larger digit than this run
     if (pass == 0 && tot <= remaining) {
@@ -194,10 +215,14 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t second, S
     // need not be looked at
     const bool whole = fs.bcast[2] == fs.bcast[1];
     prefix |= (uint32_t)d << shift;
-    mask |= dmask << shift;
+    // every bit at and above the digit is fixed now (those above the first
+    // digit are zero for every candidate)
+    mask = ~((1u << shift) - 1u);
     remaining = fs.bcast[1];
     __syncthreads();                                       // bcast and hist read before the next pass writes them
-    if (whole) break;
+    if (whole || shift == 0) break;
+    width = min(8, shift);
+    shift -= width;
   }
   const uint32_t thr = prefix;
   const int take_eq = remaining;                           // keys equal to thr still to take, in index order
@@ -211,7 +236,7 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t second, S
       const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int e = 0; e < 4; e++) {
-        const uint32_t km = kk[e] & mask;                  // digits fixed so far
+        const uint32_t km = (kk[e] - lo) & mask;           // digits fixed so far
         const uint64_t bit = 1ull << (4 * v + e);
         if (kk[e] >= lo) {
           if (take_all || km > thr) gtm |= bit;
@@ -243,7 +268,7 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t second, S
 
 __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams p) {
   extern __shared__ unsigned char smem_raw[];
-  RxSmem& sm = *reinterpret_cast<RxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  RxSmem& sm = *reinterpret_cast<RxSmem*>(tc::align_smem_1k(smem_raw));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bq = (int)blockIdx.x;
   const int b = bq / p.Q;
@@ -411,7 +436,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
   // ---- 4. exact top-K over the pool's slot keys, written in slot order
   int32_t* sel = p.sel + (int64_t)bq * p.K;
   static_assert(RX_TILE % 64 == 0 && RX_SLOTS / 64 == RX_THREADS, "one key row per select thread");
-  const int ns = cta_select(sm.keys, n_tiles * RX_TILE, p.K, second, sm,
+  const int ns = cta_select(sm.keys, n_tiles * RX_TILE, p.K, first, second, sm,
                                                   [&](int u, int r) {
     sel[r] = sm.pool[u / BLK] * BLK + (u % BLK);
   });

@@ -13,6 +13,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// The 1 KB-aligned start of a dynamic shared-memory array, derived from the
+// array by pointer arithmetic: the compiler then keeps shared-memory addressing
+// (ld.shared / st.shared) for every access through it.  A round trip through an
+// integer would hide the address space and leave generic loads and stores.
+__device__ __forceinline__ unsigned char* align_smem_1k(unsigned char* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // ------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
