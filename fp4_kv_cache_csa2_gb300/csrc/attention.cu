@@ -209,7 +209,7 @@ __device__ __forceinline__ float lane_columns(float* r, int lane) {
 __global__ void __launch_bounds__(A_THREADS, 1)
 attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_swa) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* smem = tc::align_smem_1k(smem_raw);
   unsigned char* kbuf = smem + A_OFF_K;
   unsigned char* qbuf = smem + A_OFF_Q;
   unsigned char* pbuf = smem + A_OFF_P;

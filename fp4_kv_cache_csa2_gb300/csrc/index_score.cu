@@ -134,8 +134,7 @@ __global__ void __launch_bounds__(IsCfg<NQ>::THREADS, IsCfg<NQ>::MIN_CTAS)
 index_score_tc_kernel(IsParams p, const __grid_constant__ CUtensorMap map_tile) {
   using C = IsCfg<NQ>;
   extern __shared__ unsigned char smem_raw[];
-  IsSmem<NQ>& sm =
-      *reinterpret_cast<IsSmem<NQ>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  IsSmem<NQ>& sm = *reinterpret_cast<IsSmem<NQ>*>(tc::align_smem_1k(smem_raw));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int groups = (p.Q + NQ - 1) / NQ;    // query groups per sequence
   // grid: x = slice of the group's tiles, y = (sequence, query group), counted
