@@ -80,6 +80,14 @@ constexpr int RX_KROW = 68;
 __device__ __forceinline__ int key_index(int u) { return (u >> 6) * RX_KROW + (u & 63); }
 static_assert(RX_SMEM <= 227 * 1024, "shared memory");
 
+// 16-byte shared-memory load at a shared-window address (kept in order with
+// the surrounding shared-memory atomics).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+
 // Exclusive prefix sum over the CTA (RX_THREADS threads); *total receives the sum.
 template <class Sm>
 __device__ int cta_exclusive_scan(int v, Sm& fs, int* total) {
@@ -134,7 +142,7 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool mine = 64 * tid < n;
   // row t holds 64 keys and 4 pad words: the look-ahead load of vector 16 stays in the row
-  const uint4* row = reinterpret_cast<const uint4*>(keys + tid * RX_KROW);
+  const uint32_t row = tc::smem_u32(keys + tid * RX_KROW);
   const uint32_t hist_base = tc::smem_u32(fs.hist);
   {
     const uint32_t wlo = __reduce_min_sync(0xFFFFFFFFu, second), whi = __reduce_max_sync(0xFFFFFFFFu, first);
@@ -164,11 +172,11 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
     for (int b = tid; b < nbins; b += RX_THREADS) fs.hist[b] = 0;
     __syncthreads();
     if (mine) {
-      uint4 nx = row[0];
+      uint4 nx = lds128(row);
 #pragma unroll 1
       for (int v = 0; v < 16; v++) {
         const uint4 q = nx;
-        nx = row[v + 1];
+        nx = lds128(row + 16u * (v + 1));
         const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int e = 0; e < 4; e++) {
@@ -228,11 +236,11 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
   const int take_eq = remaining;                           // keys equal to thr still to take, in index order
   uint64_t gtm = 0, eqm = 0;                               // this thread's keys above / at the threshold
   if (mine) {
-    uint4 nx = row[0];
+    uint4 nx = lds128(row);
 #pragma unroll 1
     for (int v = 0; v < 16; v++) {
       const uint4 q = nx;
-      nx = row[v + 1];
+      nx = lds128(row + 16u * (v + 1));
       const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int e = 0; e < 4; e++) {
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
     sm.pool[i] = blk;
   }
-  if (warp == RX_WARPS - 1) quantize_index_query_warp(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
+  if (warp == RX_WARPS - 1) quantize_index_query_warp_loads_first(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
   tc::fence_proxy_async_smem();                                 // the query codes feed the tensor cores
   tc::fence_before_sync();
   __syncthreads();
