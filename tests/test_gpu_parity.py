@@ -518,14 +518,16 @@ def test_decode_packed_selection_must_be_aligned(csa2):
                     scale=case.scale, sel=sel, out=out, ws=ws, packed_sel=packed[8:])
 
 
-def test_decode_reindex_cluster_select_ties_and_short_pool(csa2):
-    """Reindex selection is one radix select across the 8 CTAs that each score an
-    eighth of the pool.  Query 0: every block in the pool, and eight blocks spread
-    over all eight eighths carry copies of one index-key row, so 65 entries have
-    bit-identical scores and K cuts through them: the lowest ids must win (score
-    desc, id asc).  Its last pooled entry is not yet visible.  Query 1: a pool of
-    30 blocks (240 entries) padded with -1 and K > 240, so every pooled entry is
-    chosen in ascending order and the tail of sel is -1."""
+def test_decode_reindex_select_ties_and_short_pool(csa2):
+    """Reindex selection is one radix select over the keys of the whole pool
+    (512 blocks = 32 tiles, scored in several rounds; each select thread owns
+    64 consecutive slots).  Query 0: every block in the pool, and eight blocks
+    spread over the pool carry copies of one index-key row, so 65 entries have
+    bit-identical scores in different rounds and different threads' key rows,
+    and K cuts through them: the lowest ids must win (score desc, id asc).  Its
+    last pooled entry is not yet visible.  Query 1: a pool of 30 blocks (240
+    entries) padded with -1 and K > 240, so every pooled entry is chosen in
+    ascending order and the tail of sel is -1."""
     T, M = 4096, 512
     case = cases.make_case(B=1, T=T, m=1, Q=2, M=M, K=1, seed=911)
     L = GpuLayer(csa2, case)
