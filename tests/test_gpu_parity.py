@@ -518,6 +518,63 @@ def test_decode_packed_selection_must_be_aligned(csa2):
                     scale=case.scale, sel=sel, out=out, ws=ws, packed_sel=packed[8:])
 
 
+def test_decode_reindex_select_equal_and_two_level_scores(csa2):
+    """Reindex selection where the scores leave the select little to separate.
+    Query 0: every entry carries the same index-key row, so every score is the
+    same: every pooled key is a candidate, the first digit pass finds all of
+    them in one bin, and the lowest ids of the pool (every other block) must
+    be taken.  Query 1: the pooled blocks with index 1 mod 8 (none of query
+    0's) carry a second row with a higher score, so the keys take two values
+    and K cuts through the lower group: all higher keys plus the lowest-id
+    lower keys.  Both compared with the oracle's exact selection, and the
+    attention over them."""
+    T, M = 4096, 512
+    case = cases.make_case(B=1, T=T, m=1, Q=2, M=M, K=1, seed=913)
+    L = GpuLayer(csa2, case)
+    main, codes, scales = cases.oracle_cache(case)
+    codes, scales = codes.copy(), scales.copy()
+    s_all = _oracle_scores(case, codes, scales, 0, 1, np.arange(T))
+    order = np.argsort(-s_all, kind="stable")
+    hi_row, lo_row = int(order[10]), int(order[2000])
+    assert s_all[hi_row] > s_all[lo_row]
+    hi_c, hi_s = codes[0, hi_row].copy(), scales[0, hi_row].copy()
+    codes[0, :] = codes[0, lo_row].copy()
+    scales[0, :] = scales[0, lo_row].copy()
+    hi_blocks = np.arange(1, 200, 8)                               # odd blocks only
+    for blk in hi_blocks:
+        codes[0, 8 * blk:8 * blk + 8] = hi_c
+        scales[0, 8 * blk:8 * blk + 8] = hi_s
+    L.cache.idx_codes[0, :T].copy_(torch.from_numpy(codes[0]))
+    L.cache.idx_scales[0, :T].copy_(torch.from_numpy(scales[0]))
+
+    K = 300
+    pool = np.full((1, 2, M), -1, np.int32)
+    pool[0, 0, :256] = np.arange(0, M, 2)                          # every other block
+    pool[0, 1, :200] = np.arange(200)
+    sel = torch.empty((1, 2, K), dtype=torch.int32, device=DEV)
+    out = torch.empty((1, 2, 64, 512), dtype=torch.int16, device=DEV)
+    ws = csa2.Workspace(csa2.decode_workspace_size(1, 1, 2, T, M, K), device=DEV)
+    csa2.decode(csa2.MODE_REINDEX, L.cache, q_pos=L.q_pos, q=L.q, swa=L.swa, swa_base_pos=L.swa_base,
+                scale=case.scale, sel=sel, out=out, ws=ws, M=M, max_n=T, q_idx=L.q_idx, w_head=L.w_head,
+                pool_blocks=dev(pool))
+    assert ws.sync_status()[0] == 0
+    got, got_out = host(sel), bf16_to_f32(out)
+    for qi in range(2):
+        nv = oracle.visible_entries(case.q_pos[0, qi], 1, T)
+        s = np.full(T, -np.inf)
+        s[:nv] = _oracle_scores(case, codes, scales, 0, qi, np.arange(nv))
+        dom = oracle.pool_entries(pool[0, qi], nv)
+        want = oracle.select_topk(s, dom, K)
+        if qi == 0:
+            assert len(np.unique(s[dom])) == 1                     # one score for the whole pool
+        else:
+            hi = np.isin(dom // 8, hi_blocks)
+            assert len(np.unique(s[dom])) == 2 and 0 < hi.sum() < K
+        np.testing.assert_array_equal(got[0, qi], want)
+        cases.check_attention(got_out[0, qi], _oracle_attention(case, main, 0, qi, got[0, qi]),
+                              f"reindex equal scores q{qi}")
+
+
 def test_decode_reindex_select_ties_and_short_pool(csa2):
     """Reindex selection is one radix select over the keys of the whole pool
     (512 blocks = 32 tiles, scored in several rounds; each select thread owns
