@@ -88,6 +88,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
+
 // Exclusive prefix sum over the CTA (RX_THREADS threads); *total receives the sum.
 template <class Sm>
 __device__ int cta_exclusive_scan(int v, Sm& fs, int* total) {
@@ -129,10 +135,11 @@ __device__ int cta_exclusive_scan(int v, Sm& fs, int* total) {
 //     that match the digits chosen so far; a scan of the bins from the top (each
 //     thread sums a run of bins) gives the threshold digit and the number of
 //     ties still to take; a threshold bin taken whole ends the passes early.
-//   * Thread t owns keys 64 t .. 64 t + 63 and walks them as 16-byte vectors in
-//     short rolled loops (the select runs once per launch, its code is fetched
-//     cold); the last walk records its keys above and at the threshold as bit
-//     masks, so the output visits the chosen keys only.
+//   * Thread t owns keys 64 t .. 64 t + 63.  The first pass walks them as
+//     16-byte vectors in a short rolled loop and records the candidates among
+//     them as a bit mask; the later passes and the final walk visit only the
+//     candidates, and the final walk records its keys above and at the
+//     threshold as bit masks, so the output visits the chosen keys only.
 // out(i, r) is called for the chosen keys in index order (r = 0, 1, ...); the
 // function returns their number.
 template <class Sm, class Out>
@@ -162,6 +169,7 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
   const uint32_t span = hi >= lo ? hi - lo : 0u;           // every candidate's kp is at most span
   const int span_bits = span ? 32 - __clz(span) : 0;
   uint32_t prefix = 0, mask = 0;                           // digits of kp fixed so far
+  uint64_t cand = 0;                                       // this thread's candidates (set by the first pass)
   int remaining = K;
   bool take_all = false;                                   // at most K candidates
   int shift = max(0, span_bits - 12), width = 12;
@@ -171,7 +179,7 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
     const uint32_t dmask = (uint32_t)nbins - 1u;
     for (int b = tid; b < nbins; b += RX_THREADS) fs.hist[b] = 0;
     __syncthreads();
-    if (mine) {
+    if (mine && pass == 0) {                               // every key: the candidates, their first digit
       uint4 nx = lds128(row);
 #pragma unroll 1
       for (int v = 0; v < 16; v++) {
@@ -180,10 +188,19 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
         const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-          const uint32_t kp = kk[e] - lo;
-          if (kk[e] >= lo && (kp & mask) == prefix)
-            asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * ((kp >> shift) & dmask)));
+          if (kk[e] >= lo) {
+            cand |= 1ull << (4 * v + e);
+            asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * (((kk[e] - lo) >> shift) & dmask)));
+          }
         }
+      }
+    } else if (mine) {                                     // the candidates only
+#pragma unroll 1
+      for (uint64_t cm = cand; cm != 0ull; cm &= cm - 1ull) {
+        const int bit = __ffsll((long long)cm) - 1;
+        const uint32_t kp = lds32(row + 4u * bit) - lo;
+        if ((kp & mask) == prefix)
+          asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * ((kp >> shift) & dmask)));
       }
     }
     __syncthreads();
@@ -235,22 +252,15 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
   const uint32_t thr = prefix;
   const int take_eq = remaining;                           // keys equal to thr still to take, in index order
   uint64_t gtm = 0, eqm = 0;                               // this thread's keys above / at the threshold
-  if (mine) {
-    uint4 nx = lds128(row);
+  if (take_all) {
+    gtm = cand;
+  } else {
 #pragma unroll 1
-    for (int v = 0; v < 16; v++) {
-      const uint4 q = nx;
-      nx = lds128(row + 16u * (v + 1));
-      const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        const uint32_t km = (kk[e] - lo) & mask;           // digits fixed so far
-        const uint64_t bit = 1ull << (4 * v + e);
-        if (kk[e] >= lo) {
-          if (take_all || km > thr) gtm |= bit;
-          else if (km == thr) eqm |= bit;
-        }
-      }
+    for (uint64_t cm = cand; cm != 0ull; cm &= cm - 1ull) {
+      const int bit = __ffsll((long long)cm) - 1;
+      const uint32_t km = (lds32(row + 4u * bit) - lo) & mask;   // digits fixed so far
+      if (km > thr) gtm |= 1ull << bit;
+      else if (km == thr) eqm |= 1ull << bit;
     }
   }
   const int gt = __popcll(gtm), eq = __popcll(eqm);
