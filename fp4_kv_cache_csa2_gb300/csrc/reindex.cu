@@ -180,19 +180,24 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
     for (int b = tid; b < nbins; b += RX_THREADS) fs.hist[b] = 0;
     __syncthreads();
     if (mine && pass == 0) {                               // every key: the candidates, their first digit
-      uint4 nx = lds128(row);
+      uint4 nx0 = lds128(row), nx1 = lds128(row + 16u);
 #pragma unroll 1
-      for (int v = 0; v < 16; v++) {
-        const uint4 q = nx;
-        nx = lds128(row + 16u * (v + 1));
-        const uint32_t kk[4] = {q.x, q.y, q.z, q.w};
+      for (int v = 0; v < 16; v += 2) {                    // two vectors (eight keys) per iteration
+        const uint4 q0 = nx0, q1 = nx1;
+        if (v + 2 < 16) {                                  // the next pair
+          nx0 = lds128(row + 16u * (v + 2));
+          nx1 = lds128(row + 16u * (v + 3));
+        }
+        const uint32_t kk[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint32_t nib = 0;
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
+        for (int e = 0; e < 8; e++) {
           if (kk[e] >= lo) {
-            cand |= 1ull << (4 * v + e);
+            nib |= 1u << e;
             asm volatile("red.shared.add.u32 [%0], 1;" :: "r"(hist_base + 4u * (((kk[e] - lo) >> shift) & dmask)));
           }
         }
+        cand |= (uint64_t)nib << (4 * v);
       }
     } else if (mine) {                                     // the candidates only
 #pragma unroll 1
