@@ -322,25 +322,7 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
     sm.pool[i] = blk;
   }
-  if (warp == RX_WARPS - 1) quantize_index_query_warp_loads_first(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
-  tc::fence_proxy_async_smem();                                 // the query codes feed the tensor cores
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = sm.tmem_base;
-  // the query's scale words to TMEM lane 32 q + head of every quarter q
-  if (warp < 4) {
-    tc::tmem_st_x1(tmem + ((uint32_t)(warp * 32) << 16) + RX_SFB_COL, sm.sfb[lane]);
-    tc::tmem_wait_st();
-  }
-
-  const int q4 = warp & 3;                                      // TMEM lane quarter of this warp
-  const int m = q4 * 32 + lane;                                 // tile row = slot within the tile
-  const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-  unsigned long long w2[HI / 2];
-  pack_head_weights(sm.w, w2);
-  bool ok_all = true;
-  uint32_t first = 0u, second = 0u;
+  __syncthreads();                                              // the pool, for round 0's copies
   // ---- 1. copies of the round of tiles r0 .. into buffer b: warp w < 7 takes
   // tile w; one warp instruction per block
   auto issue_copies = [&](int r0, int b) {
@@ -374,6 +356,27 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
+  // round 0's copies fly while warp 7 quantises the query
+  issue_copies(0, 0);
+  if (warp == RX_WARPS - 1) quantize_index_query_warp_loads_first(p.q_idx + (int64_t)bq * HI * DI, sm.qcodes, sm.sfb);
+  tc::fence_proxy_async_smem();                                 // the query codes feed the tensor cores
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+  // the query's scale words to TMEM lane 32 q + head of every quarter q
+  if (warp < 4) {
+    tc::tmem_st_x1(tmem + ((uint32_t)(warp * 32) << 16) + RX_SFB_COL, sm.sfb[lane]);
+    tc::tmem_wait_st();
+  }
+
+  const int q4 = warp & 3;                                      // TMEM lane quarter of this warp
+  const int m = q4 * 32 + lane;                                 // tile row = slot within the tile
+  const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+  unsigned long long w2[HI / 2];
+  pack_head_weights(sm.w, w2);
+  bool ok_all = true;
+  uint32_t first = 0u, second = 0u;
   // ---- 3. keys of the round of tiles r0 .. from accumulator buffer b: warps
   // 0..3 take the even tiles and warps 4..7 the odd ones, all TMEM loads in flight
   auto form_keys = [&](int r0, int b) {
@@ -409,7 +412,6 @@ __global__ void __launch_bounds__(RX_THREADS, 1) reindex_select_kernel(IsParams 
     }
   };
   const int n_rounds = (n_tiles + RX_ROUND - 1) / RX_ROUND;
-  issue_copies(0, 0);
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   tc::fence_proxy_async_smem();                                 // the copies feed the tensor cores
   tc::fence_before_sync();
