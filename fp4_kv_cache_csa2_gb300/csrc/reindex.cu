@@ -29,11 +29,14 @@
 // is fp32.  Ties go to the lower pool slot (= lower entry for an ascending
 // pool).  The MMA wait is bounded and reports CSA2_ERR_TIMEOUT.
 //
+// The query is quantised by warp 7 while warps 0..6 issue round 0's copies.
+//
 // (A cluster of six CTAs per query, each scoring a sixth of the pool and
 // exchanging digit histograms for the select, decoded 2.42M query-token-layers
-// per second at 1M entries and batch 16, against 2.88M with this kernel: a
-// cluster holds its six SMs for its slowest member's whole run, and the
-// select's exchange rounds were most of that run.)
+// per second at 1M entries and batch 16, against 2.63M with the first version
+// of this one-CTA kernel and 3.36M with the current one: a cluster holds its
+// six SMs for its slowest member's whole run, and the select's exchange rounds
+// were most of that run.)
 #include <cstddef>
 
 #include "index_query.cuh"
@@ -135,11 +138,12 @@ __device__ int cta_exclusive_scan(int v, Sm& fs, int* total) {
 //     that match the digits chosen so far; a scan of the bins from the top (each
 //     thread sums a run of bins) gives the threshold digit and the number of
 //     ties still to take; a threshold bin taken whole ends the passes early.
-//   * Thread t owns keys 64 t .. 64 t + 63.  The first pass walks them as
-//     16-byte vectors in a short rolled loop and records the candidates among
-//     them as a bit mask; the later passes and the final walk visit only the
-//     candidates, and the final walk records its keys above and at the
-//     threshold as bit masks, so the output visits the chosen keys only.
+//   * Thread t owns keys 64 t .. 64 t + 63.  The first pass walks them two
+//     16-byte vectors at a time in a short rolled loop and records the
+//     candidates among them as a bit mask; the later passes and the final
+//     walk visit only the candidates, and the final walk records its keys
+//     above and at the threshold as bit masks, so the output visits the
+//     chosen keys only.
 // out(i, r) is called for the chosen keys in index order (r = 0, 1, ...); the
 // function returns their number.
 template <class Sm, class Out>
@@ -148,7 +152,7 @@ __device__ int cta_select(const uint32_t* keys, int n, int K, uint32_t first, ui
   if (K <= 0) return 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool mine = 64 * tid < n;
-  // row t holds 64 keys and 4 pad words: the look-ahead load of vector 16 stays in the row
+  // row t: 64 keys (16 vectors of 16 bytes) and 4 pad words
   const uint32_t row = tc::smem_u32(keys + tid * RX_KROW);
   const uint32_t hist_base = tc::smem_u32(fs.hist);
   {
