@@ -504,7 +504,7 @@ def run_decode1m(args, torch, csa2):
     traffic = ncu_traffic(dom_kernel + (":fp8_window" if fp8 else "")) if w.N == 1 << 20 else None
     e2e = None if fp8 else run_decode1m_e2e(args, torch, csa2, w)
     return {
-        "value": value, "ms_per_step": ms_step, "dtype": "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+        "value": value, "ms_per_step": ms_step, "dtype": "fp4-e2m1 cache, mxfp4 index, f16 mma fp32 acc",
         "config": {"workload": f"decode Reindex + 3 Reuse, {w.N:,} entries/seq, batch 16 per layer call",
                    "global_batch": w.B, "seq_len": w.N, "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                    "window_rows": "E4M3, 512 B per row" if fp8 else "bf16, 1 KB per row",
@@ -835,7 +835,7 @@ def run_full131k(args, torch, csa2):
     per_query = N * IDX_ENTRY + HI * DI * 2 + HI * 4 + ATTN_BYTES + M_BLK * 4 + K_SEL * 4
     achieved = scan_bytes / (scan_ms / 1e3) / 1e9
     return _line(args, world, "CSA2 Full decode query-tokens/s/layer at 131K ctx, batch 64", "query-tokens/s",
-                 B * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 B * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, f16 mma fp32 acc",
                  {"workload": "decode Full mode, m=1, 64 sequences x 131,072 entries, one query each",
                   "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                   "l2": "inputs larger than L2 (2.99 GB of cache; the scan reads 570 MB per step)",
@@ -954,7 +954,7 @@ def _hisa_workload(args, torch, csa2, B, N, seed):
     per_query = (8 * IDX_ENTRY + IDX_ENTRY) + nb * (IDX_ENTRY + 4 + 4) + M_BLK * 4 + REINDEX_BYTES
     kname = "index_score_tc_kernel<1>"
     return _line(args, world, f"CSA2 HISA decode query-tokens/s/layer at {N // 1024}K ctx, batch {B}",
-                 "query-tokens/s", B * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 "query-tokens/s", B * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, f16 mma fp32 acc",
                  {"workload": f"HISA decode, m=1, {B} sequences x {N:,} entries, one query each: newest block "
                               f"summary, top-{M_BLK} blocks by mean-key score, Reindex top-{K_SEL} over them, "
                               f"attention",
@@ -1046,7 +1046,7 @@ def run_decoder1m(args, torch, csa2):
     achieved = scan_bytes / (scan_ms / 1e3) / 1e9
     return _line(args, world, "CSA2 whole-decoder query-token-layers/s at 1M ctx (Full + 3 Reuse, 4 x (Reindex + "
                  "3 Reuse)), batch 16", UNIT, B * n_layers * world / (ms / 1e3), ms,
-                 "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 "fp4-e2m1 cache, mxfp4 index, f16 mma fp32 acc",
                  {"workload": f"one token through a 20-layer decoder block chain, {N:,} entries/seq, batch 16: "
                               "Full source layer + 3 Reuse, then 4 x (Reindex on the Full layer's pool + 3 Reuse), "
                               "one cache", "global_batch": B, "seq_len": N, "M_blocks": M_BLK, "K": K_SEL,
@@ -1117,7 +1117,7 @@ def run_prefill8k(args, torch, csa2):
     fp4_peak = bf16 * FP4_PER_BF16
     achieved = flops / (scan_ms / 1e3) / 1e12
     return _line(args, world, "CSA2 prefill-chunk query-tokens/s, 8192 new tokens on a 131K prefix",
-                 "query-tokens/s", Q * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 "query-tokens/s", Q * world / (ms / 1e3), ms, "fp4-e2m1 cache, mxfp4 index, f16 mma fp32 acc",
                  {"workload": "prefill chunk, m=2, 131,072-token prefix + 8192 new tokens (69,632 entries), "
                               "8192 causal queries, batch 1",
                   "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
@@ -1191,7 +1191,7 @@ def run_prefillblock(args, torch, csa2):
     attn_flops = n_layers * Q * (K_SEL + WIN) * H * D * 4
     return _line(args, world, "CSA2 encoder-block prefill query-token-layers/s (Full + 5 Reuse), 8192 new tokens "
                  "on a 131K prefix", UNIT, Q * n_layers * world / (ms / 1e3), ms,
-                 "fp4-e2m1 cache, mxfp4 index, bf16 mma fp32 acc",
+                 "fp4-e2m1 cache, mxfp4 index, f16 mma fp32 acc",
                  {"workload": "encoder block on a prefill chunk, m=2, 131,072-token prefix + 8192 new tokens "
                               "(69,632 entries): the Full source layer + 5 Reuse layers (fresh queries and windows) "
                               "on its selection, batch 1",
