@@ -1473,7 +1473,7 @@ def main():
                              "hisa131k", "hisa1m"])
     ap.add_argument("--seq-len", type=int, default=1 << 20)
     ap.add_argument("--pipeline-distance", type=int, default=3)
-    ap.add_argument("--cpu-sample-queries", type=int, default=384)
+    ap.add_argument("--cpu-sample-queries", type=int, default=768)
     ap.add_argument("--packed-selection", type=int, default=1,
                     help="decode: the Reindex call packs its selected entries for the Reuse calls (1) or not (0)")
     ap.add_argument("--lanes", type=int, default=10,
