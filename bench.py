@@ -348,6 +348,21 @@ class Decode1M:
             self.step(s)
 
 
+def latency_split(torch, B: int, Q: int, K: int = K_SEL) -> int:
+    """CTAs per query in the attention of a call that runs alone (one call at a
+    time, so one CTA per query would leave most SMs idle): as many as keep the
+    call within one wave, at most one per key chunk (the window and every run
+    of 128 selected entries), and none (1) unless that is at least 3 (64
+    queries split in 2 were slower than one CTA each) or above the library's
+    split limit."""
+    bq = B * Q
+    if bq > 128:
+        return 1
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s = min(1 + -(-K // 128), sms // bq)
+    return s if s >= 3 else 1
+
+
 def _clone_cache(c):
     import fp4_kv_cache_csa2_gb300 as csa2
     n = csa2.Cache.__new__(csa2.Cache)
@@ -804,11 +819,13 @@ def run_full131k(args, torch, csa2):
     sel = torch.empty((B, 1, K_SEL), dtype=torch.int32, device=dev)
     out = torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev)
     ws = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_FULL, B, 1, N, M_BLK, K_SEL), device=dev)
+    split = latency_split(torch, B, 1)
 
     def step():
         csa2.decode(csa2.MODE_FULL, cache, q_pos=q_pos, q=q.view(torch.int16), swa=swa.view(torch.int16),
                     swa_base_pos=swa_base, scale=1 / math.sqrt(D), sel=sel, out=out.view(torch.int16), ws=ws,
-                    M=M_BLK, max_n=N, q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool)
+                    M=M_BLK, max_n=N, q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool,
+                    attn_split=split)
     graph = _capture(torch, step)
     for _ in range(args.warmup):
         graph.replay()
@@ -839,7 +856,8 @@ def run_full131k(args, torch, csa2):
                  {"workload": "decode Full mode, m=1, 64 sequences x 131,072 entries, one query each",
                   "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                   "l2": "inputs larger than L2 (2.99 GB of cache; the scan reads 570 MB per step)",
-                  "launch": "one CUDA graph per step (index scan, block and entry selection, attention)"},
+                  "launch": "one CUDA graph per step (index scan, block and entry selection, attention)",
+                  "attention": f"{split} CTAs per query (the key chunks split, partial softmax states merged)"},
                  {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                   "traffic": ncu_traffic("index_score_tc_kernel<1>"), "kernel": "index_score_tc_kernel<1>",
                   "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
@@ -882,9 +900,10 @@ def _hisa_workload(args, torch, csa2, B, N, seed):
     ws_s = csa2.Workspace(1 << 16, device=dev)
     ws_h = csa2.Workspace(csa2.hisa_blocks_workspace_size(B, 1, N), device=dev)
     ws_r = csa2.Workspace(csa2.decode_workspace_size(csa2.MODE_REINDEX, B, 1, N, M_BLK, K_SEL), device=dev)
+    split = latency_split(torch, B, 1)
     common = dict(q_pos=q_pos, q=q.view(torch.int16), swa=swa.view(torch.int16), swa_base_pos=swa_base,
                   scale=1 / math.sqrt(D), sel=sel, out=out.view(torch.int16), M=M_BLK, max_n=N,
-                  q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool)
+                  q_idx=q_idx.view(torch.int16), w_head=w_head, pool_blocks=pool, attn_split=split)
 
     def summary():
         csa2.block_summary(cache, store, newest, 1, ws_s)
@@ -961,7 +980,8 @@ def _hisa_workload(args, torch, csa2, B, N, seed):
                   "M_blocks": M_BLK, "K": K_SEL, "window": WIN,
                   "l2": "inputs larger than L2 (the summary store and cache exceed 129 MB)",
                   "launch": "one CUDA graph per step (summary update, view, summary scan, block selection, "
-                            "Reindex scan+select, attention)"},
+                            "Reindex scan+select, attention)",
+                  "attention": f"{split} CTAs per query (the key chunks split, partial softmax states merged)"},
                  {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                   "traffic": ncu_traffic(f"{kname}:summaries_{B}x{nb}"), "kernel": kname + " over the summary store",
                   "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},
@@ -1013,6 +1033,7 @@ def run_decoder1m(args, torch, csa2):
     outs = [torch.empty((B, 1, H, D), dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
     modes = [csa2.MODE_FULL, csa2.MODE_REINDEX, csa2.MODE_REUSE]
     wss = {m: csa2.Workspace(csa2.decode_workspace_size(m, B, 1, N, M_BLK, K_SEL), device=dev) for m in modes}
+    split = latency_split(torch, B, 1)
 
     def step():
         for l in range(n_layers):
@@ -1021,7 +1042,7 @@ def run_decoder1m(args, torch, csa2):
             csa2.decode(mode, cache, q_pos=q_pos, q=qs[l].view(torch.int16), swa=swas[l].view(torch.int16),
                         swa_base_pos=swa_base, scale=1 / math.sqrt(D), sel=sels[g], out=outs[l].view(torch.int16),
                         ws=wss[mode], M=M_BLK, max_n=N, q_idx=q_idx[g].view(torch.int16), w_head=w_head[g],
-                        pool_blocks=pool, packed_sel=packs[g])
+                        pool_blocks=pool, packed_sel=packs[g], attn_split=split)
     graph = _capture(torch, step)
     for _ in range(args.warmup):
         graph.replay()
@@ -1054,7 +1075,8 @@ def run_decoder1m(args, torch, csa2):
                   "l2": "the Full scan reads the 1.1 GB of index K every token (larger than L2); the Reindex layers "
                         "share the Full layer's pool",
                   "selection": "each Full/Reindex call packs its selected entries for its 3 Reuse calls",
-                  "launch": "one CUDA graph per token, the 20 calls in order on one stream"},
+                  "launch": "one CUDA graph per token, the 20 calls in order on one stream",
+                  "attention": f"{split} CTAs per query (the key chunks split, partial softmax states merged)"},
                  {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                   "traffic": None, "kernel": "index_score_tc_kernel<1> (Full layer at 1M)",
                   "algorithmic_bytes_per_launch": scan_bytes, "avg_launch_ms": scan_ms, "peak_source": which},

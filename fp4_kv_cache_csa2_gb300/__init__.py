@@ -46,7 +46,7 @@ class DecodeArgs(ctypes.Structure):
                 ("w_head", ctypes.c_void_p), ("swa", ctypes.c_void_p),
                 ("swa_base_pos", ctypes.c_void_p), ("pool_blocks", ctypes.c_void_p),
                 ("sel", ctypes.c_void_p), ("out", ctypes.c_void_p), ("packed_sel", ctypes.c_void_p),
-                ("swa_fp8", ctypes.c_int32)]
+                ("swa_fp8", ctypes.c_int32), ("attn_split", ctypes.c_int32)]
 
 
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -290,13 +290,15 @@ def decode_workspace_size(mode: int, B: int, Q: int, max_n: int, M: int, K: int)
 
 def decode(mode: int, cache: Cache, *, q_pos, q, swa, swa_base_pos, scale: float, sel, out,
            ws: Workspace, M: int = 0, max_n: int = 0, q_idx=None, w_head=None, pool_blocks=None,
-           packed_sel=None, swa_fp8: bool = False, stream=None):
+           packed_sel=None, swa_fp8: bool = False, attn_split: int = 0, stream=None):
     """swa: bf16 rows [B][S][512] (as int16), or with swa_fp8 the uint8 rows of
-    swa_quantize_fp8."""
+    swa_quantize_fp8.  attn_split: CTAs per query in the attention (0 / 1: one;
+    S >= 2 splits the query's key chunks over S CTAs and merges their states)."""
     B, Q = q_pos.shape
     a = DecodeArgs(mode, B, Q, M, sel.shape[-1], swa.shape[1], max_n, float(scale), _ptr(q_pos),
                    _ptr(q), _ptr(q_idx), _ptr(w_head), _ptr(swa), _ptr(swa_base_pos),
-                   _ptr(pool_blocks), _ptr(sel), _ptr(out), _ptr(packed_sel), 1 if swa_fp8 else 0)
+                   _ptr(pool_blocks), _ptr(sel), _ptr(out), _ptr(packed_sel), 1 if swa_fp8 else 0,
+                   int(attn_split))
     c = cache.struct()
     _check("csa2_decode", load().csa2_decode(ctypes.byref(c), ctypes.byref(a), ws.ptr, ws.nbytes,
                                              _stream(stream)))

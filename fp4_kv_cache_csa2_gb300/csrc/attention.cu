@@ -73,6 +73,10 @@ constexpr int A_TMEM_COLS = 512;
 constexpr int A_S_COL = 0;                              // S^T partial of tile t at 64 t
 constexpr int A_O_COL = 256;                            // O^T tile t at 256 + 64 t
 constexpr float A_LOG2E = 1.4426950408889634f;
+// split mode: one partial softmax state per (query, CTA): the maxima in use and
+// the sums per head (base-2 units), then the unnormalised O [head][dim]
+constexpr int A_PART_FLOATS = 2 * H + H * D;
+constexpr int A_SPLIT_MAX_BQ = CSA2_ATTN_SPLIT_MAX_QUERIES;   // queries of a call that may be split
 constexpr float A_TAU = 8.0f * A_LOG2E;                 // lazy rescale threshold: 2^A_TAU = e^8
 
 struct AsSmall {
@@ -206,6 +210,10 @@ __device__ __forceinline__ float lane_columns(float* r, int lane) {
   return r[0];
 }
 
+// SPLIT: the query's chunks are divided among p.split CTAs, which write partial
+// states for attn_combine_kernel (a separate instance, so that the one-CTA
+// kernel carries none of it).
+template <bool SPLIT>
 __global__ void __launch_bounds__(A_THREADS, 1)
 attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_swa) {
   extern __shared__ unsigned char smem_raw[];
@@ -215,11 +223,16 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
   unsigned char* pbuf = smem + A_OFF_P;
   AsSmall& sm = *reinterpret_cast<AsSmall*>(smem + A_OFF_SMALL);
 
-  const int bq = blockIdx.x;
+  const int split = SPLIT ? p.split : 1;                 // CTAs per query
+  const int bq = blockIdx.x / split, sp = blockIdx.x % split;
   const int b = bq / p.Q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K;
   const int nc = 1 + (K + A_KEYS - 1) / A_KEYS;          // window chunk + selected chunks
+  // this CTA's chunks (all of them unless the query is split; split <= nc)
+  const int c_lo = sp * nc / split, c_hi = (sp + 1) * nc / split;
+  // its selected entries: slots e_lo .. e_hi - 1
+  const int e_lo = c_lo > 0 ? A_KEYS * (c_lo - 1) : 0, e_hi = min(K, A_KEYS * (c_hi - 1));
 
   // ---------------- set-up (reads no input: overlaps the previous kernel under PDL)
   if (warp == A_MATH_WARPS + 3) tc::tmem_alloc(&sm.tmem_base, A_TMEM_COLS);
@@ -250,7 +263,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
     tc::bar_arrive_expect_tx(&sm.q_full[u], 2u * A_QCHUNK_BYTES);
     for (int c = 2 * u; c < 2 * u + 2; c++)
       tc::tma_load_2d(qbuf + c * A_QCHUNK_BYTES, &map_q, c * 64, bq * H, &sm.q_full[u]);
-    if (p.S > 0) {           // rows outside this sequence's window are masked, but finite
+    if (p.S > 0 && c_lo == 0) {   // rows outside this sequence's window are masked, but finite
       const int32_t row0 = (int32_t)((int64_t)b * p.S + (t - (WIN - 1) - p.swa_base[b]));
       if (p.swa_fp8) {       // [128 rows][64 B] E4M3 slices into the upper half of each column chunk
         tc::bar_arrive_expect_tx(&sm.win_full[u], 2u * (A_CHUNK_BYTES / 2));
@@ -266,11 +279,12 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
     // (by the copy engine: the load pipe stays free): a quarter of the packed
     // selection per issuing warp here, or one 288-byte entry per id once the ids
     // are in shared memory
-    if (p.packed_in) {
-      const uint64_t total = (uint64_t)K * MAIN_BYTES;
+    if (p.packed_in && e_hi > e_lo) {
+      const uint64_t first = (uint64_t)e_lo * MAIN_BYTES, total = (uint64_t)(e_hi - e_lo) * MAIN_BYTES;
       const uint64_t a0 = (total * u / 4) & ~(uint64_t)15;
       const uint64_t a1 = u == 3 ? total : ((total * (u + 1) / 4) & ~(uint64_t)15);
-      if (a1 > a0) tc::prefetch_l2(p.packed_in + (int64_t)bq * K * MAIN_BYTES + a0, (uint32_t)(a1 - a0));
+      if (a1 > a0)
+        tc::prefetch_l2(p.packed_in + (int64_t)bq * K * MAIN_BYTES + first + a0, (uint32_t)(a1 - a0));
     }
   }
   for (int i = tid; i < K; i += A_THREADS) sm.ids[i] = p.sel[(int64_t)bq * K + i];
@@ -284,7 +298,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
     // chain of tile u (dims 128u .. 128u + 127); warp 8 also issues the four O^T tiles
     const int u = warp - A_MATH_WARPS;
     if (!p.packed_in) {      // the gathered entries into L2 (the packed ones went at the start)
-      for (int i = u * 32 + lane; i < K; i += 128) {
+      for (int i = e_lo + u * 32 + lane; i < e_hi; i += 128) {
         const int32_t id = sm.ids[i];
         if (id >= 0 && id < p.cap) tc::prefetch_l2(p.main_kv + ((int64_t)b * p.cap + id) * MAIN_BYTES, MAIN_BYTES);
       }
@@ -300,8 +314,8 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
       const uint64_t b_o = tc::smem_desc(tc::smem_u32(pbuf), 8192, 1024, tc::SW_128B);
       const uint32_t s_acc = tmem + A_S_COL + 64 * u;
       bool ok = true;
-      for (int c = 0; c < nc; c++) {
-        const uint32_t ph = (uint32_t)c & 1u;
+      for (int c = c_lo; c < c_hi; c++) {
+        const uint32_t ph = (uint32_t)(c - c_lo) & 1u;
         ok = as_wait_sleepy(&sm.kready[u], ph, sm, p.hdr, 31) && ok;
         tc::fence_after_sync();
         if (ok) {                                     // S^T partial of tile u: column chunks 2u, 2u + 1
@@ -326,7 +340,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
 #pragma unroll
             for (int ks = 0; ks < A_KEYS / 16; ks++)
               tc::mma_f16(tmem + A_O_COL + 64 * v, a_v + (uint32_t)(ks * 2048 >> 4),
-                           b_o + (uint32_t)(ks * 2048 >> 4), idesc_o, (c > 0 || ks) ? 1u : 0u);
+                           b_o + (uint32_t)(ks * 2048 >> 4), idesc_o, (c > c_lo || ks) ? 1u : 0u);
           }
           tc::commit(&sm.pv_done[v]);
         }
@@ -388,12 +402,21 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
         *reinterpret_cast<uint4*>(dst + (((2u * g + 1u) ^ xr) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     };
-    if (nc > 1) prefetch(1);
+    if (max(c_lo, 1) < c_hi) prefetch(max(c_lo, 1));
     float m_used = -INFINITY;                         // max in use for head 32 hh + lane
     float l_part = 0.f;                               // sum of P over this warp's keys, head 32 hh + lane
     bool ok = true;
-    for (int c = 0; c < nc; c++) {
-      const uint32_t ph = (uint32_t)c & 1u;
+    // Q column chunks 2u, 2u + 1 (bf16 by TMA) rounded to f16 in place
+    auto convert_q = [&](int u) {
+      uint4* qv = reinterpret_cast<uint4*>(qbuf + 2 * u * A_QCHUNK_BYTES);
+#pragma unroll
+      for (int i = tid; i < 2 * A_QCHUNK_BYTES / 16; i += A_MATH) {
+        const uint4 x = qv[i];
+        qv[i] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+      }
+    };
+    for (int c = c_lo; c < c_hi; c++) {
+      const uint32_t ph = (uint32_t)(c - c_lo) & 1u;
       // ---------------- the chunk's keys into the key buffer
       if (c == 0) {
         // Q and the window rows tile by tile (column chunks 2u, 2u + 1): bf16 rounded
@@ -401,15 +424,7 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
 #pragma unroll 1
         for (int u = 0; u < 4; u++) {
           ok = as_wait(&sm.q_full[u], 0, sm, p.hdr, 32) && ok;
-          {
-            uint4* qv = reinterpret_cast<uint4*>(qbuf + 2 * u * A_QCHUNK_BYTES);
-#pragma unroll
-            for (int i = tid; i < 2 * A_QCHUNK_BYTES / 16; i += A_MATH) {
-              const uint4 x = qv[i];
-              qv[i] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
-                                 bf16x2_to_f16x2(x.w));
-            }
-          }
+          convert_q(u);
           unsigned char* kt = kbuf + 2 * u * A_CHUNK_BYTES;
           if (p.S == 0) {                             // no window rows supplied: zero keys (all masked)
 #pragma unroll
@@ -458,10 +473,15 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
         }
       } else {
         // selected chunk: tile u's column chunks are free once chunk c-1's O^T tile u is done
+        // (the first chunk of a CTA without the window also rounds Q's tile u first)
 #pragma unroll
         for (int u = 0; u < 4; u++) {
           ok = as_wait(&sm.pv_done[u], ph ^ 1u, sm, p.hdr, 35) && ok;
           tc::fence_after_sync();
+          if (SPLIT && c == c_lo) {
+            ok = as_wait(&sm.q_full[u], 0, sm, p.hdr, 32) && ok;
+            convert_q(u);
+          }
           dequant_tile(u);
           tc::fence_proxy_async_smem();
           __syncwarp();
@@ -573,11 +593,11 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
       if (lane == 0) tc::bar_arrive(&sm.p_ready);
       // the next chunk's FP4 bytes: issued after the softmax, whose shared-memory and
       // TMEM traffic would otherwise queue behind these loads
-      if (c + 1 < nc) prefetch(c + 1);
+      if (c + 1 < c_hi) prefetch(c + 1);
     }
 
     // ---------------- output: O^T / L, bf16 rows out[head][dim]
-    for (int u = 0; u < 4; u++) ok = as_wait(&sm.pv_done[u], (uint32_t)(nc - 1) & 1u, sm, p.hdr, 37) && ok;
+    for (int u = 0; u < 4; u++) ok = as_wait(&sm.pv_done[u], (uint32_t)(c_hi - 1 - c_lo) & 1u, sm, p.hdr, 37) && ok;
     tc::fence_after_sync();
     // the next kernel of the stream may be scheduled now (triggered at the start,
     // its CTAs would hold SMs idle in their own wait for this whole kernel)
@@ -586,18 +606,36 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
     named_sync(2 + hh, 128);
     const float lsum = sm.red[4 * hh][lane] + sm.red[4 * hh + 1][lane] + sm.red[4 * hh + 2][lane] +
                        sm.red[4 * hh + 3][lane];
-    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-    float il[32];
+    if (!SPLIT) {
+      const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+      float il[32];
 #pragma unroll
-    for (int j = 0; j < 32; j++) il[j] = __shfl_sync(0xFFFFFFFFu, inv, j);
-    uint16_t* out = p.out + (int64_t)bq * H * D + (int64_t)(32 * hh) * D + m;
+      for (int j = 0; j < 32; j++) il[j] = __shfl_sync(0xFFFFFFFFu, inv, j);
+      uint16_t* out = p.out + (int64_t)bq * H * D + (int64_t)(32 * hh) * D + m;
 #pragma unroll 1
-    for (int u = 0; u < 4; u++) {
-      uint32_t o[32];
-      tmem_ld32(tmem + lane_off + A_O_COL + 64 * u + 32 * hh, o);
+      for (int u = 0; u < 4; u++) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + A_O_COL + 64 * u + 32 * hh, o);
 #pragma unroll
-      for (int j = 0; j < 32; j++)
-        out[j * D + 128 * u] = (uint16_t)(pack_bf16x2(__uint_as_float(o[j]) * il[j], 0.f) & 0xFFFFu);
+        for (int j = 0; j < 32; j++)
+          out[j * D + 128 * u] = (uint16_t)(pack_bf16x2(__uint_as_float(o[j]) * il[j], 0.f) & 0xFFFFu);
+      }
+    } else {
+      // this CTA's partial state: maxima in use and sums of heads 32 hh + lane,
+      // then the unnormalised O^T rows (dim 128 u + m of heads 32 hh ..) as O[head][dim]
+      float* part = p.opart + (int64_t)blockIdx.x * A_PART_FLOATS;
+      if (q4 == 0) {
+        part[32 * hh + lane] = m_used;
+        part[H + 32 * hh + lane] = lsum;
+      }
+      float* op = part + 2 * H + (int64_t)(32 * hh) * D + m;
+#pragma unroll 1
+      for (int u = 0; u < 4; u++) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + A_O_COL + 64 * u + 32 * hh, o);
+#pragma unroll
+        for (int j = 0; j < 32; j++) op[j * D + 128 * u] = __uint_as_float(o[j]);
+      }
     }
   }
   tc::fence_before_sync();
@@ -606,6 +644,50 @@ attn_stream_kernel(AttnParams p, const __grid_constant__ CUtensorMap map_q, cons
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, A_TMEM_COLS);
   }
+}
+
+// Split mode: the output of one query from its CTAs' partial states.  With m_s,
+// l_s, O_s the maxima in use, sums and unnormalised outputs of CTA s (base-2
+// units), m = max_s m_s and w_s = 2^(m_s - m): O = sum_s w_s O_s / sum_s w_s l_s,
+// the softmax over the union of the CTAs' keys.  Four CTAs per query (16 heads
+// each), thread = (head, 32 dims); a head whose keys are all masked gets zeros,
+// as in the one-CTA path.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part, int split,
+                                                           uint16_t* __restrict__ out) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int bq = blockIdx.x >> 2;
+  const int h = (blockIdx.x & 3) * 16 + (threadIdx.x >> 4), d0 = (threadIdx.x & 15) * 32;
+  const float* pb = part + (int64_t)bq * split * A_PART_FLOATS;
+  float mx = -INFINITY;
+  for (int s = 0; s < split; s++) mx = fmaxf(mx, pb[(int64_t)s * A_PART_FLOATS + h]);
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; i++) acc[i] = 0.f;
+  float L = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < split; s++) {
+      const float* ps = pb + (int64_t)s * A_PART_FLOATS;
+      const float ms = ps[h];
+      if (ms == -INFINITY) continue;                       // no unmasked key in this CTA's chunks
+      const float w = exp2f(ms - mx);
+      L += w * ps[H + h];
+      const float4* o4 = reinterpret_cast<const float4*>(ps + 2 * H + (int64_t)h * D + d0);
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const float4 v = o4[i];
+        acc[4 * i] += w * v.x;
+        acc[4 * i + 1] += w * v.y;
+        acc[4 * i + 2] += w * v.z;
+        acc[4 * i + 3] += w * v.w;
+      }
+    }
+  }
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+  uint4* o = reinterpret_cast<uint4*>(out + ((int64_t)bq * H + h) * D + d0);
+#pragma unroll
+  for (int i = 0; i < 4; i++)
+    o[i] = make_uint4(pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv), pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                      pack_bf16x2(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv), pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
 }
 
 // ------------------------------------------------------------------ host side
@@ -635,14 +717,29 @@ static bool encode_bf16_rows512(CUtensorMap* map, const void* base, uint64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t attn_partials_bytes(int64_t, int) { return 0; }
+// Partial states for a split call: calls of up to A_SPLIT_MAX_BQ queries may be
+// split over as many CTAs per query as they have chunks.
+size_t attn_partials_bytes(int64_t BQ, int K) {
+  if (BQ <= 0 || BQ > A_SPLIT_MAX_BQ) return 0;
+  const int64_t nc = 1 + (K + A_KEYS - 1) / A_KEYS;
+  return (size_t)(BQ * nc * A_PART_FLOATS) * sizeof(float);
+}
 
-cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
+int attn_split_max_queries() { return A_SPLIT_MAX_BQ; }
+
+cudaError_t launch_attention(AttnParams p, int B, float* part, cudaStream_t stream) {
   const int64_t BQ = (int64_t)B * p.Q;
   if (BQ == 0) return cudaSuccess;
+  const int nc = 1 + (p.K + A_KEYS - 1) / A_KEYS;
+  if (p.split < 1) p.split = 1;
+  if (p.split > nc) p.split = nc;                               // at least one chunk per CTA
+  if (p.split > 1 && (part == nullptr || BQ > A_SPLIT_MAX_BQ)) return cudaErrorInvalidValue;
+  p.opart = part;
   static PerDeviceOnce attrs;
   cudaError_t e = attrs.ensure([](int) {
-    return cudaFuncSetAttribute(attn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM);
+    cudaError_t r = cudaFuncSetAttribute(attn_stream_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(attn_stream_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM);
   });
   if (e != cudaSuccess) return e;
   CUtensorMap map_q, map_swa;
@@ -652,7 +749,7 @@ cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
                                 : encode_bf16_rows512(&map_swa, p.swa, swa_rows, A_KEYS);
   if (!swa_ok) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)BQ);
+  cfg.gridDim = dim3((unsigned)(BQ * p.split));
   cfg.blockDim = dim3(A_THREADS);
   cfg.dynamicSmemBytes = A_SMEM;
   cfg.stream = stream;
@@ -661,7 +758,16 @@ cudaError_t launch_attention(AttnParams p, int B, float*, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_stream_kernel, p, map_q, map_swa);
+  e = p.split > 1 ? cudaLaunchKernelEx(&cfg, attn_stream_kernel<true>, p, map_q, map_swa)
+                   : cudaLaunchKernelEx(&cfg, attn_stream_kernel<false>, p, map_q, map_swa);
+  if (e != cudaSuccess || p.split == 1) return e;
+  cudaLaunchConfig_t cc = {};
+  cc.gridDim = dim3((unsigned)(BQ * 4));
+  cc.blockDim = dim3(256);
+  cc.stream = stream;
+  cc.attrs = attr;
+  cc.numAttrs = 1;
+  return cudaLaunchKernelEx(&cc, attn_combine_kernel, (const float*)part, p.split, p.out);
 }
 
 }  // namespace csa2

@@ -88,7 +88,8 @@ csa2_status do_index_score(const csa2_cache* cache, const uint16_t* q_idx, const
 csa2_status do_attention(const csa2_cache* cache, const uint16_t* q, const int32_t* sel, int K,
                          const uint16_t* swa, const int64_t* swa_base, int S, const int64_t* q_pos, float scale,
                          uint16_t* out, int B, int Q, void* part_ws, WsHeader* hdr, cudaStream_t stream,
-                         const uint8_t* packed_in = nullptr, uint8_t* packed_out = nullptr, bool swa_fp8 = false) {
+                         const uint8_t* packed_in = nullptr, uint8_t* packed_out = nullptr, bool swa_fp8 = false,
+                         int split = 1) {
   AttnParams p{};
   p.main_kv = cache->main_kv;
   p.cap = cache->cap;
@@ -106,6 +107,7 @@ csa2_status do_attention(const csa2_cache* cache, const uint16_t* q, const int32
   p.hdr = hdr;
   p.packed_in = packed_in;
   p.packed_out = packed_out;
+  p.split = split;
   return from_cuda(launch_attention(p, B, reinterpret_cast<float*>(part_ws), stream));
 }
 
@@ -423,6 +425,9 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
   if (a->mode != CSA2_MODE_REUSE && !aligned16(a->q_idx)) return CSA2_ERR_INVALID_ARG;
   if (a->packed_sel && !aligned16(a->packed_sel)) return CSA2_ERR_INVALID_ARG;
   if (a->swa_fp8 != 0 && a->swa_fp8 != 1) return CSA2_ERR_INVALID_ARG;
+  if (a->attn_split < 0) return CSA2_ERR_INVALID_ARG;
+  const int split = a->attn_split > 1 ? a->attn_split : 1;
+  if (split > 1 && (int64_t)a->B * a->Q > attn_split_max_queries()) return CSA2_ERR_UNSUPPORTED;
   const uint8_t* packed_in = a->mode == CSA2_MODE_REUSE ? a->packed_sel : nullptr;
   uint8_t* packed_out = a->mode == CSA2_MODE_REUSE ? nullptr : a->packed_sel;
 
@@ -442,7 +447,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
                                        a->sel, a->M, a->pool_blocks, cur, s));
       if (st != CSA2_OK) return st;
       return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out,
-                          a->B, a->Q, part, hdr, s, packed_in, packed_out, a->swa_fp8 != 0);
+                          a->B, a->Q, part, hdr, s, packed_in, packed_out, a->swa_fp8 != 0, split);
     }
     st = from_cuda(launch_block_topk(scores, a->q_pos, cache->n_entries, cache->m, a->B, a->Q, a->max_n, a->M,
                                      a->pool_blocks, gkeys, s));
@@ -473,7 +478,7 @@ csa2_status csa2_decode(const csa2_cache* cache, const csa2_decode_args* a, void
     if (st != CSA2_OK) return st;
   }
   return do_attention(cache, a->q, a->sel, a->K, a->swa, a->swa_base_pos, a->S, a->q_pos, a->scale, a->out, a->B,
-                      a->Q, part, hdr, s, packed_in, packed_out, a->swa_fp8 != 0);
+                      a->Q, part, hdr, s, packed_in, packed_out, a->swa_fp8 != 0, split);
 }
 
 }  // extern "C"

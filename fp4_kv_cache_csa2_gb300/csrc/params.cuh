@@ -57,12 +57,11 @@ struct AttnParams {
   const int64_t* q_pos;       // [BQ]
   float scale;
   uint16_t* out;              // [BQ][64][512]
-  int Q, n_chunks;            // n_chunks set by the launcher
+  int Q;
   const uint8_t* packed_in;   // [BQ][K][288] selected entries to read instead of gathering, or null
   uint8_t* packed_out;        // [BQ][K][288] where to write the gathered selected entries, or null
-  float* opart;               // [BQ][n_chunks][64][512]
-  float* mpart;               // [BQ][n_chunks][64]
-  float* lpart;               // [BQ][n_chunks][64]
+  int split;                  // CTAs per query (1: the whole query in one CTA)
+  float* opart;               // split > 1: the partial states, [BQ * split][2 * 64 + 64 * 512]
   WsHeader* hdr;
 };
 
@@ -108,6 +107,7 @@ cudaError_t launch_row_select(const float* scores, const int64_t* q_pos, const i
                               cudaStream_t stream);
 cudaError_t launch_attention(AttnParams p, int B, float* partials, cudaStream_t stream);
 size_t attn_partials_bytes(int64_t BQ, int K);
+int attn_split_max_queries();
 cudaError_t launch_block_summary(const HsParams& p, cudaStream_t stream);
 cudaError_t launch_hisa_view(const HvParams& p, cudaStream_t stream);
 

@@ -64,6 +64,7 @@ extern "C" {
 #define CSA2_INDEX_CODE_BYTES 64
 #define CSA2_INDEX_SCALE_BYTES 4
 #define CSA2_MAX_K 512
+#define CSA2_ATTN_SPLIT_MAX_QUERIES 128   /* B * Q of a call whose attention may be split */
 #define CSA2_MAX_M 2048
 #define CSA2_WS_HEADER_BYTES 256
 
@@ -340,6 +341,19 @@ csa2_status csa2_hisa_blocks(const csa2_cache *cache, const uint8_t *sum_codes, 
  * swa_fp8 = 1 reads the window rows as E4M3 bytes, uint8 [B][S][512] from
  * csa2_swa_quantize_fp8 (16-byte aligned); the attention takes their E4M3
  * values exactly.  Other values of swa_fp8 return CSA2_ERR_INVALID_ARG.
+ * attn_split (appended last) chooses how the attention spreads a query over
+ * CTAs.  0 or 1: one CTA per query walks the window and every run of 128
+ * selected entries (the least SM time per query: for calls that run beside
+ * others or fill the GPU).  S >= 2: the query's chunks (the window, then the
+ * runs of 128 selected entries) are divided among S CTAs (at most one per
+ * chunk; larger S is reduced to the chunk count), each keeping its own
+ * softmax state, and a second kernel merges the states into the output
+ * (the shortest call: for a call that alone leaves most SMs idle, such as a
+ * small batch going through the layers one after another).  The merged
+ * softmax is the same function of the scores up to rounding.  Split calls
+ * need B * Q <= CSA2_ATTN_SPLIT_MAX_QUERIES (CSA2_ERR_UNSUPPORTED otherwise);
+ * csa2_decode_workspace_size includes their partial states for such calls.
+ * Negative values return CSA2_ERR_INVALID_ARG.
  */
 typedef struct {
     csa2_mode mode;
@@ -359,6 +373,7 @@ typedef struct {
     uint16_t *out;              /* [B][Q][64][512]                              */
     uint8_t *packed_sel;        /* [B][Q][K][288] or NULL: Full/Reindex out, Reuse in */
     int32_t swa_fp8;            /* 0: swa is bf16; 1: swa is E4M3 [B][S][512]   */
+    int32_t attn_split;         /* CTAs per query in the attention (0 / 1: one) */
 } csa2_decode_args;
 
 size_t csa2_decode_workspace_size(csa2_mode mode, int B, int Q, int64_t max_n, int M, int K);

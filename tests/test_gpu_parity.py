@@ -506,6 +506,58 @@ def test_decode_packed_selection_roundtrip(csa2, mode_out, K, Q, T):
     assert torch.equal(out_gather, out)     # Reuse with the same selection and queries = the writing call
 
 
+@pytest.mark.parametrize("split,K,Q,T", [(2, 512, 2, 4096), (5, 512, 1, 4096), (3, 200, 3, 1200), (9, 20, 2, 300)])
+def test_decode_attention_split(csa2, split, K, Q, T):
+    """The attention of a query split over several CTAs (attn_split), each
+    walking a contiguous range of its key chunks (the window, then the runs of
+    128 selected entries) with its own softmax state, merged by the combine
+    kernel.  A Full call with the split selects exactly what the call without it
+    selects and writes the same packed copy; every output matches the oracle's
+    attention over the selection; Reuse calls with the split, gathering and
+    reading the packed copy, agree with each other and with the Full call bit
+    for bit.  Split 9 exceeds the chunk count (K = 20: the window and one run)
+    and is reduced to it; K = 200 ends in a partial run of 72 entries."""
+    M = 150 if T >= 1200 else 40
+    case = cases.make_case(B=2, T=T, m=1, Q=Q, M=M, K=K, seed=833 + K + split)
+    L = GpuLayer(csa2, case)
+    B, max_n = 2, T
+    pool = torch.empty((B, Q, M), dtype=torch.int32, device=DEV)
+    sel = torch.empty((B, Q, K), dtype=torch.int32, device=DEV)
+    out1 = torch.empty((B, Q, 64, 512), dtype=torch.int16, device=DEV)
+    ws = csa2.Workspace(max(csa2.decode_workspace_size(m, B, Q, max_n, M, K) for m in (0, 1, 2)), device=DEV)
+    common = dict(q_pos=L.q_pos, q=L.q, swa=L.swa, swa_base_pos=L.swa_base, scale=case.scale, ws=ws, M=M,
+                  max_n=max_n, q_idx=L.q_idx, w_head=L.w_head)
+    csa2.decode(csa2.MODE_FULL, L.cache, sel=sel, out=out1, pool_blocks=pool, **common)
+    pool_s = torch.empty_like(pool)
+    sel_s = torch.empty_like(sel)
+    out_s = torch.empty_like(out1)
+    packed = torch.full((B, Q, K, 288), 0xA5, dtype=torch.uint8, device=DEV)
+    csa2.decode(csa2.MODE_FULL, L.cache, sel=sel_s, out=out_s, pool_blocks=pool_s, packed_sel=packed,
+                attn_split=split, **common)
+    assert ws.sync_status()[0] == 0
+    assert torch.equal(sel, sel_s) and torch.equal(pool, pool_s)
+    s_h, p_h, main_dev = host(sel_s), host(packed), host(L.cache.main_kv)
+    valid = s_h >= 0
+    for b in range(B):
+        for qi in range(Q):
+            assert np.array_equal(p_h[b, qi][valid[b, qi]], main_dev[b, s_h[b, qi][valid[b, qi]]])
+    main, _, _ = cases.oracle_cache(case)
+    got = bf16_to_f32(out_s)
+    for b in range(B):
+        for qi in range(Q):
+            cases.check_attention(got[b, qi], _oracle_attention(case, main, b, qi, s_h[b, qi]),
+                                  f"split {split} b{b} q{qi}")
+    out_g = torch.empty_like(out1)
+    out_p = torch.empty_like(out1)
+    csa2.decode(csa2.MODE_REUSE, L.cache, sel=sel_s, out=out_g, attn_split=split, **common)
+    csa2.decode(csa2.MODE_REUSE, L.cache, sel=sel_s, out=out_p, packed_sel=packed, attn_split=split, **common)
+    assert ws.sync_status()[0] == 0
+    assert torch.equal(out_g, out_p)
+    assert torch.equal(out_g, out_s)
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):
+        csa2.decode(csa2.MODE_REUSE, L.cache, sel=sel_s, out=out_g, attn_split=-1, **common)
+
+
 def test_decode_packed_selection_must_be_aligned(csa2):
     case = cases.make_case(B=1, T=300, m=1, Q=1, M=40, K=20, seed=815)
     L = GpuLayer(csa2, case)
