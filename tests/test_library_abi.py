@@ -95,6 +95,18 @@ def test_variant_calls_host_logic_without_gpu(lib_path):
     a.swa_fp8 = 2
     need = lib.csa2_decode_workspace_size(2, 1, 1, 64, 8, 8)
     assert lib.csa2_decode(ctypes.byref(cache), ctypes.byref(a), ws, need, None) == 1
+    # decode: attn_split must not be negative, and a split call holds at most 128 queries
+    a.swa_fp8 = 0
+    a.attn_split = -1
+    assert lib.csa2_decode(ctypes.byref(cache), ctypes.byref(a), ws, need, None) == 1
+    a.B, a.attn_split = 129, 5
+    need = lib.csa2_decode_workspace_size(2, 129, 1, 64, 8, 8)
+    assert lib.csa2_decode(ctypes.byref(cache), ctypes.byref(a), ws, need, None) == 2
+    # the partial states of a split call are part of the workspace up to 128 queries, none beyond
+    per_query = 2 * (2 * 64 + 64 * 512) * 4                       # K = 8: the window and one run, 2 CTAs
+    assert (lib.csa2_decode_workspace_size(2, 128, 1, 64, 8, 8) - lib.csa2_decode_workspace_size(2, 1, 1, 64, 8, 8)
+            >= 127 * per_query)
+    assert lib.csa2_decode_workspace_size(2, 129, 1, 64, 8, 8) < per_query
 
 
 def test_query_count_limit_and_concurrent_argument_checks(lib_path):
